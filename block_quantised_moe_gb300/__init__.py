@@ -1,0 +1,8 @@
+"""GB300-native fused routed-expert MoE FFN over FP4 block-quantised experts.
+
+The compute lives in ``libmoe.so`` (hand-written CUDA for sm_103a behind a C
+ABI, declared in ``include/moe.h``).  ``block_quantised_moe_gb300.abi`` is the
+thin ctypes binding with the same function names; ``synth`` holds the seeded
+synthetic input generators.  Importing this package does not load the library;
+importing ``abi`` does, and raises if it has not been built.
+"""
