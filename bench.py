@@ -1,0 +1,419 @@
+#!/usr/bin/env python
+"""MoE-layer throughput of libmoe on GB300, one JSON line on rank 0.
+
+Workload: the decode layer E=128 experts, hidden 2048, intermediate 768, top-8,
+NVFP4 weights with BF16 activations and gated SiLU, at T tokens per step
+(default 64; 1, 4 and 16 are the other decode batch sizes of this layer).  A
+step is one full forward of the layer (routing, GEMM1 + SiLU, GEMM2 x topk
+weight, combine) through the C ABI over one batch of seeded synthetic input.
+Steps rotate over R independent layer replicas and routing draws whose packed
+weights together exceed L2, so every step streams its experts from HBM.
+
+``value`` is tokens/s with inputs resident in HBM, timed with CUDA events on
+the launching stream; ``e2e`` is the same through ``moe_run_host`` with pinned
+host buffers (H2D of x / ids / weights and D2H of the output inside the timed
+loop).  ``roofline`` is for the dominant kernel, from per-stage CUDA events
+recorded by ``moe_run_timed`` inside the timed region.  ``cpu_baseline`` times
+the CPU oracle on a bounded sample.  ``--impl reference`` times only the oracle
+(the reference arm).  Multi-GPU runs (torchrun) are independent replicas: one
+layer per rank, no collective on the data path, weak scaling.
+"""
+
+from __future__ import annotations
+
+import argparse
+import ctypes
+import hashlib
+import json
+import os
+import statistics
+import sys
+import threading
+import time
+
+import numpy as np
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+DEFAULT_CONFIG = "decode_e128_h2048_i768_k8"
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=50)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--config", default=DEFAULT_CONFIG)
+    ap.add_argument("--tokens", type=int, default=64)
+    ap.add_argument("--replicas", type=int, default=4)
+    ap.add_argument("--e2e-steps", type=int, default=300)
+    ap.add_argument("--cpu-budget-s", type=float, default=12.0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    return ap.parse_args()
+
+
+# ------------------------------------------------------------- distributed
+
+def dist_setup(args):
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    else:
+        torch.cuda.set_device(0)
+    return world, rank, local
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(v, world):
+    if world == 1:
+        return v
+    import torch.distributed as dist
+    t = torch.tensor([v], dtype=torch.float64, device="cuda")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+# ----------------------------------------------------------------- clocks
+
+class ClockSampler:
+    """SM clock and clock-event reasons sampled through NVML (read-only) while running."""
+
+    REASONS = {0x4: "sw_power_cap", 0x8: "hw_slowdown", 0x20: "sw_thermal_slowdown",
+               0x40: "hw_thermal_slowdown", 0x80: "hw_power_brake_slowdown", 0x2: "applications_clocks_setting"}
+
+    def __init__(self, interval=0.002):
+        self.samples, self.reasons, self.max_mhz = [], 0, None
+        self.interval, self._stop = interval, threading.Event()
+        self.nvml = self.handle = None
+        try:
+            nvml = ctypes.CDLL("libnvidia-ml.so.1")
+            if nvml.nvmlInit_v2() != 0:
+                return
+            h = ctypes.c_void_p()
+            p = torch.cuda.get_device_properties(torch.cuda.current_device())
+            bus = getattr(p, "pci_bus_id", None)
+            ok = -1
+            if bus is not None:
+                busid = f"{getattr(p, 'pci_domain_id', 0):08x}:{bus:02x}:{getattr(p, 'pci_device_id', 0):02x}.0"
+                ok = nvml.nvmlDeviceGetHandleByPciBusId_v2(busid.encode(), ctypes.byref(h))
+            if ok != 0:
+                ok = nvml.nvmlDeviceGetHandleByIndex_v2(0, ctypes.byref(h))
+            if ok != 0:
+                return
+            mx = ctypes.c_uint()
+            if nvml.nvmlDeviceGetMaxClockInfo(h, 1, ctypes.byref(mx)) == 0:
+                self.max_mhz = mx.value
+            self.nvml, self.handle = nvml, h
+        except OSError:
+            pass
+
+    def _run(self):
+        mhz, rs = ctypes.c_uint(), ctypes.c_ulonglong()
+        while not self._stop.is_set():
+            if self.nvml.nvmlDeviceGetClockInfo(self.handle, 1, ctypes.byref(mhz)) == 0:
+                self.samples.append(mhz.value)
+            if self.nvml.nvmlDeviceGetCurrentClocksEventReasons(self.handle, ctypes.byref(rs)) == 0:
+                self.reasons |= rs.value
+            time.sleep(self.interval)
+
+    def __enter__(self):
+        if self.nvml is not None:
+            self._t = threading.Thread(target=self._run, daemon=True)
+            self._t.start()
+        return self
+
+    def __exit__(self, *a):
+        if self.nvml is not None:
+            self._stop.set()
+            self._t.join()
+
+    def summary(self):
+        if not self.samples:
+            return {"sm_mhz": None, "sm_max_mhz": self.max_mhz, "reasons": [], "samples": 0,
+                    "note": "NVML unavailable"}
+        return {"sm_mhz": statistics.median(self.samples), "sm_max_mhz": self.max_mhz,
+                "reasons": [n for b, n in self.REASONS.items() if self.reasons & b],
+                "samples": len(self.samples)}
+
+
+# ------------------------------------------------------------------ helpers
+
+def peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            p = json.load(f)
+        return float(p["hbm_gbs"]), "measured"
+    except (OSError, KeyError, ValueError):
+        return 6800.0, "fallback"
+
+
+def expert_bytes(cfg):
+    """Packed bytes of one expert: codes + block scales + globals."""
+    H, I, wfmt, act = cfg["H"], cfg["I"], cfg["wfmt"], cfg["act"]
+    n13 = 2 * I if act == "silu" else I
+    bs = 16 if wfmt == "nvfp4" else 32
+    per = lambda rows, K: rows * K // 2 + rows * K // bs  # noqa: E731
+    g13 = 4 * (n13 // I) if wfmt == "nvfp4" else 0
+    g2 = 4 if wfmt == "nvfp4" else 0
+    return per(n13, H) + g13, per(H, I) + g2
+
+
+def traffic_record(kernel_src):
+    """ncu DRAM bytes per launch recorded in profiles/, valid only for the current kernel source."""
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    try:
+        rec = json.load(open(path))
+    except (OSError, ValueError):
+        return None, None
+    src = open(os.path.join(ROOT, "block_quantised_moe_gb300", "csrc", kernel_src), "rb").read()
+    return rec, hashlib.sha256(src).hexdigest()[:16]
+
+
+# --------------------------------------------------------------- oracle arm
+
+def oracle_prepare(cfg, x, ids, w, n_pairs, seed=0):
+    """CPU oracle on the first n_pairs (token, slot) pairs of a batch.
+
+    Returns (forward callable, tokens-equivalent of the sample, description).
+    Pairs outside the sample get an out-of-range id, which the oracle skips, so
+    its work is proportional to the sample.  The oracle's experts are quantised
+    here (untimed) from the same seeded FP32 draws the GPU layer was built from.
+    """
+    from oracle import moe
+    from block_quantised_moe_gb300 import synth
+    T, K = ids.shape
+    E, H, I = cfg["E"], cfg["H"], cfg["I"]
+    flat = np.full(T * K, -1, dtype=np.int64)
+    flat[:n_pairs] = ids.reshape(-1)[:n_pairs]
+    ids_s = flat.reshape(T, K)
+    toks = np.unique(np.nonzero(ids_s >= 0)[0])
+    used = np.unique(ids_s[ids_s >= 0])
+    remap = np.full(E, -1)
+    remap[used] = np.arange(len(used))
+    ids_c = np.where(ids_s >= 0, remap[np.clip(ids_s, 0, E - 1)], -1)[toks]
+    gated = cfg["act"] == "silu"
+    w13s, w2s = [], []
+    for e in used:
+        a, b = synth.make_expert_weights(int(e), H, I, gated, seed, device="cuda")
+        w13s.append([m.cpu().numpy() for m in a]), w2s.append(b.cpu().numpy())
+    L = moe.quantize_layer(w13s, w2s, cfg["wfmt"], cfg["act"])
+    xs, ws = x[toks], w[toks]
+    afmt = cfg["afmt"]
+
+    def forward():
+        return moe.moe_forward(xs, ids_c, ws, L, afmt)
+
+    desc = f"{n_pairs} (token, slot) pairs of a {T}x{K} batch ({len(toks)} tokens, {len(used)} experts)"
+    return forward, n_pairs / K, desc
+
+
+def time_repeated(fn, min_seconds):
+    """Mean seconds per call over repeated calls lasting at least min_seconds."""
+    n, t0 = 0, time.perf_counter()
+    while True:
+        fn()
+        n += 1
+        el = time.perf_counter() - t0
+        if el >= min_seconds:
+            return el / n, n
+
+
+def run_reference(args, cfg, world, rank):
+    if rank != 0:
+        return
+    from block_quantised_moe_gb300 import synth
+    T, K = args.tokens, cfg["K"]
+    x = synth.make_x(T, cfg["H"], 0).float().numpy()
+    ids, w = synth.make_routing(T, cfg["E"], K, 0, zipf=cfg["zipf"])
+    ids, w = ids.numpy(), w.numpy()
+    # one (token, slot) pair per step keeps any --steps run within minutes
+    fwd, tok, desc = oracle_prepare(cfg, x, ids, w, 1)
+    for _ in range(args.warmup):
+        fwd()
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        fwd()
+    total = time.perf_counter() - t0
+    value = args.steps * tok / total
+    cores = len(os.sched_getaffinity(0))
+    line = {
+        "impl": "reference", "metric": "moe_layer_tokens_per_s", "value": value, "unit": "tokens/s",
+        "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": 1e3 * total / args.steps, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+        "config": {"workload": f"{args.config} T={T}", "sample_per_step": desc},
+        "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": cores, "kind": "oracle",
+                         "sample": f"per step: {desc}; oracle forward only (weights quantised untimed)"},
+        "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+# ------------------------------------------------------------------ our arm
+
+def main():
+    args = parse()
+    from block_quantised_moe_gb300 import synth
+    cfg = synth.CONFIGS[args.config]
+    world, rank, local = dist_setup(args)
+    if args.impl == "reference":
+        run_reference(args, cfg, world, rank)
+        return
+
+    from block_quantised_moe_gb300 import build
+    if local == 0:
+        build.build()
+    barrier(world)
+    from block_quantised_moe_gb300 import abi, layer
+
+    E, H, I, K, T = cfg["E"], cfg["H"], cfg["I"], cfg["K"], args.tokens
+    afmt = cfg["afmt"]
+    R = max(1, args.replicas)
+    seed_base = 1000 * rank
+    ck = layer.make_experts_gpu(E, H, I, cfg["wfmt"], cfg["act"], seed=0)
+    packed0 = layer.PackedLayer(ck, H, I)
+    del ck
+    packed = [packed0.packed] + [packed0.packed.clone() for _ in range(R - 1)]
+    plan = layer.Plan(packed0, K, T, afmt)
+    xs, idss, ws, outs, binds, touched = [], [], [], [], [], []
+    for r in range(R):
+        x = synth.make_x(T, H, seed_base + r).cuda()
+        ids, w = synth.make_routing(T, E, K, seed_base + r, zipf=cfg["zipf"])
+        touched.append(len(np.unique(ids.numpy())))
+        ids, w = ids.cuda(), w.cuda()
+        out = torch.empty(T, H, dtype=torch.bfloat16, device="cuda")
+        xs.append(x), idss.append(ids), ws.append(w), outs.append(out)
+        binds.append(plan.bind(x, ids, w, out, packed=packed[r]))
+    stream = torch.cuda.current_stream()
+    torch.cuda.synchronize()
+
+    # events for the per-stage timing, recorded once so that the handles exist
+    n_ev = abi.MOE_NUM_STAGES + 1
+    n_timed_steps = min(args.steps, 512)
+    every = max(1, args.steps // n_timed_steps)
+    ev_sets = []
+    for _ in range(n_timed_steps):
+        evs = [torch.cuda.Event(enable_timing=True) for _ in range(n_ev)]
+        for e in evs:
+            e.record(stream)
+        ev_sets.append(evs)
+    torch.cuda.synchronize()
+
+    for i in range(args.warmup):
+        binds[i % R].run(stream)
+    torch.cuda.synchronize()
+    barrier(world)
+
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    used_sets = []
+    with ClockSampler() as clk:
+        torch.cuda.synchronize()
+        barrier(world)
+        start.record(stream)
+        for i in range(args.steps):
+            b = binds[i % R]
+            if i % every == 0 and len(used_sets) < n_timed_steps:
+                evs = ev_sets[len(used_sets)]
+                abi.moe_run_timed(b.handle, [e.cuda_event for e in evs], stream)
+                used_sets.append((i % R, evs))
+            else:
+                b.run(stream)
+        end.record(stream)
+        torch.cuda.synchronize()
+        barrier(world)
+    ms = max_over_ranks(start.elapsed_time(end), world)
+    value = world * T * args.steps / (ms / 1e3)
+
+    stage_ms = np.zeros(abi.MOE_NUM_STAGES)
+    for _, evs in used_sets:
+        for s in range(abi.MOE_NUM_STAGES):
+            stage_ms[s] += evs[s].elapsed_time(evs[s + 1])
+    stage_ms /= max(1, len(used_sets))
+
+    # algorithmic bytes (HBM) of the whole layer and of each kernel, per step
+    b13, b2 = expert_bytes(cfg)
+    tch = float(np.mean(touched))
+    x_bytes, out_bytes, route_bytes = T * H * 2, T * H * 2, T * K * 8
+    layer_bytes = tch * (b13 + b2) + x_bytes + out_bytes + route_bytes
+    kernel_bytes = {"gemm1": tch * b13 + x_bytes, "gemm2": tch * b2 + T * K * 4,
+                    "combine": out_bytes, "route": T * K * 4}
+    flops = 2 * T * K * (3 if cfg["act"] == "silu" else 2) * H * I
+    names = abi.STAGES
+    dom = int(np.argmax(stage_ms))
+    dom_name = names[dom]
+    hbm, peak_kind = peaks()
+    dom_bytes = kernel_bytes.get(dom_name, 0.0)
+    achieved = dom_bytes / (stage_ms[dom] * 1e-3) / 1e9 if stage_ms[dom] > 0 else 0.0
+    rec, src_hash = traffic_record("k_grouped_cc.cu")
+    traffic = None
+    if rec and rec.get("src_sha256_16") == src_hash and rec.get("workload") == f"{args.config} T={T}":
+        traffic = rec.get("per_launch", {}).get(dom_name)
+
+    # end to end through moe_run_host: pinned host buffers, copies inside the loop
+    xh = xs[0].cpu().pin_memory()
+    ih = idss[0].cpu().pin_memory()
+    wh = ws[0].cpu().pin_memory()
+    oh = torch.empty(T, H, dtype=torch.bfloat16).pin_memory()
+    n_e2e = max(1, min(args.e2e_steps, args.steps))
+    for _ in range(3):
+        abi.moe_run_host(binds[0].handle, xh, ih, wh, oh, stream)
+    barrier(world)
+    t0 = time.perf_counter()
+    for i in range(n_e2e):
+        abi.moe_run_host(binds[i % R].handle, xh, ih, wh, oh, stream)
+    e2e_s = max_over_ranks(time.perf_counter() - t0, world)
+    e2e_value = world * T * n_e2e / e2e_s
+
+    line = {
+        "metric": "moe_layer_tokens_per_s", "value": value, "unit": "tokens/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms / args.steps,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+        "data": "synthetic",
+        "config": {"workload": f"{args.config} T={T}", "experts": E, "hidden": H, "intermediate": I,
+                   "top_k": K, "weights": cfg["wfmt"], "activations": afmt, "act": cfg["act"],
+                   "tokens": T, "parallelism": f"replicas x{world}",
+                   "l2": f"{R} layer replicas x {packed0.packed.numel() / 1e6:.0f} MB rotated per step (> L2)",
+                   "touched_experts_mean": tch},
+        "hbm_gbs_layer": layer_bytes / (ms / args.steps * 1e-3) / 1e9,
+        "tflops": flops / (ms / args.steps * 1e-3) / 1e12,
+        "stage_us": {n: round(1e3 * v, 3) for n, v in zip(names, stage_ms)},
+        "roofline": {"kernel": dom_name, "bound": "hbm", "achieved": achieved, "peak": hbm,
+                     "peak_kind": peak_kind, "unit": "GB/s", "frac": achieved / hbm, "traffic": traffic,
+                     "algorithmic_bytes": dom_bytes},
+        "layer_roofline_frac": layer_bytes / (ms / args.steps * 1e-3) / 1e9 / hbm,
+        "gpu_launches": args.steps * (4 + (2 if afmt != "bf16" else 0)),
+        "e2e": {"value": e2e_value, "unit": "tokens/s", "h2d_bytes_per_step": T * H * 2 + T * K * 8,
+                "d2h_bytes_per_step": T * H * 2, "steps": n_e2e},
+        "clocks": clk.summary(),
+    }
+
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        x_np = xs[0].float().cpu().numpy()
+        ids_np, w_np = idss[0].cpu().numpy(), ws[0].cpu().numpy()
+        # two tokens' pairs, forward repeated for about cpu_budget_s
+        fwd, tok, desc = oracle_prepare(cfg, x_np, ids_np, w_np, min(T * K, 2 * K))
+        dt, n = time_repeated(fwd, args.cpu_budget_s)
+        line["cpu_baseline"] = {"value": tok / dt, "unit": "tokens/s", "cores": len(os.sched_getaffinity(0)),
+                                "kind": "oracle",
+                                "sample": f"{desc} of {args.config} T={T}; forward only, mean of {n} calls"}
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,89 @@
+// Host-side layouts and kernel launchers of libmoe (internal; not part of the ABI).
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+namespace bqmoe {
+
+constexpr size_t kAlign = 256;
+inline size_t align_up(size_t v, size_t a = kAlign) { return (v + a - 1) / a * a; }
+
+// Packed expert buffer written by the packer.  Per expert, row-major with K
+// contiguous, in this order; each segment starts on a 256-byte boundary.
+//   c13  uint8 [E][N13][H/2]    E2M1 codes of W13 (gate rows then up rows, or W1)
+//   s13  uint8 [E][N13][H/bs]   block scales of W13
+//   c2   uint8 [E][H][I/2]      E2M1 codes of W2
+//   s2   uint8 [E][H][I/bs]     block scales of W2
+//   g    float [E][4]           global scales (gate|w1, up, down, 1); all 1 for MXFP4
+struct WeightLayout {
+  int E = 0, H = 0, I = 0, wfmt = 0, act = 0;
+  int bs = 16;   // elements per block scale
+  int n13 = 0;   // rows of W13
+  size_t off_c13 = 0, off_s13 = 0, off_c2 = 0, off_s2 = 0, off_g = 0, total = 0;
+  size_t c13_expert() const { return (size_t)n13 * H / 2; }
+  size_t s13_expert() const { return (size_t)n13 * H / bs; }
+  size_t c2_expert() const { return (size_t)H * I / 2; }
+  size_t s2_expert() const { return (size_t)H * I / bs; }
+};
+
+// Scratch owned by the caller and carved by the plan (offsets in bytes).
+struct ScratchLayout {
+  int64_t cap_sorted = 0;  // rows of the padded, expert-sorted pair list
+  size_t status = 0, counts = 0, offsets = 0, sorted = 0, pair_pos = 0;
+  size_t xq_codes = 0, xq_scales = 0, xq_g = 0;
+  size_t h = 0, hq_codes = 0, hq_scales = 0, hq_g = 0;
+  size_t part = 0, total = 0;
+};
+
+// Activation sources the grouped kernels can stage.
+enum Src { SRC_X_BF16 = 0, SRC_X_NVFP4 = 1, SRC_X_MXFP8 = 2, SRC_H_F32 = 3, SRC_H_NVFP4 = 4, SRC_H_MXFP8 = 5 };
+// Grouped-kernel stage.
+enum Stage { STAGE_GATED = 0, STAGE_RELU2 = 1, STAGE_DOWN = 2 };
+
+struct GroupedArgs {
+  // expert weights of this stage
+  const uint8_t *codes, *scales;  // expert 0 base
+  size_t codes_expert, scales_expert;  // bytes per expert
+  const float *globals;  // [E][4]
+  int K;       // reduction length
+  int n_rows;  // I (GEMM1 features) or H (GEMM2 rows)
+  int I;       // intermediate (gated: up rows start at I)
+  // activation source
+  const void *act;            // bf16 x [T][H] | f32 h [cap][I] | codes
+  const uint8_t *act_scales;  // block scales (quantised sources)
+  const float *act_g;         // per-row NVFP4 global
+  // routing
+  const int32_t *counts, *offsets, *sorted_pair;
+  int top_k;
+  const float *topk_weights;
+  // output: h [cap][I] (GEMM1) or partials [cap][H] (GEMM2)
+  float *out;
+};
+
+cudaError_t launch_route(const int32_t *ids, int P, int E, int pad, int32_t *counts, int32_t *offsets,
+                         int32_t *sorted_pair, int32_t *pair_pos, int32_t *status, cudaStream_t s);
+
+cudaError_t launch_grouped_cc(int wfmt, int src, int stage, const GroupedArgs &a, int E, cudaStream_t s);
+
+cudaError_t launch_combine(const float *part, int H, const int32_t *pair_pos, int T, int K, void *out_bf16,
+                           cudaStream_t s);
+
+// Quantisers.  `rows_dev`, when non-null, is a device int with the number of
+// rows that are live; rows at or beyond it are skipped.
+cudaError_t launch_quant_rows_nvfp4(const void *src, bool src_bf16, int64_t rows, int64_t cols,
+                                    uint8_t *codes, uint8_t *scales, float *g, const int32_t *rows_dev,
+                                    cudaStream_t s);
+cudaError_t launch_quant_blocks(int qfmt, const void *src, bool src_bf16, int64_t rows, int64_t cols,
+                                int64_t rows_per_global, const float *g, uint8_t *codes, uint8_t *scales,
+                                const int32_t *rows_dev, cudaStream_t s);
+cudaError_t launch_amax_tensor(const void *src, bool src_bf16, int64_t batch, int64_t elems, float *amax,
+                               cudaStream_t s);
+cudaError_t launch_amax_to_global(float *g, int64_t n, cudaStream_t s);
+
+cudaError_t launch_pack(const WeightLayout &L, const void *w13_codes, const void *w13_scales,
+                        const float *w13_global, const void *w2_codes, const void *w2_scales,
+                        const float *w2_global, uint8_t *packed, cudaStream_t s);
+
+}  // namespace bqmoe

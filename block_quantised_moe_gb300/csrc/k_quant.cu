@@ -1,0 +1,253 @@
+// Block quantisers: NVFP4 (E2M1 + E4M3 per 16 + FP32 global) and MX
+// (E2M1 or E4M3 elements + E8M0 per 32), the row quantizers quantization.nvfp4 /
+// quantization.mxfp8 of the b12x project page (section "What's in here").
+//
+// NVFP4:  g = amax/(6*448);  s = E4M3_rne_sat((amax_b/6)/g);  d = s*g;
+//         q = E2M1_rne_sat(x/d)  (0 when d == 0)
+// MX:     X = floor(log2(amax_b)) - emax (2 for E2M1, 8 for E4M3), clamped to
+//         [-127, 127], -127 for an all-zero block;  s = X+127;  q = ELEM_rne_sat(x/2^X)
+//
+// Every step is a correctly rounded FP32 operation (__fdiv_rn, __fmul_rn) and
+// the element conversions are the cvt.rn.satfinite instructions, so the codes
+// and scales are a pure function of the input bits.  HBM-bound: one pass over
+// the input (two for a per-row or per-tensor global).
+#include <algorithm>
+
+#include "common.cuh"
+#include "internal.h"
+
+namespace bqmoe {
+
+constexpr int kQThreads = 256;
+
+template <bool BF16>
+__device__ __forceinline__ void load8(const void *src, int64_t idx, float (&v)[8]) {
+  if (BF16) {
+    const uint4 r = *reinterpret_cast<const uint4 *>(reinterpret_cast<const __nv_bfloat16 *>(src) + idx);
+    const uint32_t w[4] = {r.x, r.y, r.z, r.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      v[2 * i] = __uint_as_float(w[i] << 16);
+      v[2 * i + 1] = __uint_as_float(w[i] & 0xFFFF0000u);
+    }
+  } else {
+    const float4 a = *reinterpret_cast<const float4 *>(reinterpret_cast<const float *>(src) + idx);
+    const float4 b = *reinterpret_cast<const float4 *>(reinterpret_cast<const float *>(src) + idx + 4);
+    v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w;
+    v[4] = b.x; v[5] = b.y; v[6] = b.z; v[7] = b.w;
+  }
+}
+
+// One NVFP4 block of 16 with global g -> 8 code bytes (uint2) and the scale byte.
+__device__ __forceinline__ void nvfp4_block(const float (&x)[16], float g, uint2 &codes, uint32_t &scale) {
+  float amax = 0.f;
+#pragma unroll
+  for (int i = 0; i < 16; ++i) amax = fmaxf(amax, fabsf(x[i]));
+  scale = 0;
+  float d = 0.f;
+  if (g > 0.f) {
+    scale = f32_to_e4m3(__fdiv_rn(__fdiv_rn(amax, 6.0f), g));
+    d = __fmul_rn(e4m3_to_f32(scale), g);
+  }
+  if (d > 0.f) {
+    float a[8], b[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      a[i] = __fdiv_rn(x[i], d);
+      b[i] = __fdiv_rn(x[8 + i], d);
+    }
+    codes = make_uint2(f32x8_to_e2m1x8(a), f32x8_to_e2m1x8(b));
+  } else {
+    codes = make_uint2(0u, 0u);
+  }
+}
+
+// One MX block of 32 -> codes (16 bytes for E2M1, 32 for E4M3) and the E8M0 byte.
+template <int QF>
+__device__ __forceinline__ void mx_block(const float (&x)[32], uint32_t (&codes)[8], uint32_t &scale) {
+  float amax = 0.f;
+#pragma unroll
+  for (int i = 0; i < 32; ++i) amax = fmaxf(amax, fabsf(x[i]));
+  constexpr int emax = (QF == Q_MXFP8) ? 8 : 2;
+  int X = amax > 0.f ? floor_log2_f32(amax) - emax : -127;
+  X = max(-127, min(127, X));
+  scale = (uint32_t)(X + 127);
+  const float p2 = exp2i_f32(X);
+  float v[32];
+#pragma unroll
+  for (int i = 0; i < 32; ++i) v[i] = __fdiv_rn(x[i], p2);
+  if (QF == Q_MXFP8) {
+#pragma unroll
+    for (int i = 0; i < 8; ++i)
+      codes[i] = f32x2_to_e4m3x2(v[4 * i], v[4 * i + 1]) | (f32x2_to_e4m3x2(v[4 * i + 2], v[4 * i + 3]) << 16);
+  } else {
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      float w[8];
+#pragma unroll
+      for (int j = 0; j < 8; ++j) w[j] = v[8 * i + j];
+      codes[i] = f32x8_to_e2m1x8(w);
+    }
+  }
+}
+
+__device__ __forceinline__ float block_max(float v, float *red) {
+  v = warp_max(v);
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  if (lane == 0) red[warp] = v;
+  __syncthreads();
+  if (warp == 0) {
+    v = lane < (int)(blockDim.x >> 5) ? red[lane] : 0.f;
+    v = warp_max(v);
+    if (lane == 0) red[0] = v;
+  }
+  __syncthreads();
+  const float r = red[0];
+  __syncthreads();
+  return r;
+}
+
+// NVFP4 with one global per row: one CTA per row.
+template <bool BF16>
+__global__ void __launch_bounds__(kQThreads)
+k_quant_rows_nvfp4(const void *__restrict__ src, int64_t cols, uint8_t *__restrict__ codes,
+                   uint8_t *__restrict__ scales, float *__restrict__ g_out, const int32_t *__restrict__ rows_dev) {
+  __shared__ float red[32];
+  const int64_t row = blockIdx.x;
+  if (rows_dev != nullptr && row >= *rows_dev) return;
+  const int64_t base = row * cols;
+  float m = 0.f;
+  for (int64_t j = (int64_t)threadIdx.x * 8; j < cols; j += kQThreads * 8) {
+    float v[8];
+    load8<BF16>(src, base + j, v);
+#pragma unroll
+    for (int i = 0; i < 8; ++i) m = fmaxf(m, fabsf(v[i]));
+  }
+  const float amax = block_max(m, red);
+  const float g = __fdiv_rn(amax, 2688.0f);
+  if (threadIdx.x == 0) g_out[row] = g;
+  for (int64_t b = threadIdx.x; b < cols / 16; b += kQThreads) {
+    float x[16];
+    float *lo = x, *hi = x + 8;
+    load8<BF16>(src, base + b * 16, *reinterpret_cast<float(*)[8]>(lo));
+    load8<BF16>(src, base + b * 16 + 8, *reinterpret_cast<float(*)[8]>(hi));
+    uint2 c;
+    uint32_t s;
+    nvfp4_block(x, g, c, s);
+    *reinterpret_cast<uint2 *>(codes + (base + b * 16) / 2) = c;
+    scales[row * (cols / 16) + b] = (uint8_t)s;
+  }
+}
+
+// One thread per block; NVFP4 reads its global from g[row / rows_per_global].
+template <int QF, bool BF16>
+__global__ void __launch_bounds__(kQThreads)
+k_quant_blocks(const void *__restrict__ src, int64_t rows, int64_t cols, int64_t rows_per_global,
+               const float *__restrict__ g, uint8_t *__restrict__ codes, uint8_t *__restrict__ scales,
+               const int32_t *__restrict__ rows_dev) {
+  constexpr int bs = QF == Q_NVFP4 ? 16 : 32;
+  const int64_t nb = cols / bs;
+  const int64_t live_rows = rows_dev ? (rows < (int64_t)*rows_dev ? rows : (int64_t)*rows_dev) : rows;
+  for (int64_t i = (int64_t)blockIdx.x * kQThreads + threadIdx.x; i < live_rows * nb;
+       i += (int64_t)gridDim.x * kQThreads) {
+    const int64_t row = i / nb, b = i % nb;
+    const int64_t e0 = row * cols + b * bs;
+    float x[bs];
+#pragma unroll
+    for (int j = 0; j < bs; j += 8) load8<BF16>(src, e0 + j, *reinterpret_cast<float(*)[8]>(x + j));
+    if (QF == Q_NVFP4) {
+      uint2 c;
+      uint32_t s;
+      nvfp4_block(*reinterpret_cast<float(*)[16]>(x), g[row / rows_per_global], c, s);
+      *reinterpret_cast<uint2 *>(codes + e0 / 2) = c;
+      scales[i] = (uint8_t)s;
+    } else {
+      uint32_t c[8], s;
+      mx_block<QF>(*reinterpret_cast<float(*)[32]>(x), c, s);
+      if (QF == Q_MXFP8) {
+        uint4 *dst = reinterpret_cast<uint4 *>(codes + e0);
+        dst[0] = make_uint4(c[0], c[1], c[2], c[3]);
+        dst[1] = make_uint4(c[4], c[5], c[6], c[7]);
+      } else {
+        *reinterpret_cast<uint4 *>(codes + e0 / 2) = make_uint4(c[0], c[1], c[2], c[3]);
+      }
+      scales[i] = (uint8_t)s;
+    }
+  }
+}
+
+template <bool BF16>
+__global__ void __launch_bounds__(kQThreads)
+k_amax_tensor(const void *__restrict__ src, int64_t elems, float *__restrict__ amax) {
+  __shared__ float red[32];
+  const int64_t b = blockIdx.y;
+  float m = 0.f;
+  for (int64_t j = ((int64_t)blockIdx.x * kQThreads + threadIdx.x) * 8; j < elems;
+       j += (int64_t)gridDim.x * kQThreads * 8) {
+    float v[8];
+    load8<BF16>(src, b * elems + j, v);
+#pragma unroll
+    for (int i = 0; i < 8; ++i) m = fmaxf(m, fabsf(v[i]));
+  }
+  m = block_max(m, red);
+  // Non-negative floats order like their bit patterns: an integer max is exact and order-free.
+  if (threadIdx.x == 0) atomicMax(reinterpret_cast<unsigned *>(amax) + b, __float_as_uint(m));
+}
+
+__global__ void k_amax_to_global(float *g, int64_t n) {
+  const int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+  if (i < n) g[i] = __fdiv_rn(g[i], 2688.0f);
+}
+
+// ------------------------------------------------------------- launchers
+
+static int grid_for(int64_t work, int per_cta) {
+  int64_t g = (work + per_cta - 1) / per_cta;
+  return (int)std::max<int64_t>(1, std::min<int64_t>(g, 152 * 64));
+}
+
+cudaError_t launch_quant_rows_nvfp4(const void *src, bool src_bf16, int64_t rows, int64_t cols, uint8_t *codes,
+                                    uint8_t *scales, float *g, const int32_t *rows_dev, cudaStream_t s) {
+  if (rows <= 0) return cudaSuccess;
+  if (rows > 0x7FFFFFFF) return cudaErrorInvalidValue;
+  if (src_bf16)
+    k_quant_rows_nvfp4<true><<<(unsigned)rows, kQThreads, 0, s>>>(src, cols, codes, scales, g, rows_dev);
+  else
+    k_quant_rows_nvfp4<false><<<(unsigned)rows, kQThreads, 0, s>>>(src, cols, codes, scales, g, rows_dev);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_quant_blocks(int qfmt, const void *src, bool src_bf16, int64_t rows, int64_t cols,
+                                int64_t rows_per_global, const float *g, uint8_t *codes, uint8_t *scales,
+                                const int32_t *rows_dev, cudaStream_t s) {
+  if (rows <= 0) return cudaSuccess;
+  const int bs = qfmt == Q_NVFP4 ? 16 : 32;
+  const int grid = grid_for(rows * (cols / bs), kQThreads);
+#define QB(QF, B) k_quant_blocks<QF, B><<<grid, kQThreads, 0, s>>>(src, rows, cols, rows_per_global, g, codes, scales, rows_dev)
+  if (qfmt == Q_NVFP4) { if (src_bf16) QB(Q_NVFP4, true); else QB(Q_NVFP4, false); }
+  else if (qfmt == Q_MXFP4) { if (src_bf16) QB(Q_MXFP4, true); else QB(Q_MXFP4, false); }
+  else if (qfmt == Q_MXFP8) { if (src_bf16) QB(Q_MXFP8, true); else QB(Q_MXFP8, false); }
+  else return cudaErrorInvalidValue;
+#undef QB
+  return cudaGetLastError();
+}
+
+cudaError_t launch_amax_tensor(const void *src, bool src_bf16, int64_t batch, int64_t elems, float *amax,
+                               cudaStream_t s) {
+  if (batch <= 0) return cudaSuccess;
+  cudaError_t err = cudaMemsetAsync(amax, 0, sizeof(float) * batch, s);
+  if (err != cudaSuccess) return err;
+  const int64_t gx = (elems / 8 + kQThreads * 4 - 1) / (kQThreads * 4);
+  dim3 grid((unsigned)std::max<int64_t>(1, std::min<int64_t>(gx, 1024)), (unsigned)batch);
+  if (src_bf16) k_amax_tensor<true><<<grid, kQThreads, 0, s>>>(src, elems, amax);
+  else k_amax_tensor<false><<<grid, kQThreads, 0, s>>>(src, elems, amax);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_amax_to_global(float *g, int64_t n, cudaStream_t s) {
+  if (n <= 0) return cudaSuccess;
+  k_amax_to_global<<<(unsigned)((n + 255) / 256), 256, 0, s>>>(g, n);
+  return cudaGetLastError();
+}
+
+}  // namespace bqmoe

@@ -1,0 +1,122 @@
+// Routing: stable counting sort of the (token, slot) pairs by expert.
+//
+// The op receives topk_ids / topk_weights from the router (b12x project page,
+// section "Using it": fused_moe.bind(..., topk_weights=tw, topk_ids=ti)) and the
+// grouped expert kernels need each expert's pairs contiguous.  One CTA of 1024
+// threads: a shared-memory histogram, a warp scan of the padded counts, then
+// the pairs are scattered in chunks of 1024 in ascending pair order; inside a
+// chunk a pair's rank among equal ids comes from __match_any_sync (within the
+// warp) plus the per-warp counts of the earlier warps, so the result is stable
+// in p = t*K + k and bit-identical from run to run.  Only integer shared-memory
+// atomics are used.
+#include "common.cuh"
+#include "internal.h"
+
+namespace bqmoe {
+
+constexpr int kRouteThreads = 1024;
+constexpr int kRouteWarps = kRouteThreads / 32;
+constexpr int kMaxExperts = 512;
+
+__global__ void __launch_bounds__(kRouteThreads)
+k_route(const int32_t *__restrict__ ids, int P, int E, int pad, int32_t *__restrict__ counts,
+        int32_t *__restrict__ offsets, int32_t *__restrict__ sorted_pair, int32_t *__restrict__ pair_pos,
+        int32_t *__restrict__ status) {
+  extern __shared__ int32_t sm[];
+  int32_t *hist = sm;                 // [E]
+  int32_t *base = hist + E;           // [E+1]
+  int32_t *cursor = base + E + 1;     // [E]
+  int32_t *warp_hist = cursor + E;    // [kRouteWarps][E]
+  __shared__ int32_t dropped;
+
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  for (int e = tid; e < E; e += kRouteThreads) { hist[e] = 0; cursor[e] = 0; }
+  for (int i = tid; i < kRouteWarps * E; i += kRouteThreads) warp_hist[i] = 0;
+  if (tid == 0) dropped = 0;
+  __syncthreads();
+
+  // 1. histogram
+  int my_drop = 0;
+  for (int p = tid; p < P; p += kRouteThreads) {
+    const int id = ids[p];
+    if (id >= 0 && id < E) atomicAdd(&hist[id], 1);
+    else ++my_drop;
+  }
+  if (my_drop) atomicAdd(&dropped, my_drop);
+  __syncthreads();
+
+  // 2. exclusive scan of the padded counts (warp 0)
+  if (warp == 0) {
+    int carry = 0;
+    for (int e0 = 0; e0 < E; e0 += 32) {
+      const int e = e0 + lane;
+      const int c = e < E ? hist[e] : 0;
+      const int v = (c + pad - 1) / pad * pad;
+      int incl = v;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int n = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += n;
+      }
+      if (e < E) base[e] = carry + incl - v;
+      carry += __shfl_sync(0xffffffffu, incl, 31);
+    }
+    if (lane == 0) base[E] = carry;
+  }
+  __syncthreads();
+  for (int e = tid; e <= E; e += kRouteThreads) offsets[e] = base[e];
+  for (int e = tid; e < E; e += kRouteThreads) counts[e] = hist[e];
+  // padding slots of every group
+  for (int e = warp; e < E; e += kRouteWarps)
+    for (int j = base[e] + hist[e] + lane; j < base[e + 1]; j += 32) sorted_pair[j] = -1;
+
+  // 3. stable scatter, 1024 pairs at a time
+  const unsigned lt_mask = (1u << lane) - 1u;
+  for (int c0 = 0; c0 < P; c0 += kRouteThreads) {
+    const int p = c0 + tid;
+    const int id = p < P ? ids[p] : -1;
+    const bool valid = id >= 0 && id < E;
+    const int key = valid ? id : E;  // E: sentinel bucket for dropped / past-the-end pairs
+    const unsigned same = __match_any_sync(0xffffffffu, key);
+    const int rank = __popc(same & lt_mask);
+    if (valid && rank == 0) warp_hist[warp * E + id] = __popc(same);
+    __syncthreads();
+    if (valid) {
+      int pre = 0;
+      for (int w = 0; w < warp; ++w) pre += warp_hist[w * E + id];
+      const int pos = base[id] + cursor[id] + pre + rank;
+      sorted_pair[pos] = p;
+      pair_pos[p] = pos;
+    } else if (p < P) {
+      pair_pos[p] = -1;
+    }
+    __syncthreads();
+    for (int e = tid; e < E; e += kRouteThreads) {
+      int n = 0;
+      for (int w = 0; w < kRouteWarps; ++w) {
+        n += warp_hist[w * E + e];
+        warp_hist[w * E + e] = 0;
+      }
+      cursor[e] += n;
+    }
+    __syncthreads();
+  }
+
+  if (tid == 0 && dropped > 0) {
+    atomicOr(&status[ST_FLAGS], ST_FLAG_DROPPED);
+    atomicAdd(&status[ST_DROPPED], dropped);
+  }
+}
+
+cudaError_t launch_route(const int32_t *ids, int P, int E, int pad, int32_t *counts, int32_t *offsets,
+                         int32_t *sorted_pair, int32_t *pair_pos, int32_t *status, cudaStream_t s) {
+  if (E > kMaxExperts) return cudaErrorInvalidValue;
+  const size_t smem = sizeof(int32_t) * ((size_t)3 * E + 1 + (size_t)kRouteWarps * E);
+  // Per-device function attribute; cheap and idempotent, so set on every launch.
+  cudaError_t err = cudaFuncSetAttribute(k_route, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (err != cudaSuccess) return err;
+  k_route<<<1, kRouteThreads, smem, s>>>(ids, P, E, pad, counts, offsets, sorted_pair, pair_pos, status);
+  return cudaGetLastError();
+}
+
+}  // namespace bqmoe

@@ -1,0 +1,413 @@
+// C ABI of libmoe: host-side planning, binding and the run sequence.
+// The contract (plan -> scratch -> bind -> run; plan may allocate host state,
+// bind only records pointers, run only launches) follows the b12x project page,
+// section "Using it"; fixed workspace capacity and live counts kept out of the
+// plan follow "b12x has moved to FlashInfer", section "Technical layout and
+// contracts".
+#include <algorithm>
+#include <new>
+
+#include "common.cuh"
+#include "internal.h"
+#include "moe.h"
+
+using namespace bqmoe;
+
+struct moe_weight_plan_s {
+  WeightLayout L;
+};
+
+struct moe_plan_s {
+  WeightLayout L;
+  int K = 0, max_tokens = 0, afmt = 0, pad = 16;
+  ScratchLayout S;
+};
+
+struct moe_binding_s {
+  moe_plan_s P;
+  uint8_t *scratch = nullptr;
+  const uint8_t *packed = nullptr;
+  const void *x = nullptr;
+  const int32_t *ids = nullptr;
+  const float *w = nullptr;
+  int T = 0;
+  void *out = nullptr;
+};
+
+namespace {
+
+constexpr int kMaxExperts = 512;
+constexpr int kMaxTopK = 16;
+constexpr int kPad = 16;  // expert groups are padded to this many pairs
+
+bool aligned(const void *p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
+
+moe_status cuda_status(cudaError_t e) { return e == cudaSuccess ? MOE_OK : MOE_ERR_CUDA; }
+
+template <typename T>
+T *at(uint8_t *base, size_t off) {
+  return reinterpret_cast<T *>(base + off);
+}
+
+}  // namespace
+
+extern "C" {
+
+const char *moe_status_str(moe_status s) {
+  switch (s) {
+    case MOE_OK: return "MOE_OK";
+    case MOE_ERR_INVALID_ARG: return "MOE_ERR_INVALID_ARG";
+    case MOE_ERR_UNSUPPORTED: return "MOE_ERR_UNSUPPORTED";
+    case MOE_ERR_CAPACITY: return "MOE_ERR_CAPACITY";
+    case MOE_ERR_SCRATCH_TOO_SMALL: return "MOE_ERR_SCRATCH_TOO_SMALL";
+    case MOE_ERR_CUDA: return "MOE_ERR_CUDA";
+    case MOE_ERR_TIMEOUT: return "MOE_ERR_TIMEOUT";
+  }
+  return "MOE_ERR_UNKNOWN";
+}
+
+moe_status moe_plan_weights(const moe_weight_desc *d, moe_weight_plan *out, size_t *packed_bytes) {
+  if (!d || !out || !packed_bytes) return MOE_ERR_INVALID_ARG;
+  *out = nullptr;
+  if (d->num_experts < 1 || d->hidden <= 0 || d->intermediate <= 0) return MOE_ERR_INVALID_ARG;
+  if (d->wfmt != MOE_W_NVFP4 && d->wfmt != MOE_W_MXFP4) return MOE_ERR_INVALID_ARG;
+  if (d->act != MOE_ACT_SILU_GATED && d->act != MOE_ACT_RELU2) return MOE_ERR_INVALID_ARG;
+  if (d->num_experts > kMaxExperts || d->hidden % 128 || d->intermediate % 64) return MOE_ERR_UNSUPPORTED;
+  WeightLayout L;
+  L.E = d->num_experts;
+  L.H = d->hidden;
+  L.I = d->intermediate;
+  L.wfmt = d->wfmt;
+  L.act = d->act;
+  L.bs = d->wfmt == MOE_W_NVFP4 ? 16 : 32;
+  L.n13 = d->act == MOE_ACT_SILU_GATED ? 2 * L.I : L.I;
+  L.off_c13 = 0;
+  L.off_s13 = align_up(L.off_c13 + (size_t)L.E * L.c13_expert());
+  L.off_c2 = align_up(L.off_s13 + (size_t)L.E * L.s13_expert());
+  L.off_s2 = align_up(L.off_c2 + (size_t)L.E * L.c2_expert());
+  L.off_g = align_up(L.off_s2 + (size_t)L.E * L.s2_expert());
+  L.total = align_up(L.off_g + (size_t)L.E * 4 * sizeof(float));
+  moe_weight_plan p = new (std::nothrow) moe_weight_plan_s{L};
+  if (!p) return MOE_ERR_CAPACITY;
+  *out = p;
+  *packed_bytes = L.total;
+  return MOE_OK;
+}
+
+moe_status moe_prepare_weights(moe_weight_plan wp, const void *w13_codes, const void *w13_scales,
+                               const float *w13_global, const void *w2_codes, const void *w2_scales,
+                               const float *w2_global, void *packed, cudaStream_t stream) {
+  if (!wp || !w13_codes || !w13_scales || !w2_codes || !w2_scales || !packed) return MOE_ERR_INVALID_ARG;
+  const WeightLayout &L = wp->L;
+  const bool nv = L.wfmt == MOE_W_NVFP4;
+  if (nv != (w13_global != nullptr) || nv != (w2_global != nullptr)) return MOE_ERR_INVALID_ARG;
+  for (const void *p : {w13_codes, w13_scales, w2_codes, w2_scales, (const void *)packed})
+    if (!aligned(p, 16)) return MOE_ERR_INVALID_ARG;
+  if (nv && (!aligned(w13_global, 4) || !aligned(w2_global, 4))) return MOE_ERR_INVALID_ARG;
+  return cuda_status(launch_pack(L, w13_codes, w13_scales, w13_global, w2_codes, w2_scales, w2_global,
+                                 static_cast<uint8_t *>(packed), stream));
+}
+
+moe_status moe_is_supported(const moe_caps *c) {
+  if (!c || !c->wplan) return MOE_ERR_INVALID_ARG;
+  if (c->top_k < 1 || c->max_tokens < 1) return MOE_ERR_INVALID_ARG;
+  if (c->afmt != MOE_A_BF16 && c->afmt != MOE_A_NVFP4 && c->afmt != MOE_A_MXFP8) return MOE_ERR_INVALID_ARG;
+  if (c->top_k > kMaxTopK) return MOE_ERR_UNSUPPORTED;
+  if ((int64_t)c->max_tokens * c->top_k > (int64_t)1 << 30) return MOE_ERR_UNSUPPORTED;
+  // Supported pairs (vLLM docs "b12x Linear and MoE Backends", "Supported
+  // Configurations"): NVFP4 weights with BF16, NVFP4 or MXFP8 activations;
+  // MXFP4 weights with BF16 or MXFP8 activations.
+  if (c->wplan->L.wfmt == MOE_W_MXFP4 && c->afmt == MOE_A_NVFP4) return MOE_ERR_UNSUPPORTED;
+  return MOE_OK;
+}
+
+moe_status moe_plan(const moe_caps *c, moe_plan_t *out, size_t *scratch_bytes, int32_t *m_tile) {
+  if (!out || !scratch_bytes) return MOE_ERR_INVALID_ARG;
+  *out = nullptr;
+  moe_status st = moe_is_supported(c);
+  if (st != MOE_OK) return st;
+  moe_plan_s P;
+  P.L = c->wplan->L;
+  P.K = c->top_k;
+  P.max_tokens = c->max_tokens;
+  P.afmt = c->afmt;
+  P.pad = kPad;
+  const WeightLayout &L = P.L;
+  const int64_t Pmax = (int64_t)c->max_tokens * c->top_k;
+  const int64_t T = c->max_tokens;
+  ScratchLayout &S = P.S;
+  S.cap_sorted = round_up(Pmax + (int64_t)L.E * (P.pad - 1), P.pad);
+  size_t o = 0;
+  auto take = [&](size_t bytes) {
+    const size_t at = o;
+    o = align_up(o + bytes);
+    return at;
+  };
+  S.status = take(16);
+  S.counts = take(4 * (size_t)L.E);
+  S.offsets = take(4 * (size_t)(L.E + 1));
+  S.sorted = take(4 * (size_t)S.cap_sorted);
+  S.pair_pos = take(4 * (size_t)Pmax);
+  if (P.afmt == MOE_A_NVFP4) {
+    S.xq_codes = take((size_t)T * L.H / 2);
+    S.xq_scales = take((size_t)T * L.H / 16);
+    S.xq_g = take(4 * (size_t)T);
+  } else if (P.afmt == MOE_A_MXFP8) {
+    S.xq_codes = take((size_t)T * L.H);
+    S.xq_scales = take((size_t)T * L.H / 32);
+  }
+  S.h = take(4 * (size_t)S.cap_sorted * L.I);
+  if (P.afmt == MOE_A_NVFP4) {
+    S.hq_codes = take((size_t)S.cap_sorted * L.I / 2);
+    S.hq_scales = take((size_t)S.cap_sorted * L.I / 16);
+    S.hq_g = take(4 * (size_t)S.cap_sorted);
+  } else if (P.afmt == MOE_A_MXFP8) {
+    S.hq_codes = take((size_t)S.cap_sorted * L.I);
+    S.hq_scales = take((size_t)S.cap_sorted * L.I / 32);
+  }
+  S.part = take(4 * (size_t)S.cap_sorted * L.H);
+  S.total = o;
+  moe_plan_t p = new (std::nothrow) moe_plan_s(P);
+  if (!p) return MOE_ERR_CAPACITY;
+  *out = p;
+  *scratch_bytes = S.total;
+  if (m_tile) *m_tile = P.pad;
+  return MOE_OK;
+}
+
+moe_status moe_bind(moe_plan_t plan, void *scratch, size_t scratch_bytes, const void *packed, const void *x,
+                    const int32_t *topk_ids, const float *topk_weights, int32_t num_tokens, void *out,
+                    moe_binding *out_binding) {
+  if (!out_binding) return MOE_ERR_INVALID_ARG;
+  *out_binding = nullptr;
+  if (!plan || num_tokens < 0) return MOE_ERR_INVALID_ARG;
+  if (num_tokens > plan->max_tokens) return MOE_ERR_CAPACITY;
+  if (!scratch || !aligned(scratch, 256)) return MOE_ERR_INVALID_ARG;
+  if (scratch_bytes < plan->S.total) return MOE_ERR_SCRATCH_TOO_SMALL;
+  if (num_tokens > 0) {
+    if (!packed || !x || !topk_ids || !topk_weights || !out) return MOE_ERR_INVALID_ARG;
+    if (!aligned(packed, 256) || !aligned(x, 16) || !aligned(out, 16) || !aligned(topk_ids, 4) ||
+        !aligned(topk_weights, 4))
+      return MOE_ERR_INVALID_ARG;
+  }
+  moe_binding b = new (std::nothrow) moe_binding_s;
+  if (!b) return MOE_ERR_CAPACITY;
+  b->P = *plan;
+  b->scratch = static_cast<uint8_t *>(scratch);
+  b->packed = static_cast<const uint8_t *>(packed);
+  b->x = x;
+  b->ids = topk_ids;
+  b->w = topk_weights;
+  b->T = num_tokens;
+  b->out = out;
+  *out_binding = b;
+  return MOE_OK;
+}
+
+static moe_status run_impl(moe_binding b, cudaStream_t stream, cudaEvent_t *ev) {
+  auto mark = [&](int i) { return ev ? cudaEventRecord(ev[i], stream) : cudaSuccess; };
+  if (b->T == 0) {
+    for (int i = 0; ev && i <= MOE_NUM_STAGES; ++i)
+      if (mark(i) != cudaSuccess) return MOE_ERR_CUDA;
+    return MOE_OK;
+  }
+  const moe_plan_s &P = b->P;
+  const WeightLayout &L = P.L;
+  const ScratchLayout &S = P.S;
+  uint8_t *sc = b->scratch;
+  const int T = b->T, K = P.K, E = L.E, H = L.H, I = L.I;
+  int32_t *status = at<int32_t>(sc, S.status);
+  int32_t *counts = at<int32_t>(sc, S.counts);
+  int32_t *offsets = at<int32_t>(sc, S.offsets);
+  int32_t *sorted = at<int32_t>(sc, S.sorted);
+  int32_t *pair_pos = at<int32_t>(sc, S.pair_pos);
+  float *h = at<float>(sc, S.h);
+  float *part = at<float>(sc, S.part);
+  cudaError_t err;
+
+  if ((err = mark(MOE_STAGE_ROUTE)) != cudaSuccess) return MOE_ERR_CUDA;
+  if ((err = cudaMemsetAsync(status, 0, 16, stream)) != cudaSuccess) return MOE_ERR_CUDA;
+  if ((err = launch_route(b->ids, T * K, E, P.pad, counts, offsets, sorted, pair_pos, status, stream)) != cudaSuccess)
+    return MOE_ERR_CUDA;
+
+  GroupedArgs a{};
+  a.counts = counts;
+  a.offsets = offsets;
+  a.sorted_pair = sorted;
+  a.top_k = K;
+  a.topk_weights = b->w;
+  a.globals = reinterpret_cast<const float *>(b->packed + L.off_g);
+  a.I = I;
+
+  // activation quantiser (x) for NVFP4 / MXFP8 activations
+  if ((err = mark(MOE_STAGE_QUANT_X)) != cudaSuccess) return MOE_ERR_CUDA;
+  int src1 = SRC_X_BF16;
+  a.act = b->x;
+  if (P.afmt == MOE_A_NVFP4) {
+    err = launch_quant_rows_nvfp4(b->x, true, T, H, at<uint8_t>(sc, S.xq_codes), at<uint8_t>(sc, S.xq_scales),
+                                  at<float>(sc, S.xq_g), nullptr, stream);
+    src1 = SRC_X_NVFP4;
+    a.act = at<uint8_t>(sc, S.xq_codes);
+    a.act_scales = at<uint8_t>(sc, S.xq_scales);
+    a.act_g = at<float>(sc, S.xq_g);
+  } else if (P.afmt == MOE_A_MXFP8) {
+    err = launch_quant_blocks(Q_MXFP8, b->x, true, T, H, 1, nullptr, at<uint8_t>(sc, S.xq_codes),
+                              at<uint8_t>(sc, S.xq_scales), nullptr, stream);
+    src1 = SRC_X_MXFP8;
+    a.act = at<uint8_t>(sc, S.xq_codes);
+    a.act_scales = at<uint8_t>(sc, S.xq_scales);
+  }
+  if (err != cudaSuccess) return MOE_ERR_CUDA;
+
+  // GEMM1 + activation -> h
+  if (mark(MOE_STAGE_GEMM1) != cudaSuccess) return MOE_ERR_CUDA;
+  a.codes = b->packed + L.off_c13;
+  a.scales = b->packed + L.off_s13;
+  a.codes_expert = L.c13_expert();
+  a.scales_expert = L.s13_expert();
+  a.K = H;
+  a.n_rows = I;
+  a.out = h;
+  const int stage1 = L.act == MOE_ACT_SILU_GATED ? STAGE_GATED : STAGE_RELU2;
+  if ((err = launch_grouped_cc(L.wfmt, src1, stage1, a, E, stream)) != cudaSuccess) return MOE_ERR_CUDA;
+
+  // re-quantise h for NVFP4 / MXFP8 activations (rows past offsets[E] are skipped)
+  if ((err = mark(MOE_STAGE_QUANT_H)) != cudaSuccess) return MOE_ERR_CUDA;
+  int src2 = SRC_H_F32;
+  a.act = h;
+  a.act_scales = nullptr;
+  a.act_g = nullptr;
+  if (P.afmt == MOE_A_NVFP4) {
+    err = launch_quant_rows_nvfp4(h, false, S.cap_sorted, I, at<uint8_t>(sc, S.hq_codes),
+                                  at<uint8_t>(sc, S.hq_scales), at<float>(sc, S.hq_g), offsets + E, stream);
+    src2 = SRC_H_NVFP4;
+    a.act = at<uint8_t>(sc, S.hq_codes);
+    a.act_scales = at<uint8_t>(sc, S.hq_scales);
+    a.act_g = at<float>(sc, S.hq_g);
+  } else if (P.afmt == MOE_A_MXFP8) {
+    err = launch_quant_blocks(Q_MXFP8, h, false, S.cap_sorted, I, 1, nullptr, at<uint8_t>(sc, S.hq_codes),
+                              at<uint8_t>(sc, S.hq_scales), offsets + E, stream);
+    src2 = SRC_H_MXFP8;
+    a.act = at<uint8_t>(sc, S.hq_codes);
+    a.act_scales = at<uint8_t>(sc, S.hq_scales);
+  }
+  if (err != cudaSuccess) return MOE_ERR_CUDA;
+
+  // GEMM2 * topk_weight -> partials, then the ordered combine
+  a.codes = b->packed + L.off_c2;
+  a.scales = b->packed + L.off_s2;
+  a.codes_expert = L.c2_expert();
+  a.scales_expert = L.s2_expert();
+  a.K = I;
+  a.n_rows = H;
+  a.out = part;
+  if (mark(MOE_STAGE_GEMM2) != cudaSuccess) return MOE_ERR_CUDA;
+  if ((err = launch_grouped_cc(L.wfmt, src2, STAGE_DOWN, a, E, stream)) != cudaSuccess) return MOE_ERR_CUDA;
+  if (mark(MOE_STAGE_COMBINE) != cudaSuccess) return MOE_ERR_CUDA;
+  if ((err = launch_combine(part, H, pair_pos, T, K, b->out, stream)) != cudaSuccess) return MOE_ERR_CUDA;
+  if (mark(MOE_NUM_STAGES) != cudaSuccess) return MOE_ERR_CUDA;
+  return MOE_OK;
+}
+
+moe_status moe_run(moe_binding b, cudaStream_t stream) {
+  if (!b) return MOE_ERR_INVALID_ARG;
+  return run_impl(b, stream, nullptr);
+}
+
+moe_status moe_run_timed(moe_binding b, cudaStream_t stream, cudaEvent_t *events) {
+  if (!b || !events) return MOE_ERR_INVALID_ARG;
+  for (int i = 0; i <= MOE_NUM_STAGES; ++i)
+    if (!events[i]) return MOE_ERR_INVALID_ARG;
+  return run_impl(b, stream, events);
+}
+
+moe_status moe_run_host(moe_binding b, const void *x_host, const int32_t *ids_host, const float *weights_host,
+                        void *out_host, cudaStream_t stream) {
+  if (!b) return MOE_ERR_INVALID_ARG;
+  if (b->T == 0) return MOE_OK;
+  if (!x_host || !ids_host || !weights_host || !out_host) return MOE_ERR_INVALID_ARG;
+  const size_t T = b->T, H = b->P.L.H, K = b->P.K;
+  if (cudaMemcpyAsync(const_cast<void *>(b->x), x_host, T * H * 2, cudaMemcpyHostToDevice, stream) != cudaSuccess ||
+      cudaMemcpyAsync(const_cast<int32_t *>(b->ids), ids_host, T * K * 4, cudaMemcpyHostToDevice, stream) !=
+          cudaSuccess ||
+      cudaMemcpyAsync(const_cast<float *>(b->w), weights_host, T * K * 4, cudaMemcpyHostToDevice, stream) !=
+          cudaSuccess)
+    return MOE_ERR_CUDA;
+  moe_status st = moe_run(b, stream);
+  if (st != MOE_OK) return st;
+  if (cudaMemcpyAsync(out_host, b->out, T * H * 2, cudaMemcpyDeviceToHost, stream) != cudaSuccess)
+    return MOE_ERR_CUDA;
+  return cuda_status(cudaStreamSynchronize(stream));
+}
+
+moe_status moe_device_status(moe_binding b, cudaStream_t stream, int32_t *status) {
+  if (!b || !status) return MOE_ERR_INVALID_ARG;
+  int32_t st[4] = {0, 0, 0, 0};
+  if (b->T > 0) {
+    if (cudaMemcpyAsync(st, b->scratch + b->P.S.status, 16, cudaMemcpyDeviceToHost, stream) != cudaSuccess)
+      return MOE_ERR_CUDA;
+    if (cudaStreamSynchronize(stream) != cudaSuccess) return MOE_ERR_CUDA;
+  }
+  for (int i = 0; i < 4; ++i) status[i] = st[i];
+  return (st[ST_FLAGS] & ST_FLAG_TIMEOUT) ? MOE_ERR_TIMEOUT : MOE_OK;
+}
+
+moe_status moe_debug_routing(moe_binding b, cudaStream_t stream, int32_t *counts, int32_t *offsets,
+                             int32_t *pair_pos, int32_t *sorted_pair, int32_t sorted_cap) {
+  if (!b || !counts || !offsets || !pair_pos || !sorted_pair || sorted_cap < 0) return MOE_ERR_INVALID_ARG;
+  const int E = b->P.L.E;
+  const size_t P = (size_t)b->T * b->P.K;
+  uint8_t *sc = b->scratch;
+  const ScratchLayout &S = b->P.S;
+  if (b->T == 0) return MOE_OK;
+  if (cudaMemcpyAsync(counts, sc + S.counts, 4 * (size_t)E, cudaMemcpyDeviceToHost, stream) != cudaSuccess ||
+      cudaMemcpyAsync(offsets, sc + S.offsets, 4 * (size_t)(E + 1), cudaMemcpyDeviceToHost, stream) != cudaSuccess ||
+      cudaMemcpyAsync(pair_pos, sc + S.pair_pos, 4 * P, cudaMemcpyDeviceToHost, stream) != cudaSuccess ||
+      cudaStreamSynchronize(stream) != cudaSuccess)
+    return MOE_ERR_CUDA;
+  const int32_t n = offsets[E];
+  if (n < 0 || n > S.cap_sorted) return MOE_ERR_CUDA;
+  if (sorted_cap < n) return MOE_ERR_CAPACITY;
+  if (n > 0 && (cudaMemcpyAsync(sorted_pair, sc + S.sorted, 4 * (size_t)n, cudaMemcpyDeviceToHost, stream) !=
+                    cudaSuccess ||
+                cudaStreamSynchronize(stream) != cudaSuccess))
+    return MOE_ERR_CUDA;
+  return MOE_OK;
+}
+
+moe_status moe_quantize(int32_t qfmt, int32_t gmode, int32_t src_bf16, const void *src, int64_t batch, int64_t rows,
+                        int64_t cols, void *codes, void *scales, float *global, cudaStream_t stream) {
+  if (qfmt != MOE_Q_NVFP4 && qfmt != MOE_Q_MXFP4 && qfmt != MOE_Q_MXFP8) return MOE_ERR_INVALID_ARG;
+  if (batch < 0 || rows < 0 || cols <= 0) return MOE_ERR_INVALID_ARG;
+  if (batch == 0 || rows == 0) return MOE_OK;
+  if (!src || !codes || !scales) return MOE_ERR_INVALID_ARG;
+  if (!aligned(src, 16) || !aligned(codes, 16) || !aligned(scales, 4)) return MOE_ERR_INVALID_ARG;
+  const bool bf = src_bf16 != 0;
+  cudaError_t err;
+  if (qfmt == MOE_Q_NVFP4) {
+    if (cols % 16 || !global || !aligned(global, 4)) return MOE_ERR_INVALID_ARG;
+    if (gmode == MOE_G_PER_ROW) {
+      err = launch_quant_rows_nvfp4(src, bf, batch * rows, cols, static_cast<uint8_t *>(codes),
+                                    static_cast<uint8_t *>(scales), global, nullptr, stream);
+    } else if (gmode == MOE_G_PER_TENSOR) {
+      err = launch_amax_tensor(src, bf, batch, rows * cols, global, stream);
+      if (err == cudaSuccess) err = launch_amax_to_global(global, batch, stream);
+      if (err == cudaSuccess)
+        err = launch_quant_blocks(Q_NVFP4, src, bf, batch * rows, cols, rows, global, static_cast<uint8_t *>(codes),
+                                  static_cast<uint8_t *>(scales), nullptr, stream);
+    } else {
+      return MOE_ERR_INVALID_ARG;
+    }
+  } else {
+    if (cols % 32 || gmode != MOE_G_NONE || global) return MOE_ERR_INVALID_ARG;
+    err = launch_quant_blocks(qfmt == MOE_Q_MXFP4 ? Q_MXFP4 : Q_MXFP8, src, bf, batch * rows, cols, 1, nullptr,
+                              static_cast<uint8_t *>(codes), static_cast<uint8_t *>(scales), nullptr, stream);
+  }
+  return cuda_status(err);
+}
+
+void moe_destroy_weight_plan(moe_weight_plan p) { delete p; }
+void moe_destroy_plan(moe_plan_t p) { delete p; }
+void moe_destroy_binding(moe_binding b) { delete b; }
+
+}  // extern "C"

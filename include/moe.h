@@ -1,0 +1,253 @@
+/*
+ * moe.h -- C ABI of the GB300 (sm_103a) block-quantised fused MoE library.
+ *
+ * The operation is the fused routed-expert FFN over FP4 block-quantised expert
+ * weights ("moe.fused_moe: fused FP4 MoE across a micro-kernel decode path, a
+ * unified dynamic path ..., and W4A16 (BF16 activations, inline FP4 weight
+ * dequant)", b12x project page (shadowgraph.io), section "What's in here"):
+ *
+ *     y_t = sum_k  w_tk * W2_e( act( W13_e x^_t ) ),   e = topk_ids[t, k]
+ *
+ * with act = SiLU(gate) * up (gated) or max(., 0)^2 (non-gated ReLU^2; vLLM
+ * docs "b12x Linear and MoE Backends", section "ModelOpt block codecs": routed
+ * experts use bias-free SiLU or non-gated ReLU^2).  Supported formats follow
+ * the same docs, section "Supported Configurations": NVFP4 weights with BF16,
+ * NVFP4 or MXFP8 activations; MXFP4 weights with BF16 or MXFP8 activations.
+ *
+ * The calls mirror the pages' plan -> scratch -> bind -> run contract (b12x
+ * project page, section "Using it"):
+ *
+ *   moe_plan_weights    host only; decides the packed layout of the experts.
+ *   moe_prepare_weights one-time repack of the checkpoint tensors into that
+ *                       layout on the GPU ("weights prepped once per model").
+ *   moe_plan            host only; fixes every launch decision for a capacity
+ *                       (max_tokens) and reports the scratch size.  Live token
+ *                       counts are not part of a plan (b12x has moved to
+ *                       FlashInfer, section "Technical layout and contracts":
+ *                       keep live request counts out of compile keys, fixed
+ *                       workspace capacity).
+ *   moe_bind            host only; records pointers ("bind only narrows/views,
+ *                       never allocates").
+ *   moe_run             launches the kernels on the caller's stream; it never
+ *                       allocates, synchronises or compiles, so it can be
+ *                       captured in a CUDA graph ("run* executes and is
+ *                       CUDA-graph-capture safe").
+ *
+ * Ownership.  The caller owns all device memory: source weights, the packed
+ * buffer, scratch, activations, ids, weights and the output.  The library owns
+ * only the host-side plan and binding objects and allocates no device memory.
+ *
+ * Errors.  Every call returns a moe_status and never throws or aborts.  Argument
+ * errors are found on the host before anything is launched.  Conditions found
+ * on the device (out-of-range expert ids, which are dropped) are recorded in a
+ * status word inside scratch and read back with moe_device_status.
+ *
+ * Shapes.  hidden must be a multiple of 128 and intermediate a multiple of 64.
+ * All device pointers must be 16-byte aligned.
+ */
+#ifndef BQMOE_MOE_H
+#define BQMOE_MOE_H
+
+#include <stddef.h>
+#include <stdint.h>
+#include <cuda_runtime_api.h>
+
+#if defined(__GNUC__)
+#define MOE_API __attribute__((visibility("default")))
+#else
+#define MOE_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum moe_status {
+  MOE_OK = 0,
+  MOE_ERR_INVALID_ARG = 1,       /* null pointer, bad size, misaligned pointer   */
+  MOE_ERR_UNSUPPORTED = 2,       /* shape / format combination not implemented  */
+  MOE_ERR_CAPACITY = 3,          /* num_tokens > max_tokens, or host buffer short */
+  MOE_ERR_SCRATCH_TOO_SMALL = 4, /* scratch_bytes below what moe_plan reported   */
+  MOE_ERR_CUDA = 5,              /* a CUDA runtime call or launch failed         */
+  MOE_ERR_TIMEOUT = 6            /* a bounded device-side wait gave up           */
+} moe_status;
+
+/* Expert weight formats.
+ * NVFP4: E2M1 codes, one E4M3 scale per 16 elements along K, one FP32 global
+ *        scale per expert and per matrix (gate, up, down).
+ * MXFP4: E2M1 codes, one E8M0 scale per 32 elements along K, no global. */
+enum { MOE_W_NVFP4 = 1, MOE_W_MXFP4 = 2 };
+
+/* Activation formats (what GEMM1 and GEMM2 consume).
+ * BF16 : x as given, h kept in floating point ("W4A16").
+ * NVFP4: x and h re-quantised per token row: E2M1 + E4M3 / 16 + FP32 global per row.
+ * MXFP8: x and h re-quantised: E4M3 elements + E8M0 scale per 32. */
+enum { MOE_A_BF16 = 1, MOE_A_NVFP4 = 2, MOE_A_MXFP8 = 3 };
+
+/* Expert activation. */
+enum { MOE_ACT_SILU_GATED = 1, MOE_ACT_RELU2 = 2 };
+
+typedef struct moe_weight_desc {
+  int32_t num_experts;   /* E, 1..512                         */
+  int32_t hidden;        /* H, multiple of 128                */
+  int32_t intermediate;  /* I, multiple of 64                 */
+  int32_t wfmt;          /* MOE_W_*                           */
+  int32_t act;           /* MOE_ACT_*                         */
+} moe_weight_desc;
+
+typedef struct moe_weight_plan_s *moe_weight_plan;
+typedef struct moe_plan_s *moe_plan_t;
+typedef struct moe_binding_s *moe_binding;
+
+typedef struct moe_caps {
+  moe_weight_plan wplan; /* from moe_plan_weights                             */
+  int32_t top_k;         /* K, 1..16                                          */
+  int32_t max_tokens;    /* capacity T_max >= 1; scratch is sized for it      */
+  int32_t afmt;          /* MOE_A_*                                           */
+} moe_caps;
+
+/* Human-readable name of a status code (static storage, never NULL). */
+MOE_API const char *moe_status_str(moe_status s);
+
+/* ----------------------------------------------------------- weights ---- */
+
+/* Validate a weight description and report the size of the packed buffer
+ * (b12x project page, "Using it": fused_moe.plan_weights(quant_modes=...,
+ * source_format="modelopt_nvfp4")).  Host only.  *out is owned by the caller
+ * and released with moe_destroy_weight_plan. */
+MOE_API moe_status moe_plan_weights(const moe_weight_desc *desc, moe_weight_plan *out,
+                            size_t *packed_bytes);
+
+/* Repack checkpoint tensors into `packed` (b12x project page, "Using it":
+ * fused_moe.prepare_weights, weights prepped once per model).  All pointers
+ * are device pointers, read-only except `packed`.  Source layout (the
+ * modelopt_nvfp4 reading: row-major, K contiguous, two E2M1 codes per byte,
+ * element 2j in the low nibble):
+ *   w13_codes  uint8 [E, N13, H/2]   N13 = 2I (gate rows [0,I) then up rows [I,2I)) or I (ReLU^2)
+ *   w13_scales uint8 [E, N13, H/bs]  bs = 16 (E4M3, NVFP4) or 32 (E8M0, MXFP4)
+ *   w13_global float [E, N13/I]      NVFP4 only (gate, up) or (w1); NULL for MXFP4
+ *   w2_codes   uint8 [E, H, I/2]
+ *   w2_scales  uint8 [E, H, I/bs]
+ *   w2_global  float [E]             NVFP4 only; NULL for MXFP4
+ *   packed     device buffer of packed_bytes (from moe_plan_weights)
+ * Asynchronous on `stream`; the sources may be freed once the stream has
+ * passed this call. */
+MOE_API moe_status moe_prepare_weights(moe_weight_plan wplan, const void *w13_codes,
+                               const void *w13_scales, const float *w13_global,
+                               const void *w2_codes, const void *w2_scales,
+                               const float *w2_global, void *packed,
+                               cudaStream_t stream);
+
+/* ------------------------------------------------------- plan / bind ---- */
+
+/* MOE_OK if the library has kernels for these caps, else MOE_ERR_UNSUPPORTED
+ * or MOE_ERR_INVALID_ARG (b12x project page, "Using it": every op exports
+ * is_supported()).  Host only. */
+MOE_API moe_status moe_is_supported(const moe_caps *caps);
+
+/* Fix every launch decision for `caps` and report the scratch size and the
+ * tile (m_tile) that expert groups are padded to (b12x project page, "Using
+ * it": plan is host-side; plan.scratch_specs()).  Host only; the weight plan
+ * may be destroyed afterwards (the plan keeps a copy). */
+MOE_API moe_status moe_plan(const moe_caps *caps, moe_plan_t *out, size_t *scratch_bytes,
+                    int32_t *m_tile);
+
+/* Record the pointers of one forward (b12x project page, "Using it":
+ * fused_moe.bind(plan, scratch=..., a=x, experts=..., topk_weights=tw,
+ * topk_ids=ti)).  Host only; nothing is read or written on the device.
+ *   scratch       device, >= scratch_bytes from moe_plan, 256-byte aligned
+ *   packed        device, the buffer written by moe_prepare_weights
+ *   x             device, BF16 [num_tokens, H]
+ *   topk_ids      device, int32 [num_tokens, K]; ids outside [0, E) are dropped
+ *   topk_weights  device, float [num_tokens, K]
+ *   num_tokens    0..max_tokens (0 makes moe_run a no-op)
+ *   out           device, BF16 [num_tokens, H]
+ * The binding holds no reference to the plan; destroy it with
+ * moe_destroy_binding. */
+MOE_API moe_status moe_bind(moe_plan_t plan, void *scratch, size_t scratch_bytes,
+                    const void *packed, const void *x, const int32_t *topk_ids,
+                    const float *topk_weights, int32_t num_tokens, void *out,
+                    moe_binding *out_binding);
+
+/* ----------------------------------------------------------------- run -- */
+
+/* Run the bound forward on `stream` (b12x project page, "Using it":
+ * fused_moe.run(binding)): routing, activation quantiser (NVFP4/MXFP8),
+ * GEMM1 + activation, re-quantisation of h (NVFP4/MXFP8), GEMM2 scaled by
+ * topk_weights, and a deterministic per-token combine into `out`.
+ * Asynchronous; no allocation, no synchronisation; capturable. */
+MOE_API moe_status moe_run(moe_binding b, cudaStream_t stream);
+
+/* End-to-end variant for callers holding host buffers: copies x, topk_ids and
+ * topk_weights from host memory into the bound device buffers, runs, copies
+ * `out` back to host memory and synchronises `stream`.  Host buffers have the
+ * shapes given to moe_bind; pinned memory makes the copies asynchronous. */
+MOE_API moe_status moe_run_host(moe_binding b, const void *x_host, const int32_t *ids_host,
+                        const float *weights_host, void *out_host,
+                        cudaStream_t stream);
+
+/* Stages of moe_run, in launch order, for moe_run_timed. */
+enum { MOE_STAGE_ROUTE = 0, MOE_STAGE_QUANT_X = 1, MOE_STAGE_GEMM1 = 2, MOE_STAGE_QUANT_H = 3,
+       MOE_STAGE_GEMM2 = 4, MOE_STAGE_COMBINE = 5, MOE_NUM_STAGES = 6 };
+
+/* moe_run that also records caller-created CUDA events around every stage
+ * (the per-kernel timing of the pages' B12X_TIMING=1 switch, b12x project
+ * page, section "PCIe DMA wire modes", last paragraph): events[i] is recorded
+ * on `stream` just before stage i and events[MOE_NUM_STAGES] after the last
+ * stage, so cudaEventElapsedTime(events[i], events[i+1]) is the device time of
+ * stage i (zero for a stage the activation format skips).  `events` is a host
+ * array of MOE_NUM_STAGES+1 cudaEvent_t created with timing enabled.  Nothing
+ * is synchronised. */
+MOE_API moe_status moe_run_timed(moe_binding b, cudaStream_t stream, cudaEvent_t *events);
+
+/* Copy the device status word of the last run to host `status[4]` and
+ * synchronise `stream`:
+ *   status[0] flags: bit 0 = out-of-range ids were dropped, bit 1 = a bounded
+ *             device wait timed out;
+ *   status[1] number of dropped (token, slot) pairs;
+ *   status[2], status[3] reserved (0).
+ * Returns MOE_ERR_TIMEOUT if bit 1 is set, else MOE_OK. */
+MOE_API moe_status moe_device_status(moe_binding b, cudaStream_t stream, int32_t *status);
+
+/* Copy the routing stage's outputs of the last run to host memory and
+ * synchronise `stream` (for bit-exact checks of the expert sort):
+ *   counts [E], offsets [E+1] (each group padded to m_tile), pair_pos [T*K]
+ *   (-1 for dropped pairs), sorted_pair [offsets[E]] (pair p = t*K + k, -1 in
+ *   padding).  MOE_ERR_CAPACITY if sorted_cap < offsets[E]. */
+MOE_API moe_status moe_debug_routing(moe_binding b, cudaStream_t stream, int32_t *counts,
+                             int32_t *offsets, int32_t *pair_pos,
+                             int32_t *sorted_pair, int32_t sorted_cap);
+
+/* ------------------------------------------------------------ quantiser -- */
+
+enum { MOE_Q_NVFP4 = 1, MOE_Q_MXFP4 = 2, MOE_Q_MXFP8 = 3 };
+enum { MOE_G_NONE = 0, MOE_G_PER_TENSOR = 1, MOE_G_PER_ROW = 2 };
+
+/* Block-quantise `batch` row-major matrices [rows, cols] (the row quantizers
+ * quantization.nvfp4 / quantization.mxfp8, b12x project page, "What's in
+ * here"; also the checkpoint-style weight quantiser).  Device pointers:
+ *   src     float [batch, rows, cols] (src_bf16 = 0) or BF16 (src_bf16 = 1)
+ *   codes   NVFP4/MXFP4: uint8 [batch, rows, cols/2], element 2j in the low
+ *           nibble; MXFP8: uint8 [batch, rows, cols] (E4M3)
+ *   scales  uint8 [batch, rows, cols/bs]: E4M3 (NVFP4, bs 16) or E8M0 (MX, bs 32)
+ *   global  float: [batch] (MOE_G_PER_TENSOR) or [batch, rows] (MOE_G_PER_ROW);
+ *           NVFP4 only, NULL for MX formats (gmode must be MOE_G_NONE)
+ * NVFP4: g = amax/(6*448); s = E4M3_rne_sat((amax_b/6)/g); q = E2M1_rne_sat(x/(s*g)).
+ * MX:    X = floor(log2(amax_b)) - emax (2 for E2M1, 8 for E4M3), clamped to
+ *        [-127,127]; s = X+127; q = ELEM_rne_sat(x/2^X).
+ * cols must be a multiple of 16 (NVFP4) or 32 (MX).  batch or rows 0 is a no-op. */
+MOE_API moe_status moe_quantize(int32_t qfmt, int32_t gmode, int32_t src_bf16,
+                        const void *src, int64_t batch, int64_t rows, int64_t cols,
+                        void *codes, void *scales, float *global,
+                        cudaStream_t stream);
+
+/* ------------------------------------------------------------- destroy -- */
+
+MOE_API void moe_destroy_weight_plan(moe_weight_plan p);
+MOE_API void moe_destroy_plan(moe_plan_t p);
+MOE_API void moe_destroy_binding(moe_binding b);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* BQMOE_MOE_H */

@@ -87,9 +87,8 @@ def _nearest_even(mag: np.ndarray, grid: np.ndarray) -> np.ndarray:
     exactly float32, so the distance comparison is exact.
     """
     mag = np.asarray(mag, dtype=np.float64)
-    hi = np.searchsorted(grid, mag, side="left")
-    hi = np.clip(hi, 0, len(grid) - 1)
-    lo = np.clip(hi - 1, 0, len(grid) - 1)
+    hi = np.minimum(np.searchsorted(grid, mag, side="left"), len(grid) - 1)  # in [0, n-1]
+    lo = np.maximum(hi - 1, 0)
     d_lo = mag - grid[lo]
     d_hi = grid[hi] - mag
     pick_hi = (d_hi < d_lo) | ((d_hi == d_lo) & (hi % 2 == 0))
