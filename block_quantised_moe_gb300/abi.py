@@ -32,6 +32,7 @@ MOE_Q_NVFP4, MOE_Q_MXFP4, MOE_Q_MXFP8 = 1, 2, 3
 MOE_G_NONE, MOE_G_PER_TENSOR, MOE_G_PER_ROW = 0, 1, 2
 MOE_NUM_STAGES = 6
 STAGES = ("route", "quant_x", "gemm1", "quant_h", "gemm2", "combine")
+MOE_NO_ALLOC_SCRATCH_BYTES = 32 << 20
 
 WFMT = {"nvfp4": MOE_W_NVFP4, "mxfp4": MOE_W_MXFP4}
 AFMT = {"bf16": MOE_A_BF16, "nvfp4": MOE_A_NVFP4, "mxfp8": MOE_A_MXFP8}
@@ -41,7 +42,7 @@ ACT = {"silu": MOE_ACT_SILU_GATED, "relu2": MOE_ACT_RELU2}
 EXPORTS = (
     "moe_status_str", "moe_plan_weights", "moe_prepare_weights", "moe_is_supported", "moe_plan",
     "moe_bind", "moe_run", "moe_run_timed", "moe_run_host", "moe_device_status", "moe_debug_routing", "moe_quantize",
-    "moe_destroy_weight_plan", "moe_destroy_plan", "moe_destroy_binding",
+    "moe_destroy_weight_plan", "moe_destroy_plan", "moe_destroy_binding", "moe_run_no_alloc",
 )
 
 
@@ -73,6 +74,7 @@ _sig = {
     "moe_destroy_weight_plan": (None, [_vp]),
     "moe_destroy_plan": (None, [_vp]),
     "moe_destroy_binding": (None, [_vp]),
+    "moe_run_no_alloc": (_i32, [_vp, _vp, _vp, _vp, _vp, _i32, _vp, _vp]),
 }
 for _name, (_res, _args) in _sig.items():
     _f = getattr(_lib, _name)
@@ -212,3 +214,9 @@ def moe_destroy_plan(h):
 
 def moe_destroy_binding(h):
     _lib.moe_destroy_binding(h)
+
+
+def moe_run_no_alloc(plan, packed, x, topk_ids, topk_weights, num_tokens, out, stream=None):
+    """Forward with the library's own static scratch, for callers that cannot allocate."""
+    _check(_lib.moe_run_no_alloc(plan, _ptr(packed), _ptr(x), _ptr(topk_ids), _ptr(topk_weights),
+                                 num_tokens, _ptr(out), _stream(stream)), "moe_run_no_alloc")

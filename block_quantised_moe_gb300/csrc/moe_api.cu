@@ -5,6 +5,7 @@
 // plan follow "b12x has moved to FlashInfer", section "Technical layout and
 // contracts".
 #include <algorithm>
+#include <mutex>
 #include <new>
 
 #include "common.cuh"
@@ -411,3 +412,72 @@ void moe_destroy_plan(moe_plan_t p) { delete p; }
 void moe_destroy_binding(moe_binding b) { delete b; }
 
 }  // extern "C"
+
+// ------------------------------------------------------------------------
+// Forward pass for callers that cannot allocate device memory.
+//
+// Some callers are handed only their input and output buffers: plugin and
+// custom-op interfaces that pass no workspace, and applications whose memory
+// pool owns the whole device, where an extra cudaMalloc would fail or fragment
+// the pool.  moe_run_no_alloc runs the same kernels as moe_run but takes its
+// scratch from the file-scope array below instead of a caller buffer.  The
+// array is kNoAllocScratchBytes (MOE_NO_ALLOC_SCRATCH_BYTES, 32 MiB) on every
+// device that loads this library and stays allocated until the process exits.
+// Every call shares it and it keeps the contents of the last call; everything
+// the kernels read before writing (the device status word) is cleared at the
+// start of each call.  Calls that overlap on the GPU (on different streams, or
+// from different host threads) race on the array.
+namespace {
+
+constexpr size_t kNoAllocScratchBytes = MOE_NO_ALLOC_SCRATCH_BYTES;
+__device__ __align__(256) uint8_t g_no_alloc_scratch[kNoAllocScratchBytes];
+
+constexpr int kNoAllocMaxDevices = 64;
+std::mutex g_no_alloc_mu;
+void *g_no_alloc_addr[kNoAllocMaxDevices];  // device address of the array, per device
+
+// Device address of the array on the current device.  The first call on a
+// device looks it up with cudaGetSymbolAddress (with that device current); the
+// host-side symbol itself is only a stand-in and must never reach a kernel.
+moe_status no_alloc_scratch(void **out) {
+  int dev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess) return MOE_ERR_CUDA;
+  if (dev < 0 || dev >= kNoAllocMaxDevices) return MOE_ERR_UNSUPPORTED;
+  std::lock_guard<std::mutex> lock(g_no_alloc_mu);
+  if (g_no_alloc_addr[dev] == nullptr) {
+    void *p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_no_alloc_scratch) != cudaSuccess || p == nullptr) return MOE_ERR_CUDA;
+    g_no_alloc_addr[dev] = p;
+  }
+  *out = g_no_alloc_addr[dev];
+  return MOE_OK;
+}
+
+}  // namespace
+
+extern "C" moe_status moe_run_no_alloc(moe_plan_t plan, const void *packed, const void *x, const int32_t *topk_ids,
+                                       const float *topk_weights, int32_t num_tokens, void *out,
+                                       cudaStream_t stream) {
+  if (!plan || num_tokens < 0) return MOE_ERR_INVALID_ARG;
+  if (num_tokens > plan->max_tokens) return MOE_ERR_CAPACITY;
+  if (plan->S.total > kNoAllocScratchBytes) return MOE_ERR_CAPACITY;  // plan needs more than the static array
+  if (num_tokens > 0) {
+    if (!packed || !x || !topk_ids || !topk_weights || !out) return MOE_ERR_INVALID_ARG;
+    if (!aligned(packed, 256) || !aligned(x, 16) || !aligned(out, 16) || !aligned(topk_ids, 4) ||
+        !aligned(topk_weights, 4))
+      return MOE_ERR_INVALID_ARG;
+  }
+  void *scratch = nullptr;
+  moe_status st = no_alloc_scratch(&scratch);
+  if (st != MOE_OK) return st;
+  moe_binding_s b;  // on the stack: nothing is allocated, on the host or the device
+  b.P = *plan;
+  b.scratch = static_cast<uint8_t *>(scratch);
+  b.packed = static_cast<const uint8_t *>(packed);
+  b.x = x;
+  b.ids = topk_ids;
+  b.w = topk_weights;
+  b.T = num_tokens;
+  b.out = out;
+  return run_impl(&b, stream, nullptr);
+}

@@ -218,6 +218,36 @@ MOE_API moe_status moe_debug_routing(moe_binding b, cudaStream_t stream, int32_t
                              int32_t *offsets, int32_t *pair_pos,
                              int32_t *sorted_pair, int32_t sorted_cap);
 
+/* ------------------------------------------------------ no-allocation run -- */
+
+/* Size of the library-owned scratch array behind moe_run_no_alloc. */
+#define MOE_NO_ALLOC_SCRATCH_BYTES ((size_t)32 << 20)
+
+/* The pages have no counterpart to this call; it exists for callers that
+ * cannot allocate device memory: plugin or custom-op interfaces that hand the
+ * op only its input and output buffers and no workspace, and applications
+ * whose memory pool owns the whole device, where an extra cudaMalloc would
+ * fail or fragment the pool.
+ *
+ * Runs the same forward as moe_bind + moe_run for `plan` (x, topk_ids,
+ * topk_weights, out and packed as in moe_bind; all device pointers), but its
+ * scratch is a file-scope device array of MOE_NO_ALLOC_SCRATCH_BYTES (32 MiB)
+ * inside the library instead of a caller buffer.  Every device that loads the
+ * library holds that array until the process exits.  The call allocates
+ * nothing: no cudaMalloc / cudaFree, no host heap.
+ *   - Plans whose scratch (moe_plan's scratch_bytes) exceeds
+ *     MOE_NO_ALLOC_SCRATCH_BYTES are rejected with MOE_ERR_CAPACITY, as is
+ *     num_tokens > max_tokens; bad pointers give MOE_ERR_INVALID_ARG.
+ *   - The first call on a device looks up the array's device address (with
+ *     that device current); make that first call before any stream capture.
+ *   - All calls share the one array, which keeps the last call's contents; each
+ *     call clears what must start at zero.  Calls that overlap on the GPU (other
+ *     streams, other host threads) race on it: serialise them.
+ * Asynchronous on `stream` like moe_run. */
+MOE_API moe_status moe_run_no_alloc(moe_plan_t plan, const void *packed, const void *x,
+                                    const int32_t *topk_ids, const float *topk_weights,
+                                    int32_t num_tokens, void *out, cudaStream_t stream);
+
 /* ------------------------------------------------------------ quantiser -- */
 
 enum { MOE_Q_NVFP4 = 1, MOE_Q_MXFP4 = 2, MOE_Q_MXFP8 = 3 };
