@@ -1,6 +1,7 @@
 // Host-side layouts and kernel launchers of libmoe (internal; not part of the ABI).
 #pragma once
 
+#include <cuda_fp16.h>
 #include <cuda_runtime.h>
 #include <stddef.h>
 #include <stdint.h>
@@ -10,15 +11,20 @@ namespace bqmoe {
 constexpr size_t kAlign = 256;
 inline size_t align_up(size_t v, size_t a = kAlign) { return (v + a - 1) / a * a; }
 
-// Packed expert buffer written by the packer.  Per expert, row-major with K
-// contiguous, in this order; each segment starts on a 256-byte boundary.
-//   c13  uint8 [E][N13][H/2]    E2M1 codes of W13 (gate rows then up rows, or W1)
-//   s13  uint8 [E][N13][H/bs]   block scales of W13
-//   c2   uint8 [E][H][I/2]      E2M1 codes of W2
-//   s2   uint8 [E][H][I/bs]     block scales of W2
-//   g    float [E][4]           global scales (gate|w1, up, down, 1); all 1 for MXFP4
+// Packed expert buffer written by the packer, segments on 256-byte boundaries:
+//   c13  E2M1 codes of W13 (gate and up rows, or W1), N13 rows x H
+//   s13  block scales of W13
+//   c2   E2M1 codes of W2, H rows x I
+//   s2   block scales of W2
+//   g    float [E][4] global scales (gate|w1, up, down, 1); all 1 for MXFP4
+// LAYOUT_ROWMAJOR keeps the checkpoint order ([E][rows][K/2] codes, [E][rows][K/bs]
+// scales).  LAYOUT_MMA16x64 (NVFP4) stores 16-row x 64-K tiles in mma.m16n8k16
+// A-fragment order (see the packer); the byte count per expert is the same.
+enum { LAYOUT_ROWMAJOR = 0, LAYOUT_MMA16x64 = 1 };
+
 struct WeightLayout {
   int E = 0, H = 0, I = 0, wfmt = 0, act = 0;
+  int layout = LAYOUT_ROWMAJOR;
   int bs = 16;   // elements per block scale
   int n13 = 0;   // rows of W13
   size_t off_c13 = 0, off_s13 = 0, off_c2 = 0, off_s2 = 0, off_g = 0, total = 0;
@@ -34,11 +40,13 @@ struct ScratchLayout {
   size_t status = 0, counts = 0, offsets = 0, sorted = 0, pair_pos = 0;
   size_t xq_codes = 0, xq_scales = 0, xq_g = 0;
   size_t h = 0, hq_codes = 0, hq_scales = 0, hq_g = 0;
+  size_t x16 = 0, xfac = 0, hamax = 0;  // tensor-core path: FP16 x, its factors, per-pair max |h|
   size_t part = 0, total = 0;
 };
 
 // Activation sources the grouped kernels can stage.
-enum Src { SRC_X_BF16 = 0, SRC_X_NVFP4 = 1, SRC_X_MXFP8 = 2, SRC_H_F32 = 3, SRC_H_NVFP4 = 4, SRC_H_MXFP8 = 5 };
+enum Src { SRC_X_BF16 = 0, SRC_X_NVFP4 = 1, SRC_X_MXFP8 = 2, SRC_H_F32 = 3, SRC_H_NVFP4 = 4, SRC_H_MXFP8 = 5,
+           SRC_X16 = 6 /* FP16 rows + per-row factor, staged by launch_stage_x16 */ };
 // Grouped-kernel stage.
 enum Stage { STAGE_GATED = 0, STAGE_RELU2 = 1, STAGE_DOWN = 2 };
 
@@ -51,9 +59,10 @@ struct GroupedArgs {
   int n_rows;  // I (GEMM1 features) or H (GEMM2 rows)
   int I;       // intermediate (gated: up rows start at I)
   // activation source
-  const void *act;            // bf16 x [T][H] | f32 h [cap][I] | codes
+  const void *act;            // bf16 x [T][H] | f32 h [cap][I] | codes | FP16 x16 [T][H]
   const uint8_t *act_scales;  // block scales (quantised sources)
-  const float *act_g;         // per-row NVFP4 global
+  const float *act_g;         // per-row NVFP4 global | x16 factor | |h| maximum per pair (SRC_H_F32, mma)
+  float *out_amax;            // GEMM1 on the mma path: per-pair max |h| (atomicMax), or null
   // routing
   const int32_t *counts, *offsets, *sorted_pair;
   int top_k;
@@ -66,6 +75,13 @@ cudaError_t launch_route(const int32_t *ids, int P, int E, int pad, int32_t *cou
                          int32_t *sorted_pair, int32_t *pair_pos, int32_t *status, cudaStream_t s);
 
 cudaError_t launch_grouped_cc(int wfmt, int src, int stage, const GroupedArgs &a, int E, cudaStream_t s);
+
+// Tensor-core grouped kernel for LAYOUT_MMA16x64 weights; rows_total = rows of
+// the stage's weight matrix (2I gated, I for ReLU^2, H for the down projection).
+cudaError_t launch_grouped_mma(int src, int stage, const GroupedArgs &a, int rows_total, int E, cudaStream_t s);
+
+cudaError_t launch_stage_x16(int src, const void *act, const uint8_t *act_scales, const float *act_g, int T, int K,
+                             __half *x16, float *fac, float *zero, int64_t zero_n, cudaStream_t s);
 
 cudaError_t launch_combine(const float *part, int H, const int32_t *pair_pos, int T, int K, void *out_bf16,
                            cudaStream_t s);

@@ -31,26 +31,27 @@ k_combine(const float *__restrict__ part, int H, const int32_t *__restrict__ pai
     while (j > 0 && pos[j - 1] > p) { pos[j] = pos[j - 1]; --j; }
     pos[j] = p;
   }
-  for (int c = (blockIdx.x * kCombThreads + threadIdx.x) * 8; c < H; c += gridDim.x * kCombThreads * 8) {
-    float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-    for (int i = 0; i < n; ++i) {
-      const float4 *src = reinterpret_cast<const float4 *>(part + (size_t)pos[i] * H + c);
-      const float4 a = src[0], b = src[1];
-      acc[0] += a.x; acc[1] += a.y; acc[2] += a.z; acc[3] += a.w;
-      acc[4] += b.x; acc[5] += b.y; acc[6] += b.z; acc[7] += b.w;
-    }
-    __align__(16) __nv_bfloat162 o[4];
+  const int c = (blockIdx.x * kCombThreads + threadIdx.x) * 4;
+  if (c >= H) return;
+  float4 v[kMaxK];
 #pragma unroll
-    for (int i = 0; i < 4; ++i) o[i] = __floats2bfloat162_rn(acc[2 * i], acc[2 * i + 1]);
-    *reinterpret_cast<uint4 *>(out + (size_t)t * H + c) = *reinterpret_cast<const uint4 *>(o);
-  }
+  for (int i = 0; i < kMaxK; ++i)  // all loads in flight before the ordered sum
+    if (i < n) v[i] = __ldcs(reinterpret_cast<const float4 *>(part + (size_t)pos[i] * H + c));
+  float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+  for (int i = 0; i < kMaxK; ++i)
+    if (i < n) {
+      acc.x += v[i].x; acc.y += v[i].y; acc.z += v[i].z; acc.w += v[i].w;
+    }
+  __align__(8) __nv_bfloat162 o[2] = {__floats2bfloat162_rn(acc.x, acc.y), __floats2bfloat162_rn(acc.z, acc.w)};
+  *reinterpret_cast<uint2 *>(out + (size_t)t * H + c) = *reinterpret_cast<const uint2 *>(o);
 }
 
 cudaError_t launch_combine(const float *part, int H, const int32_t *pair_pos, int T, int K, void *out,
                            cudaStream_t s) {
   if (T <= 0) return cudaSuccess;
   if (K > kMaxK) return cudaErrorInvalidValue;
-  const int gx = (H + kCombThreads * 8 - 1) / (kCombThreads * 8);
+  const int gx = (H + kCombThreads * 4 - 1) / (kCombThreads * 4);
   k_combine<<<dim3(gx, T), kCombThreads, 0, s>>>(part, H, pair_pos, K, reinterpret_cast<__nv_bfloat16 *>(out));
   return cudaGetLastError();
 }
@@ -81,6 +82,73 @@ __global__ void k_pack_globals(const float *__restrict__ g13, int n13m, const fl
   reinterpret_cast<float4 *>(gout)[e] = make_float4(a, b, c, 1.f);
 }
 
+// NVFP4 experts are re-tiled for the register-dequant tensor-core kernel: every
+// 16-row x 64-K tile becomes 32 lanes x 16 bytes in mma.m16n8k16 A-fragment
+// order.  Lane t (g = t/4, c = t%4), k16 sub-step i, byte j holds the source
+// byte (two codes, even element low) at tile row g (+8 for j odd) and K offset
+// 64q + 16i + 2c (+8 for j >= 2).  Scales: per (tile, q, g) 8 bytes, byte 2i =
+// scale of (row g, block 4q+i), byte 2i+1 = scale of (row g+8, block 4q+i).
+// For gated W13, tile j's rows 0..7 are gate features 8j..8j+7 and rows 8..15
+// the up rows of the same features; otherwise tile rows are consecutive rows.
+__device__ __forceinline__ int64_t tile_src_row(int tile, int rr, int gated, int I) {
+  if (gated) return rr < 8 ? (int64_t)tile * 8 + rr : (int64_t)I + tile * 8 + rr - 8;
+  return (int64_t)tile * 16 + rr;
+}
+
+__global__ void k_pack_mma_codes(const uint8_t *__restrict__ src, uint8_t *__restrict__ dst, int E, int rows, int K,
+                                 int gated, int I) {
+  const int nsteps = K / 64, ntiles = rows / 16;
+  const int64_t n_chunks = (int64_t)E * ntiles * nsteps * 32;
+  const int64_t row_bytes = K / 2;
+  for (int64_t idx = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; idx < n_chunks;
+       idx += (int64_t)gridDim.x * blockDim.x) {
+    const int t = (int)(idx & 31);
+    int64_t r = idx >> 5;
+    const int q = (int)(r % nsteps);
+    r /= nsteps;
+    const int tile = (int)(r % ntiles);
+    const int64_t e = r / ntiles;
+    const int g = t >> 2, c = t & 3;
+    const uint8_t *se = src + e * rows * row_bytes;
+    const int64_t row_lo = tile_src_row(tile, g, gated, I), row_hi = tile_src_row(tile, g + 8, gated, I);
+    uint32_t w[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const int64_t kb = (64 * q + 16 * i + 2 * c) / 2;
+      w[i] = (uint32_t)se[row_lo * row_bytes + kb] | ((uint32_t)se[row_hi * row_bytes + kb] << 8) |
+             ((uint32_t)se[row_lo * row_bytes + kb + 4] << 16) | ((uint32_t)se[row_hi * row_bytes + kb + 4] << 24);
+    }
+    reinterpret_cast<uint4 *>(dst)[idx] = make_uint4(w[0], w[1], w[2], w[3]);
+  }
+}
+
+__global__ void k_pack_mma_scales(const uint8_t *__restrict__ src, uint8_t *__restrict__ dst, int E, int rows, int K,
+                                  int gated, int I) {
+  const int nsteps = K / 64, ntiles = rows / 16;
+  const int64_t n_groups = (int64_t)E * ntiles * nsteps * 8;
+  const int64_t row_bytes = K / 16;
+  for (int64_t idx = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; idx < n_groups;
+       idx += (int64_t)gridDim.x * blockDim.x) {
+    const int g = (int)(idx & 7);
+    int64_t r = idx >> 3;
+    const int q = (int)(r % nsteps);
+    r /= nsteps;
+    const int tile = (int)(r % ntiles);
+    const int64_t e = r / ntiles;
+    const uint8_t *se = src + e * rows * row_bytes;
+    const int64_t row_lo = tile_src_row(tile, g, gated, I), row_hi = tile_src_row(tile, g + 8, gated, I);
+    uint32_t w[2] = {0u, 0u};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const uint32_t pair = (uint32_t)se[row_lo * row_bytes + 4 * q + i] | ((uint32_t)se[row_hi * row_bytes + 4 * q + i] << 8);
+      w[i >> 1] |= pair << (16 * (i & 1));
+    }
+    reinterpret_cast<uint2 *>(dst)[idx] = make_uint2(w[0], w[1]);
+  }
+}
+
+static int pack_grid(int64_t n) { return (int)std::max<int64_t>(1, std::min<int64_t>((n + 255) / 256, 152 * 32)); }
+
 static cudaError_t copy_seg(const void *src, void *dst, size_t bytes, cudaStream_t s) {
   const int64_t n16 = (int64_t)(bytes / 16);
   if (n16 == 0) return cudaSuccess;
@@ -93,6 +161,23 @@ cudaError_t launch_pack(const WeightLayout &L, const void *w13_codes, const void
                         const void *w2_codes, const void *w2_scales, const float *w2_global, uint8_t *packed,
                         cudaStream_t s) {
   cudaError_t err;
+  if (L.layout == LAYOUT_MMA16x64) {
+    const int gated = L.n13 == 2 * L.I;
+    const int64_t c13 = (int64_t)L.E * (L.n13 / 16) * (L.H / 64) * 32, s13 = c13 / 4;
+    const int64_t c2 = (int64_t)L.E * (L.H / 16) * (L.I / 64) * 32, s2 = c2 / 4;
+    k_pack_mma_codes<<<pack_grid(c13), 256, 0, s>>>(static_cast<const uint8_t *>(w13_codes), packed + L.off_c13, L.E,
+                                                    L.n13, L.H, gated, L.I);
+    k_pack_mma_scales<<<pack_grid(s13), 256, 0, s>>>(static_cast<const uint8_t *>(w13_scales), packed + L.off_s13,
+                                                     L.E, L.n13, L.H, gated, L.I);
+    k_pack_mma_codes<<<pack_grid(c2), 256, 0, s>>>(static_cast<const uint8_t *>(w2_codes), packed + L.off_c2, L.E,
+                                                   L.H, L.I, 0, L.I);
+    k_pack_mma_scales<<<pack_grid(s2), 256, 0, s>>>(static_cast<const uint8_t *>(w2_scales), packed + L.off_s2, L.E,
+                                                    L.H, L.I, 0, L.I);
+    if ((err = cudaGetLastError()) != cudaSuccess) return err;
+    k_pack_globals<<<(L.E + 127) / 128, 128, 0, s>>>(w13_global, L.n13 / L.I, w2_global, L.E,
+                                                       reinterpret_cast<float *>(packed + L.off_g));
+    return cudaGetLastError();
+  }
   if ((err = copy_seg(w13_codes, packed + L.off_c13, L.E * L.c13_expert(), s)) != cudaSuccess) return err;
   if ((err = copy_seg(w13_scales, packed + L.off_s13, L.E * L.s13_expert(), s)) != cudaSuccess) return err;
   if ((err = copy_seg(w2_codes, packed + L.off_c2, L.E * L.c2_expert(), s)) != cudaSuccess) return err;

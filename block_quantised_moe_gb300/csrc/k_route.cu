@@ -102,9 +102,12 @@ k_route(const int32_t *__restrict__ ids, int P, int E, int pad, int32_t *__restr
     __syncthreads();
   }
 
-  if (tid == 0 && dropped > 0) {
-    atomicOr(&status[ST_FLAGS], ST_FLAG_DROPPED);
-    atomicAdd(&status[ST_DROPPED], dropped);
+  // Routing runs first in every forward, so it (re)initialises the whole status word.
+  if (tid == 0) {
+    status[ST_FLAGS] = dropped > 0 ? ST_FLAG_DROPPED : 0;
+    status[ST_DROPPED] = dropped;
+    status[2] = 0;
+    status[3] = 0;
   }
 }
 

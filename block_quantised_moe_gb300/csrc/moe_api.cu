@@ -82,6 +82,7 @@ moe_status moe_plan_weights(const moe_weight_desc *d, moe_weight_plan *out, size
   L.act = d->act;
   L.bs = d->wfmt == MOE_W_NVFP4 ? 16 : 32;
   L.n13 = d->act == MOE_ACT_SILU_GATED ? 2 * L.I : L.I;
+  L.layout = d->wfmt == MOE_W_NVFP4 ? LAYOUT_MMA16x64 : LAYOUT_ROWMAJOR;
   L.off_c13 = 0;
   L.off_s13 = align_up(L.off_c13 + (size_t)L.E * L.c13_expert());
   L.off_c2 = align_up(L.off_s13 + (size_t)L.E * L.s13_expert());
@@ -119,6 +120,8 @@ moe_status moe_is_supported(const moe_caps *c) {
   // Configurations"): NVFP4 weights with BF16, NVFP4 or MXFP8 activations;
   // MXFP4 weights with BF16 or MXFP8 activations.
   if (c->wplan->L.wfmt == MOE_W_MXFP4 && c->afmt == MOE_A_NVFP4) return MOE_ERR_UNSUPPORTED;
+  // The tensor-core kernel works on 128-row blocks of each weight matrix.
+  if (c->wplan->L.layout == LAYOUT_MMA16x64 && c->wplan->L.n13 % 128 != 0) return MOE_ERR_UNSUPPORTED;
   return MOE_OK;
 }
 
@@ -165,6 +168,11 @@ moe_status moe_plan(const moe_caps *c, moe_plan_t *out, size_t *scratch_bytes, i
   } else if (P.afmt == MOE_A_MXFP8) {
     S.hq_codes = take((size_t)S.cap_sorted * L.I);
     S.hq_scales = take((size_t)S.cap_sorted * L.I / 32);
+  }
+  if (L.layout == LAYOUT_MMA16x64) {
+    S.x16 = take(2 * (size_t)T * L.H);
+    S.xfac = take(4 * (size_t)T);
+    S.hamax = take(4 * (size_t)S.cap_sorted);
   }
   S.part = take(4 * (size_t)S.cap_sorted * L.H);
   S.total = o;
@@ -227,7 +235,6 @@ static moe_status run_impl(moe_binding b, cudaStream_t stream, cudaEvent_t *ev) 
   cudaError_t err;
 
   if ((err = mark(MOE_STAGE_ROUTE)) != cudaSuccess) return MOE_ERR_CUDA;
-  if ((err = cudaMemsetAsync(status, 0, 16, stream)) != cudaSuccess) return MOE_ERR_CUDA;
   if ((err = launch_route(b->ids, T * K, E, P.pad, counts, offsets, sorted, pair_pos, status, stream)) != cudaSuccess)
     return MOE_ERR_CUDA;
 
@@ -259,6 +266,18 @@ static moe_status run_impl(moe_binding b, cudaStream_t stream, cudaEvent_t *ev) 
     a.act_scales = at<uint8_t>(sc, S.xq_scales);
   }
   if (err != cudaSuccess) return MOE_ERR_CUDA;
+  const bool mma = L.layout == LAYOUT_MMA16x64;
+  if (mma) {
+    // tensor-core path: x^ as FP16 rows + per-row factor; clears the per-pair |h| maxima
+    err = launch_stage_x16(src1, a.act, a.act_scales, a.act_g, T, H, at<__half>(sc, S.x16), at<float>(sc, S.xfac),
+                           at<float>(sc, S.hamax), S.cap_sorted, stream);
+    if (err != cudaSuccess) return MOE_ERR_CUDA;
+    src1 = SRC_X16;
+    a.act = at<__half>(sc, S.x16);
+    a.act_scales = nullptr;
+    a.act_g = at<float>(sc, S.xfac);
+    a.out_amax = P.afmt == MOE_A_BF16 ? at<float>(sc, S.hamax) : nullptr;
+  }
 
   // GEMM1 + activation -> h
   if (mark(MOE_STAGE_GEMM1) != cudaSuccess) return MOE_ERR_CUDA;
@@ -270,14 +289,17 @@ static moe_status run_impl(moe_binding b, cudaStream_t stream, cudaEvent_t *ev) 
   a.n_rows = I;
   a.out = h;
   const int stage1 = L.act == MOE_ACT_SILU_GATED ? STAGE_GATED : STAGE_RELU2;
-  if ((err = launch_grouped_cc(L.wfmt, src1, stage1, a, E, stream)) != cudaSuccess) return MOE_ERR_CUDA;
+  err = mma ? launch_grouped_mma(src1, stage1, a, L.n13, E, stream)
+            : launch_grouped_cc(L.wfmt, src1, stage1, a, E, stream);
+  a.out_amax = nullptr;
+  if (err != cudaSuccess) return MOE_ERR_CUDA;
 
   // re-quantise h for NVFP4 / MXFP8 activations (rows past offsets[E] are skipped)
   if ((err = mark(MOE_STAGE_QUANT_H)) != cudaSuccess) return MOE_ERR_CUDA;
   int src2 = SRC_H_F32;
   a.act = h;
   a.act_scales = nullptr;
-  a.act_g = nullptr;
+  a.act_g = mma ? at<float>(sc, S.hamax) : nullptr;
   if (P.afmt == MOE_A_NVFP4) {
     err = launch_quant_rows_nvfp4(h, false, S.cap_sorted, I, at<uint8_t>(sc, S.hq_codes),
                                   at<uint8_t>(sc, S.hq_scales), at<float>(sc, S.hq_g), offsets + E, stream);
@@ -303,7 +325,9 @@ static moe_status run_impl(moe_binding b, cudaStream_t stream, cudaEvent_t *ev) 
   a.n_rows = H;
   a.out = part;
   if (mark(MOE_STAGE_GEMM2) != cudaSuccess) return MOE_ERR_CUDA;
-  if ((err = launch_grouped_cc(L.wfmt, src2, STAGE_DOWN, a, E, stream)) != cudaSuccess) return MOE_ERR_CUDA;
+  err = mma ? launch_grouped_mma(src2, STAGE_DOWN, a, H, E, stream)
+            : launch_grouped_cc(L.wfmt, src2, STAGE_DOWN, a, E, stream);
+  if (err != cudaSuccess) return MOE_ERR_CUDA;
   if (mark(MOE_STAGE_COMBINE) != cudaSuccess) return MOE_ERR_CUDA;
   if ((err = launch_combine(part, H, pair_pos, T, K, b->out, stream)) != cudaSuccess) return MOE_ERR_CUDA;
   if (mark(MOE_NUM_STAGES) != cudaSuccess) return MOE_ERR_CUDA;
