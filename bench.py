@@ -301,8 +301,9 @@ def main():
 
     # events for the per-stage timing, recorded once so that the handles exist
     n_ev = abi.MOE_NUM_STAGES + 1
-    n_timed_steps = min(args.steps, 512)
-    every = max(1, args.steps // n_timed_steps)
+    # per-stage events on every 4th step (at most 512 steps), plain runs in between
+    every = 4
+    n_timed_steps = min((args.steps + every - 1) // every, 512)
     ev_sets = []
     for _ in range(n_timed_steps):
         evs = [torch.cuda.Event(enable_timing=True) for _ in range(n_ev)]

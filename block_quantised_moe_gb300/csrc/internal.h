@@ -18,8 +18,9 @@ inline size_t align_up(size_t v, size_t a = kAlign) { return (v + a - 1) / a * a
 //   s2   block scales of W2
 //   g    float [E][4] global scales (gate|w1, up, down, 1); all 1 for MXFP4
 // LAYOUT_ROWMAJOR keeps the checkpoint order ([E][rows][K/2] codes, [E][rows][K/bs]
-// scales).  LAYOUT_MMA16x64 (NVFP4) stores 16-row x 64-K tiles in mma.m16n8k16
-// A-fragment order (see the packer); the byte count per expert is the same.
+// scales).  LAYOUT_MMA16x64 (NVFP4) interleaves codes and scales per 128-row
+// block and 64-wide K step in mma.m16n8k16 A-fragment order (see the packer):
+// c13 / c2 then hold codes and scales together and s13 / s2 are empty.
 enum { LAYOUT_ROWMAJOR = 0, LAYOUT_MMA16x64 = 1 };
 
 struct WeightLayout {
@@ -32,12 +33,15 @@ struct WeightLayout {
   size_t s13_expert() const { return (size_t)n13 * H / bs; }
   size_t c2_expert() const { return (size_t)H * I / 2; }
   size_t s2_expert() const { return (size_t)H * I / bs; }
+  // LAYOUT_MMA16x64: bytes of one expert's interleaved W13 / W2 segment
+  size_t blk13_expert() const { return c13_expert() + s13_expert(); }
+  size_t blk2_expert() const { return c2_expert() + s2_expert(); }
 };
 
 // Scratch owned by the caller and carved by the plan (offsets in bytes).
 struct ScratchLayout {
   int64_t cap_sorted = 0;  // rows of the padded, expert-sorted pair list
-  size_t status = 0, counts = 0, offsets = 0, sorted = 0, pair_pos = 0;
+  size_t status = 0, counts = 0, offsets = 0, sorted = 0, pair_pos = 0, active = 0, passes = 0;
   size_t xq_codes = 0, xq_scales = 0, xq_g = 0;
   size_t h = 0, hq_codes = 0, hq_scales = 0, hq_g = 0;
   size_t x16 = 0, xfac = 0, hamax = 0;  // tensor-core path: FP16 x, its factors, per-pair max |h|
@@ -56,6 +60,7 @@ struct GroupedArgs {
   size_t codes_expert, scales_expert;  // bytes per expert
   const float *globals;  // [E][4]
   int K;       // reduction length
+  int n_blocks;  // 128-row blocks of the stage's weight matrix (set by the mma launcher)
   int n_rows;  // I (GEMM1 features) or H (GEMM2 rows)
   int I;       // intermediate (gated: up rows start at I)
   // activation source
@@ -65,20 +70,29 @@ struct GroupedArgs {
   float *out_amax;            // GEMM1 on the mma path: per-pair max |h| (atomicMax), or null
   // routing
   const int32_t *counts, *offsets, *sorted_pair;
+  const int32_t *active;  // [0] = number of experts with pairs, [1..] their ids (ascending)
+  const int32_t *passes;  // [i] = passes of active experts before i (prefix, n_active + 1 entries)
+  int32_t *status;        // device status word (timeout flag)
   int top_k;
   const float *topk_weights;
   // output: h [cap][I] (GEMM1) or partials [cap][H] (GEMM2)
   float *out;
 };
 
-cudaError_t launch_route(const int32_t *ids, int P, int E, int pad, int32_t *counts, int32_t *offsets,
-                         int32_t *sorted_pair, int32_t *pair_pos, int32_t *status, cudaStream_t s);
+// ntok: tokens per pass of the tensor-core kernels (for the per-expert pass prefix).
+cudaError_t launch_route(const int32_t *ids, int P, int E, int pad, int ntok, int32_t *counts, int32_t *offsets,
+                         int32_t *sorted_pair, int32_t *pair_pos, int32_t *active, int32_t *passes, int32_t *status,
+                         cudaStream_t s);
 
 cudaError_t launch_grouped_cc(int wfmt, int src, int stage, const GroupedArgs &a, int E, cudaStream_t s);
 
 // Tensor-core grouped kernel for LAYOUT_MMA16x64 weights; rows_total = rows of
 // the stage's weight matrix (2I gated, I for ReLU^2, H for the down projection).
-cudaError_t launch_grouped_mma(int src, int stage, const GroupedArgs &a, int rows_total, int E, cudaStream_t s);
+// Tokens per pass of the tensor-core kernels (8, or 16 when `wide` and the
+// staging fits); the routing kernel's pass prefix must use the same value.
+int mma_tokens_per_pass(int H, int I, bool wide);
+cudaError_t launch_grouped_mma(int src, int stage, const GroupedArgs &a, int rows_total, int E, int ntok,
+                               cudaStream_t s);
 
 cudaError_t launch_stage_x16(int src, const void *act, const uint8_t *act_scales, const float *act_g, int T, int K,
                              __half *x16, float *fac, float *zero, int64_t zero_n, cudaStream_t s);

@@ -82,17 +82,29 @@ __global__ void k_pack_globals(const float *__restrict__ g13, int n13m, const fl
   reinterpret_cast<float4 *>(gout)[e] = make_float4(a, b, c, 1.f);
 }
 
-// NVFP4 experts are re-tiled for the register-dequant tensor-core kernel: every
-// 16-row x 64-K tile becomes 32 lanes x 16 bytes in mma.m16n8k16 A-fragment
-// order.  Lane t (g = t/4, c = t%4), k16 sub-step i, byte j holds the source
-// byte (two codes, even element low) at tile row g (+8 for j odd) and K offset
-// 64q + 16i + 2c (+8 for j >= 2).  Scales: per (tile, q, g) 8 bytes, byte 2i =
-// scale of (row g, block 4q+i), byte 2i+1 = scale of (row g+8, block 4q+i).
-// For gated W13, tile j's rows 0..7 are gate features 8j..8j+7 and rows 8..15
+// NVFP4 experts are re-tiled for the tensor-core kernel.  Rows are grouped in
+// 128-row blocks of eight 16-row tiles; for every 64-wide K step a block stores
+// 4608 contiguous bytes: 4096 bytes of codes (tile-major, 32 lanes x 16 bytes
+// in mma.m16n8k16 A-fragment order) then 512 bytes of scales (tile-major, 8
+// groups x 8 bytes).  Lane t (g = t/4, c = t%4), k16 sub-step i, byte j of a
+// code chunk holds the source byte (two codes, even element low) at tile row g
+// (+8 for j odd) and K offset 64q + 16i + 2c (+8 for j >= 2).  Scale group g:
+// byte 2i = scale of (row g, block 4q+i), byte 2i+1 = (row g+8, block 4q+i).
+// For gated W13, tile t's rows 0..7 are gate features 8t..8t+7 and rows 8..15
 // the up rows of the same features; otherwise tile rows are consecutive rows.
+// A block's K steps are contiguous, so the kernel streams a block with 1-D bulk
+// copies.
+constexpr int64_t kMmaStepBytes = 4608;
+
 __device__ __forceinline__ int64_t tile_src_row(int tile, int rr, int gated, int I) {
   if (gated) return rr < 8 ? (int64_t)tile * 8 + rr : (int64_t)I + tile * 8 + rr - 8;
   return (int64_t)tile * 16 + rr;
+}
+
+// byte offset of (expert, 16-row tile, K step) inside a stage's packed segment
+__device__ __forceinline__ int64_t mma_step_base(int64_t e, int tile, int q, int ntiles, int nsteps) {
+  const int nblk = ntiles / 8;
+  return ((e * nblk + tile / 8) * nsteps + q) * kMmaStepBytes;
 }
 
 __global__ void k_pack_mma_codes(const uint8_t *__restrict__ src, uint8_t *__restrict__ dst, int E, int rows, int K,
@@ -118,7 +130,8 @@ __global__ void k_pack_mma_codes(const uint8_t *__restrict__ src, uint8_t *__res
       w[i] = (uint32_t)se[row_lo * row_bytes + kb] | ((uint32_t)se[row_hi * row_bytes + kb] << 8) |
              ((uint32_t)se[row_lo * row_bytes + kb + 4] << 16) | ((uint32_t)se[row_hi * row_bytes + kb + 4] << 24);
     }
-    reinterpret_cast<uint4 *>(dst)[idx] = make_uint4(w[0], w[1], w[2], w[3]);
+    uint8_t *d = dst + mma_step_base(e, tile, q, ntiles, nsteps) + (tile % 8) * 512 + t * 16;
+    *reinterpret_cast<uint4 *>(d) = make_uint4(w[0], w[1], w[2], w[3]);
   }
 }
 
@@ -143,7 +156,8 @@ __global__ void k_pack_mma_scales(const uint8_t *__restrict__ src, uint8_t *__re
       const uint32_t pair = (uint32_t)se[row_lo * row_bytes + 4 * q + i] | ((uint32_t)se[row_hi * row_bytes + 4 * q + i] << 8);
       w[i >> 1] |= pair << (16 * (i & 1));
     }
-    reinterpret_cast<uint2 *>(dst)[idx] = make_uint2(w[0], w[1]);
+    uint8_t *d = dst + mma_step_base(e, tile, q, ntiles, nsteps) + 4096 + (tile % 8) * 64 + g * 8;
+    *reinterpret_cast<uint2 *>(d) = make_uint2(w[0], w[1]);
   }
 }
 
@@ -167,11 +181,11 @@ cudaError_t launch_pack(const WeightLayout &L, const void *w13_codes, const void
     const int64_t c2 = (int64_t)L.E * (L.H / 16) * (L.I / 64) * 32, s2 = c2 / 4;
     k_pack_mma_codes<<<pack_grid(c13), 256, 0, s>>>(static_cast<const uint8_t *>(w13_codes), packed + L.off_c13, L.E,
                                                     L.n13, L.H, gated, L.I);
-    k_pack_mma_scales<<<pack_grid(s13), 256, 0, s>>>(static_cast<const uint8_t *>(w13_scales), packed + L.off_s13,
+    k_pack_mma_scales<<<pack_grid(s13), 256, 0, s>>>(static_cast<const uint8_t *>(w13_scales), packed + L.off_c13,
                                                      L.E, L.n13, L.H, gated, L.I);
     k_pack_mma_codes<<<pack_grid(c2), 256, 0, s>>>(static_cast<const uint8_t *>(w2_codes), packed + L.off_c2, L.E,
                                                    L.H, L.I, 0, L.I);
-    k_pack_mma_scales<<<pack_grid(s2), 256, 0, s>>>(static_cast<const uint8_t *>(w2_scales), packed + L.off_s2, L.E,
+    k_pack_mma_scales<<<pack_grid(s2), 256, 0, s>>>(static_cast<const uint8_t *>(w2_scales), packed + L.off_c2, L.E,
                                                     L.H, L.I, 0, L.I);
     if ((err = cudaGetLastError()) != cudaSuccess) return err;
     k_pack_globals<<<(L.E + 127) / 128, 128, 0, s>>>(w13_global, L.n13 / L.I, w2_global, L.E,

@@ -9,9 +9,10 @@
 //
 // * The packer stores every 16-row x 64-K tile of E2M1 codes as 32 x 16-byte
 //   lanes in mma.m16n8k16 A-fragment order, and its 16 x 4 E4M3 block scales
-//   as 8-byte groups (rows r and r+8 interleaved).  A warp streams a tile with
-//   one coalesced 128-bit load per lane (plus an 8-byte scale load shared by 4
-//   lanes), four tiles ahead of use.
+//   as 8-byte groups (rows r and r+8 interleaved), codes and scales of a
+//   128-row block contiguous per K step.  A producer warp streams them into a
+//   shared-memory ring with bulk copies (TMA), and each consumer lane reads its
+//   16-byte fragment chunk with one conflict-free shared load.
 // * Codes become FP16 with cvt.rn.f16x2.e2m1x2 and are multiplied by their E4M3
 //   scale in FP16 (the product of an E2M1 and an E4M3 value has at most 6
 //   significant bits and lies in [2^-10, 2688]: exact), straight into A
@@ -27,16 +28,15 @@
 //   each thread owns matching gate / up accumulators and computes SiLU(g) * u
 //   in registers.
 //
-// One CTA = 8 warps = 128 weight rows of one expert; it walks the expert's
-// sorted pairs in tiles of 8 * NT tokens.
+// A unit of work is 128 weight rows of one expert (one per consumer warp) for
+// the expert's sorted pairs, in passes of 8 * NT tokens.
+#include <algorithm>
+
 #include "common.cuh"
 #include "internal.h"
 
 namespace bqmoe {
 
-constexpr int kMmaWarps = 8;
-constexpr int kMmaThreads = kMmaWarps * 32;
-constexpr int kPF = 8;  // 64-K super-steps loaded ahead of use
 
 __device__ __forceinline__ void mma_16816(float (&d)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
   asm volatile(
@@ -190,114 +190,286 @@ k_stage_x16(const void *__restrict__ act, const uint8_t *__restrict__ act_scales
 }
 
 // ------------------------------------------------------------ grouped kernel
+//
+// Persistent, one CTA per SM: warp 8 is the producer, warps 0-7 the consumers.
+// The work list is every (expert with pairs, 128-row block) of the stage; CTA c
+// takes a contiguous range of it, so consecutive units usually share an expert
+// and its staged activations.  The producer streams each unit's packed bytes
+// (4608 per 64-K step: codes + scales of the whole 128-row block) with 1-D bulk
+// copies (cp.async.bulk, completion on an mbarrier) into a ring of shared-memory
+// stages, up to the ring's depth ahead of the consumers, across unit
+// boundaries.  Consumer warp w dequantises tile w of each step straight into
+// mma fragments.  Every mbarrier wait is bounded: on timeout the status word
+// gets MOE timeout flag, the warp stops, and the producer waits (bounded) for
+// its own copies in flight before the CTA exits.
+
+constexpr int kConsumers = 8;
+constexpr int kTmaThreads = (kConsumers + 1) * 32;
+constexpr int kStepBytes = 4608;  // one 64-K step of a 128-row block
+constexpr int kSPS = 4;           // K steps per ring stage
+constexpr int kStageBytes = kStepBytes * kSPS;
+constexpr int kMaxStages = 8;
+constexpr unsigned long long kWaitNs = 2000000000ull;  // 2 s
+
+__device__ __forceinline__ unsigned long long globaltimer_ns() {
+  unsigned long long t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count));
+}
+__device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes) : "memory");
+}
+__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
+}
+__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tmbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\tselp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+// Bounded wait; false on timeout.
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const unsigned long long t0 = globaltimer_ns();
+  for (uint32_t it = 1;; ++it) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if ((it & 255u) == 0 && globaltimer_ns() - t0 > kWaitNs) return false;
+  }
+}
+__device__ __forceinline__ void bulk_g2s(uint32_t dst, const void *src, uint32_t bytes, uint32_t bar) {
+  asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
+               "l"(src), "r"(bytes), "r"(bar)
+               : "memory");
+}
+// Barrier among the consumer warps only (the producer never joins), built on an
+// mbarrier so that its wait is bounded too.  Lane 0 of each warp arrives after
+// the warp's own shared-memory writes and cp.async copies are complete.
+__device__ __forceinline__ bool consumer_sync(uint32_t cbar, uint32_t &cphase) {
+  __syncwarp();
+  if ((threadIdx.x & 31) == 0) mbar_arrive(cbar);
+  const bool ok = mbar_wait(cbar, cphase);
+  cphase ^= 1u;
+  __syncwarp();
+  return ok;
+}
+
+// A work item is (active expert i, pass, 128-row block), ordered that way, so
+// consecutive items share staged activations.  passes[] is the per-expert
+// prefix of passes written by the routing kernel.
+struct Item {
+  int e, pass, blk, cnt, off;
+};
+
+struct ItemCursor {
+  int i = 0;  // active-expert index of the current item
+  __device__ __forceinline__ void seek(const GroupedArgs &a, int w, int nblk) {
+    // smallest i with passes[i+1] * nblk > w (items only move forward)
+    int lo = 0, hi = a.active[0] - 1;
+    while (lo < hi) {
+      const int mid = (lo + hi) >> 1;
+      if (a.passes[mid + 1] * nblk > w) hi = mid;
+      else lo = mid + 1;
+    }
+    i = lo;
+  }
+  __device__ __forceinline__ Item at(const GroupedArgs &a, int w, int nblk) {
+    while (a.passes[i + 1] * nblk <= w) ++i;
+    Item it;
+    it.e = a.active[1 + i];
+    const int local = w - a.passes[i] * nblk;
+    it.pass = local / nblk;
+    it.blk = local % nblk;
+    it.cnt = a.counts[it.e];
+    it.off = a.offsets[it.e];
+    return it;
+  }
+};
 
 template <int SRC, int STAGE, int NT>
-__global__ void __launch_bounds__(kMmaThreads, 2) k_grouped_mma(const GroupedArgs a) {
-  extern __shared__ __align__(16) uint8_t smem[];
+__global__ void __launch_bounds__(kTmaThreads, 1) k_grouped_mma(const GroupedArgs a, int nst) {
+  extern __shared__ __align__(1024) uint8_t smem[];
   constexpr int NTOK = 8 * NT;
   const int K = a.K;
-  const int pitch = 2 * K + 16;  // bytes per staged row; +16 keeps ldmatrix conflict-free
-  __half *xs = reinterpret_cast<__half *>(smem);
-  float *fac = reinterpret_cast<float *>(smem + (size_t)NTOK * pitch);
+  const int pitch = 2 * K + 16;  // bytes per staged activation row; +16 keeps ldmatrix conflict-free
+  uint8_t *ring = smem;
+  __half *xs = reinterpret_cast<__half *>(smem + (size_t)nst * kStageBytes);
+  float *fac = reinterpret_cast<float *>(reinterpret_cast<uint8_t *>(xs) + (size_t)NTOK * pitch);
   int64_t *rows = reinterpret_cast<int64_t *>(fac + NTOK);
+  uint64_t *bars = reinterpret_cast<uint64_t *>(rows + NTOK);  // full[nst], empty[nst], consumer barrier
+  const uint32_t ring_s = (uint32_t)__cvta_generic_to_shared(ring);
+  const uint32_t full0 = (uint32_t)__cvta_generic_to_shared(bars);
+  const uint32_t empty0 = full0 + 8u * nst;
+  const uint32_t cbar = empty0 + 8u * nst;
 
-  const int e = blockIdx.y;
-  const int cnt = a.counts[e];
-  if (cnt == 0) return;
-  const int off = a.offsets[e];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  constexpr bool by_token = SRC == SRC_X16;
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < nst; ++i) {
+      mbar_init(full0 + 8u * i, 1);
+      mbar_init(empty0 + 8u * i, kConsumers);
+    }
+    mbar_init(cbar, kConsumers);
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+  __syncthreads();
 
-  const int tile = blockIdx.x * kMmaWarps + warp;  // 16-row tile of this expert
   const int nsteps = K / 64;
-  const uint4 *ctile = reinterpret_cast<const uint4 *>(a.codes + (size_t)e * a.codes_expert) + (size_t)tile * nsteps * 32 + lane;
-  const uint2 *stile = reinterpret_cast<const uint2 *>(a.scales + (size_t)e * a.scales_expert) + (size_t)tile * nsteps * 8 + (lane >> 2);
-  const float *gl = a.globals + 4 * e;
+  const int nblk = a.n_blocks;
+  const int n_active = a.active[0];
+  const int W = n_active > 0 ? a.passes[n_active] * nblk : 0;
+  const int u0 = (int)((int64_t)blockIdx.x * W / gridDim.x);
+  const int u1 = (int)((int64_t)(blockIdx.x + 1) * W / gridDim.x);
+  const int stages_per_pass = (nsteps + kSPS - 1) / kSPS;
+  ItemCursor cur;
+  if (u0 < u1) cur.seek(a, u0, nblk);
+
+  if (warp == kConsumers) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0) {
+      int slot = 0;
+      uint32_t phase = 0;
+      uint32_t issued = 0, issued_parity = 0;  // per-slot: has a copy, parity of its last phase
+      bool ok = true;
+      for (int u = u0; u < u1 && ok; ++u) {
+        const Item w = cur.at(a, u, nblk);
+        const uint8_t *base = a.codes + (size_t)w.e * a.codes_expert + (size_t)w.blk * nsteps * kStepBytes;
+        {
+          for (int st = 0; st < stages_per_pass; ++st) {
+            if (!mbar_wait(empty0 + 8u * slot, phase ^ 1u)) {
+              ok = false;
+              break;
+            }
+            const uint32_t bytes = (uint32_t)min(kSPS, nsteps - st * kSPS) * kStepBytes;
+            mbar_expect_tx(full0 + 8u * slot, bytes);
+            bulk_g2s(ring_s + (uint32_t)slot * kStageBytes, base + (size_t)st * kStageBytes, bytes, full0 + 8u * slot);
+            issued |= 1u << slot;
+            issued_parity = (issued_parity & ~(1u << slot)) | (phase << slot);
+            if (++slot == nst) {
+              slot = 0;
+              phase ^= 1u;
+            }
+          }
+        }
+      }
+      if (!ok) atomicOr(&a.status[ST_FLAGS], ST_FLAG_TIMEOUT);
+      // Never leave with a copy in flight into this CTA's shared memory.
+      for (int i = 0; i < nst; ++i)
+        if (issued & (1u << i)) mbar_wait(full0 + 8u * i, (issued_parity >> i) & 1u);
+    }
+    return;
+  }
+
+  // ------------------------------------------------------------- consumers
+  constexpr bool by_token = SRC == SRC_X16;
   const uint32_t xs_base = (uint32_t)__cvta_generic_to_shared(xs);
   // ldmatrix row addresses: lanes 0-7 rows 0-7 at k, 8-15 rows 0-7 at k+8,
   // 16-23 rows 8-15 at k, 24-31 rows 8-15 at k+8.
   const int lrow = (lane & 7) + ((lane >> 4) << 3);
   const uint32_t b_addr = xs_base + lrow * pitch + ((lane >> 3) & 1) * 16;
+  const int r = lane >> 2;
+  int slot = 0;
+  uint32_t phase = 0;
+  int staged_e = -1, staged_pass = -1;
+  uint32_t cphase = 0;
+  bool ok = true;
 
-  for (int s0 = off; s0 < off + cnt; s0 += NTOK) {
-    const int ntok = min(NTOK, off + cnt - s0);
-    // Weight prefetch first: it does not depend on the activations.
-    uint4 cbuf[kPF];
-    uint2 sbuf[kPF];
-#pragma unroll
-    for (int p = 0; p < kPF; ++p) {
-      if (p < nsteps) {
-        cbuf[p] = __ldg(ctile + (size_t)p * 32);
-        sbuf[p] = __ldg(stile + (size_t)p * 8);
-      }
-    }
-    __syncthreads();  // the previous tile's staging buffer is free
-    if (threadIdx.x < NTOK) {
-      int64_t rid = -1;
-      if ((int)threadIdx.x < ntok) {
-        const int s = s0 + threadIdx.x;
-        rid = by_token ? (int64_t)(a.sorted_pair[s] / a.top_k) : (int64_t)s;
-      }
-      rows[threadIdx.x] = rid;
-    }
-    __syncthreads();
-    // Stage NTOK activation rows as FP16 (warp w: rows w, w+8, ...).
-    for (int j = warp; j < NTOK; j += kMmaWarps) {
-      const int64_t rid = rows[j];
-      uint8_t *dst = reinterpret_cast<uint8_t *>(xs) + (size_t)j * pitch;
-      if (SRC == SRC_X16) {
-        const __half *src = reinterpret_cast<const __half *>(a.act) + (rid < 0 ? 0 : rid) * K;
-        const uint32_t d0 = (uint32_t)__cvta_generic_to_shared(dst);
-        for (int k = lane * 8; k < K; k += 256) cp_async16(d0 + 2 * k, src + k, rid >= 0);
-        if (lane == 0) fac[j] = rid < 0 ? 0.f : a.act_g[rid];
-        continue;
-      }
-      if (rid < 0) {
-        for (int k = lane * 8; k < K; k += 256) *reinterpret_cast<uint4 *>(dst + 2 * k) = make_uint4(0, 0, 0, 0);
-        if (lane == 0) fac[j] = 0.f;
-        continue;
-      }
-      float f;
-      if (SRC == SRC_H_NVFP4) {
-        f = a.act_g[rid];
-      } else if (SRC == SRC_H_F32) {
-        f = stage_factor(a.act_g[rid]);  // the |h| maximum GEMM1 recorded for this pair
-      } else {
-        float m = 0.f;
-        for (int k = lane * 8; k < K; k += 256) {
-          float v[8];
-          src_load8<SRC>(a.act, a.act_scales, rid, k, K, v);
-#pragma unroll
-          for (int i = 0; i < 8; ++i) m = fmaxf(m, fabsf(v[i]));
+  for (int u = u0; u < u1 && ok; ++u) {
+    const Item w = cur.at(a, u, nblk);
+    const int tile = w.blk * kConsumers + warp;  // 16-row tile of this warp
+    const float *gl = a.globals + 4 * w.e;
+    {
+      const int pass = w.pass;
+      const int s0 = w.off + pass * NTOK;
+      const int ntok = min(NTOK, w.off + w.cnt - s0);
+      if (w.e != staged_e || pass != staged_pass) {
+        // Stage NTOK activation rows as FP16 (warp j: rows j, j+8, ...).
+        if (!consumer_sync(cbar, cphase)) {  // everyone is done with the previous rows
+          ok = false;
+          break;
         }
-        f = stage_factor(warp_max(m));
-      }
-      const float inv = SRC == SRC_H_NVFP4 ? 1.f : __frcp_rn(f);
-      for (int k = lane * 8; k < K; k += 256) {
-        float v[8];
-        src_load8<SRC>(a.act, a.act_scales, rid, k, K, v);
-        *reinterpret_cast<uint4 *>(dst + 2 * k) = to_half8(v, inv);
-      }
-      if (lane == 0) fac[j] = f;
-    }
-    if (SRC == SRC_X16) cp_async_wait_all();
-    __syncthreads();
-
-    float acc[NT][4];
-#pragma unroll
-    for (int j = 0; j < NT; ++j) acc[j][0] = acc[j][1] = acc[j][2] = acc[j][3] = 0.f;
-
-    for (int q = 0; q < nsteps; q += kPF) {
-#pragma unroll
-      for (int p = 0; p < kPF; ++p) {
-        const int qq = q + p;
-        if (qq < nsteps) {
-          const uint4 c = cbuf[p];
-          const uint2 sc = sbuf[p];
-          if (qq + kPF < nsteps) {
-            cbuf[p] = __ldg(ctile + (size_t)(qq + kPF) * 32);
-            sbuf[p] = __ldg(stile + (size_t)(qq + kPF) * 8);
+        if (threadIdx.x < NTOK) {
+          int64_t rid = -1;
+          if ((int)threadIdx.x < ntok) {
+            const int s = s0 + threadIdx.x;
+            rid = by_token ? (int64_t)(a.sorted_pair[s] / a.top_k) : (int64_t)s;
           }
+          rows[threadIdx.x] = rid;
+        }
+        if (!consumer_sync(cbar, cphase)) {
+          ok = false;
+          break;
+        }
+        for (int j = warp; j < NTOK; j += kConsumers) {
+          const int64_t rid = rows[j];
+          uint8_t *dst = reinterpret_cast<uint8_t *>(xs) + (size_t)j * pitch;
+          if (SRC == SRC_X16) {
+            const __half *src = reinterpret_cast<const __half *>(a.act) + (rid < 0 ? 0 : rid) * K;
+            const uint32_t d0 = (uint32_t)__cvta_generic_to_shared(dst);
+            for (int k = lane * 8; k < K; k += 256) cp_async16(d0 + 2 * k, src + k, rid >= 0);
+            if (lane == 0) fac[j] = rid < 0 ? 0.f : a.act_g[rid];
+            continue;
+          }
+          if (rid < 0) {
+            for (int k = lane * 8; k < K; k += 256) *reinterpret_cast<uint4 *>(dst + 2 * k) = make_uint4(0, 0, 0, 0);
+            if (lane == 0) fac[j] = 0.f;
+            continue;
+          }
+          float f;
+          if (SRC == SRC_H_NVFP4) {
+            f = a.act_g[rid];
+          } else if (SRC == SRC_H_F32) {
+            f = stage_factor(a.act_g[rid]);  // the |h| maximum GEMM1 recorded for this pair
+          } else {
+            float m = 0.f;
+            for (int k = lane * 8; k < K; k += 256) {
+              float v[8];
+              src_load8<SRC>(a.act, a.act_scales, rid, k, K, v);
+#pragma unroll
+              for (int i = 0; i < 8; ++i) m = fmaxf(m, fabsf(v[i]));
+            }
+            f = stage_factor(warp_max(m));
+          }
+          const float inv = SRC == SRC_H_NVFP4 ? 1.f : __frcp_rn(f);
+          for (int k = lane * 8; k < K; k += 256) {
+            float v[8];
+            src_load8<SRC>(a.act, a.act_scales, rid, k, K, v);
+            *reinterpret_cast<uint4 *>(dst + 2 * k) = to_half8(v, inv);
+          }
+          if (lane == 0) fac[j] = f;
+        }
+        if (SRC == SRC_X16) cp_async_wait_all();
+        if (!consumer_sync(cbar, cphase)) {
+          ok = false;
+          break;
+        }
+        staged_e = w.e;
+        staged_pass = pass;
+      }
+
+      // Two accumulator sets (even / odd k16 sub-steps) halve the dependent mma chain.
+      float acc[NT][4], acc2[NT][4];
+#pragma unroll
+      for (int j = 0; j < NT; ++j)
+#pragma unroll
+        for (int c = 0; c < 4; ++c) acc[j][c] = acc2[j][c] = 0.f;
+
+      for (int st = 0; st < stages_per_pass; ++st) {
+        if (!mbar_wait(full0 + 8u * slot, phase)) {
+          ok = false;
+          break;
+        }
+        const uint8_t *stage = ring + (size_t)slot * kStageBytes;
+        const int nq = min(kSPS, nsteps - st * kSPS);
+        for (int i4 = 0; i4 < nq; ++i4) {
+          const int q = st * kSPS + i4;
+          const uint4 c = *reinterpret_cast<const uint4 *>(stage + i4 * kStepBytes + warp * 512 + lane * 16);
+          const uint2 sc = *reinterpret_cast<const uint2 *>(stage + i4 * kStepBytes + 4096 + warp * 64 + r * 8);
           const uint32_t cw[4] = {c.x, c.y, c.z, c.w};
           uint32_t spairs[4];  // (s_r, s_r8) of k16 block i as f16x2
           e4m3x4_to_f16x2x2(sc.x, spairs[0], spairs[1]);
@@ -312,72 +484,110 @@ __global__ void __launch_bounds__(kMmaThreads, 2) k_grouped_mma(const GroupedArg
             af[1] = hmul2(af[1], s_hi);
             af[2] = hmul2(af[2], s_lo);
             af[3] = hmul2(af[3], s_hi);
-            const uint32_t kb = (uint32_t)(qq * 64 + i * 16) * 2;
+            const uint32_t kb = (uint32_t)(q * 64 + i * 16) * 2;
+            float(&ac)[NT][4] = (i & 1) ? acc2 : acc;
             if (NT == 2) {
               uint32_t b0, b1, b2, b3;
               ldmatrix_x4(b_addr + kb, b0, b1, b2, b3);
-              mma_16816(acc[0], af, b0, b1);
-              mma_16816(acc[NT - 1], af, b2, b3);
+              mma_16816(ac[0], af, b0, b1);
+              mma_16816(ac[NT - 1], af, b2, b3);
             } else {
               uint32_t b0, b1;
               ldmatrix_x2(b_addr + kb, b0, b1);
-              mma_16816(acc[0], af, b0, b1);
+              mma_16816(ac[0], af, b0, b1);
             }
           }
         }
-      }
-    }
-
-    // Epilogue.  Thread owns rows r = lane/4 and r+8, tokens n = 2*(lane%4) + {0,1} of each n8 tile.
-    const int r = lane >> 2;
-#pragma unroll
-    for (int j = 0; j < NT; ++j) {
-#pragma unroll
-      for (int c = 0; c < 2; ++c) {
-        const int n = j * 8 + 2 * (lane & 3) + c;
-        const bool live = n < ntok;
-        const int s = s0 + n;
-        const float f = live ? fac[n] : 0.f;
-        const float lo = acc[j][c] * f, hi = acc[j][2 + c] * f;
-        float hmax = 0.f;
-        if (STAGE == STAGE_GATED) {
-          const float h = silu_f32(lo * gl[0]) * (hi * gl[1]);
-          if (live) a.out[(size_t)s * a.n_rows + tile * 8 + r] = h;
-          hmax = fabsf(h);
-        } else if (STAGE == STAGE_RELU2) {
-          const float v0 = fmaxf(lo * gl[0], 0.f), v1 = fmaxf(hi * gl[0], 0.f);
-          if (live) {
-            a.out[(size_t)s * a.n_rows + tile * 16 + r] = v0 * v0;
-            a.out[(size_t)s * a.n_rows + tile * 16 + r + 8] = v1 * v1;
-          }
-          hmax = fmaxf(v0 * v0, v1 * v1);
-        } else if (live) {
-          const float w = a.topk_weights[a.sorted_pair[s]] * gl[2];
-          a.out[(size_t)s * a.n_rows + tile * 16 + r] = w * lo;
-          a.out[(size_t)s * a.n_rows + tile * 16 + r + 8] = w * hi;
+        __syncwarp();
+        if (lane == 0) mbar_arrive(empty0 + 8u * slot);
+        if (++slot == nst) {
+          slot = 0;
+          phase ^= 1u;
         }
-        if (STAGE != STAGE_DOWN && a.out_amax != nullptr) {
-          // max over the 8 lanes holding this token (same lane % 4), then one atomic per warp;
-          // a max of non-negative floats is exact and order-free, so the result is deterministic.
-          hmax = fmaxf(hmax, __shfl_xor_sync(0xffffffffu, hmax, 4));
-          hmax = fmaxf(hmax, __shfl_xor_sync(0xffffffffu, hmax, 8));
-          hmax = fmaxf(hmax, __shfl_xor_sync(0xffffffffu, hmax, 16));
-          if (live && r == 0) atomicMax(reinterpret_cast<unsigned *>(a.out_amax) + s, __float_as_uint(hmax));
+      }
+      if (!ok) break;
+#pragma unroll
+      for (int j = 0; j < NT; ++j)
+#pragma unroll
+        for (int c = 0; c < 4; ++c) acc[j][c] += acc2[j][c];
+
+      // Epilogue.  Thread owns rows r and r+8 of its tile, tokens n = 2*(lane%4) + {0,1} of each n8 tile.
+#pragma unroll
+      for (int j = 0; j < NT; ++j) {
+#pragma unroll
+        for (int c = 0; c < 2; ++c) {
+          const int n = j * 8 + 2 * (lane & 3) + c;
+          const bool live = n < ntok;
+          const int s = s0 + n;
+          const float f = live ? fac[n] : 0.f;
+          const float lo = acc[j][c] * f, hi = acc[j][2 + c] * f;
+          float hmax = 0.f;
+          if (STAGE == STAGE_GATED) {
+            const float h = silu_f32(lo * gl[0]) * (hi * gl[1]);
+            if (live) a.out[(size_t)s * a.n_rows + tile * 8 + r] = h;
+            hmax = fabsf(h);
+          } else if (STAGE == STAGE_RELU2) {
+            const float v0 = fmaxf(lo * gl[0], 0.f), v1 = fmaxf(hi * gl[0], 0.f);
+            if (live) {
+              a.out[(size_t)s * a.n_rows + tile * 16 + r] = v0 * v0;
+              a.out[(size_t)s * a.n_rows + tile * 16 + r + 8] = v1 * v1;
+            }
+            hmax = fmaxf(v0 * v0, v1 * v1);
+          } else if (live) {
+            const float wt = a.topk_weights[a.sorted_pair[s]] * gl[2];
+            a.out[(size_t)s * a.n_rows + tile * 16 + r] = wt * lo;
+            a.out[(size_t)s * a.n_rows + tile * 16 + r + 8] = wt * hi;
+          }
+          if (STAGE != STAGE_DOWN && a.out_amax != nullptr) {
+            // max over the 8 lanes holding this token, then one atomic per warp; a max of
+            // non-negative floats is exact and order-free, so the result is deterministic.
+            hmax = fmaxf(hmax, __shfl_xor_sync(0xffffffffu, hmax, 4));
+            hmax = fmaxf(hmax, __shfl_xor_sync(0xffffffffu, hmax, 8));
+            hmax = fmaxf(hmax, __shfl_xor_sync(0xffffffffu, hmax, 16));
+            if (live && r == 0) atomicMax(reinterpret_cast<unsigned *>(a.out_amax) + s, __float_as_uint(hmax));
+          }
         }
       }
     }
   }
+  if (!ok && lane == 0) atomicOr(&a.status[ST_FLAGS], ST_FLAG_TIMEOUT);
 }
 
-size_t mma_smem_bytes(int K, int NT) { return (size_t)8 * NT * (2 * K + 16) + 8 * NT * (4 + 8); }
+static size_t tma_smem_bytes(int K, int NT, int nst) {
+  return (size_t)nst * kStageBytes + (size_t)8 * NT * (2 * K + 16) + 8 * NT * (4 + 8) + 16 * (size_t)nst + 8;
+}
+
+static int num_sms() {
+  int dev = 0, n = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+    return 0;
+  return n;
+}
 
 template <int SRC, int STAGE, int NT>
 static cudaError_t launch_mma_one(const GroupedArgs &a, int rows_total, int E, cudaStream_t s) {
-  const size_t smem = mma_smem_bytes(a.K, NT);
+  constexpr size_t kSmemMax = 227 * 1024;
+  constexpr size_t kSmemHalf = 112 * 1024;  // two CTAs per SM below this
+  // Prefer two CTAs per SM (16 consumer warps) with a 4-stage ring each; else one
+  // CTA with the deepest ring that fits.
+  int ctas_per_sm = 2, nst = 4;
+  if (tma_smem_bytes(a.K, NT, nst) > kSmemHalf) {
+    ctas_per_sm = 1;
+    nst = kMaxStages;
+    while (nst > 2 && tma_smem_bytes(a.K, NT, nst) > kSmemMax) --nst;
+  }
+  const size_t smem = tma_smem_bytes(a.K, NT, nst);
+  if (smem > kSmemMax) return cudaErrorInvalidValue;
   cudaError_t err = cudaFuncSetAttribute(k_grouped_mma<SRC, STAGE, NT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          (int)smem);
   if (err != cudaSuccess) return err;
-  k_grouped_mma<SRC, STAGE, NT><<<dim3(rows_total / (16 * kMmaWarps), E), kMmaThreads, smem, s>>>(a);
+  const int sms = num_sms();
+  if (sms <= 0) return cudaErrorInvalidDevice;
+  GroupedArgs g = a;
+  g.n_blocks = rows_total / (16 * kConsumers);
+  const int units_max = E * g.n_blocks;
+  const int grid = std::max(1, std::min(sms * ctas_per_sm, units_max));
+  k_grouped_mma<SRC, STAGE, NT><<<grid, kTmaThreads, smem, s>>>(g, nst);
   return cudaGetLastError();
 }
 
@@ -405,12 +615,18 @@ static cudaError_t launch_mma_nt(int src, int stage, const GroupedArgs &a, int r
   return cudaErrorInvalidValue;
 }
 
+int mma_tokens_per_pass(int H, int I, bool wide) {
+  const int K = H > I ? H : I;
+  return wide && tma_smem_bytes(K, 2, 4) <= 227 * 1024 ? 16 : 8;
+}
+
 // rows_total: rows of the weight matrix of this stage (2I gated, I for ReLU^2, H down).
-cudaError_t launch_grouped_mma(int src, int stage, const GroupedArgs &a, int rows_total, int E, cudaStream_t s) {
-  if (rows_total % (16 * kMmaWarps) != 0 || a.K % 64 != 0) return cudaErrorInvalidValue;
-  // Two n8 token tiles per pass when their staging fits comfortably, else one.
-  if (mma_smem_bytes(a.K, 2) <= 100 * 1024) return launch_mma_nt<2>(src, stage, a, rows_total, E, s);
-  if (mma_smem_bytes(a.K, 1) <= 200 * 1024) return launch_mma_nt<1>(src, stage, a, rows_total, E, s);
+// ntok: tokens per pass (8 or 16, from mma_tokens_per_pass; must match routing's).
+cudaError_t launch_grouped_mma(int src, int stage, const GroupedArgs &a, int rows_total, int E, int ntok,
+                               cudaStream_t s) {
+  if (rows_total % (16 * kConsumers) != 0 || a.K % 64 != 0) return cudaErrorInvalidValue;
+  if (ntok == 16) return launch_mma_nt<2>(src, stage, a, rows_total, E, s);
+  if (ntok == 8) return launch_mma_nt<1>(src, stage, a, rows_total, E, s);
   return cudaErrorInvalidValue;
 }
 

@@ -19,9 +19,9 @@ constexpr int kRouteWarps = kRouteThreads / 32;
 constexpr int kMaxExperts = 512;
 
 __global__ void __launch_bounds__(kRouteThreads)
-k_route(const int32_t *__restrict__ ids, int P, int E, int pad, int32_t *__restrict__ counts,
+k_route(const int32_t *__restrict__ ids, int P, int E, int pad, int ntok, int32_t *__restrict__ counts,
         int32_t *__restrict__ offsets, int32_t *__restrict__ sorted_pair, int32_t *__restrict__ pair_pos,
-        int32_t *__restrict__ status) {
+        int32_t *__restrict__ active, int32_t *__restrict__ passes, int32_t *__restrict__ status) {
   extern __shared__ int32_t sm[];
   int32_t *hist = sm;                 // [E]
   int32_t *base = hist + E;           // [E+1]
@@ -62,6 +62,33 @@ k_route(const int32_t *__restrict__ ids, int P, int E, int pad, int32_t *__restr
       carry += __shfl_sync(0xffffffffu, incl, 31);
     }
     if (lane == 0) base[E] = carry;
+    // compact, ascending list of experts that received pairs: active[0] = n, active[1..n]
+    int n = 0;
+    for (int e0 = 0; e0 < E; e0 += 32) {
+      const int e = e0 + lane;
+      const bool on = e < E && hist[e] > 0;
+      const unsigned m = __ballot_sync(0xffffffffu, on);
+      if (on) active[1 + n + __popc(m & ((1u << lane) - 1u))] = e;
+      n += __popc(m);
+    }
+    if (lane == 0) active[0] = n;
+    __syncwarp();
+    // passes[i] = sum over the first i active experts of ceil(count / ntok): the
+    // grouped kernels split (expert, pass, row block) work items evenly over CTAs.
+    int carry2 = 0;
+    for (int i0 = 0; i0 < n; i0 += 32) {
+      const int i = i0 + lane;
+      const int v = i < n ? (hist[active[1 + i]] + ntok - 1) / ntok : 0;
+      int incl = v;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int t = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += t;
+      }
+      if (i < n) passes[i] = carry2 + incl - v;
+      carry2 += __shfl_sync(0xffffffffu, incl, 31);
+    }
+    if (lane == 0) passes[n] = carry2;
   }
   __syncthreads();
   for (int e = tid; e <= E; e += kRouteThreads) offsets[e] = base[e];
@@ -111,14 +138,16 @@ k_route(const int32_t *__restrict__ ids, int P, int E, int pad, int32_t *__restr
   }
 }
 
-cudaError_t launch_route(const int32_t *ids, int P, int E, int pad, int32_t *counts, int32_t *offsets,
-                         int32_t *sorted_pair, int32_t *pair_pos, int32_t *status, cudaStream_t s) {
+cudaError_t launch_route(const int32_t *ids, int P, int E, int pad, int ntok, int32_t *counts, int32_t *offsets,
+                         int32_t *sorted_pair, int32_t *pair_pos, int32_t *active, int32_t *passes, int32_t *status,
+                         cudaStream_t s) {
   if (E > kMaxExperts) return cudaErrorInvalidValue;
   const size_t smem = sizeof(int32_t) * ((size_t)3 * E + 1 + (size_t)kRouteWarps * E);
   // Per-device function attribute; cheap and idempotent, so set on every launch.
   cudaError_t err = cudaFuncSetAttribute(k_route, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (err != cudaSuccess) return err;
-  k_route<<<1, kRouteThreads, smem, s>>>(ids, P, E, pad, counts, offsets, sorted_pair, pair_pos, status);
+  k_route<<<1, kRouteThreads, smem, s>>>(ids, P, E, pad, ntok, counts, offsets, sorted_pair, pair_pos, active, passes,
+                                          status);
   return cudaGetLastError();
 }
 

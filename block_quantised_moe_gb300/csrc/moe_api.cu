@@ -84,10 +84,17 @@ moe_status moe_plan_weights(const moe_weight_desc *d, moe_weight_plan *out, size
   L.n13 = d->act == MOE_ACT_SILU_GATED ? 2 * L.I : L.I;
   L.layout = d->wfmt == MOE_W_NVFP4 ? LAYOUT_MMA16x64 : LAYOUT_ROWMAJOR;
   L.off_c13 = 0;
-  L.off_s13 = align_up(L.off_c13 + (size_t)L.E * L.c13_expert());
-  L.off_c2 = align_up(L.off_s13 + (size_t)L.E * L.s13_expert());
-  L.off_s2 = align_up(L.off_c2 + (size_t)L.E * L.c2_expert());
-  L.off_g = align_up(L.off_s2 + (size_t)L.E * L.s2_expert());
+  if (L.layout == LAYOUT_MMA16x64) {  // codes and scales interleaved per block and K step
+    L.off_s13 = align_up(L.off_c13 + (size_t)L.E * L.blk13_expert());
+    L.off_c2 = L.off_s13;
+    L.off_s2 = align_up(L.off_c2 + (size_t)L.E * L.blk2_expert());
+    L.off_g = L.off_s2;
+  } else {
+    L.off_s13 = align_up(L.off_c13 + (size_t)L.E * L.c13_expert());
+    L.off_c2 = align_up(L.off_s13 + (size_t)L.E * L.s13_expert());
+    L.off_s2 = align_up(L.off_c2 + (size_t)L.E * L.c2_expert());
+    L.off_g = align_up(L.off_s2 + (size_t)L.E * L.s2_expert());
+  }
   L.total = align_up(L.off_g + (size_t)L.E * 4 * sizeof(float));
   moe_weight_plan p = new (std::nothrow) moe_weight_plan_s{L};
   if (!p) return MOE_ERR_CAPACITY;
@@ -152,6 +159,8 @@ moe_status moe_plan(const moe_caps *c, moe_plan_t *out, size_t *scratch_bytes, i
   S.offsets = take(4 * (size_t)(L.E + 1));
   S.sorted = take(4 * (size_t)S.cap_sorted);
   S.pair_pos = take(4 * (size_t)Pmax);
+  S.active = take(4 * (size_t)(L.E + 1));
+  S.passes = take(4 * (size_t)(L.E + 1));
   if (P.afmt == MOE_A_NVFP4) {
     S.xq_codes = take((size_t)T * L.H / 2);
     S.xq_scales = take((size_t)T * L.H / 16);
@@ -235,13 +244,22 @@ static moe_status run_impl(moe_binding b, cudaStream_t stream, cudaEvent_t *ev) 
   cudaError_t err;
 
   if ((err = mark(MOE_STAGE_ROUTE)) != cudaSuccess) return MOE_ERR_CUDA;
-  if ((err = launch_route(b->ids, T * K, E, P.pad, counts, offsets, sorted, pair_pos, status, stream)) != cudaSuccess)
+  int32_t *active = at<int32_t>(sc, S.active);
+  int32_t *passes = at<int32_t>(sc, S.passes);
+  // one n8 token tile per pass when the plan expects at most 8 pairs per expert
+  const bool wide = (int64_t)P.max_tokens * K > (int64_t)8 * E;
+  const int ntok = mma_tokens_per_pass(H, I, wide);
+  if ((err = launch_route(b->ids, T * K, E, P.pad, ntok, counts, offsets, sorted, pair_pos, active, passes,
+                          status, stream)) != cudaSuccess)
     return MOE_ERR_CUDA;
 
   GroupedArgs a{};
   a.counts = counts;
   a.offsets = offsets;
   a.sorted_pair = sorted;
+  a.active = active;
+  a.passes = passes;
+  a.status = status;
   a.top_k = K;
   a.topk_weights = b->w;
   a.globals = reinterpret_cast<const float *>(b->packed + L.off_g);
@@ -283,13 +301,13 @@ static moe_status run_impl(moe_binding b, cudaStream_t stream, cudaEvent_t *ev) 
   if (mark(MOE_STAGE_GEMM1) != cudaSuccess) return MOE_ERR_CUDA;
   a.codes = b->packed + L.off_c13;
   a.scales = b->packed + L.off_s13;
-  a.codes_expert = L.c13_expert();
+  a.codes_expert = mma ? L.blk13_expert() : L.c13_expert();
   a.scales_expert = L.s13_expert();
   a.K = H;
   a.n_rows = I;
   a.out = h;
   const int stage1 = L.act == MOE_ACT_SILU_GATED ? STAGE_GATED : STAGE_RELU2;
-  err = mma ? launch_grouped_mma(src1, stage1, a, L.n13, E, stream)
+  err = mma ? launch_grouped_mma(src1, stage1, a, L.n13, E, ntok, stream)
             : launch_grouped_cc(L.wfmt, src1, stage1, a, E, stream);
   a.out_amax = nullptr;
   if (err != cudaSuccess) return MOE_ERR_CUDA;
@@ -319,13 +337,13 @@ static moe_status run_impl(moe_binding b, cudaStream_t stream, cudaEvent_t *ev) 
   // GEMM2 * topk_weight -> partials, then the ordered combine
   a.codes = b->packed + L.off_c2;
   a.scales = b->packed + L.off_s2;
-  a.codes_expert = L.c2_expert();
+  a.codes_expert = mma ? L.blk2_expert() : L.c2_expert();
   a.scales_expert = L.s2_expert();
   a.K = I;
   a.n_rows = H;
   a.out = part;
   if (mark(MOE_STAGE_GEMM2) != cudaSuccess) return MOE_ERR_CUDA;
-  err = mma ? launch_grouped_mma(src2, STAGE_DOWN, a, H, E, stream)
+  err = mma ? launch_grouped_mma(src2, STAGE_DOWN, a, H, E, ntok, stream)
             : launch_grouped_cc(L.wfmt, src2, STAGE_DOWN, a, E, stream);
   if (err != cudaSuccess) return MOE_ERR_CUDA;
   if (mark(MOE_STAGE_COMBINE) != cudaSuccess) return MOE_ERR_CUDA;
