@@ -357,7 +357,7 @@ def main():
     hbm, peak_kind = peaks()
     dom_bytes = kernel_bytes.get(dom_name, 0.0)
     achieved = dom_bytes / (stage_ms[dom] * 1e-3) / 1e9 if stage_ms[dom] > 0 else 0.0
-    rec, src_hash = traffic_record("k_grouped_cc.cu")
+    rec, src_hash = traffic_record("k_grouped_mma.cu")
     traffic = None
     if rec and rec.get("src_sha256_16") == src_hash and rec.get("workload") == f"{args.config} T={T}":
         traffic = rec.get("per_launch", {}).get(dom_name)
