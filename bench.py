@@ -52,6 +52,8 @@ def parse():
     ap.add_argument("--e2e-steps", type=int, default=300)
     ap.add_argument("--cpu-budget-s", type=float, default=12.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--experts", type=int, default=None,
+                    help="override the workload's expert count (small captures for ncu)")
     return ap.parse_args()
 
 
@@ -266,7 +268,9 @@ def run_reference(args, cfg, world, rank):
 def main():
     args = parse()
     from block_quantised_moe_gb300 import synth
-    cfg = synth.CONFIGS[args.config]
+    cfg = dict(synth.CONFIGS[args.config])
+    if args.experts:
+        cfg["E"] = args.experts
     world, rank, local = dist_setup(args)
     if args.impl == "reference":
         run_reference(args, cfg, world, rank)
@@ -382,7 +386,7 @@ def main():
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms / args.steps,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
         "data": "synthetic",
-        "config": {"workload": f"{args.config} T={T}", "experts": E, "hidden": H, "intermediate": I,
+        "config": {"workload": f"{args.config} T={T}" + (f" E={E}" if args.experts else ""), "experts": E, "hidden": H, "intermediate": I,
                    "top_k": K, "weights": cfg["wfmt"], "activations": afmt, "act": cfg["act"],
                    "tokens": T, "parallelism": f"replicas x{world}",
                    "l2": f"{R} layer replicas x {packed0.packed.numel() / 1e6:.0f} MB rotated per step (> L2)",

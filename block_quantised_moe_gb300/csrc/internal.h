@@ -41,10 +41,11 @@ struct WeightLayout {
 // Scratch owned by the caller and carved by the plan (offsets in bytes).
 struct ScratchLayout {
   int64_t cap_sorted = 0;  // rows of the padded, expert-sorted pair list
-  size_t status = 0, counts = 0, offsets = 0, sorted = 0, pair_pos = 0, active = 0, passes = 0;
+  size_t status = 0, counts = 0, offsets = 0, sorted = 0, pair_pos = 0, active = 0, passes = 0, large = 0, large_tiles = 0;
   size_t xq_codes = 0, xq_scales = 0, xq_g = 0;
   size_t h = 0, hq_codes = 0, hq_scales = 0, hq_g = 0;
   size_t x16 = 0, xfac = 0, hamax = 0;  // tensor-core path: FP16 x, its factors, per-pair max |h|
+  size_t h16 = 0, h16fac = 0;           // tcgen05 path: FP16 h rows and their factors
   size_t part = 0, total = 0;
 };
 
@@ -72,6 +73,9 @@ struct GroupedArgs {
   const int32_t *counts, *offsets, *sorted_pair;
   const int32_t *active;  // [0] = number of experts with pairs, [1..] their ids (ascending)
   const int32_t *passes;  // [i] = passes of active experts before i (prefix, n_active + 1 entries)
+  const int32_t *large;        // experts for the tcgen05 kernel: [0] = n, [1..] ids
+  const int32_t *large_tiles;  // [i] = 128-token tiles of large experts before i (prefix)
+  int act_by_token;            // tcgen05 kernel: B rows indexed by token (GEMM1) or by slot (GEMM2)
   int32_t *status;        // device status word (timeout flag)
   int top_k;
   const float *topk_weights;
@@ -79,10 +83,11 @@ struct GroupedArgs {
   float *out;
 };
 
-// ntok: tokens per pass of the tensor-core kernels (for the per-expert pass prefix).
-cudaError_t launch_route(const int32_t *ids, int P, int E, int pad, int ntok, int32_t *counts, int32_t *offsets,
-                         int32_t *sorted_pair, int32_t *pair_pos, int32_t *active, int32_t *passes, int32_t *status,
-                         cudaStream_t s);
+// ntok: tokens per pass of the register-dequant kernel; experts with at least
+// large_min pairs go to the tcgen05 kernel in tiles of large_tile tokens.
+cudaError_t launch_route(const int32_t *ids, int P, int E, int pad, int ntok, int large_min, int large_tile,
+                         int32_t *counts, int32_t *offsets, int32_t *sorted_pair, int32_t *pair_pos, int32_t *active,
+                         int32_t *passes, int32_t *large, int32_t *large_tiles, int32_t *status, cudaStream_t s);
 
 cudaError_t launch_grouped_cc(int wfmt, int src, int stage, const GroupedArgs &a, int E, cudaStream_t s);
 
@@ -96,6 +101,12 @@ cudaError_t launch_grouped_mma(int src, int stage, const GroupedArgs &a, int row
 
 cudaError_t launch_stage_x16(int src, const void *act, const uint8_t *act_scales, const float *act_g, int T, int K,
                              __half *x16, float *fac, float *zero, int64_t zero_n, cudaStream_t s);
+
+// tcgen05 kernels for experts with many pairs (NVFP4 weights, FP16 operands).
+bool tc_supported(int rows_total, int K);
+cudaError_t launch_grouped_tc(int stage, const GroupedArgs &a, int rows_total, int E, cudaStream_t s);
+cudaError_t launch_stage_h16(int src, const void *act, const uint8_t *act_scales, const float *act_g, int K,
+                             int64_t rows, const int32_t *rows_dev, __half *h16, float *fac, cudaStream_t s);
 
 cudaError_t launch_combine(const float *part, int H, const int32_t *pair_pos, int T, int K, void *out_bf16,
                            cudaStream_t s);

@@ -34,6 +34,8 @@
 
 #include "common.cuh"
 #include "internal.h"
+#include "dequant.cuh"
+#include "sync.cuh"
 
 namespace bqmoe {
 
@@ -54,95 +56,6 @@ __device__ __forceinline__ void ldmatrix_x4(uint32_t addr, uint32_t &r0, uint32_
 
 __device__ __forceinline__ void ldmatrix_x2(uint32_t addr, uint32_t &r0, uint32_t &r1) {
   asm volatile("ldmatrix.sync.aligned.m8n8.x2.shared.b16 {%0,%1}, [%2];" : "=r"(r0), "=r"(r1) : "r"(addr));
-}
-
-// Four bytes of E2M1 pairs -> four f16x2 (byte j -> r[j], low nibble in the low half).
-__device__ __forceinline__ void e2m1x8_to_f16x2x4(uint32_t w, uint32_t (&r)[4]) {
-  asm("{\n\t.reg .b8 b0, b1, b2, b3;\n\t"
-      "mov.b32 {b0, b1, b2, b3}, %4;\n\t"
-      "cvt.rn.f16x2.e2m1x2 %0, b0;\n\t"
-      "cvt.rn.f16x2.e2m1x2 %1, b1;\n\t"
-      "cvt.rn.f16x2.e2m1x2 %2, b2;\n\t"
-      "cvt.rn.f16x2.e2m1x2 %3, b3;\n\t}"
-      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
-      : "r"(w));
-}
-
-// Four E4M3 bytes -> two f16x2: bytes (0,1) -> lo, bytes (2,3) -> hi, first byte in the low half.
-__device__ __forceinline__ void e4m3x4_to_f16x2x2(uint32_t w, uint32_t &lo, uint32_t &hi) {
-  asm("{\n\t.reg .b16 h0, h1;\n\t"
-      "mov.b32 {h0, h1}, %2;\n\t"
-      "cvt.rn.f16x2.e4m3x2 %0, h0;\n\t"
-      "cvt.rn.f16x2.e4m3x2 %1, h1;\n\t}"
-      : "=r"(lo), "=r"(hi)
-      : "r"(w));
-}
-
-__device__ __forceinline__ uint32_t hmul2(uint32_t a, uint32_t b) {
-  __half2 r = __hmul2(*reinterpret_cast<__half2 *>(&a), *reinterpret_cast<__half2 *>(&b));
-  return *reinterpret_cast<uint32_t *>(&r);
-}
-
-__device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel) {
-  uint32_t r;
-  asm("prmt.b32 %0, %1, %2, %3;" : "=r"(r) : "r"(a), "r"(b), "r"(sel));
-  return r;
-}
-
-// Power-of-two factor for staging a row with largest magnitude `amax` in FP16:
-// amax / f lands in [2^14, 2^15).
-__device__ __forceinline__ float stage_factor(float amax) {
-  if (!(amax > 0.f)) return 1.f;
-  int k = floor_log2_f32(amax) - 14;
-  k = max(-126, min(127, k));
-  return exp2i_f32(k);
-}
-
-__device__ __forceinline__ void cp_async16(uint32_t dst, const void *src, bool valid) {
-  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src), "r"(valid ? 16 : 0));
-}
-__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
-
-// Eight activation values (k % 8 == 0) of a quantised / FP32 row as FP32.
-template <int SRC>
-__device__ __forceinline__ void src_load8(const void *act, const uint8_t *act_scales, int64_t rid, int k, int K,
-                                          float (&v)[8]) {
-  if (SRC == SRC_X_BF16) {
-    const uint4 r = *reinterpret_cast<const uint4 *>(reinterpret_cast<const __nv_bfloat16 *>(act) + rid * K + k);
-    const uint32_t w[4] = {r.x, r.y, r.z, r.w};
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      v[2 * i] = __uint_as_float(w[i] << 16);
-      v[2 * i + 1] = __uint_as_float(w[i] & 0xFFFF0000u);
-    }
-  } else if (SRC == SRC_H_F32) {
-    const float4 p = *reinterpret_cast<const float4 *>(reinterpret_cast<const float *>(act) + rid * K + k);
-    const float4 q = *reinterpret_cast<const float4 *>(reinterpret_cast<const float *>(act) + rid * K + k + 4);
-    v[0] = p.x; v[1] = p.y; v[2] = p.z; v[3] = p.w; v[4] = q.x; v[5] = q.y; v[6] = q.z; v[7] = q.w;
-  } else if (SRC == SRC_X_NVFP4 || SRC == SRC_H_NVFP4) {
-    // E2M1 * E4M3 only (exact in FP16); the row's FP32 global becomes the factor.
-    const uint32_t w = *reinterpret_cast<const uint32_t *>(reinterpret_cast<const uint8_t *>(act) + rid * (K / 2) + k / 2);
-    float f[8];
-    e2m1x8_to_f32(w, f);
-    const float s = e4m3_to_f32(act_scales[rid * (K / 16) + k / 16]);
-#pragma unroll
-    for (int i = 0; i < 8; ++i) v[i] = f[i] * s;
-  } else {  // MXFP8
-    const uint2 w = *reinterpret_cast<const uint2 *>(reinterpret_cast<const uint8_t *>(act) + rid * K + k);
-    const float s = e8m0_to_f32(act_scales[rid * (K / 32) + k / 32]);
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      v[i] = e4m3_to_f32((w.x >> (8 * i)) & 0xFFu) * s;
-      v[4 + i] = e4m3_to_f32((w.y >> (8 * i)) & 0xFFu) * s;
-    }
-  }
-}
-
-__device__ __forceinline__ uint4 to_half8(const float (&v)[8], float inv) {
-  __align__(16) __half2 h[4];
-#pragma unroll
-  for (int i = 0; i < 4; ++i) h[i] = __floats2half2_rn(v[2 * i] * inv, v[2 * i + 1] * inv);
-  return *reinterpret_cast<uint4 *>(h);
 }
 
 // ---------------------------------------------------------- x -> FP16 rows
@@ -209,45 +122,6 @@ constexpr int kStepBytes = 4608;  // one 64-K step of a 128-row block
 constexpr int kSPS = 4;           // K steps per ring stage
 constexpr int kStageBytes = kStepBytes * kSPS;
 constexpr int kMaxStages = 8;
-constexpr unsigned long long kWaitNs = 2000000000ull;  // 2 s
-
-__device__ __forceinline__ unsigned long long globaltimer_ns() {
-  unsigned long long t;
-  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
-  return t;
-}
-__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
-  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count));
-}
-__device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes) {
-  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes) : "memory");
-}
-__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
-  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
-}
-__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
-  uint32_t ok;
-  asm volatile(
-      "{\n\t.reg .pred p;\n\tmbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\tselp.u32 %0, 1, 0, p;\n\t}"
-      : "=r"(ok)
-      : "r"(bar), "r"(parity)
-      : "memory");
-  return ok != 0;
-}
-// Bounded wait; false on timeout.
-__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity) {
-  if (mbar_try_wait(bar, parity)) return true;
-  const unsigned long long t0 = globaltimer_ns();
-  for (uint32_t it = 1;; ++it) {
-    if (mbar_try_wait(bar, parity)) return true;
-    if ((it & 255u) == 0 && globaltimer_ns() - t0 > kWaitNs) return false;
-  }
-}
-__device__ __forceinline__ void bulk_g2s(uint32_t dst, const void *src, uint32_t bytes, uint32_t bar) {
-  asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
-               "l"(src), "r"(bytes), "r"(bar)
-               : "memory");
-}
 // Barrier among the consumer warps only (the producer never joins), built on an
 // mbarrier so that its wait is bounded too.  Lane 0 of each warp arrives after
 // the warp's own shared-memory writes and cp.async copies are complete.

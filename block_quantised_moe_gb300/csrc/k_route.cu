@@ -19,9 +19,10 @@ constexpr int kRouteWarps = kRouteThreads / 32;
 constexpr int kMaxExperts = 512;
 
 __global__ void __launch_bounds__(kRouteThreads)
-k_route(const int32_t *__restrict__ ids, int P, int E, int pad, int ntok, int32_t *__restrict__ counts,
-        int32_t *__restrict__ offsets, int32_t *__restrict__ sorted_pair, int32_t *__restrict__ pair_pos,
-        int32_t *__restrict__ active, int32_t *__restrict__ passes, int32_t *__restrict__ status) {
+k_route(const int32_t *__restrict__ ids, int P, int E, int pad, int ntok, int large_min, int large_tile,
+        int32_t *__restrict__ counts, int32_t *__restrict__ offsets, int32_t *__restrict__ sorted_pair,
+        int32_t *__restrict__ pair_pos, int32_t *__restrict__ active, int32_t *__restrict__ passes,
+        int32_t *__restrict__ large, int32_t *__restrict__ large_tiles, int32_t *__restrict__ status) {
   extern __shared__ int32_t sm[];
   int32_t *hist = sm;                 // [E]
   int32_t *base = hist + E;           // [E+1]
@@ -62,33 +63,48 @@ k_route(const int32_t *__restrict__ ids, int P, int E, int pad, int ntok, int32_
       carry += __shfl_sync(0xffffffffu, incl, 31);
     }
     if (lane == 0) base[E] = carry;
-    // compact, ascending list of experts that received pairs: active[0] = n, active[1..n]
-    int n = 0;
+    // Two compact, ascending expert lists: "small" experts (1..large_min-1 pairs)
+    // with the prefix of their passes of ntok tokens, and "large" experts
+    // (>= large_min pairs) with the prefix of their tiles of large_tile tokens.
+    // The grouped kernels split (expert, pass | tile, row block) items evenly.
+    int ns = 0, nl = 0, cs = 0, cl = 0;
     for (int e0 = 0; e0 < E; e0 += 32) {
       const int e = e0 + lane;
-      const bool on = e < E && hist[e] > 0;
-      const unsigned m = __ballot_sync(0xffffffffu, on);
-      if (on) active[1 + n + __popc(m & ((1u << lane) - 1u))] = e;
-      n += __popc(m);
-    }
-    if (lane == 0) active[0] = n;
-    __syncwarp();
-    // passes[i] = sum over the first i active experts of ceil(count / ntok): the
-    // grouped kernels split (expert, pass, row block) work items evenly over CTAs.
-    int carry2 = 0;
-    for (int i0 = 0; i0 < n; i0 += 32) {
-      const int i = i0 + lane;
-      const int v = i < n ? (hist[active[1 + i]] + ntok - 1) / ntok : 0;
-      int incl = v;
+      const int c = e < E ? hist[e] : 0;
+      const bool sm = c > 0 && c < large_min, lg = c >= large_min;
+      const unsigned msm = __ballot_sync(0xffffffffu, sm), mlg = __ballot_sync(0xffffffffu, lg);
+      const unsigned below = (1u << lane) - 1u;
+      const int vs = sm ? (c + ntok - 1) / ntok : 0, vl = lg ? (c + large_tile - 1) / large_tile : 0;
+      int is = vs, il = vl;
 #pragma unroll
       for (int o = 1; o < 32; o <<= 1) {
-        const int t = __shfl_up_sync(0xffffffffu, incl, o);
-        if (lane >= o) incl += t;
+        const int ts = __shfl_up_sync(0xffffffffu, is, o), tl = __shfl_up_sync(0xffffffffu, il, o);
+        if (lane >= o) {
+          is += ts;
+          il += tl;
+        }
       }
-      if (i < n) passes[i] = carry2 + incl - v;
-      carry2 += __shfl_sync(0xffffffffu, incl, 31);
+      if (sm) {
+        const int i = ns + __popc(msm & below);
+        active[1 + i] = e;
+        passes[i] = cs + is - vs;
+      }
+      if (lg) {
+        const int i = nl + __popc(mlg & below);
+        large[1 + i] = e;
+        large_tiles[i] = cl + il - vl;
+      }
+      ns += __popc(msm);
+      nl += __popc(mlg);
+      cs += __shfl_sync(0xffffffffu, is, 31);
+      cl += __shfl_sync(0xffffffffu, il, 31);
     }
-    if (lane == 0) passes[n] = carry2;
+    if (lane == 0) {
+      active[0] = ns;
+      passes[ns] = cs;
+      large[0] = nl;
+      large_tiles[nl] = cl;
+    }
   }
   __syncthreads();
   for (int e = tid; e <= E; e += kRouteThreads) offsets[e] = base[e];
@@ -138,16 +154,16 @@ k_route(const int32_t *__restrict__ ids, int P, int E, int pad, int ntok, int32_
   }
 }
 
-cudaError_t launch_route(const int32_t *ids, int P, int E, int pad, int ntok, int32_t *counts, int32_t *offsets,
-                         int32_t *sorted_pair, int32_t *pair_pos, int32_t *active, int32_t *passes, int32_t *status,
-                         cudaStream_t s) {
+cudaError_t launch_route(const int32_t *ids, int P, int E, int pad, int ntok, int large_min, int large_tile,
+                         int32_t *counts, int32_t *offsets, int32_t *sorted_pair, int32_t *pair_pos, int32_t *active,
+                         int32_t *passes, int32_t *large, int32_t *large_tiles, int32_t *status, cudaStream_t s) {
   if (E > kMaxExperts) return cudaErrorInvalidValue;
   const size_t smem = sizeof(int32_t) * ((size_t)3 * E + 1 + (size_t)kRouteWarps * E);
   // Per-device function attribute; cheap and idempotent, so set on every launch.
   cudaError_t err = cudaFuncSetAttribute(k_route, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (err != cudaSuccess) return err;
-  k_route<<<1, kRouteThreads, smem, s>>>(ids, P, E, pad, ntok, counts, offsets, sorted_pair, pair_pos, active, passes,
-                                          status);
+  k_route<<<1, kRouteThreads, smem, s>>>(ids, P, E, pad, ntok, large_min, large_tile, counts, offsets, sorted_pair,
+                                          pair_pos, active, passes, large, large_tiles, status);
   return cudaGetLastError();
 }
 

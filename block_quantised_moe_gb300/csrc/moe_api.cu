@@ -21,6 +21,8 @@ struct moe_weight_plan_s {
 struct moe_plan_s {
   WeightLayout L;
   int K = 0, max_tokens = 0, afmt = 0, pad = 16;
+  bool tc_on = false;  // experts with >= large_min pairs run on the tcgen05 kernel
+  int large_min = 0x7FFFFFFF;
   ScratchLayout S;
 };
 
@@ -40,6 +42,7 @@ namespace {
 constexpr int kMaxExperts = 512;
 constexpr int kMaxTopK = 16;
 constexpr int kPad = 16;  // expert groups are padded to this many pairs
+constexpr int kLargeMin = 32;  // pairs from which an expert runs on the tcgen05 kernel
 
 bool aligned(const void *p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
 
@@ -161,6 +164,8 @@ moe_status moe_plan(const moe_caps *c, moe_plan_t *out, size_t *scratch_bytes, i
   S.pair_pos = take(4 * (size_t)Pmax);
   S.active = take(4 * (size_t)(L.E + 1));
   S.passes = take(4 * (size_t)(L.E + 1));
+  S.large = take(4 * (size_t)(L.E + 1));
+  S.large_tiles = take(4 * (size_t)(L.E + 1));
   if (P.afmt == MOE_A_NVFP4) {
     S.xq_codes = take((size_t)T * L.H / 2);
     S.xq_scales = take((size_t)T * L.H / 16);
@@ -182,6 +187,14 @@ moe_status moe_plan(const moe_caps *c, moe_plan_t *out, size_t *scratch_bytes, i
     S.x16 = take(2 * (size_t)T * L.H);
     S.xfac = take(4 * (size_t)T);
     S.hamax = take(4 * (size_t)S.cap_sorted);
+    // Plans for batches of 1024+ (token, slot) pairs send experts with at least
+    // kLargeMin pairs to the tcgen05 kernel (dense tiles of 128 tokens).
+    P.tc_on = Pmax >= 1024 && tc_supported(L.n13, L.H) && tc_supported(L.H, L.I);
+    if (P.tc_on) {
+      P.large_min = kLargeMin;
+      S.h16 = take(2 * (size_t)S.cap_sorted * L.I);
+      S.h16fac = take(4 * (size_t)S.cap_sorted);
+    }
   }
   S.part = take(4 * (size_t)S.cap_sorted * L.H);
   S.total = o;
@@ -249,8 +262,10 @@ static moe_status run_impl(moe_binding b, cudaStream_t stream, cudaEvent_t *ev) 
   // one n8 token tile per pass when the plan expects at most 8 pairs per expert
   const bool wide = (int64_t)P.max_tokens * K > (int64_t)8 * E;
   const int ntok = mma_tokens_per_pass(H, I, wide);
-  if ((err = launch_route(b->ids, T * K, E, P.pad, ntok, counts, offsets, sorted, pair_pos, active, passes,
-                          status, stream)) != cudaSuccess)
+  int32_t *large = at<int32_t>(sc, S.large);
+  int32_t *large_tiles = at<int32_t>(sc, S.large_tiles);
+  if ((err = launch_route(b->ids, T * K, E, P.pad, ntok, P.large_min, 128, counts, offsets, sorted, pair_pos, active,
+                          passes, large, large_tiles, status, stream)) != cudaSuccess)
     return MOE_ERR_CUDA;
 
   GroupedArgs a{};
@@ -259,6 +274,8 @@ static moe_status run_impl(moe_binding b, cudaStream_t stream, cudaEvent_t *ev) 
   a.sorted_pair = sorted;
   a.active = active;
   a.passes = passes;
+  a.large = large;
+  a.large_tiles = large_tiles;
   a.status = status;
   a.top_k = K;
   a.topk_weights = b->w;
@@ -309,6 +326,10 @@ static moe_status run_impl(moe_binding b, cudaStream_t stream, cudaEvent_t *ev) 
   const int stage1 = L.act == MOE_ACT_SILU_GATED ? STAGE_GATED : STAGE_RELU2;
   err = mma ? launch_grouped_mma(src1, stage1, a, L.n13, E, ntok, stream)
             : launch_grouped_cc(L.wfmt, src1, stage1, a, E, stream);
+  if (err == cudaSuccess && P.tc_on) {
+    a.act_by_token = 1;
+    err = launch_grouped_tc(stage1, a, L.n13, E, stream);
+  }
   a.out_amax = nullptr;
   if (err != cudaSuccess) return MOE_ERR_CUDA;
 
@@ -335,6 +356,11 @@ static moe_status run_impl(moe_binding b, cudaStream_t stream, cudaEvent_t *ev) 
   if (err != cudaSuccess) return MOE_ERR_CUDA;
 
   // GEMM2 * topk_weight -> partials, then the ordered combine
+  if (P.tc_on) {  // FP16 rows of h (or of its re-quantised codes) for the tcgen05 GEMM2
+    err = launch_stage_h16(src2, a.act, a.act_scales, a.act_g, I, S.cap_sorted, offsets + E, at<__half>(sc, S.h16),
+                           at<float>(sc, S.h16fac), stream);
+    if (err != cudaSuccess) return MOE_ERR_CUDA;
+  }
   a.codes = b->packed + L.off_c2;
   a.scales = b->packed + L.off_s2;
   a.codes_expert = mma ? L.blk2_expert() : L.c2_expert();
@@ -345,6 +371,14 @@ static moe_status run_impl(moe_binding b, cudaStream_t stream, cudaEvent_t *ev) 
   if (mark(MOE_STAGE_GEMM2) != cudaSuccess) return MOE_ERR_CUDA;
   err = mma ? launch_grouped_mma(src2, STAGE_DOWN, a, H, E, ntok, stream)
             : launch_grouped_cc(L.wfmt, src2, STAGE_DOWN, a, E, stream);
+  if (err == cudaSuccess && P.tc_on) {
+    GroupedArgs t = a;
+    t.act = at<__half>(sc, S.h16);
+    t.act_scales = nullptr;
+    t.act_g = at<float>(sc, S.h16fac);
+    t.act_by_token = 0;
+    err = launch_grouped_tc(STAGE_DOWN, t, H, E, stream);
+  }
   if (err != cudaSuccess) return MOE_ERR_CUDA;
   if (mark(MOE_STAGE_COMBINE) != cudaSuccess) return MOE_ERR_CUDA;
   if ((err = launch_combine(part, H, pair_pos, T, K, b->out, stream)) != cudaSuccess) return MOE_ERR_CUDA;

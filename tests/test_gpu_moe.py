@@ -125,3 +125,33 @@ def test_prefill_e256_h7168(lib, name):
     tl.check_close(out.float().cpu().numpy()[toks], y_ref, name)
     # every output row is finite and no row was left unwritten
     assert torch.isfinite(out.float()).all()
+
+
+# ------------------------------------------- tcgen05 path (experts with many pairs)
+
+TC_MODES = [("nvfp4", "silu", "bf16"), ("nvfp4", "silu", "nvfp4"), ("nvfp4", "silu", "mxfp8"),
+            ("nvfp4", "relu2", "bf16")]
+
+
+@pytest.mark.parametrize("wfmt,act,afmt", TC_MODES)
+@pytest.mark.parametrize("T", [512, 700])
+def test_tcgen05_path_small_layer(lib, wfmt, act, afmt, T):
+    # 8 experts x top-2: ~128-175 pairs per expert -> ragged 128-token tiles on the tcgen05 kernel
+    cfg = dict(cfg_of("tiny_e8_h256_i512_k2"))
+    E, H, I, K = cfg["E"], cfg["H"], cfg["I"], cfg["K"]
+    ck, packed = gpu_layer(lib, E, H, I, wfmt, act)
+    x, ids, w = tl.make_inputs(cfg, T, seed=T)
+    out, _, _ = run(lib, packed, x, ids, w, K, afmt)
+    y_ref = tl.oracle_forward(ck, H, I, x, ids, w, afmt)
+    tl.check_close(out.float().cpu().numpy(), y_ref, f"tcgen05 {wfmt}/{act}/{afmt} T={T}")
+
+
+def test_tcgen05_and_decode_kernels_share_a_forward(lib):
+    # skewed routing: hot experts (>= 32 pairs) on tcgen05, the rest on the decode kernel
+    cfg = dict(E=64, H=256, I=512, K=4, zipf=1.5)
+    ck, packed = gpu_layer(lib, cfg["E"], cfg["H"], cfg["I"], "nvfp4", "silu")
+    x, ids, w = tl.make_inputs(cfg, 256, seed=5)
+    counts = np.bincount(ids.cpu().numpy().reshape(-1), minlength=cfg["E"])
+    assert counts.max() >= 32 and (counts[counts > 0] < 32).any()
+    out, _, _ = run(lib, packed, x, ids, w, cfg["K"], "bf16")
+    tl.check_close(out.float().cpu().numpy(), tl.oracle_forward(ck, cfg["H"], cfg["I"], x, ids, w, "bf16"))
