@@ -106,6 +106,13 @@ __device__ __forceinline__ float exp2i_f32(int X) {
   return X >= -126 ? __uint_as_float((uint32_t)(X + 127) << 23) : __uint_as_float(0x00400000u);
 }
 
+// ------------------------------------------------- programmatic dependent launch
+
+// Let the next kernel in the stream start launching (see launch.h for the protocol).
+__device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+// Wait until the preceding kernel has completed and its writes are visible.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
 // --------------------------------------------------------------- misc
 
 __device__ __forceinline__ float silu_f32(float a) { return a * (1.0f / (1.0f + expf(-a))); }

@@ -1,6 +1,7 @@
 // Host-side layouts and kernel launchers of libmoe (internal; not part of the ABI).
 #pragma once
 
+#include <cuda_bf16.h>
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
 #include <stddef.h>
@@ -83,11 +84,22 @@ struct GroupedArgs {
   float *out;
 };
 
+// Optional staging done by extra CTAs of the routing launch: BF16 x [T][H] ->
+// FP16 rows + per-row factor, and clearing of `zero` (zero_n floats).
+struct RouteStaging {
+  const __nv_bfloat16 *x;
+  int T, H;
+  __half *x16;
+  float *xfac, *zero;
+  int64_t zero_n;
+};
+
 // ntok: tokens per pass of the register-dequant kernel; experts with at least
 // large_min pairs go to the tcgen05 kernel in tiles of large_tile tokens.
 cudaError_t launch_route(const int32_t *ids, int P, int E, int pad, int ntok, int large_min, int large_tile,
                          int32_t *counts, int32_t *offsets, int32_t *sorted_pair, int32_t *pair_pos, int32_t *active,
-                         int32_t *passes, int32_t *large, int32_t *large_tiles, int32_t *status, cudaStream_t s);
+                         int32_t *passes, int32_t *large, int32_t *large_tiles, int32_t *status,
+                         const RouteStaging *stg, cudaStream_t s);
 
 cudaError_t launch_grouped_cc(int wfmt, int src, int stage, const GroupedArgs &a, int E, cudaStream_t s);
 

@@ -3,6 +3,7 @@
 
 #include "common.cuh"
 #include "internal.h"
+#include "launch.h"
 
 namespace bqmoe {
 
@@ -21,6 +22,8 @@ constexpr int kMaxK = 16;
 __global__ void __launch_bounds__(kCombThreads)
 k_combine(const float *__restrict__ part, int H, const int32_t *__restrict__ pair_pos, int K,
           __nv_bfloat16 *__restrict__ out) {
+  pdl_trigger();
+  pdl_wait();
   const int t = blockIdx.y;
   int pos[kMaxK];
   int n = 0;
@@ -52,8 +55,8 @@ cudaError_t launch_combine(const float *part, int H, const int32_t *pair_pos, in
   if (T <= 0) return cudaSuccess;
   if (K > kMaxK) return cudaErrorInvalidValue;
   const int gx = (H + kCombThreads * 4 - 1) / (kCombThreads * 4);
-  k_combine<<<dim3(gx, T), kCombThreads, 0, s>>>(part, H, pair_pos, K, reinterpret_cast<__nv_bfloat16 *>(out));
-  return cudaGetLastError();
+  return launch_pdl(k_combine, dim3(gx, T), dim3(kCombThreads), 0, s, part, H, pair_pos, K,
+                    reinterpret_cast<__nv_bfloat16 *>(out));
 }
 
 // ------------------------------------------------------------------- packer

@@ -15,6 +15,7 @@
 // every output element is written by exactly one thread.
 #include "common.cuh"
 #include "internal.h"
+#include "launch.h"
 
 namespace bqmoe {
 
@@ -66,6 +67,8 @@ __global__ void __launch_bounds__(kThreads) k_grouped_cc(const GroupedArgs a) {
   __shared__ __align__(16) float act[kPT * kKC];
   __shared__ float dots[kRows][kPT + 1];
   __shared__ int64_t row_of_pt[kPT];
+  pdl_trigger();
+  pdl_wait();
 
   const int e = blockIdx.y;
   const int cnt = a.counts[e];
@@ -188,8 +191,7 @@ __global__ void __launch_bounds__(kThreads) k_grouped_cc(const GroupedArgs a) {
 template <int WFMT, int SRC, int STAGE>
 static cudaError_t launch_one(const GroupedArgs &a, int E, cudaStream_t s) {
   const int nb = STAGE == STAGE_GATED ? a.n_rows / 16 : a.n_rows / kRows;
-  k_grouped_cc<WFMT, SRC, STAGE><<<dim3(nb, E), kThreads, 0, s>>>(a);
-  return cudaGetLastError();
+  return launch_pdl(k_grouped_cc<WFMT, SRC, STAGE>, dim3(nb, E), dim3(kThreads), 0, s, a);
 }
 
 template <int WFMT, int STAGE>

@@ -34,6 +34,7 @@
 
 #include "common.cuh"
 #include "internal.h"
+#include "launch.h"
 #include "dequant.cuh"
 #include "sync.cuh"
 
@@ -70,6 +71,8 @@ __global__ void __launch_bounds__(kStageThreads)
 k_stage_x16(const void *__restrict__ act, const uint8_t *__restrict__ act_scales, const float *__restrict__ act_g,
             int K, __half *__restrict__ x16, float *__restrict__ fac, float *__restrict__ zero, int64_t zero_n) {
   __shared__ float red[32];
+  pdl_trigger();
+  pdl_wait();
   const int64_t row = blockIdx.x;
   for (int64_t i = (int64_t)blockIdx.x * kStageThreads + threadIdx.x; i < zero_n; i += (int64_t)gridDim.x * kStageThreads)
     zero[i] = 0.f;
@@ -183,6 +186,7 @@ __global__ void __launch_bounds__(kTmaThreads, 1) k_grouped_mma(const GroupedArg
   const uint32_t cbar = empty0 + 8u * nst;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  pdl_trigger();
   if (threadIdx.x == 0) {
     for (int i = 0; i < nst; ++i) {
       mbar_init(full0 + 8u * i, 1);
@@ -236,6 +240,7 @@ __global__ void __launch_bounds__(kTmaThreads, 1) k_grouped_mma(const GroupedArg
       for (int i = 0; i < nst; ++i)
         if (issued & (1u << i)) mbar_wait(full0 + 8u * i, (issued_parity >> i) & 1u);
     }
+    pdl_wait();  // the producer only read routing outputs and weights; complete after the predecessor
     return;
   }
 
@@ -252,6 +257,7 @@ __global__ void __launch_bounds__(kTmaThreads, 1) k_grouped_mma(const GroupedArg
   int staged_e = -1, staged_pass = -1;
   uint32_t cphase = 0;
   bool ok = true;
+  pdl_wait();  // activations / h come from the preceding kernels
 
   for (int u = u0; u < u1 && ok; ++u) {
     const Item w = cur.at(a, u, nblk);
@@ -461,8 +467,7 @@ static cudaError_t launch_mma_one(const GroupedArgs &a, int rows_total, int E, c
   g.n_blocks = rows_total / (16 * kConsumers);
   const int units_max = E * g.n_blocks;
   const int grid = std::max(1, std::min(sms * ctas_per_sm, units_max));
-  k_grouped_mma<SRC, STAGE, NT><<<grid, kTmaThreads, smem, s>>>(g, nst);
-  return cudaGetLastError();
+  return launch_pdl(k_grouped_mma<SRC, STAGE, NT>, dim3(grid), dim3(kTmaThreads), smem, s, g, nst);
 }
 
 template <int STAGE, int NT>
@@ -509,14 +514,14 @@ cudaError_t launch_stage_x16(int src, const void *act, const uint8_t *act_scales
   if (T <= 0) return cudaSuccess;
   switch (src) {
     case SRC_X_BF16:
-      k_stage_x16<SRC_X_BF16><<<T, kStageThreads, 0, s>>>(act, act_scales, act_g, K, x16, fac, zero, zero_n);
-      break;
+      return launch_pdl(k_stage_x16<SRC_X_BF16>, dim3(T), dim3(kStageThreads), 0, s, act, act_scales, act_g, K, x16, fac,
+                        zero, zero_n);
     case SRC_X_NVFP4:
-      k_stage_x16<SRC_X_NVFP4><<<T, kStageThreads, 0, s>>>(act, act_scales, act_g, K, x16, fac, zero, zero_n);
-      break;
+      return launch_pdl(k_stage_x16<SRC_X_NVFP4>, dim3(T), dim3(kStageThreads), 0, s, act, act_scales, act_g, K, x16, fac,
+                        zero, zero_n);
     case SRC_X_MXFP8:
-      k_stage_x16<SRC_X_MXFP8><<<T, kStageThreads, 0, s>>>(act, act_scales, act_g, K, x16, fac, zero, zero_n);
-      break;
+      return launch_pdl(k_stage_x16<SRC_X_MXFP8>, dim3(T), dim3(kStageThreads), 0, s, act, act_scales, act_g, K, x16, fac,
+                        zero, zero_n);
     default: return cudaErrorInvalidValue;
   }
   return cudaGetLastError();

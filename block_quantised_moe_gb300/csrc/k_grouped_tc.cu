@@ -29,6 +29,7 @@
 #include "common.cuh"
 #include "dequant.cuh"
 #include "internal.h"
+#include "launch.h"
 #include "sync.cuh"
 
 namespace bqmoe {
@@ -158,6 +159,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) k_grouped_tc(const GroupedArgs 
   const uint32_t drain = tempty0 + 16u;               // 1
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  pdl_trigger();
   if (threadIdx.x == 0) {
     for (int i = 0; i < kTcAStages; ++i) {
       mbar_init(afull0 + 8u * i, kTcAWarps);
@@ -283,6 +285,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) k_grouped_tc(const GroupedArgs 
     int slot = 0, issued = 0;
     uint32_t phase = 0;
     const __half *act = reinterpret_cast<const __half *>(a.act);
+    pdl_wait();  // activation rows come from the preceding kernels
     for (int w = w0; w < W && ok; w += wstep) {
       const TcItem it = cur.at(a, w, nbp);
       int rid[kTcBRows];
@@ -381,6 +384,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) k_grouped_tc(const GroupedArgs 
     // ------------------------------------------------------ epilogue
     const int m = warp * 32 + lane;  // accumulator row = TMEM lane
     const float *gl_all = a.globals;
+    pdl_wait();  // row factors come from the preceding kernels
     int li = 0;
     for (int w = w0; w < W && ok; w += wstep, ++li) {
       const TcItem it = cur.at(a, w, nbp);
@@ -456,6 +460,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) k_grouped_tc(const GroupedArgs 
   }
 
   if (!ok && lane == 0) atomicOr(&a.status[ST_FLAGS], ST_FLAG_TIMEOUT);
+  pdl_wait();  // completion implies the predecessor's (a no-op for threads that already waited)
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
@@ -481,8 +486,7 @@ static cudaError_t launch_tc_one(const GroupedArgs &a, int rows_total, int E, cu
   if (sms <= 0) return cudaErrorInvalidDevice;
   GroupedArgs g = a;
   g.n_blocks = rows_total / 128;
-  k_grouped_tc<STAGE><<<sms, kTcThreads, smem, s>>>(g);
-  return cudaGetLastError();
+  return launch_pdl(k_grouped_tc<STAGE>, dim3(sms), dim3(kTcThreads), smem, s, g);
 }
 
 bool tc_supported(int rows_total, int K) { return rows_total % (128 * kTcMB) == 0 && K % 64 == 0; }
@@ -507,6 +511,8 @@ __global__ void __launch_bounds__(256) k_stage_h16(const void *__restrict__ act,
                                                    const int32_t *__restrict__ rows_dev, __half *__restrict__ h16,
                                                    float *__restrict__ fac) {
   const int lane = threadIdx.x & 31;
+  pdl_trigger();
+  pdl_wait();
   const int64_t live = rows < (int64_t)*rows_dev ? rows : (int64_t)*rows_dev;
   for (int64_t row = (int64_t)blockIdx.x * 8 + (threadIdx.x >> 5); row < live; row += (int64_t)gridDim.x * 8) {
     float f;
@@ -539,9 +545,9 @@ cudaError_t launch_stage_h16(int src, const void *act, const uint8_t *act_scales
   if (rows <= 0) return cudaSuccess;
   const int grid = (int)std::min<int64_t>((rows + 7) / 8, 152 * 16);
   switch (src) {
-    case SRC_H_F32: k_stage_h16<SRC_H_F32><<<grid, 256, 0, s>>>(act, act_scales, act_g, K, rows, rows_dev, h16, fac); break;
-    case SRC_H_NVFP4: k_stage_h16<SRC_H_NVFP4><<<grid, 256, 0, s>>>(act, act_scales, act_g, K, rows, rows_dev, h16, fac); break;
-    case SRC_H_MXFP8: k_stage_h16<SRC_H_MXFP8><<<grid, 256, 0, s>>>(act, act_scales, act_g, K, rows, rows_dev, h16, fac); break;
+    case SRC_H_F32: return launch_pdl(k_stage_h16<SRC_H_F32>, dim3(grid), dim3(256), 0, s, act, act_scales, act_g, K, rows, rows_dev, h16, fac);
+    case SRC_H_NVFP4: return launch_pdl(k_stage_h16<SRC_H_NVFP4>, dim3(grid), dim3(256), 0, s, act, act_scales, act_g, K, rows, rows_dev, h16, fac);
+    case SRC_H_MXFP8: return launch_pdl(k_stage_h16<SRC_H_MXFP8>, dim3(grid), dim3(256), 0, s, act, act_scales, act_g, K, rows, rows_dev, h16, fac);
     default: return cudaErrorInvalidValue;
   }
   return cudaGetLastError();

@@ -15,6 +15,7 @@
 
 #include "common.cuh"
 #include "internal.h"
+#include "launch.h"
 
 namespace bqmoe {
 
@@ -113,6 +114,8 @@ __global__ void __launch_bounds__(kQThreads)
 k_quant_rows_nvfp4(const void *__restrict__ src, int64_t cols, uint8_t *__restrict__ codes,
                    uint8_t *__restrict__ scales, float *__restrict__ g_out, const int32_t *__restrict__ rows_dev) {
   __shared__ float red[32];
+  pdl_trigger();
+  pdl_wait();
   const int64_t row = blockIdx.x;
   if (rows_dev != nullptr && row >= *rows_dev) return;
   const int64_t base = row * cols;
@@ -146,6 +149,8 @@ k_quant_blocks(const void *__restrict__ src, int64_t rows, int64_t cols, int64_t
                const float *__restrict__ g, uint8_t *__restrict__ codes, uint8_t *__restrict__ scales,
                const int32_t *__restrict__ rows_dev) {
   constexpr int bs = QF == Q_NVFP4 ? 16 : 32;
+  pdl_trigger();
+  pdl_wait();
   const int64_t nb = cols / bs;
   const int64_t live_rows = rows_dev ? (rows < (int64_t)*rows_dev ? rows : (int64_t)*rows_dev) : rows;
   for (int64_t i = (int64_t)blockIdx.x * kQThreads + threadIdx.x; i < live_rows * nb;
@@ -180,6 +185,8 @@ template <bool BF16>
 __global__ void __launch_bounds__(kQThreads)
 k_amax_tensor(const void *__restrict__ src, int64_t elems, float *__restrict__ amax) {
   __shared__ float red[32];
+  pdl_trigger();
+  pdl_wait();
   const int64_t b = blockIdx.y;
   float m = 0.f;
   for (int64_t j = ((int64_t)blockIdx.x * kQThreads + threadIdx.x) * 8; j < elems;
@@ -195,6 +202,8 @@ k_amax_tensor(const void *__restrict__ src, int64_t elems, float *__restrict__ a
 }
 
 __global__ void k_amax_to_global(float *g, int64_t n) {
+  pdl_trigger();
+  pdl_wait();
   const int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
   if (i < n) g[i] = __fdiv_rn(g[i], 2688.0f);
 }
@@ -211,10 +220,10 @@ cudaError_t launch_quant_rows_nvfp4(const void *src, bool src_bf16, int64_t rows
   if (rows <= 0) return cudaSuccess;
   if (rows > 0x7FFFFFFF) return cudaErrorInvalidValue;
   if (src_bf16)
-    k_quant_rows_nvfp4<true><<<(unsigned)rows, kQThreads, 0, s>>>(src, cols, codes, scales, g, rows_dev);
-  else
-    k_quant_rows_nvfp4<false><<<(unsigned)rows, kQThreads, 0, s>>>(src, cols, codes, scales, g, rows_dev);
-  return cudaGetLastError();
+    return launch_pdl(k_quant_rows_nvfp4<true>, dim3((unsigned)rows), dim3(kQThreads), 0, s, src, cols, codes, scales,
+                      g, rows_dev);
+  return launch_pdl(k_quant_rows_nvfp4<false>, dim3((unsigned)rows), dim3(kQThreads), 0, s, src, cols, codes, scales, g,
+                    rows_dev);
 }
 
 cudaError_t launch_quant_blocks(int qfmt, const void *src, bool src_bf16, int64_t rows, int64_t cols,
@@ -223,13 +232,14 @@ cudaError_t launch_quant_blocks(int qfmt, const void *src, bool src_bf16, int64_
   if (rows <= 0) return cudaSuccess;
   const int bs = qfmt == Q_NVFP4 ? 16 : 32;
   const int grid = grid_for(rows * (cols / bs), kQThreads);
-#define QB(QF, B) k_quant_blocks<QF, B><<<grid, kQThreads, 0, s>>>(src, rows, cols, rows_per_global, g, codes, scales, rows_dev)
+#define QB(QF, B) \
+  return launch_pdl(k_quant_blocks<QF, B>, dim3(grid), dim3(kQThreads), 0, s, src, rows, cols, rows_per_global, g, \
+                    codes, scales, rows_dev)
   if (qfmt == Q_NVFP4) { if (src_bf16) QB(Q_NVFP4, true); else QB(Q_NVFP4, false); }
   else if (qfmt == Q_MXFP4) { if (src_bf16) QB(Q_MXFP4, true); else QB(Q_MXFP4, false); }
   else if (qfmt == Q_MXFP8) { if (src_bf16) QB(Q_MXFP8, true); else QB(Q_MXFP8, false); }
-  else return cudaErrorInvalidValue;
 #undef QB
-  return cudaGetLastError();
+  return cudaErrorInvalidValue;
 }
 
 cudaError_t launch_amax_tensor(const void *src, bool src_bf16, int64_t batch, int64_t elems, float *amax,
@@ -239,15 +249,13 @@ cudaError_t launch_amax_tensor(const void *src, bool src_bf16, int64_t batch, in
   if (err != cudaSuccess) return err;
   const int64_t gx = (elems / 8 + kQThreads * 4 - 1) / (kQThreads * 4);
   dim3 grid((unsigned)std::max<int64_t>(1, std::min<int64_t>(gx, 1024)), (unsigned)batch);
-  if (src_bf16) k_amax_tensor<true><<<grid, kQThreads, 0, s>>>(src, elems, amax);
-  else k_amax_tensor<false><<<grid, kQThreads, 0, s>>>(src, elems, amax);
-  return cudaGetLastError();
+  if (src_bf16) return launch_pdl(k_amax_tensor<true>, grid, dim3(kQThreads), 0, s, src, elems, amax);
+  return launch_pdl(k_amax_tensor<false>, grid, dim3(kQThreads), 0, s, src, elems, amax);
 }
 
 cudaError_t launch_amax_to_global(float *g, int64_t n, cudaStream_t s) {
   if (n <= 0) return cudaSuccess;
-  k_amax_to_global<<<(unsigned)((n + 255) / 256), 256, 0, s>>>(g, n);
-  return cudaGetLastError();
+  return launch_pdl(k_amax_to_global, dim3((unsigned)((n + 255) / 256)), dim3(256), 0, s, g, n);
 }
 
 }  // namespace bqmoe

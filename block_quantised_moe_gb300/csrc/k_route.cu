@@ -10,6 +10,7 @@
 // in p = t*K + k and bit-identical from run to run.  Only integer shared-memory
 // atomics are used.
 #include "common.cuh"
+#include "dequant.cuh"
 #include "internal.h"
 
 namespace bqmoe {
@@ -22,8 +23,39 @@ __global__ void __launch_bounds__(kRouteThreads)
 k_route(const int32_t *__restrict__ ids, int P, int E, int pad, int ntok, int large_min, int large_tile,
         int32_t *__restrict__ counts, int32_t *__restrict__ offsets, int32_t *__restrict__ sorted_pair,
         int32_t *__restrict__ pair_pos, int32_t *__restrict__ active, int32_t *__restrict__ passes,
-        int32_t *__restrict__ large, int32_t *__restrict__ large_tiles, int32_t *__restrict__ status) {
+        int32_t *__restrict__ large, int32_t *__restrict__ large_tiles, int32_t *__restrict__ status,
+        const __nv_bfloat16 *__restrict__ x, int H, __half *__restrict__ x16, float *__restrict__ xfac,
+        float *__restrict__ zero, int64_t zero_n) {
   extern __shared__ int32_t sm[];
+  if (blockIdx.x > 0) {
+    // CTAs 1..T: BF16 token rows -> FP16 rows with a power-of-two factor (the
+    // tensor-core kernels' B operand), and clear the per-pair max |h| array.
+    __shared__ float red[kRouteWarps];
+    const int64_t row = blockIdx.x - 1;
+    for (int64_t i = row * kRouteThreads + threadIdx.x; i < zero_n; i += (int64_t)(gridDim.x - 1) * kRouteThreads)
+      zero[i] = 0.f;
+    float m = 0.f;
+    for (int k = threadIdx.x * 8; k < H; k += kRouteThreads * 8) {
+      float v[8];
+      src_load8<SRC_X_BF16>(x, nullptr, row, k, H, v);
+#pragma unroll
+      for (int i = 0; i < 8; ++i) m = fmaxf(m, fabsf(v[i]));
+    }
+    m = warp_max(m);
+    if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = m;
+    __syncthreads();
+    m = 0.f;
+    for (int w = 0; w < kRouteWarps; ++w) m = fmaxf(m, red[w]);
+    const float f = stage_factor(m);
+    const float inv = __frcp_rn(f);
+    for (int k = threadIdx.x * 8; k < H; k += kRouteThreads * 8) {
+      float v[8];
+      src_load8<SRC_X_BF16>(x, nullptr, row, k, H, v);
+      *reinterpret_cast<uint4 *>(x16 + row * H + k) = to_half8(v, inv);
+    }
+    if (threadIdx.x == 0) xfac[row] = f;
+    return;
+  }
   int32_t *hist = sm;                 // [E]
   int32_t *base = hist + E;           // [E+1]
   int32_t *cursor = base + E + 1;     // [E]
@@ -156,14 +188,21 @@ k_route(const int32_t *__restrict__ ids, int P, int E, int pad, int ntok, int la
 
 cudaError_t launch_route(const int32_t *ids, int P, int E, int pad, int ntok, int large_min, int large_tile,
                          int32_t *counts, int32_t *offsets, int32_t *sorted_pair, int32_t *pair_pos, int32_t *active,
-                         int32_t *passes, int32_t *large, int32_t *large_tiles, int32_t *status, cudaStream_t s) {
+                         int32_t *passes, int32_t *large, int32_t *large_tiles, int32_t *status,
+                         const RouteStaging *stg, cudaStream_t s) {
   if (E > kMaxExperts) return cudaErrorInvalidValue;
   const size_t smem = sizeof(int32_t) * ((size_t)3 * E + 1 + (size_t)kRouteWarps * E);
   // Per-device function attribute; cheap and idempotent, so set on every launch.
   cudaError_t err = cudaFuncSetAttribute(k_route, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (err != cudaSuccess) return err;
-  k_route<<<1, kRouteThreads, smem, s>>>(ids, P, E, pad, ntok, large_min, large_tile, counts, offsets, sorted_pair,
-                                          pair_pos, active, passes, large, large_tiles, status);
+  // Launched without programmatic dependent launch: later kernels of the forward
+  // may read the routing outputs as soon as they start.
+  const int T = stg ? stg->T : 0;
+  k_route<<<1 + T, kRouteThreads, smem, s>>>(ids, P, E, pad, ntok, large_min, large_tile, counts, offsets, sorted_pair,
+                                              pair_pos, active, passes, large, large_tiles, status,
+                                              stg ? stg->x : nullptr, stg ? stg->H : 0, stg ? stg->x16 : nullptr,
+                                              stg ? stg->xfac : nullptr, stg ? stg->zero : nullptr,
+                                              stg ? stg->zero_n : 0);
   return cudaGetLastError();
 }
 

@@ -1,0 +1,34 @@
+// Kernel launch with programmatic dependent launch (PDL).
+//
+// Every kernel of a forward except the routing kernel is launched with
+// programmatic stream serialisation: it may start while its predecessor is
+// still running.  Protocol (all kernels of this library follow it):
+//   * the routing kernel is launched normally and never triggers early, so its
+//     outputs (the expert lists, offsets, sorted pairs) are complete when any
+//     later kernel of the forward starts, and may be read before waiting;
+//   * a kernel calls pdl_trigger() on entry and pdl_wait() before it reads any
+//     other output of an earlier kernel; every thread that did not wait waits
+//     before it exits, so a kernel's completion implies its predecessor's.
+#pragma once
+
+#include <cuda_runtime.h>
+
+namespace bqmoe {
+
+template <typename... KArgs, typename... Args>
+inline cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t s,
+                              Args... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, static_cast<KArgs>(args)...);
+}
+
+}  // namespace bqmoe

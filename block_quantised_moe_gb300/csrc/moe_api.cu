@@ -264,8 +264,14 @@ static moe_status run_impl(moe_binding b, cudaStream_t stream, cudaEvent_t *ev) 
   const int ntok = mma_tokens_per_pass(H, I, wide);
   int32_t *large = at<int32_t>(sc, S.large);
   int32_t *large_tiles = at<int32_t>(sc, S.large_tiles);
+  // With BF16 activations on the tensor-core path, extra CTAs of the routing
+  // launch stage x as FP16 rows and clear the per-pair |h| maxima.
+  const bool mma_layout = L.layout == LAYOUT_MMA16x64;
+  RouteStaging stg{static_cast<const __nv_bfloat16 *>(b->x), T, H, at<__half>(sc, S.x16), at<float>(sc, S.xfac),
+                   at<float>(sc, S.hamax), S.cap_sorted};
+  const bool staged = mma_layout && P.afmt == MOE_A_BF16;
   if ((err = launch_route(b->ids, T * K, E, P.pad, ntok, P.large_min, 128, counts, offsets, sorted, pair_pos, active,
-                          passes, large, large_tiles, status, stream)) != cudaSuccess)
+                          passes, large, large_tiles, status, staged ? &stg : nullptr, stream)) != cudaSuccess)
     return MOE_ERR_CUDA;
 
   GroupedArgs a{};
@@ -301,12 +307,14 @@ static moe_status run_impl(moe_binding b, cudaStream_t stream, cudaEvent_t *ev) 
     a.act_scales = at<uint8_t>(sc, S.xq_scales);
   }
   if (err != cudaSuccess) return MOE_ERR_CUDA;
-  const bool mma = L.layout == LAYOUT_MMA16x64;
+  const bool mma = mma_layout;
   if (mma) {
     // tensor-core path: x^ as FP16 rows + per-row factor; clears the per-pair |h| maxima
-    err = launch_stage_x16(src1, a.act, a.act_scales, a.act_g, T, H, at<__half>(sc, S.x16), at<float>(sc, S.xfac),
-                           at<float>(sc, S.hamax), S.cap_sorted, stream);
-    if (err != cudaSuccess) return MOE_ERR_CUDA;
+    if (!staged) {
+      err = launch_stage_x16(src1, a.act, a.act_scales, a.act_g, T, H, at<__half>(sc, S.x16), at<float>(sc, S.xfac),
+                             at<float>(sc, S.hamax), S.cap_sorted, stream);
+      if (err != cudaSuccess) return MOE_ERR_CUDA;
+    }
     src1 = SRC_X16;
     a.act = at<__half>(sc, S.x16);
     a.act_scales = nullptr;
