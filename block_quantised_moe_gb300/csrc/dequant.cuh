@@ -91,4 +91,11 @@ __device__ __forceinline__ uint4 to_half8(const float (&v)[8], float inv) {
   return *reinterpret_cast<uint4 *>(h);
 }
 
+__device__ __forceinline__ uint4 to_bf16x8(const float (&v)[8]) {
+  __align__(16) __nv_bfloat162 h[4];
+#pragma unroll
+  for (int i = 0; i < 4; ++i) h[i] = __floats2bfloat162_rn(v[2 * i], v[2 * i + 1]);
+  return *reinterpret_cast<uint4 *>(h);
+}
+
 }  // namespace bqmoe

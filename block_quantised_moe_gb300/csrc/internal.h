@@ -77,6 +77,7 @@ struct GroupedArgs {
   const int32_t *large;        // experts for the tcgen05 kernel: [0] = n, [1..] ids
   const int32_t *large_tiles;  // [i] = 128-token tiles of large experts before i (prefix)
   int act_by_token;            // tcgen05 kernel: B rows indexed by token (GEMM1) or by slot (GEMM2)
+  int tc_min_pairs;            // CUDA-core kernel: > 0 leaves experts with this many pairs to tcgen05
   int32_t *status;        // device status word (timeout flag)
   int top_k;
   const float *topk_weights;
@@ -114,11 +115,16 @@ cudaError_t launch_grouped_mma(int src, int stage, const GroupedArgs &a, int row
 cudaError_t launch_stage_x16(int src, const void *act, const uint8_t *act_scales, const float *act_g, int T, int K,
                              __half *x16, float *fac, float *zero, int64_t zero_n, cudaStream_t s);
 
-// tcgen05 kernels for experts with many pairs (NVFP4 weights, FP16 operands).
+// tcgen05 kernels for experts with many pairs: NVFP4 weights (packed blocks,
+// FP16 operands) or MXFP4 weights (row-major, BF16 operands).
 bool tc_supported(int rows_total, int K);
-cudaError_t launch_grouped_tc(int stage, const GroupedArgs &a, int rows_total, int E, cudaStream_t s);
+cudaError_t launch_grouped_tc(int stage, int wfmt, const GroupedArgs &a, int rows_total, int E, cudaStream_t s);
+// h (or its re-quantised codes) as 16-bit rows for the tcgen05 GEMM2: FP16 with a
+// per-row factor, or BF16 with factor 1 (out_bf16; also MXFP8 x^ -> BF16 rows).
+// rows_dev (device, nullable) caps the rows actually converted.
 cudaError_t launch_stage_h16(int src, const void *act, const uint8_t *act_scales, const float *act_g, int K,
-                             int64_t rows, const int32_t *rows_dev, __half *h16, float *fac, cudaStream_t s);
+                             int64_t rows, const int32_t *rows_dev, __half *h16, float *fac, bool out_bf16,
+                             cudaStream_t s);
 
 cudaError_t launch_combine(const float *part, int H, const int32_t *pair_pos, int T, int K, void *out_bf16,
                            cudaStream_t s);

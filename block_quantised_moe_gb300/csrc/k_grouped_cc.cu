@@ -72,7 +72,7 @@ __global__ void __launch_bounds__(kThreads) k_grouped_cc(const GroupedArgs a) {
 
   const int e = blockIdx.y;
   const int cnt = a.counts[e];
-  if (cnt == 0) return;
+  if (cnt == 0 || (a.tc_min_pairs > 0 && cnt >= a.tc_min_pairs)) return;  // nothing, or the tcgen05 kernel's
   const int off = a.offsets[e];
   const int K = a.K;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;

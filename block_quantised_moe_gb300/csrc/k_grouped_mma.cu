@@ -449,7 +449,8 @@ static cudaError_t launch_mma_one(const GroupedArgs &a, int rows_total, int E, c
   constexpr size_t kSmemMax = 227 * 1024;
   constexpr size_t kSmemHalf = 112 * 1024;  // two CTAs per SM below this
   // Prefer two CTAs per SM (16 consumer warps) with a 4-stage ring each; else one
-  // CTA with the deepest ring that fits.
+  // CTA with the deepest ring that fits.  (Three CTAs with 2-stage rings measured
+  // slower at every decode batch size.)
   int ctas_per_sm = 2, nst = 4;
   if (tma_smem_bytes(a.K, NT, nst) > kSmemHalf) {
     ctas_per_sm = 1;

@@ -139,7 +139,9 @@ struct TcCursor {
 
 // ------------------------------------------------------------------ kernel
 
-template <int STAGE>
+// WF: W_NVFP4 (packed 128-row blocks, FP16 operands) or W_MXFP4 (row-major
+// checkpoint layout, BF16 operands: E2M1 * 2^X is exact in BF16 for any E8M0 X).
+template <int STAGE, int WF>
 __global__ void __launch_bounds__(kTcThreads, 1) k_grouped_tc(const GroupedArgs a) {
   extern __shared__ uint8_t smem_raw[];
   // 1024-byte aligned base for the swizzled tiles
@@ -199,8 +201,87 @@ __global__ void __launch_bounds__(kTcThreads, 1) k_grouped_tc(const GroupedArgs 
   if (w0 < W) cur.seek(a, w0, nbp);
   bool ok = true;
 
-  if (warp >= kTcEpiWarps && warp < kTcEpiWarps + kTcAWarps) {
-    // ------------------------------------------------------ A producers
+  if (WF == W_MXFP4 && warp >= kTcEpiWarps && warp < kTcEpiWarps + kTcAWarps) {
+    // ---------------------------------------------- A producers (MXFP4, BF16)
+    // One weight row per thread per k-block: 32 code bytes and 2 E8M0 scales,
+    // decoded to BF16 (E2M1 * 2^X, exact) and written as 8 swizzled 16-byte chunks.
+    const int t = threadIdx.x - kTcEpiWarps * 32;  // row of the item's 256
+    const int blk_l = t >> 7, m = t & 127;
+    const bool gated = STAGE == STAGE_GATED;
+    int slot = 0;
+    uint32_t phase = 0;
+    uint4 c0, c1, n0, n1;
+    uint32_t sc = 0, nsc = 0;
+    auto load = [&](const TcItem &it, int kb, uint4 &d0, uint4 &d1, uint32_t &ds) {
+      const int blk = 2 * it.bp + blk_l;
+      const int64_t row = gated ? (m & 15) < 8 ? (int64_t)(8 * blk + (m >> 4)) * 8 + (m & 15)
+                                             : (int64_t)a.I + (int64_t)(8 * blk + (m >> 4)) * 8 + (m & 15) - 8
+                                : (int64_t)blk * 128 + m;
+      const uint4 *cp = reinterpret_cast<const uint4 *>(a.codes + (size_t)it.e * a.codes_expert + row * (K / 2) + kb * 32);
+      d0 = __ldg(cp);
+      d1 = __ldg(cp + 1);
+      const uint8_t *sp = a.scales + (size_t)it.e * a.scales_expert + row * (K / 32) + kb * 2;
+      ds = (uint32_t)__ldg(sp) | ((uint32_t)__ldg(sp + 1) << 8);
+    };
+    TcCursor pcur = cur;
+    int pw = w0, pkb = 0;
+    TcItem pit;
+    if (pw < W) {
+      pit = pcur.at(a, pw, nbp);
+      load(pit, 0, n0, n1, nsc);
+    }
+    for (int w = w0; w < W && ok; w += wstep) {
+      for (int kb = 0; kb < nk; ++kb) {
+        c0 = n0;
+        c1 = n1;
+        sc = nsc;
+        if (++pkb == nk) {
+          pkb = 0;
+          pw += wstep;
+          if (pw < W) pit = pcur.at(a, pw, nbp);
+        }
+        if (pw < W) load(pit, pkb, n0, n1, nsc);
+        if (!mbar_wait(aempty0 + 8u * slot, phase ^ 1u)) {
+          ok = false;
+          break;
+        }
+        uint8_t *tileA = base + (size_t)slot * kTcAStageBytes + blk_l * kTcABytes;
+        const uint32_t words[8] = {c0.x, c0.y, c0.z, c0.w, c1.x, c1.y, c1.z, c1.w};
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {  // two 32-element MX blocks
+          const float p2 = e8m0_to_f32((sc >> (8 * h)) & 0xFFu);
+#pragma unroll
+          for (int q = 0; q < 2; ++q) {  // 16 elements -> 2 chunks of 8
+            uint32_t out[8];
+#pragma unroll
+            for (int wq = 0; wq < 2; ++wq) {
+              float v[8];
+              e2m1x8_to_f32(words[4 * h + 2 * q + wq], v);
+#pragma unroll
+              for (int i = 0; i < 4; ++i) {
+                __nv_bfloat162 b2 = __floats2bfloat162_rn(v[2 * i] * p2, v[2 * i + 1] * p2);
+                out[4 * wq + i] = *reinterpret_cast<uint32_t *>(&b2);
+              }
+            }
+#pragma unroll
+            for (int cc = 0; cc < 2; ++cc) {
+              const int c = 4 * h + 2 * q + cc;  // 16-byte chunk of the 128-byte row
+              *reinterpret_cast<uint4 *>(tileA + (m >> 3) * 1024 + (m & 7) * 128 + (((c ^ m) & 7) << 4)) =
+                  make_uint4(out[4 * cc], out[4 * cc + 1], out[4 * cc + 2], out[4 * cc + 3]);
+            }
+          }
+        }
+        fence_async_smem();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(afull0 + 8u * slot);
+        if (++slot == kTcAStages) {
+          slot = 0;
+          phase ^= 1u;
+        }
+      }
+    }
+  } else if (WF == W_NVFP4 && warp >= kTcEpiWarps && warp < kTcEpiWarps + kTcAWarps) {
+    // ---------------------------------------------- A producers (NVFP4, FP16)
     const int t = threadIdx.x - kTcEpiWarps * 32;  // 0..kTcAWarps*32-1
     int slot = 0;
     uint32_t phase = 0;
@@ -332,7 +413,9 @@ __global__ void __launch_bounds__(kTcThreads, 1) k_grouped_tc(const GroupedArgs 
   } else if (warp == kTcMmaWarp) {
     // ------------------------------------------------------ MMA issuer
     if (lane == 0) {
-      const uint32_t idesc = (1u << 4) | ((uint32_t)(kTcN >> 3) << 17) | ((uint32_t)(128 >> 4) << 24);
+      constexpr uint32_t fmt = WF == W_MXFP4 ? 1u : 0u;  // operand type: 0 = F16, 1 = BF16
+      const uint32_t idesc = (1u << 4) | (fmt << 7) | (fmt << 10) | ((uint32_t)(kTcN >> 3) << 17) |
+                             ((uint32_t)(128 >> 4) << 24);
       int sa = 0, sb = 0, li = 0;
       uint32_t pa = 0, pb = 0;
       bool any = false;
@@ -406,7 +489,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) k_grouped_tc(const GroupedArgs 
           float f_l = 0.f, w_l = 0.f;
           if (nl < it.ntok) {
             const int p = a.sorted_pair[sl];
-            f_l = a.act_g[a.act_by_token ? (int64_t)(p / a.top_k) : (int64_t)sl];
+            f_l = a.act_g ? a.act_g[a.act_by_token ? (int64_t)(p / a.top_k) : (int64_t)sl] : 1.f;
             if (STAGE == STAGE_DOWN) w_l = a.topk_weights[p] * gl[2];
           }
           uint32_t raw[32];
@@ -477,27 +560,34 @@ static int tc_num_sms() {
 
 size_t tc_smem_bytes() { return (size_t)kTcRingBytes + 1024 + 8 * (2 * kTcAStages + 2 * kTcBStages + 5) + 16; }
 
-template <int STAGE>
+template <int STAGE, int WF>
 static cudaError_t launch_tc_one(const GroupedArgs &a, int rows_total, int E, cudaStream_t s) {
   const size_t smem = tc_smem_bytes();
-  cudaError_t err = cudaFuncSetAttribute(k_grouped_tc<STAGE>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  cudaError_t err = cudaFuncSetAttribute(k_grouped_tc<STAGE, WF>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (err != cudaSuccess) return err;
   const int sms = tc_num_sms();
   if (sms <= 0) return cudaErrorInvalidDevice;
   GroupedArgs g = a;
   g.n_blocks = rows_total / 128;
-  return launch_pdl(k_grouped_tc<STAGE>, dim3(sms), dim3(kTcThreads), smem, s, g);
+  return launch_pdl(k_grouped_tc<STAGE, WF>, dim3(sms), dim3(kTcThreads), smem, s, g);
 }
 
 bool tc_supported(int rows_total, int K) { return rows_total % (128 * kTcMB) == 0 && K % 64 == 0; }
 
-cudaError_t launch_grouped_tc(int stage, const GroupedArgs &a, int rows_total, int E, cudaStream_t s) {
-  if (!tc_supported(rows_total, a.K)) return cudaErrorInvalidValue;
+template <int WF>
+static cudaError_t launch_tc_wf(int stage, const GroupedArgs &a, int rows_total, int E, cudaStream_t s) {
   switch (stage) {
-    case STAGE_GATED: return launch_tc_one<STAGE_GATED>(a, rows_total, E, s);
-    case STAGE_RELU2: return launch_tc_one<STAGE_RELU2>(a, rows_total, E, s);
-    case STAGE_DOWN: return launch_tc_one<STAGE_DOWN>(a, rows_total, E, s);
+    case STAGE_GATED: return launch_tc_one<STAGE_GATED, WF>(a, rows_total, E, s);
+    case STAGE_RELU2: return launch_tc_one<STAGE_RELU2, WF>(a, rows_total, E, s);
+    case STAGE_DOWN: return launch_tc_one<STAGE_DOWN, WF>(a, rows_total, E, s);
   }
+  return cudaErrorInvalidValue;
+}
+
+cudaError_t launch_grouped_tc(int stage, int wfmt, const GroupedArgs &a, int rows_total, int E, cudaStream_t s) {
+  if (!tc_supported(rows_total, a.K)) return cudaErrorInvalidValue;
+  if (wfmt == W_NVFP4) return launch_tc_wf<W_NVFP4>(stage, a, rows_total, E, s);
+  if (wfmt == W_MXFP4) return launch_tc_wf<W_MXFP4>(stage, a, rows_total, E, s);
   return cudaErrorInvalidValue;
 }
 
@@ -505,7 +595,7 @@ cudaError_t launch_grouped_tc(int stage, const GroupedArgs &a, int rows_total, i
 //
 // One warp per live slot row: FP32 h with the factor from GEMM1's per-pair max |h|,
 // NVFP4 (E2M1*E4M3 exact, factor = row global) or MXFP8 (two passes) -> FP16 + factor.
-template <int SRC>
+template <int SRC, bool OUT_BF16>
 __global__ void __launch_bounds__(256) k_stage_h16(const void *__restrict__ act, const uint8_t *__restrict__ act_scales,
                                                    const float *__restrict__ act_g, int K, int64_t rows,
                                                    const int32_t *__restrict__ rows_dev, __half *__restrict__ h16,
@@ -513,8 +603,16 @@ __global__ void __launch_bounds__(256) k_stage_h16(const void *__restrict__ act,
   const int lane = threadIdx.x & 31;
   pdl_trigger();
   pdl_wait();
-  const int64_t live = rows < (int64_t)*rows_dev ? rows : (int64_t)*rows_dev;
+  const int64_t live = rows_dev == nullptr || rows < (int64_t)*rows_dev ? rows : (int64_t)*rows_dev;
   for (int64_t row = (int64_t)blockIdx.x * 8 + (threadIdx.x >> 5); row < live; row += (int64_t)gridDim.x * 8) {
+    if (OUT_BF16) {  // BF16 rows, no factor (the MXFP4 path's BF16 operands)
+      for (int k = lane * 8; k < K; k += 256) {
+        float v[8];
+        src_load8<SRC>(act, act_scales, row, k, K, v);
+        *reinterpret_cast<uint4 *>(h16 + row * K + k) = to_bf16x8(v);
+      }
+      continue;
+    }
     float f;
     if (SRC == SRC_H_NVFP4) {
       f = act_g[row];
@@ -541,13 +639,21 @@ __global__ void __launch_bounds__(256) k_stage_h16(const void *__restrict__ act,
 }
 
 cudaError_t launch_stage_h16(int src, const void *act, const uint8_t *act_scales, const float *act_g, int K,
-                             int64_t rows, const int32_t *rows_dev, __half *h16, float *fac, cudaStream_t s) {
+                             int64_t rows, const int32_t *rows_dev, __half *h16, float *fac, bool out_bf16,
+                             cudaStream_t s) {
   if (rows <= 0) return cudaSuccess;
   const int grid = (int)std::min<int64_t>((rows + 7) / 8, 152 * 16);
+  if (out_bf16) {
+    switch (src) {
+      case SRC_H_F32: return launch_pdl(k_stage_h16<SRC_H_F32, true>, dim3(grid), dim3(256), 0, s, act, act_scales, act_g, K, rows, rows_dev, h16, fac);
+      case SRC_H_MXFP8: return launch_pdl(k_stage_h16<SRC_H_MXFP8, true>, dim3(grid), dim3(256), 0, s, act, act_scales, act_g, K, rows, rows_dev, h16, fac);
+      default: return cudaErrorInvalidValue;
+    }
+  }
   switch (src) {
-    case SRC_H_F32: return launch_pdl(k_stage_h16<SRC_H_F32>, dim3(grid), dim3(256), 0, s, act, act_scales, act_g, K, rows, rows_dev, h16, fac);
-    case SRC_H_NVFP4: return launch_pdl(k_stage_h16<SRC_H_NVFP4>, dim3(grid), dim3(256), 0, s, act, act_scales, act_g, K, rows, rows_dev, h16, fac);
-    case SRC_H_MXFP8: return launch_pdl(k_stage_h16<SRC_H_MXFP8>, dim3(grid), dim3(256), 0, s, act, act_scales, act_g, K, rows, rows_dev, h16, fac);
+    case SRC_H_F32: return launch_pdl(k_stage_h16<SRC_H_F32, false>, dim3(grid), dim3(256), 0, s, act, act_scales, act_g, K, rows, rows_dev, h16, fac);
+    case SRC_H_NVFP4: return launch_pdl(k_stage_h16<SRC_H_NVFP4, false>, dim3(grid), dim3(256), 0, s, act, act_scales, act_g, K, rows, rows_dev, h16, fac);
+    case SRC_H_MXFP8: return launch_pdl(k_stage_h16<SRC_H_MXFP8, false>, dim3(grid), dim3(256), 0, s, act, act_scales, act_g, K, rows, rows_dev, h16, fac);
     default: return cudaErrorInvalidValue;
   }
   return cudaGetLastError();

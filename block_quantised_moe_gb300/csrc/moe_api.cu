@@ -195,6 +195,16 @@ moe_status moe_plan(const moe_caps *c, moe_plan_t *out, size_t *scratch_bytes, i
       S.h16 = take(2 * (size_t)S.cap_sorted * L.I);
       S.h16fac = take(4 * (size_t)S.cap_sorted);
     }
+  } else if (L.wfmt == MOE_W_MXFP4) {
+    // MXFP4 experts with at least kLargeMin pairs run on the tcgen05 kernel with
+    // BF16 operands (E2M1 * 2^X and E4M3 * 2^X are exact in BF16); the rest stay
+    // on the CUDA-core kernel.
+    P.tc_on = Pmax >= 1024 && tc_supported(L.n13, L.H) && tc_supported(L.H, L.I);
+    if (P.tc_on) {
+      P.large_min = kLargeMin;
+      if (P.afmt == MOE_A_MXFP8) S.x16 = take(2 * (size_t)T * L.H);
+      S.h16 = take(2 * (size_t)S.cap_sorted * L.I);
+    }
   }
   S.part = take(4 * (size_t)S.cap_sorted * L.H);
   S.total = o;
@@ -332,11 +342,23 @@ static moe_status run_impl(moe_binding b, cudaStream_t stream, cudaEvent_t *ev) 
   a.n_rows = I;
   a.out = h;
   const int stage1 = L.act == MOE_ACT_SILU_GATED ? STAGE_GATED : STAGE_RELU2;
+  a.tc_min_pairs = P.tc_on ? P.large_min : 0;
+  if (!mma && P.tc_on && P.afmt == MOE_A_MXFP8) {  // x^ as BF16 rows for the tcgen05 kernel
+    err = launch_stage_h16(SRC_H_MXFP8, a.act, a.act_scales, nullptr, H, T, nullptr, at<__half>(sc, S.x16), nullptr,
+                           true, stream);
+    if (err != cudaSuccess) return MOE_ERR_CUDA;
+  }
   err = mma ? launch_grouped_mma(src1, stage1, a, L.n13, E, ntok, stream)
             : launch_grouped_cc(L.wfmt, src1, stage1, a, E, stream);
   if (err == cudaSuccess && P.tc_on) {
-    a.act_by_token = 1;
-    err = launch_grouped_tc(stage1, a, L.n13, E, stream);
+    GroupedArgs t = a;
+    t.act_by_token = 1;
+    if (!mma) {  // MXFP4: BF16 rows of x (BF16 activations) or of x^ (MXFP8), factor 1
+      t.act = P.afmt == MOE_A_MXFP8 ? static_cast<const void *>(at<__half>(sc, S.x16)) : b->x;
+      t.act_scales = nullptr;
+      t.act_g = nullptr;
+    }
+    err = launch_grouped_tc(stage1, L.wfmt, t, L.n13, E, stream);
   }
   a.out_amax = nullptr;
   if (err != cudaSuccess) return MOE_ERR_CUDA;
@@ -364,9 +386,9 @@ static moe_status run_impl(moe_binding b, cudaStream_t stream, cudaEvent_t *ev) 
   if (err != cudaSuccess) return MOE_ERR_CUDA;
 
   // GEMM2 * topk_weight -> partials, then the ordered combine
-  if (P.tc_on) {  // FP16 rows of h (or of its re-quantised codes) for the tcgen05 GEMM2
+  if (P.tc_on) {  // 16-bit rows of h (or of its re-quantised codes) for the tcgen05 GEMM2
     err = launch_stage_h16(src2, a.act, a.act_scales, a.act_g, I, S.cap_sorted, offsets + E, at<__half>(sc, S.h16),
-                           at<float>(sc, S.h16fac), stream);
+                           mma ? at<float>(sc, S.h16fac) : nullptr, !mma, stream);
     if (err != cudaSuccess) return MOE_ERR_CUDA;
   }
   a.codes = b->packed + L.off_c2;
@@ -383,9 +405,9 @@ static moe_status run_impl(moe_binding b, cudaStream_t stream, cudaEvent_t *ev) 
     GroupedArgs t = a;
     t.act = at<__half>(sc, S.h16);
     t.act_scales = nullptr;
-    t.act_g = at<float>(sc, S.h16fac);
+    t.act_g = mma ? at<float>(sc, S.h16fac) : nullptr;
     t.act_by_token = 0;
-    err = launch_grouped_tc(STAGE_DOWN, t, H, E, stream);
+    err = launch_grouped_tc(STAGE_DOWN, L.wfmt, t, H, E, stream);
   }
   if (err != cudaSuccess) return MOE_ERR_CUDA;
   if (mark(MOE_STAGE_COMBINE) != cudaSuccess) return MOE_ERR_CUDA;

@@ -130,7 +130,8 @@ def test_prefill_e256_h7168(lib, name):
 # ------------------------------------------- tcgen05 path (experts with many pairs)
 
 TC_MODES = [("nvfp4", "silu", "bf16"), ("nvfp4", "silu", "nvfp4"), ("nvfp4", "silu", "mxfp8"),
-            ("nvfp4", "relu2", "bf16")]
+            ("nvfp4", "relu2", "bf16"), ("mxfp4", "relu2", "mxfp8"), ("mxfp4", "relu2", "bf16"),
+            ("mxfp4", "silu", "mxfp8")]
 
 
 @pytest.mark.parametrize("wfmt,act,afmt", TC_MODES)
@@ -146,12 +147,14 @@ def test_tcgen05_path_small_layer(lib, wfmt, act, afmt, T):
     tl.check_close(out.float().cpu().numpy(), y_ref, f"tcgen05 {wfmt}/{act}/{afmt} T={T}")
 
 
-def test_tcgen05_and_decode_kernels_share_a_forward(lib):
-    # skewed routing: hot experts (>= 32 pairs) on tcgen05, the rest on the decode kernel
+@pytest.mark.parametrize("wfmt,act,afmt", [("nvfp4", "silu", "bf16"), ("mxfp4", "relu2", "mxfp8")])
+def test_tcgen05_and_decode_kernels_share_a_forward(lib, wfmt, act, afmt):
+    # skewed routing: hot experts (>= 32 pairs) on tcgen05, the rest on the
+    # register-dequant (NVFP4) or CUDA-core (MXFP4) kernel
     cfg = dict(E=64, H=256, I=512, K=4, zipf=1.5)
-    ck, packed = gpu_layer(lib, cfg["E"], cfg["H"], cfg["I"], "nvfp4", "silu")
+    ck, packed = gpu_layer(lib, cfg["E"], cfg["H"], cfg["I"], wfmt, act)
     x, ids, w = tl.make_inputs(cfg, 256, seed=5)
     counts = np.bincount(ids.cpu().numpy().reshape(-1), minlength=cfg["E"])
     assert counts.max() >= 32 and (counts[counts > 0] < 32).any()
-    out, _, _ = run(lib, packed, x, ids, w, cfg["K"], "bf16")
-    tl.check_close(out.float().cpu().numpy(), tl.oracle_forward(ck, cfg["H"], cfg["I"], x, ids, w, "bf16"))
+    out, _, _ = run(lib, packed, x, ids, w, cfg["K"], afmt)
+    tl.check_close(out.float().cpu().numpy(), tl.oracle_forward(ck, cfg["H"], cfg["I"], x, ids, w, afmt))
