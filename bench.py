@@ -303,49 +303,64 @@ def main():
     stream = torch.cuda.current_stream()
     torch.cuda.synchronize()
 
-    # events for the per-stage timing, recorded once so that the handles exist
+    # The timed steps replay CUDA graphs of L = 4R forwards (replicas in
+    # rotation, so every step streams a different layer copy).  The first
+    # forward of each of the NG graphs records per-stage events (external event
+    # nodes), so after the timed loop each event set holds the stage times of
+    # its graph's last replay inside the timed region.
     n_ev = abi.MOE_NUM_STAGES + 1
-    # per-stage events on every 4th step (at most 512 steps), plain runs in between
-    every = 4
-    n_timed_steps = min((args.steps + every - 1) // every, 512)
+    L, NG = 4 * R, 8
     ev_sets = []
-    for _ in range(n_timed_steps):
+    for _ in range(NG):
         evs = [torch.cuda.Event(enable_timing=True) for _ in range(n_ev)]
         for e in evs:
-            e.record(stream)
+            e.record(stream)  # creates the handles
         ev_sets.append(evs)
-    torch.cuda.synchronize()
-
     for i in range(args.warmup):
         binds[i % R].run(stream)
     torch.cuda.synchronize()
+    launches_per_fwd = abi.moe_launch_count(binds[0].handle)
+    cap = torch.cuda.Stream()
+    graphs = []
+    with torch.cuda.stream(cap):
+        for j in range(NG):
+            g = torch.cuda.CUDAGraph()
+            g.capture_begin()
+            for i in range(L):
+                if i == 0:
+                    abi.moe_run_timed(binds[0].handle, [e.cuda_event for e in ev_sets[j]], cap)
+                else:
+                    binds[i % R].run(cap)
+            g.capture_end()
+            graphs.append(g)
+    torch.cuda.synchronize()
+    for g in graphs:  # upload and warm every graph
+        g.replay()
+    torch.cuda.synchronize()
     barrier(world)
 
+    n_rep, rem = divmod(args.steps, L)
     start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    used_sets = []
     with ClockSampler() as clk:
         torch.cuda.synchronize()
         barrier(world)
         start.record(stream)
-        for i in range(args.steps):
-            b = binds[i % R]
-            if i % every == 0 and len(used_sets) < n_timed_steps:
-                evs = ev_sets[len(used_sets)]
-                abi.moe_run_timed(b.handle, [e.cuda_event for e in evs], stream)
-                used_sets.append((i % R, evs))
-            else:
-                b.run(stream)
+        for c in range(n_rep):
+            graphs[c % NG].replay()
+        for i in range(rem):
+            binds[i % R].run(stream)
         end.record(stream)
         torch.cuda.synchronize()
         barrier(world)
     ms = max_over_ranks(start.elapsed_time(end), world)
     value = world * T * args.steps / (ms / 1e3)
 
+    used = ev_sets[:max(1, min(NG, n_rep))]
     stage_ms = np.zeros(abi.MOE_NUM_STAGES)
-    for _, evs in used_sets:
-        for s in range(abi.MOE_NUM_STAGES):
-            stage_ms[s] += evs[s].elapsed_time(evs[s + 1])
-    stage_ms /= max(1, len(used_sets))
+    for evs in used:
+        for s_ in range(abi.MOE_NUM_STAGES):
+            stage_ms[s_] += evs[s_].elapsed_time(evs[s_ + 1])
+    stage_ms /= len(used)
 
     # algorithmic bytes (HBM) of the whole layer and of each kernel, per step
     b13, b2 = expert_bytes(cfg)
@@ -398,7 +413,9 @@ def main():
                      "peak_kind": peak_kind, "unit": "GB/s", "frac": achieved / hbm, "traffic": traffic,
                      "algorithmic_bytes": dom_bytes},
         "layer_roofline_frac": layer_bytes / (ms / args.steps * 1e-3) / 1e9 / hbm,
-        "gpu_launches": args.steps * (4 + (2 if afmt != "bf16" else 0)),
+        "gpu_launches": args.steps * launches_per_fwd,
+        "timing": f"CUDA graphs of {L} forwards replayed; stage events from the last replay of each of "
+                  f"{len(used)} graphs",
         "e2e": {"value": e2e_value, "unit": "tokens/s", "h2d_bytes_per_step": T * H * 2 + T * K * 8,
                 "d2h_bytes_per_step": T * H * 2, "steps": n_e2e},
         "clocks": clk.summary(),

@@ -42,7 +42,7 @@ ACT = {"silu": MOE_ACT_SILU_GATED, "relu2": MOE_ACT_RELU2}
 EXPORTS = (
     "moe_status_str", "moe_plan_weights", "moe_prepare_weights", "moe_is_supported", "moe_plan",
     "moe_bind", "moe_run", "moe_run_timed", "moe_run_host", "moe_device_status", "moe_debug_routing", "moe_quantize",
-    "moe_destroy_weight_plan", "moe_destroy_plan", "moe_destroy_binding", "moe_run_no_alloc",
+    "moe_destroy_weight_plan", "moe_destroy_plan", "moe_destroy_binding", "moe_run_no_alloc", "moe_launch_count",
 )
 
 
@@ -67,6 +67,7 @@ _sig = {
     "moe_bind": (_i32, [_vp, _vp, _sz, _vp, _vp, _vp, _vp, _i32, _vp, _P(_vp)]),
     "moe_run": (_i32, [_vp, _vp]),
     "moe_run_timed": (_i32, [_vp, _vp, _P(_vp)]),
+    "moe_launch_count": (_i32, [_vp, _P(_i32)]),
     "moe_run_host": (_i32, [_vp, _vp, _vp, _vp, _vp, _vp]),
     "moe_device_status": (_i32, [_vp, _vp, _P(_i32)]),
     "moe_debug_routing": (_i32, [_vp, _vp, _P(_i32), _P(_i32), _P(_i32), _P(_i32), _i32]),
@@ -169,6 +170,13 @@ def moe_run_timed(binding, events, stream=None):
     """``events``: MOE_NUM_STAGES+1 raw cudaEvent_t handles (ints) created with timing enabled."""
     arr = (_vp * (MOE_NUM_STAGES + 1))(*events)
     _check(_lib.moe_run_timed(binding, _stream(stream), arr), "moe_run_timed")
+
+
+def moe_launch_count(binding):
+    """Kernels enqueued by the last forward on ``binding``."""
+    n = ctypes.c_int32(0)
+    _check(_lib.moe_launch_count(binding, ctypes.byref(n)), "moe_launch_count")
+    return n.value
 
 
 def moe_run_host(binding, x_host, ids_host, weights_host, out_host, stream=None):

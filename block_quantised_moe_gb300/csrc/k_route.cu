@@ -12,6 +12,7 @@
 #include "common.cuh"
 #include "dequant.cuh"
 #include "internal.h"
+#include "launch.h"
 
 namespace bqmoe {
 
@@ -198,6 +199,7 @@ cudaError_t launch_route(const int32_t *ids, int P, int E, int pad, int ntok, in
   // Launched without programmatic dependent launch: later kernels of the forward
   // may read the routing outputs as soon as they start.
   const int T = stg ? stg->T : 0;
+  ++launch_counter();
   k_route<<<1 + T, kRouteThreads, smem, s>>>(ids, P, E, pad, ntok, large_min, large_tile, counts, offsets, sorted_pair,
                                               pair_pos, active, passes, large, large_tiles, status,
                                               stg ? stg->x : nullptr, stg ? stg->H : 0, stg ? stg->x16 : nullptr,

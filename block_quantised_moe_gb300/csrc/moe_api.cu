@@ -10,6 +10,7 @@
 
 #include "common.cuh"
 #include "internal.h"
+#include "launch.h"
 #include "moe.h"
 
 using namespace bqmoe;
@@ -35,7 +36,15 @@ struct moe_binding_s {
   const float *w = nullptr;
   int T = 0;
   void *out = nullptr;
+  int32_t launches = 0;  // kernels enqueued by the last forward on this binding
 };
+
+namespace bqmoe {
+int &launch_counter() {
+  thread_local int n = 0;
+  return n;
+}
+}  // namespace bqmoe
 
 namespace {
 
@@ -245,8 +254,22 @@ moe_status moe_bind(moe_plan_t plan, void *scratch, size_t scratch_bytes, const 
   return MOE_OK;
 }
 
+static moe_status run_forward(moe_binding b, cudaStream_t stream, cudaEvent_t *ev);
+
 static moe_status run_impl(moe_binding b, cudaStream_t stream, cudaEvent_t *ev) {
-  auto mark = [&](int i) { return ev ? cudaEventRecord(ev[i], stream) : cudaSuccess; };
+  launch_counter() = 0;
+  const moe_status st = run_forward(b, stream, ev);
+  b->launches = launch_counter();
+  return st;
+}
+
+static moe_status run_forward(moe_binding b, cudaStream_t stream, cudaEvent_t *ev) {
+  // Inside stream capture the stage events become event-record nodes of the
+  // graph, so a replayed graph still times its stages.
+  cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
+  if (ev && cudaStreamIsCapturing(stream, &cap) != cudaSuccess) return MOE_ERR_CUDA;
+  const unsigned ev_flags = cap == cudaStreamCaptureStatusActive ? cudaEventRecordExternal : cudaEventRecordDefault;
+  auto mark = [&](int i) { return ev ? cudaEventRecordWithFlags(ev[i], stream, ev_flags) : cudaSuccess; };
   if (b->T == 0) {
     for (int i = 0; ev && i <= MOE_NUM_STAGES; ++i)
       if (mark(i) != cudaSuccess) return MOE_ERR_CUDA;
@@ -426,6 +449,12 @@ moe_status moe_run_timed(moe_binding b, cudaStream_t stream, cudaEvent_t *events
   for (int i = 0; i <= MOE_NUM_STAGES; ++i)
     if (!events[i]) return MOE_ERR_INVALID_ARG;
   return run_impl(b, stream, events);
+}
+
+moe_status moe_launch_count(moe_binding b, int32_t *n) {
+  if (!b || !n) return MOE_ERR_INVALID_ARG;
+  *n = b->launches;
+  return MOE_OK;
 }
 
 moe_status moe_run_host(moe_binding b, const void *x_host, const int32_t *ids_host, const float *weights_host,

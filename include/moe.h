@@ -197,8 +197,16 @@ enum { MOE_STAGE_ROUTE = 0, MOE_STAGE_QUANT_X = 1, MOE_STAGE_GEMM1 = 2, MOE_STAG
  * stage, so cudaEventElapsedTime(events[i], events[i+1]) is the device time of
  * stage i (zero for a stage the activation format skips).  `events` is a host
  * array of MOE_NUM_STAGES+1 cudaEvent_t created with timing enabled.  Nothing
- * is synchronised. */
+ * is synchronised.  Under stream capture the events are recorded as external
+ * event nodes (cudaEventRecordExternal), so every replay of the graph records
+ * them again. */
 MOE_API moe_status moe_run_timed(moe_binding b, cudaStream_t stream, cudaEvent_t *events);
+
+/* Number of kernels the last forward on `b` (moe_run, moe_run_timed or
+ * moe_run_host) enqueued, counted on the host as they were launched; 0 before
+ * the first forward.  Lets a caller count device launches per forward (for
+ * example to size a CUDA graph or to report launches per step).  No CUDA call. */
+MOE_API moe_status moe_launch_count(moe_binding b, int32_t *n);
 
 /* Copy the device status word of the last run to host `status[4]` and
  * synchronise `stream`:
