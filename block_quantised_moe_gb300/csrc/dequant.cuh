@@ -91,6 +91,43 @@ __device__ __forceinline__ uint4 to_half8(const float (&v)[8], float inv) {
   return *reinterpret_cast<uint4 *>(h);
 }
 
+// FP16 activation rows for the NVFP4 tensor-core kernels are stored in "slot
+// order", the K order in which the packer pairs weight codes: inside every
+// 64-element K step, the 16 k-slots of mma i (i = 0..3) hold elements
+// 8 * (i & 1) + m (m = 0..7) of the step's 16-element scale blocks 2 * (i >> 1)
+// (even slots 2m) and 2 * (i >> 1) + 1 (odd slots 2m + 1).  Slot group
+// g = 4 * step + i covers row positions [16g, 16g + 16); slot_group_k(g) is the
+// natural K offset of its even-slot elements (the odd-slot ones sit 16 further).
+__device__ __forceinline__ int slot_group_k(int g) { return 64 * (g >> 2) + 32 * ((g >> 1) & 1) + 8 * (g & 1); }
+
+// Natural elements lo = [k, k + 8) and hi = [k + 16, k + 24) of a slot group,
+// times inv, as its 16 FP16 slots (interleaved lo / hi).
+__device__ __forceinline__ void to_half16_slots(const float (&lo)[8], const float (&hi)[8], float inv, uint4 &o0,
+                                                uint4 &o1) {
+  __align__(16) __half2 h[8];
+#pragma unroll
+  for (int m = 0; m < 8; ++m) h[m] = __floats2half2_rn(lo[m] * inv, hi[m] * inv);
+  o0 = *reinterpret_cast<uint4 *>(&h[0]);
+  o1 = *reinterpret_cast<uint4 *>(&h[4]);
+}
+
+// Row `rid` of a source as FP16 slot-ordered values times inv, written to dst
+// (K halves); lanes 0..nl-1 of the calling group share the work.
+template <int SRC>
+__device__ __forceinline__ void stage_row_slots(const void *act, const uint8_t *act_scales, int64_t rid, int K,
+                                                float inv, __half *dst, int lane, int nl) {
+  for (int g = lane; g < K / 16; g += nl) {
+    const int k = slot_group_k(g);
+    float lo[8], hi[8];
+    src_load8<SRC>(act, act_scales, rid, k, K, lo);
+    src_load8<SRC>(act, act_scales, rid, k + 16, K, hi);
+    uint4 o0, o1;
+    to_half16_slots(lo, hi, inv, o0, o1);
+    reinterpret_cast<uint4 *>(dst + 16 * g)[0] = o0;
+    reinterpret_cast<uint4 *>(dst + 16 * g)[1] = o1;
+  }
+}
+
 __device__ __forceinline__ uint4 to_bf16x8(const float (&v)[8]) {
   __align__(16) __nv_bfloat162 h[4];
 #pragma unroll

@@ -85,14 +85,19 @@ __global__ void k_pack_globals(const float *__restrict__ g13, int n13m, const fl
   reinterpret_cast<float4 *>(gout)[e] = make_float4(a, b, c, 1.f);
 }
 
-// NVFP4 experts are re-tiled for the tensor-core kernel.  Rows are grouped in
+// NVFP4 experts are re-tiled for the tensor-core kernels.  Rows are grouped in
 // 128-row blocks of eight 16-row tiles; for every 64-wide K step a block stores
 // 4608 contiguous bytes: 4096 bytes of codes (tile-major, 32 lanes x 16 bytes
 // in mma.m16n8k16 A-fragment order) then 512 bytes of scales (tile-major, 8
-// groups x 8 bytes).  Lane t (g = t/4, c = t%4), k16 sub-step i, byte j of a
-// code chunk holds the source byte (two codes, even element low) at tile row g
-// (+8 for j odd) and K offset 64q + 16i + 2c (+8 for j >= 2).  Scale group g:
-// byte 2i = scale of (row g, block 4q+i), byte 2i+1 = (row g+8, block 4q+i).
+// groups x 8 bytes).  The K order inside a step is the "slot order" (the
+// activations are staged in the same order): the two codes of every fragment
+// register come from two different 16-element scale blocks, so a register's
+// f16x2 scale multiplier is the conversion of two adjacent scale bytes.  Lane t
+// (g = t/4, c = t%4), mma i, byte j of a code chunk: tile row g (+8 for j odd),
+// m = c + 4 * (j >> 1); low nibble = code at K offset 64q + 32(i >> 1) + 8(i & 1)
+// + m (block 2(i >> 1)), high nibble = the code 16 further (the next block).
+// Scale group g: bytes (s[g][4q], s[g][4q+1], s[g+8][4q], s[g+8][4q+1],
+// s[g][4q+2], s[g][4q+3], s[g+8][4q+2], s[g+8][4q+3]).
 // For gated W13, tile t's rows 0..7 are gate features 8t..8t+7 and rows 8..15
 // the up rows of the same features; otherwise tile rows are consecutive rows.
 // A block's K steps are contiguous, so the kernel streams a block with 1-D bulk
@@ -126,12 +131,17 @@ __global__ void k_pack_mma_codes(const uint8_t *__restrict__ src, uint8_t *__res
     const int g = t >> 2, c = t & 3;
     const uint8_t *se = src + e * rows * row_bytes;
     const int64_t row_lo = tile_src_row(tile, g, gated, I), row_hi = tile_src_row(tile, g + 8, gated, I);
+    auto code = [&](int64_t row, int k) { return (uint32_t)(se[row * row_bytes + k / 2] >> (4 * (k & 1))) & 0xFu; };
     uint32_t w[4];
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
-      const int64_t kb = (64 * q + 16 * i + 2 * c) / 2;
-      w[i] = (uint32_t)se[row_lo * row_bytes + kb] | ((uint32_t)se[row_hi * row_bytes + kb] << 8) |
-             ((uint32_t)se[row_lo * row_bytes + kb + 4] << 16) | ((uint32_t)se[row_hi * row_bytes + kb + 4] << 24);
+      w[i] = 0u;
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        const int64_t row = (j & 1) ? row_hi : row_lo;
+        const int k = 64 * q + 32 * (i >> 1) + 8 * (i & 1) + c + 4 * (j >> 1);
+        w[i] |= (code(row, k) | (code(row, k + 16) << 4)) << (8 * j);
+      }
     }
     uint8_t *d = dst + mma_step_base(e, tile, q, ntiles, nsteps) + (tile % 8) * 512 + t * 16;
     *reinterpret_cast<uint4 *>(d) = make_uint4(w[0], w[1], w[2], w[3]);
@@ -153,12 +163,9 @@ __global__ void k_pack_mma_scales(const uint8_t *__restrict__ src, uint8_t *__re
     const int64_t e = r / ntiles;
     const uint8_t *se = src + e * rows * row_bytes;
     const int64_t row_lo = tile_src_row(tile, g, gated, I), row_hi = tile_src_row(tile, g + 8, gated, I);
-    uint32_t w[2] = {0u, 0u};
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      const uint32_t pair = (uint32_t)se[row_lo * row_bytes + 4 * q + i] | ((uint32_t)se[row_hi * row_bytes + 4 * q + i] << 8);
-      w[i >> 1] |= pair << (16 * (i & 1));
-    }
+    auto sc = [&](int64_t row, int b) { return (uint32_t)se[row * row_bytes + 4 * q + b]; };
+    const uint32_t w[2] = {sc(row_lo, 0) | sc(row_lo, 1) << 8 | sc(row_hi, 0) << 16 | sc(row_hi, 1) << 24,
+                           sc(row_lo, 2) | sc(row_lo, 3) << 8 | sc(row_hi, 2) << 16 | sc(row_hi, 3) << 24};
     uint8_t *d = dst + mma_step_base(e, tile, q, ntiles, nsteps) + 4096 + (tile % 8) * 64 + g * 8;
     *reinterpret_cast<uint2 *>(d) = make_uint2(w[0], w[1]);
   }

@@ -97,11 +97,7 @@ k_stage_x16(const void *__restrict__ act, const uint8_t *__restrict__ act_scales
     f = stage_factor(m);
   }
   const float inv = nv ? 1.f : __frcp_rn(f);  // exact: f is a power of two
-  for (int k = threadIdx.x * 8; k < K; k += kStageThreads * 8) {
-    float v[8];
-    src_load8<SRC>(act, act_scales, row, k, K, v);
-    *reinterpret_cast<uint4 *>(x16 + row * K + k) = to_half8(v, inv);
-  }
+  stage_row_slots<SRC>(act, act_scales, row, K, inv, x16 + row * K, threadIdx.x, kStageThreads);
   if (threadIdx.x == 0) fac[row] = f;
 }
 
@@ -125,6 +121,9 @@ constexpr int kStepBytes = 4608;  // one 64-K step of a 128-row block
 constexpr int kSPS = 4;           // K steps per ring stage
 constexpr int kStageBytes = kStepBytes * kSPS;
 constexpr int kMaxStages = 8;
+// Two 9-warp CTAs per SM put five warps on some SM sub-partitions, whose
+// register files hold 16K registers each: 5 x 32 x 96 <= 16384.
+constexpr int kMmaMaxRegs = 96;
 // Barrier among the consumer warps only (the producer never joins), built on an
 // mbarrier so that its wait is bounded too.  Lane 0 of each warp arrives after
 // the warp's own shared-memory writes and cp.async copies are complete.
@@ -170,7 +169,7 @@ struct ItemCursor {
 };
 
 template <int SRC, int STAGE, int NT>
-__global__ void __launch_bounds__(kTmaThreads, 1) k_grouped_mma(const GroupedArgs a, int nst) {
+__global__ void __maxnreg__(kMmaMaxRegs) k_grouped_mma(const GroupedArgs a, int nst) {
   extern __shared__ __align__(1024) uint8_t smem[];
   constexpr int NTOK = 8 * NT;
   const int K = a.K;
@@ -316,11 +315,7 @@ __global__ void __launch_bounds__(kTmaThreads, 1) k_grouped_mma(const GroupedArg
             f = stage_factor(warp_max(m));
           }
           const float inv = SRC == SRC_H_NVFP4 ? 1.f : __frcp_rn(f);
-          for (int k = lane * 8; k < K; k += 256) {
-            float v[8];
-            src_load8<SRC>(a.act, a.act_scales, rid, k, K, v);
-            *reinterpret_cast<uint4 *>(dst + 2 * k) = to_half8(v, inv);
-          }
+          stage_row_slots<SRC>(a.act, a.act_scales, rid, K, inv, reinterpret_cast<__half *>(dst), lane, 32);
           if (lane == 0) fac[j] = f;
         }
         if (SRC == SRC_X16) cp_async_wait_all();
@@ -344,39 +339,47 @@ __global__ void __launch_bounds__(kTmaThreads, 1) k_grouped_mma(const GroupedArg
           ok = false;
           break;
         }
-        const uint8_t *stage = ring + (size_t)slot * kStageBytes;
+        // This warp's fragment chunks of the stage, and the B row address of its first step.
+        const uint8_t *stage = ring + (size_t)slot * kStageBytes + warp * 512 + lane * 16;
+        const uint32_t bq = b_addr + (uint32_t)(st * kSPS * 64 * 2);
         const int nq = min(kSPS, nsteps - st * kSPS);
-        for (int i4 = 0; i4 < nq; ++i4) {
-          const int q = st * kSPS + i4;
-          const uint4 c = *reinterpret_cast<const uint4 *>(stage + i4 * kStepBytes + warp * 512 + lane * 16);
-          const uint2 sc = *reinterpret_cast<const uint2 *>(stage + i4 * kStepBytes + 4096 + warp * 64 + r * 8);
+        auto step = [&](int i4) {
+          const uint4 c = *reinterpret_cast<const uint4 *>(stage + i4 * kStepBytes);
+          const uint2 sc = *reinterpret_cast<const uint2 *>(stage + i4 * kStepBytes + 4096 - warp * 448 - lane * 16 + r * 8);
           const uint32_t cw[4] = {c.x, c.y, c.z, c.w};
-          uint32_t spairs[4];  // (s_r, s_r8) of k16 block i as f16x2
+          // f16x2 scale multipliers: (block 0, block 1) and (block 2, block 3) of rows r and r + 8
+          uint32_t spairs[4];
           e4m3x4_to_f16x2x2(sc.x, spairs[0], spairs[1]);
           e4m3x4_to_f16x2x2(sc.y, spairs[2], spairs[3]);
 #pragma unroll
           for (int i = 0; i < 4; ++i) {
-            const uint32_t s_lo = prmt(spairs[i], 0, 0x1010);  // (s_r, s_r)
-            const uint32_t s_hi = prmt(spairs[i], 0, 0x3232);  // (s_r8, s_r8)
+            const uint32_t s_lo = spairs[2 * (i >> 1)];      // row r
+            const uint32_t s_hi = spairs[2 * (i >> 1) + 1];  // row r + 8
             uint32_t af[4];
             e2m1x8_to_f16x2x4(cw[i], af);
             af[0] = hmul2(af[0], s_lo);
             af[1] = hmul2(af[1], s_hi);
             af[2] = hmul2(af[2], s_lo);
             af[3] = hmul2(af[3], s_hi);
-            const uint32_t kb = (uint32_t)(q * 64 + i * 16) * 2;
+            const uint32_t kb = bq + (uint32_t)(i4 * 64 + i * 16) * 2;
             float(&ac)[NT][4] = (i & 1) ? acc2 : acc;
             if (NT == 2) {
               uint32_t b0, b1, b2, b3;
-              ldmatrix_x4(b_addr + kb, b0, b1, b2, b3);
+              ldmatrix_x4(kb, b0, b1, b2, b3);
               mma_16816(ac[0], af, b0, b1);
               mma_16816(ac[NT - 1], af, b2, b3);
             } else {
               uint32_t b0, b1;
-              ldmatrix_x2(b_addr + kb, b0, b1);
+              ldmatrix_x2(kb, b0, b1);
               mma_16816(ac[0], af, b0, b1);
             }
           }
+        };
+        if (nq == kSPS) {  // full stage: constant offsets
+#pragma unroll
+          for (int i4 = 0; i4 < kSPS; ++i4) step(i4);
+        } else {
+          for (int i4 = 0; i4 < nq; ++i4) step(i4);
         }
         __syncwarp();
         if (lane == 0) mbar_arrive(empty0 + 8u * slot);

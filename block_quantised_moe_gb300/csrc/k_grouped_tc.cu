@@ -338,7 +338,8 @@ __global__ void __launch_bounds__(kTcThreads, 1) k_grouped_tc(const GroupedArgs 
           e4m3x4_to_f16x2x2(sch[i].y, sp[2], sp[3]);
 #pragma unroll
           for (int j = 0; j < 4; ++j) {
-            const uint32_t s_lo = prmt(sp[j], 0, 0x1010), s_hi = prmt(sp[j], 0, 0x3232);
+            // scale pairs (block 2(j>>1), block 2(j>>1)+1) of rows r0 and r1, as f16x2
+            const uint32_t s_lo = sp[2 * (j >> 1)], s_hi = sp[2 * (j >> 1) + 1];
             uint32_t af[4];
             e2m1x8_to_f16x2x4(cw[j], af);
             const int k = 16 * j + 2 * c4;
@@ -629,11 +630,7 @@ __global__ void __launch_bounds__(256) k_stage_h16(const void *__restrict__ act,
       f = stage_factor(warp_max(mx));
     }
     const float inv = SRC == SRC_H_NVFP4 ? 1.f : __frcp_rn(f);
-    for (int k = lane * 8; k < K; k += 256) {
-      float v[8];
-      src_load8<SRC>(act, act_scales, row, k, K, v);
-      *reinterpret_cast<uint4 *>(h16 + row * K + k) = to_half8(v, inv);
-    }
+    stage_row_slots<SRC>(act, act_scales, row, K, inv, h16 + row * K, lane, 32);
     if (lane == 0) fac[row] = f;
   }
 }

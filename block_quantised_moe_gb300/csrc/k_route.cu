@@ -49,11 +49,7 @@ k_route(const int32_t *__restrict__ ids, int P, int E, int pad, int ntok, int la
     for (int w = 0; w < kRouteWarps; ++w) m = fmaxf(m, red[w]);
     const float f = stage_factor(m);
     const float inv = __frcp_rn(f);
-    for (int k = threadIdx.x * 8; k < H; k += kRouteThreads * 8) {
-      float v[8];
-      src_load8<SRC_X_BF16>(x, nullptr, row, k, H, v);
-      *reinterpret_cast<uint4 *>(x16 + row * H + k) = to_half8(v, inv);
-    }
+    stage_row_slots<SRC_X_BF16>(x, nullptr, row, H, inv, x16 + row * H, threadIdx.x, kRouteThreads);
     if (threadIdx.x == 0) xfac[row] = f;
     return;
   }
