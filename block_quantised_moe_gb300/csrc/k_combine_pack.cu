@@ -23,7 +23,8 @@ __global__ void __launch_bounds__(kCombThreads)
 k_combine(const float *__restrict__ part, int H, const int32_t *__restrict__ pair_pos, int K,
           __nv_bfloat16 *__restrict__ out) {
   pdl_trigger();
-  pdl_wait();
+  // pair_pos is a routing output (complete before this kernel started): read and
+  // sort it while the preceding GEMM finishes.
   const int t = blockIdx.y;
   int pos[kMaxK];
   int n = 0;
@@ -34,6 +35,7 @@ k_combine(const float *__restrict__ part, int H, const int32_t *__restrict__ pai
     while (j > 0 && pos[j - 1] > p) { pos[j] = pos[j - 1]; --j; }
     pos[j] = p;
   }
+  pdl_wait();
   const int c = (blockIdx.x * kCombThreads + threadIdx.x) * 4;
   if (c >= H) return;
   float4 v[kMaxK];

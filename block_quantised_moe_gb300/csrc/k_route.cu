@@ -4,11 +4,12 @@
 // section "Using it": fused_moe.bind(..., topk_weights=tw, topk_ids=ti)) and the
 // grouped expert kernels need each expert's pairs contiguous.  One CTA of 1024
 // threads: a shared-memory histogram, a warp scan of the padded counts, then
-// the pairs are scattered in chunks of 1024 in ascending pair order; inside a
-// chunk a pair's rank among equal ids comes from __match_any_sync (within the
-// warp) plus the per-warp counts of the earlier warps, so the result is stable
-// in p = t*K + k and bit-identical from run to run.  Only integer shared-memory
-// atomics are used.
+// the pairs are scattered in chunks of 1024 in ascending pair order (one chunk,
+// with no atomics at all, for decode batches); inside a chunk a pair's rank
+// among equal ids comes from __match_any_sync (within the warp) plus the
+// per-warp counts of the earlier warps, so the result is stable in p = t*K + k
+// and bit-identical from run to run.  Only integer shared-memory atomics are
+// used.
 #include "common.cuh"
 #include "dequant.cuh"
 #include "internal.h"
@@ -28,6 +29,10 @@ k_route(const int32_t *__restrict__ ids, int P, int E, int pad, int ntok, int la
         const __nv_bfloat16 *__restrict__ x, int H, __half *__restrict__ x16, float *__restrict__ xfac,
         float *__restrict__ zero, int64_t zero_n) {
   extern __shared__ int32_t sm[];
+  // Launched with programmatic dependent launch so that its CTAs are resident
+  // before the previous kernel ends; it waits for that kernel before touching
+  // memory and never triggers early (later kernels read its outputs freely).
+  pdl_wait();
   if (blockIdx.x > 0) {
     // CTAs 1..T: BF16 token rows -> FP16 rows with a power-of-two factor (the
     // tensor-core kernels' B operand), and clear the per-pair max |h| array.
@@ -65,14 +70,44 @@ k_route(const int32_t *__restrict__ ids, int P, int E, int pad, int ntok, int la
   if (tid == 0) dropped = 0;
   __syncthreads();
 
-  // 1. histogram
-  int my_drop = 0;
-  for (int p = tid; p < P; p += kRouteThreads) {
-    const int id = ids[p];
-    if (id >= 0 && id < E) atomicAdd(&hist[id], 1);
-    else ++my_drop;
+  // 1. histogram.  Up to kRouteThreads pairs (decode) one thread per pair:
+  // per-warp counts from __match_any_sync, then for every expert an exclusive
+  // prefix of those counts over the warps (one warp-wide scan per expert), so
+  // the scatter below needs no further pass.  Otherwise shared-memory atomics.
+  const bool one_pass = P <= kRouteThreads;
+  int my_id = -1, my_rank = 0;
+  if (one_pass) {
+    const int p = tid;
+    my_id = p < P ? ids[p] : -1;
+    const bool valid = my_id >= 0 && my_id < E;
+    const unsigned same = __match_any_sync(0xffffffffu, valid ? my_id : E);
+    my_rank = __popc(same & ((1u << lane) - 1u));
+    // expert-major [E][kRouteWarps] here, so the per-expert scans read consecutive words
+    if (valid && my_rank == 0) warp_hist[my_id * kRouteWarps + warp] = __popc(same);
+    const unsigned drops = __ballot_sync(0xffffffffu, p < P && !valid);
+    if (lane == 0 && drops) atomicAdd(&dropped, __popc(drops));
+    if (!valid) my_id = -1;
+    __syncthreads();
+    for (int e = warp; e < E; e += kRouteWarps) {
+      const int v = warp_hist[e * kRouteWarps + lane];
+      int incl = v;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int n = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += n;
+      }
+      warp_hist[e * kRouteWarps + lane] = incl - v;
+      if (lane == 31) hist[e] = incl;
+    }
+  } else {
+    int my_drop = 0;
+    for (int p = tid; p < P; p += kRouteThreads) {
+      const int id = ids[p];
+      if (id >= 0 && id < E) atomicAdd(&hist[id], 1);
+      else ++my_drop;
+    }
+    if (my_drop) atomicAdd(&dropped, my_drop);
   }
-  if (my_drop) atomicAdd(&dropped, my_drop);
   __syncthreads();
 
   // 2. exclusive scan of the padded counts (warp 0)
@@ -142,9 +177,20 @@ k_route(const int32_t *__restrict__ ids, int P, int E, int pad, int ntok, int la
   for (int e = warp; e < E; e += kRouteWarps)
     for (int j = base[e] + hist[e] + lane; j < base[e + 1]; j += 32) sorted_pair[j] = -1;
 
-  // 3. stable scatter, 1024 pairs at a time
+  // 3. stable scatter: position = expert base + pairs of the expert in earlier
+  // warps + rank in the warp (one pass), else 1024 pairs at a time
+  if (one_pass) {
+    const int p = tid;
+    if (my_id >= 0) {
+      const int pos = base[my_id] + warp_hist[my_id * kRouteWarps + warp] + my_rank;
+      sorted_pair[pos] = p;
+      pair_pos[p] = pos;
+    } else if (p < P) {
+      pair_pos[p] = -1;
+    }
+  }
   const unsigned lt_mask = (1u << lane) - 1u;
-  for (int c0 = 0; c0 < P; c0 += kRouteThreads) {
+  for (int c0 = 0; c0 < P && !one_pass; c0 += kRouteThreads) {
     const int p = c0 + tid;
     const int id = p < P ? ids[p] : -1;
     const bool valid = id >= 0 && id < E;
@@ -192,16 +238,14 @@ cudaError_t launch_route(const int32_t *ids, int P, int E, int pad, int ntok, in
   // Per-device function attribute; cheap and idempotent, so set on every launch.
   cudaError_t err = cudaFuncSetAttribute(k_route, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (err != cudaSuccess) return err;
-  // Launched without programmatic dependent launch: later kernels of the forward
-  // may read the routing outputs as soon as they start.
+  // Programmatic launch (the kernel waits before touching memory and never
+  // triggers): later kernels of the forward may read the routing outputs as
+  // soon as they start.
   const int T = stg ? stg->T : 0;
-  ++launch_counter();
-  k_route<<<1 + T, kRouteThreads, smem, s>>>(ids, P, E, pad, ntok, large_min, large_tile, counts, offsets, sorted_pair,
-                                              pair_pos, active, passes, large, large_tiles, status,
-                                              stg ? stg->x : nullptr, stg ? stg->H : 0, stg ? stg->x16 : nullptr,
-                                              stg ? stg->xfac : nullptr, stg ? stg->zero : nullptr,
-                                              stg ? stg->zero_n : 0);
-  return cudaGetLastError();
+  return launch_pdl(k_route, dim3(1 + T), dim3(kRouteThreads), smem, s, ids, P, E, pad, ntok, large_min, large_tile,
+                    counts, offsets, sorted_pair, pair_pos, active, passes, large, large_tiles, status,
+                    stg ? stg->x : nullptr, stg ? stg->H : 0, stg ? stg->x16 : nullptr, stg ? stg->xfac : nullptr,
+                    stg ? stg->zero : nullptr, stg ? stg->zero_n : (int64_t)0);
 }
 
 }  // namespace bqmoe

@@ -3,9 +3,10 @@
 // Every kernel of a forward except the routing kernel is launched with
 // programmatic stream serialisation: it may start while its predecessor is
 // still running.  Protocol (all kernels of this library follow it):
-//   * the routing kernel is launched normally and never triggers early, so its
-//     outputs (the expert lists, offsets, sorted pairs) are complete when any
-//     later kernel of the forward starts, and may be read before waiting;
+//   * the routing kernel waits for its predecessor before it touches memory and
+//     never triggers early, so its outputs (the expert lists, offsets, sorted
+//     pairs) are complete when any later kernel of the forward starts, and may
+//     be read before waiting;
 //   * a kernel calls pdl_trigger() on entry and pdl_wait() before it reads any
 //     other output of an earlier kernel; every thread that did not wait waits
 //     before it exits, so a kernel's completion implies its predecessor's.
