@@ -101,19 +101,29 @@ __device__ __forceinline__ uint4 to_half8(const float (&v)[8], float inv) {
 __device__ __forceinline__ int slot_group_k(int g) { return 64 * (g >> 2) + 32 * ((g >> 1) & 1) + 8 * (g & 1); }
 
 // Natural elements lo = [k, k + 8) and hi = [k + 16, k + 24) of a slot group,
-// times inv, as its 16 FP16 slots (interleaved lo / hi).
-__device__ __forceinline__ void to_half16_slots(const float (&lo)[8], const float (&hi)[8], float inv, uint4 &o0,
-                                                uint4 &o1) {
-  __align__(16) __half2 h[8];
+// times inv, as its 16 FP16 (or BF16) slots (interleaved lo / hi).
+template <bool BF16OUT>
+__device__ __forceinline__ void to_16bit_slots(const float (&lo)[8], const float (&hi)[8], float inv, uint4 &o0,
+                                               uint4 &o1) {
+  __align__(16) uint32_t h[8];
 #pragma unroll
-  for (int m = 0; m < 8; ++m) h[m] = __floats2half2_rn(lo[m] * inv, hi[m] * inv);
-  o0 = *reinterpret_cast<uint4 *>(&h[0]);
-  o1 = *reinterpret_cast<uint4 *>(&h[4]);
+  for (int m = 0; m < 8; ++m) {
+    if (BF16OUT) {
+      __nv_bfloat162 b = __floats2bfloat162_rn(lo[m] * inv, hi[m] * inv);
+      h[m] = *reinterpret_cast<uint32_t *>(&b);
+    } else {
+      __half2 f = __floats2half2_rn(lo[m] * inv, hi[m] * inv);
+      h[m] = *reinterpret_cast<uint32_t *>(&f);
+    }
+  }
+  o0 = make_uint4(h[0], h[1], h[2], h[3]);
+  o1 = make_uint4(h[4], h[5], h[6], h[7]);
 }
 
-// Row `rid` of a source as FP16 slot-ordered values times inv, written to dst
-// (K halves); lanes 0..nl-1 of the calling group share the work.
-template <int SRC>
+// Row `rid` of a source as FP16 (or BF16) slot-ordered values times inv,
+// written to dst (K 16-bit values); lanes 0..nl-1 of the calling group share
+// the work.
+template <int SRC, bool BF16OUT = false>
 __device__ __forceinline__ void stage_row_slots(const void *act, const uint8_t *act_scales, int64_t rid, int K,
                                                 float inv, __half *dst, int lane, int nl) {
   for (int g = lane; g < K / 16; g += nl) {
@@ -122,17 +132,11 @@ __device__ __forceinline__ void stage_row_slots(const void *act, const uint8_t *
     src_load8<SRC>(act, act_scales, rid, k, K, lo);
     src_load8<SRC>(act, act_scales, rid, k + 16, K, hi);
     uint4 o0, o1;
-    to_half16_slots(lo, hi, inv, o0, o1);
+    to_16bit_slots<BF16OUT>(lo, hi, inv, o0, o1);
     reinterpret_cast<uint4 *>(dst + 16 * g)[0] = o0;
     reinterpret_cast<uint4 *>(dst + 16 * g)[1] = o1;
   }
 }
 
-__device__ __forceinline__ uint4 to_bf16x8(const float (&v)[8]) {
-  __align__(16) __nv_bfloat162 h[4];
-#pragma unroll
-  for (int i = 0; i < 4; ++i) h[i] = __floats2bfloat162_rn(v[2 * i], v[2 * i + 1]);
-  return *reinterpret_cast<uint4 *>(h);
-}
 
 }  // namespace bqmoe

@@ -13,30 +13,21 @@ constexpr size_t kAlign = 256;
 inline size_t align_up(size_t v, size_t a = kAlign) { return (v + a - 1) / a * a; }
 
 // Packed expert buffer written by the packer, segments on 256-byte boundaries:
-//   c13  E2M1 codes of W13 (gate and up rows, or W1), N13 rows x H
-//   s13  block scales of W13
-//   c2   E2M1 codes of W2, H rows x I
-//   s2   block scales of W2
+//   c13  W13 (gate and up rows, or W1; N13 rows x H) codes and block scales,
+//        interleaved per 128-row block and 64-wide K step in mma.m16n8k16
+//        A-fragment order (see the packer)
+//   c2   W2 (H rows x I), same layout
 //   g    float [E][4] global scales (gate|w1, up, down, 1); all 1 for MXFP4
-// LAYOUT_ROWMAJOR keeps the checkpoint order ([E][rows][K/2] codes, [E][rows][K/bs]
-// scales).  LAYOUT_MMA16x64 (NVFP4) interleaves codes and scales per 128-row
-// block and 64-wide K step in mma.m16n8k16 A-fragment order (see the packer):
-// c13 / c2 then hold codes and scales together and s13 / s2 are empty.
-enum { LAYOUT_ROWMAJOR = 0, LAYOUT_MMA16x64 = 1 };
-
 struct WeightLayout {
   int E = 0, H = 0, I = 0, wfmt = 0, act = 0;
-  int layout = LAYOUT_ROWMAJOR;
-  int bs = 16;   // elements per block scale
+  int bs = 16;   // elements per block scale (16 NVFP4, 32 MXFP4)
   int n13 = 0;   // rows of W13
-  size_t off_c13 = 0, off_s13 = 0, off_c2 = 0, off_s2 = 0, off_g = 0, total = 0;
-  size_t c13_expert() const { return (size_t)n13 * H / 2; }
-  size_t s13_expert() const { return (size_t)n13 * H / bs; }
-  size_t c2_expert() const { return (size_t)H * I / 2; }
-  size_t s2_expert() const { return (size_t)H * I / bs; }
-  // LAYOUT_MMA16x64: bytes of one expert's interleaved W13 / W2 segment
-  size_t blk13_expert() const { return c13_expert() + s13_expert(); }
-  size_t blk2_expert() const { return c2_expert() + s2_expert(); }
+  size_t off_c13 = 0, off_c2 = 0, off_g = 0, total = 0;
+  // bytes of one expert's W13 / W2 segment (codes + block scales)
+  size_t blk13_expert() const { return (size_t)n13 * H / 2 + (size_t)n13 * H / bs; }
+  size_t blk2_expert() const { return (size_t)H * I / 2 + (size_t)H * I / bs; }
+  // bytes of one 64-K step of a 128-row block
+  int step_bytes() const { return 4096 + 128 * 64 / bs; }
 };
 
 // Scratch owned by the caller and carved by the plan (offsets in bytes).
@@ -46,7 +37,8 @@ struct ScratchLayout {
   size_t xq_codes = 0, xq_scales = 0, xq_g = 0;
   size_t h = 0, hq_codes = 0, hq_scales = 0, hq_g = 0;
   size_t x16 = 0, xfac = 0, hamax = 0;  // tensor-core path: FP16 x, its factors, per-pair max |h|
-  size_t h16 = 0, h16fac = 0;           // tcgen05 path: FP16 h rows and their factors
+  size_t h16 = 0, h16fac = 0;           // tcgen05 path: 16-bit h rows (and their FP16 factors)
+  size_t xb16 = 0;                      // tcgen05 path, MXFP4: BF16 slot-order x rows
   size_t part = 0, total = 0;
 };
 
@@ -58,8 +50,8 @@ enum Stage { STAGE_GATED = 0, STAGE_RELU2 = 1, STAGE_DOWN = 2 };
 
 struct GroupedArgs {
   // expert weights of this stage
-  const uint8_t *codes, *scales;  // expert 0 base
-  size_t codes_expert, scales_expert;  // bytes per expert
+  const uint8_t *codes;  // expert 0 base of the packed segment (codes + block scales)
+  size_t codes_expert;   // bytes per expert
   const float *globals;  // [E][4]
   int K;       // reduction length
   int n_blocks;  // 128-row blocks of the stage's weight matrix (set by the mma launcher)
@@ -77,7 +69,6 @@ struct GroupedArgs {
   const int32_t *large;        // experts for the tcgen05 kernel: [0] = n, [1..] ids
   const int32_t *large_tiles;  // [i] = 128-token tiles of large experts before i (prefix)
   int act_by_token;            // tcgen05 kernel: B rows indexed by token (GEMM1) or by slot (GEMM2)
-  int tc_min_pairs;            // CUDA-core kernel: > 0 leaves experts with this many pairs to tcgen05
   int32_t *status;        // device status word (timeout flag)
   int top_k;
   const float *topk_weights;
@@ -102,21 +93,20 @@ cudaError_t launch_route(const int32_t *ids, int P, int E, int pad, int ntok, in
                          int32_t *passes, int32_t *large, int32_t *large_tiles, int32_t *status,
                          const RouteStaging *stg, cudaStream_t s);
 
-cudaError_t launch_grouped_cc(int wfmt, int src, int stage, const GroupedArgs &a, int E, cudaStream_t s);
-
-// Tensor-core grouped kernel for LAYOUT_MMA16x64 weights; rows_total = rows of
-// the stage's weight matrix (2I gated, I for ReLU^2, H for the down projection).
-// Tokens per pass of the tensor-core kernels (8, or 16 when `wide` and the
-// staging fits); the routing kernel's pass prefix must use the same value.
+// Register-dequant tensor-core grouped kernel (experts with few pairs), NVFP4 or
+// MXFP4 weights (wfmt); rows_total = rows of the stage's weight matrix (2I gated,
+// I for ReLU^2, H for the down projection).  Tokens per pass (8, or 16 when
+// `wide` and the staging fits); the routing kernel's pass prefix must use the
+// same value.
 int mma_tokens_per_pass(int H, int I, bool wide);
-cudaError_t launch_grouped_mma(int src, int stage, const GroupedArgs &a, int rows_total, int E, int ntok,
+cudaError_t launch_grouped_mma(int wfmt, int src, int stage, const GroupedArgs &a, int rows_total, int E, int ntok,
                                cudaStream_t s);
 
 cudaError_t launch_stage_x16(int src, const void *act, const uint8_t *act_scales, const float *act_g, int T, int K,
                              __half *x16, float *fac, float *zero, int64_t zero_n, cudaStream_t s);
 
-// tcgen05 kernels for experts with many pairs: NVFP4 weights (packed blocks,
-// FP16 operands) or MXFP4 weights (row-major, BF16 operands).
+// tcgen05 kernels for experts with many pairs: NVFP4 weights (FP16 operands)
+// or MXFP4 weights (BF16 operands), both from the packed fragment layout.
 bool tc_supported(int rows_total, int K);
 cudaError_t launch_grouped_tc(int stage, int wfmt, const GroupedArgs &a, int rows_total, int E, cudaStream_t s);
 // h (or its re-quantised codes) as 16-bit rows for the tcgen05 GEMM2: FP16 with a

@@ -65,15 +65,9 @@ cudaError_t launch_combine(const float *part, int H, const int32_t *pair_pos, in
 //
 // One-time preparation of the experts (b12x project page, section "Using it":
 // "weights prepped once per model", fused_moe.prepare_weights).  The packed
-// buffer keeps the checkpoint's row-major, K-contiguous code and scale arrays
-// (what the CUDA-core grouped kernels stream with 8-byte coalesced loads) in
-// 256-byte aligned segments, and gathers the global scales into an [E][4] FP32
-// table (gate|w1, up, down, 1); MXFP4 has no globals and gets 1.0.
-__global__ void k_copy16(const uint4 *__restrict__ src, uint4 *__restrict__ dst, int64_t n16) {
-  for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n16; i += (int64_t)gridDim.x * blockDim.x)
-    dst[i] = __ldg(src + i);
-}
-
+// buffer holds W13 and W2 re-tiled for the tensor-core kernels (below) in
+// 256-byte aligned segments, and the global scales gathered into an [E][4]
+// FP32 table (gate|w1, up, down, 1); MXFP4 has no globals and gets 1.0.
 __global__ void k_pack_globals(const float *__restrict__ g13, int n13m, const float *__restrict__ g2, int E,
                                float *__restrict__ gout) {
   const int e = blockIdx.x * blockDim.x + threadIdx.x;
@@ -87,24 +81,27 @@ __global__ void k_pack_globals(const float *__restrict__ g13, int n13m, const fl
   reinterpret_cast<float4 *>(gout)[e] = make_float4(a, b, c, 1.f);
 }
 
-// NVFP4 experts are re-tiled for the tensor-core kernels.  Rows are grouped in
+// Experts are re-tiled for the tensor-core kernels.  Rows are grouped in
 // 128-row blocks of eight 16-row tiles; for every 64-wide K step a block stores
-// 4608 contiguous bytes: 4096 bytes of codes (tile-major, 32 lanes x 16 bytes
-// in mma.m16n8k16 A-fragment order) then 512 bytes of scales (tile-major, 8
-// groups x 8 bytes).  The K order inside a step is the "slot order" (the
+// 4096 bytes of codes (tile-major, 32 lanes x 16 bytes in mma.m16n8k16
+// A-fragment order) then the block scales: NVFP4 512 bytes (tile-major, 8
+// groups x 8 bytes; 4608 per step), MXFP4 256 bytes (8 groups x 4 bytes; 4352).  The K order inside a step is the "slot order" (the
 // activations are staged in the same order): the two codes of every fragment
 // register come from two different 16-element scale blocks, so a register's
 // f16x2 scale multiplier is the conversion of two adjacent scale bytes.  Lane t
 // (g = t/4, c = t%4), mma i, byte j of a code chunk: tile row g (+8 for j odd),
 // m = c + 4 * (j >> 1); low nibble = code at K offset 64q + 32(i >> 1) + 8(i & 1)
 // + m (block 2(i >> 1)), high nibble = the code 16 further (the next block).
-// Scale group g: bytes (s[g][4q], s[g][4q+1], s[g+8][4q], s[g+8][4q+1],
-// s[g][4q+2], s[g][4q+3], s[g+8][4q+2], s[g+8][4q+3]).
+// NVFP4 scale group g: bytes (s[g][4q], s[g][4q+1], s[g+8][4q], s[g+8][4q+1],
+// s[g][4q+2], s[g][4q+3], s[g+8][4q+2], s[g+8][4q+3]).  MXFP4 (32-element
+// blocks; mma 0-1 of a step lie in block 2q, mma 2-3 in block 2q+1):
+// (s[g][2q], s[g][2q+1], s[g+8][2q], s[g+8][2q+1]).
 // For gated W13, tile t's rows 0..7 are gate features 8t..8t+7 and rows 8..15
 // the up rows of the same features; otherwise tile rows are consecutive rows.
 // A block's K steps are contiguous, so the kernel streams a block with 1-D bulk
 // copies.
-constexpr int64_t kMmaStepBytes = 4608;
+// Bytes of one 64-K step of a 128-row block: codes, then the block scales.
+__host__ __device__ constexpr int64_t mma_step_bytes(int bs) { return 4096 + 128 * 64 / bs; }
 
 __device__ __forceinline__ int64_t tile_src_row(int tile, int rr, int gated, int I) {
   if (gated) return rr < 8 ? (int64_t)tile * 8 + rr : (int64_t)I + tile * 8 + rr - 8;
@@ -112,13 +109,13 @@ __device__ __forceinline__ int64_t tile_src_row(int tile, int rr, int gated, int
 }
 
 // byte offset of (expert, 16-row tile, K step) inside a stage's packed segment
-__device__ __forceinline__ int64_t mma_step_base(int64_t e, int tile, int q, int ntiles, int nsteps) {
+__device__ __forceinline__ int64_t mma_step_base(int64_t e, int tile, int q, int ntiles, int nsteps, int bs) {
   const int nblk = ntiles / 8;
-  return ((e * nblk + tile / 8) * nsteps + q) * kMmaStepBytes;
+  return ((e * nblk + tile / 8) * nsteps + q) * mma_step_bytes(bs);
 }
 
 __global__ void k_pack_mma_codes(const uint8_t *__restrict__ src, uint8_t *__restrict__ dst, int E, int rows, int K,
-                                 int gated, int I) {
+                                 int gated, int I, int bs) {
   const int nsteps = K / 64, ntiles = rows / 16;
   const int64_t n_chunks = (int64_t)E * ntiles * nsteps * 32;
   const int64_t row_bytes = K / 2;
@@ -145,16 +142,17 @@ __global__ void k_pack_mma_codes(const uint8_t *__restrict__ src, uint8_t *__res
         w[i] |= (code(row, k) | (code(row, k + 16) << 4)) << (8 * j);
       }
     }
-    uint8_t *d = dst + mma_step_base(e, tile, q, ntiles, nsteps) + (tile % 8) * 512 + t * 16;
+    uint8_t *d = dst + mma_step_base(e, tile, q, ntiles, nsteps, bs) + (tile % 8) * 512 + t * 16;
     *reinterpret_cast<uint4 *>(d) = make_uint4(w[0], w[1], w[2], w[3]);
   }
 }
 
+template <int BS>
 __global__ void k_pack_mma_scales(const uint8_t *__restrict__ src, uint8_t *__restrict__ dst, int E, int rows, int K,
                                   int gated, int I) {
   const int nsteps = K / 64, ntiles = rows / 16;
   const int64_t n_groups = (int64_t)E * ntiles * nsteps * 8;
-  const int64_t row_bytes = K / 16;
+  const int64_t row_bytes = K / BS;
   for (int64_t idx = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; idx < n_groups;
        idx += (int64_t)gridDim.x * blockDim.x) {
     const int g = (int)(idx & 7);
@@ -165,49 +163,41 @@ __global__ void k_pack_mma_scales(const uint8_t *__restrict__ src, uint8_t *__re
     const int64_t e = r / ntiles;
     const uint8_t *se = src + e * rows * row_bytes;
     const int64_t row_lo = tile_src_row(tile, g, gated, I), row_hi = tile_src_row(tile, g + 8, gated, I);
-    auto sc = [&](int64_t row, int b) { return (uint32_t)se[row * row_bytes + 4 * q + b]; };
-    const uint32_t w[2] = {sc(row_lo, 0) | sc(row_lo, 1) << 8 | sc(row_hi, 0) << 16 | sc(row_hi, 1) << 24,
-                           sc(row_lo, 2) | sc(row_lo, 3) << 8 | sc(row_hi, 2) << 16 | sc(row_hi, 3) << 24};
-    uint8_t *d = dst + mma_step_base(e, tile, q, ntiles, nsteps) + 4096 + (tile % 8) * 64 + g * 8;
-    *reinterpret_cast<uint2 *>(d) = make_uint2(w[0], w[1]);
+    constexpr int per_step = 64 / BS;  // block scales per row and K step
+    auto sc = [&](int64_t row, int b) { return (uint32_t)se[row * row_bytes + per_step * q + b]; };
+    uint8_t *d = dst + mma_step_base(e, tile, q, ntiles, nsteps, BS) + 4096 + (tile % 8) * 8 * 2 * per_step +
+                 g * 2 * per_step;
+    if (BS == 16) {
+      const uint32_t w[2] = {sc(row_lo, 0) | sc(row_lo, 1) << 8 | sc(row_hi, 0) << 16 | sc(row_hi, 1) << 24,
+                             sc(row_lo, 2) | sc(row_lo, 3) << 8 | sc(row_hi, 2) << 16 | sc(row_hi, 3) << 24};
+      *reinterpret_cast<uint2 *>(d) = make_uint2(w[0], w[1]);
+    } else {
+      *reinterpret_cast<uint32_t *>(d) = sc(row_lo, 0) | sc(row_lo, 1) << 8 | sc(row_hi, 0) << 16 | sc(row_hi, 1) << 24;
+    }
   }
 }
 
 static int pack_grid(int64_t n) { return (int)std::max<int64_t>(1, std::min<int64_t>((n + 255) / 256, 152 * 32)); }
 
-static cudaError_t copy_seg(const void *src, void *dst, size_t bytes, cudaStream_t s) {
-  const int64_t n16 = (int64_t)(bytes / 16);
-  if (n16 == 0) return cudaSuccess;
-  const int grid = (int)std::min<int64_t>((n16 + 255) / 256, 152 * 16);
-  k_copy16<<<grid, 256, 0, s>>>(reinterpret_cast<const uint4 *>(src), reinterpret_cast<uint4 *>(dst), n16);
-  return cudaGetLastError();
-}
-
 cudaError_t launch_pack(const WeightLayout &L, const void *w13_codes, const void *w13_scales, const float *w13_global,
                         const void *w2_codes, const void *w2_scales, const float *w2_global, uint8_t *packed,
                         cudaStream_t s) {
-  cudaError_t err;
-  if (L.layout == LAYOUT_MMA16x64) {
-    const int gated = L.n13 == 2 * L.I;
-    const int64_t c13 = (int64_t)L.E * (L.n13 / 16) * (L.H / 64) * 32, s13 = c13 / 4;
-    const int64_t c2 = (int64_t)L.E * (L.H / 16) * (L.I / 64) * 32, s2 = c2 / 4;
-    k_pack_mma_codes<<<pack_grid(c13), 256, 0, s>>>(static_cast<const uint8_t *>(w13_codes), packed + L.off_c13, L.E,
-                                                    L.n13, L.H, gated, L.I);
-    k_pack_mma_scales<<<pack_grid(s13), 256, 0, s>>>(static_cast<const uint8_t *>(w13_scales), packed + L.off_c13,
-                                                     L.E, L.n13, L.H, gated, L.I);
-    k_pack_mma_codes<<<pack_grid(c2), 256, 0, s>>>(static_cast<const uint8_t *>(w2_codes), packed + L.off_c2, L.E,
-                                                   L.H, L.I, 0, L.I);
-    k_pack_mma_scales<<<pack_grid(s2), 256, 0, s>>>(static_cast<const uint8_t *>(w2_scales), packed + L.off_c2, L.E,
-                                                    L.H, L.I, 0, L.I);
-    if ((err = cudaGetLastError()) != cudaSuccess) return err;
-    k_pack_globals<<<(L.E + 127) / 128, 128, 0, s>>>(w13_global, L.n13 / L.I, w2_global, L.E,
-                                                       reinterpret_cast<float *>(packed + L.off_g));
-    return cudaGetLastError();
+  const int gated = L.n13 == 2 * L.I;
+  const int64_t c13 = (int64_t)L.E * (L.n13 / 16) * (L.H / 64) * 32, g13 = c13 / 4;
+  const int64_t c2 = (int64_t)L.E * (L.H / 16) * (L.I / 64) * 32, g2 = c2 / 4;
+  const auto *w13c = static_cast<const uint8_t *>(w13_codes), *w2c = static_cast<const uint8_t *>(w2_codes);
+  const auto *w13s = static_cast<const uint8_t *>(w13_scales), *w2s = static_cast<const uint8_t *>(w2_scales);
+  k_pack_mma_codes<<<pack_grid(c13), 256, 0, s>>>(w13c, packed + L.off_c13, L.E, L.n13, L.H, gated, L.I, L.bs);
+  k_pack_mma_codes<<<pack_grid(c2), 256, 0, s>>>(w2c, packed + L.off_c2, L.E, L.H, L.I, 0, L.I, L.bs);
+  if (L.bs == 16) {
+    k_pack_mma_scales<16><<<pack_grid(g13), 256, 0, s>>>(w13s, packed + L.off_c13, L.E, L.n13, L.H, gated, L.I);
+    k_pack_mma_scales<16><<<pack_grid(g2), 256, 0, s>>>(w2s, packed + L.off_c2, L.E, L.H, L.I, 0, L.I);
+  } else {
+    k_pack_mma_scales<32><<<pack_grid(g13), 256, 0, s>>>(w13s, packed + L.off_c13, L.E, L.n13, L.H, gated, L.I);
+    k_pack_mma_scales<32><<<pack_grid(g2), 256, 0, s>>>(w2s, packed + L.off_c2, L.E, L.H, L.I, 0, L.I);
   }
-  if ((err = copy_seg(w13_codes, packed + L.off_c13, L.E * L.c13_expert(), s)) != cudaSuccess) return err;
-  if ((err = copy_seg(w13_scales, packed + L.off_s13, L.E * L.s13_expert(), s)) != cudaSuccess) return err;
-  if ((err = copy_seg(w2_codes, packed + L.off_c2, L.E * L.c2_expert(), s)) != cudaSuccess) return err;
-  if ((err = copy_seg(w2_scales, packed + L.off_s2, L.E * L.s2_expert(), s)) != cudaSuccess) return err;
+  cudaError_t err = cudaGetLastError();
+  if (err != cudaSuccess) return err;
   k_pack_globals<<<(L.E + 127) / 128, 128, 0, s>>>(w13_global, L.n13 / L.I, w2_global, L.E,
                                                      reinterpret_cast<float *>(packed + L.off_g));
   return cudaGetLastError();

@@ -49,6 +49,15 @@ __device__ __forceinline__ void mma_16816(float (&d)[4], const uint32_t (&a)[4],
       : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
 }
 
+// The same with a zero accumulator input (a fresh partial sum).
+__device__ __forceinline__ void mma_16816_zc(float (&d)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+      "{%10,%10,%10,%10};"
+      : "=f"(d[0]), "=f"(d[1]), "=f"(d[2]), "=f"(d[3])
+      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1), "f"(0.f));
+}
+
 __device__ __forceinline__ void ldmatrix_x4(uint32_t addr, uint32_t &r0, uint32_t &r1, uint32_t &r2, uint32_t &r3) {
   asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
                : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
@@ -117,7 +126,11 @@ k_stage_x16(const void *__restrict__ act, const uint8_t *__restrict__ act_scales
 
 constexpr int kConsumers = 8;
 constexpr int kTmaThreads = (kConsumers + 1) * 32;
-constexpr int kStepBytes = 4608;  // one 64-K step of a 128-row block
+// One 64-K step of a 128-row block: 4096 code bytes + block scales (NVFP4 512,
+// MXFP4 256).  Ring stages are sized for the larger.
+template <int WF>
+constexpr int step_bytes() { return WF == W_NVFP4 ? 4608 : 4352; }
+constexpr int kStepBytes = 4608;
 constexpr int kSPS = 4;           // K steps per ring stage
 constexpr int kStageBytes = kStepBytes * kSPS;
 constexpr int kMaxStages = 8;
@@ -168,7 +181,7 @@ struct ItemCursor {
   }
 };
 
-template <int SRC, int STAGE, int NT>
+template <int WF, int SRC, int STAGE, int NT>
 __global__ void __maxnreg__(kMmaMaxRegs) k_grouped_mma(const GroupedArgs a, int nst) {
   extern __shared__ __align__(1024) uint8_t smem[];
   constexpr int NTOK = 8 * NT;
@@ -215,16 +228,17 @@ __global__ void __maxnreg__(kMmaMaxRegs) k_grouped_mma(const GroupedArgs a, int 
       bool ok = true;
       for (int u = u0; u < u1 && ok; ++u) {
         const Item w = cur.at(a, u, nblk);
-        const uint8_t *base = a.codes + (size_t)w.e * a.codes_expert + (size_t)w.blk * nsteps * kStepBytes;
+        const uint8_t *base = a.codes + (size_t)w.e * a.codes_expert + (size_t)w.blk * nsteps * step_bytes<WF>();
         {
           for (int st = 0; st < stages_per_pass; ++st) {
             if (!mbar_wait(empty0 + 8u * slot, phase ^ 1u)) {
               ok = false;
               break;
             }
-            const uint32_t bytes = (uint32_t)min(kSPS, nsteps - st * kSPS) * kStepBytes;
+            const uint32_t bytes = (uint32_t)min(kSPS, nsteps - st * kSPS) * step_bytes<WF>();
             mbar_expect_tx(full0 + 8u * slot, bytes);
-            bulk_g2s(ring_s + (uint32_t)slot * kStageBytes, base + (size_t)st * kStageBytes, bytes, full0 + 8u * slot);
+            bulk_g2s(ring_s + (uint32_t)slot * kStageBytes, base + (size_t)st * kSPS * step_bytes<WF>(), bytes,
+                     full0 + 8u * slot);
             issued |= 1u << slot;
             issued_parity = (issued_parity & ~(1u << slot)) | (phase << slot);
             if (++slot == nst) {
@@ -344,34 +358,79 @@ __global__ void __maxnreg__(kMmaMaxRegs) k_grouped_mma(const GroupedArgs a, int 
         const uint32_t bq = b_addr + (uint32_t)(st * kSPS * 64 * 2);
         const int nq = min(kSPS, nsteps - st * kSPS);
         auto step = [&](int i4) {
-          const uint4 c = *reinterpret_cast<const uint4 *>(stage + i4 * kStepBytes);
-          const uint2 sc = *reinterpret_cast<const uint2 *>(stage + i4 * kStepBytes + 4096 - warp * 448 - lane * 16 + r * 8);
+          constexpr int SB = step_bytes<WF>();
+          const uint4 c = *reinterpret_cast<const uint4 *>(stage + i4 * SB);
           const uint32_t cw[4] = {c.x, c.y, c.z, c.w};
-          // f16x2 scale multipliers: (block 0, block 1) and (block 2, block 3) of rows r and r + 8
-          uint32_t spairs[4];
-          e4m3x4_to_f16x2x2(sc.x, spairs[0], spairs[1]);
-          e4m3x4_to_f16x2x2(sc.y, spairs[2], spairs[3]);
+          if (WF == W_NVFP4) {
+            const uint2 sc = *reinterpret_cast<const uint2 *>(stage + i4 * SB + 4096 - warp * 448 - lane * 16 + r * 8);
+            // f16x2 scale multipliers: (block 0, block 1) and (block 2, block 3) of rows r and r + 8
+            uint32_t spairs[4];
+            e4m3x4_to_f16x2x2(sc.x, spairs[0], spairs[1]);
+            e4m3x4_to_f16x2x2(sc.y, spairs[2], spairs[3]);
 #pragma unroll
-          for (int i = 0; i < 4; ++i) {
-            const uint32_t s_lo = spairs[2 * (i >> 1)];      // row r
-            const uint32_t s_hi = spairs[2 * (i >> 1) + 1];  // row r + 8
-            uint32_t af[4];
-            e2m1x8_to_f16x2x4(cw[i], af);
-            af[0] = hmul2(af[0], s_lo);
-            af[1] = hmul2(af[1], s_hi);
-            af[2] = hmul2(af[2], s_lo);
-            af[3] = hmul2(af[3], s_hi);
-            const uint32_t kb = bq + (uint32_t)(i4 * 64 + i * 16) * 2;
-            float(&ac)[NT][4] = (i & 1) ? acc2 : acc;
-            if (NT == 2) {
-              uint32_t b0, b1, b2, b3;
-              ldmatrix_x4(kb, b0, b1, b2, b3);
-              mma_16816(ac[0], af, b0, b1);
-              mma_16816(ac[NT - 1], af, b2, b3);
-            } else {
-              uint32_t b0, b1;
-              ldmatrix_x2(kb, b0, b1);
-              mma_16816(ac[0], af, b0, b1);
+            for (int i = 0; i < 4; ++i) {
+              const uint32_t s_lo = spairs[2 * (i >> 1)];      // row r
+              const uint32_t s_hi = spairs[2 * (i >> 1) + 1];  // row r + 8
+              uint32_t af[4];
+              e2m1x8_to_f16x2x4(cw[i], af);
+              af[0] = hmul2(af[0], s_lo);
+              af[1] = hmul2(af[1], s_hi);
+              af[2] = hmul2(af[2], s_lo);
+              af[3] = hmul2(af[3], s_hi);
+              const uint32_t kb = bq + (uint32_t)(i4 * 64 + i * 16) * 2;
+              float(&ac)[NT][4] = (i & 1) ? acc2 : acc;
+              if (NT == 2) {
+                uint32_t b0, b1, b2, b3;
+                ldmatrix_x4(kb, b0, b1, b2, b3);
+                mma_16816(ac[0], af, b0, b1);
+                mma_16816(ac[NT - 1], af, b2, b3);
+              } else {
+                uint32_t b0, b1;
+                ldmatrix_x2(kb, b0, b1);
+                mma_16816(ac[0], af, b0, b1);
+              }
+            }
+          } else {
+            // MXFP4: mma 0-1 and 2-3 of the step each lie in one 32-element block
+            // (slot order); the E2M1 codes go in unscaled (exact in FP16) and the
+            // block's E8M0 scale 2^X multiplies the two mmas' FP32 partial sum.
+            const uint32_t sw = *reinterpret_cast<const uint32_t *>(stage + i4 * SB + 4096 - warp * 480 - lane * 16 + r * 4);
+#pragma unroll
+            for (int hb = 0; hb < 2; ++hb) {
+              const float s_lo = e8m0_to_f32((sw >> (8 * hb)) & 0xFFu);        // row r
+              const float s_hi = e8m0_to_f32((sw >> (16 + 8 * hb)) & 0xFFu);   // row r + 8
+              float t[NT][4];
+#pragma unroll
+              for (int ii = 0; ii < 2; ++ii) {
+                const int i = 2 * hb + ii;
+                uint32_t af[4];
+                e2m1x8_to_f16x2x4(cw[i], af);
+                const uint32_t kb = bq + (uint32_t)(i4 * 64 + i * 16) * 2;
+                if (NT == 2) {
+                  uint32_t b0, b1, b2, b3;
+                  ldmatrix_x4(kb, b0, b1, b2, b3);
+                  if (ii == 0) {
+                    mma_16816_zc(t[0], af, b0, b1);
+                    mma_16816_zc(t[NT - 1], af, b2, b3);
+                  } else {
+                    mma_16816(t[0], af, b0, b1);
+                    mma_16816(t[NT - 1], af, b2, b3);
+                  }
+                } else {
+                  uint32_t b0, b1;
+                  ldmatrix_x2(kb, b0, b1);
+                  if (ii == 0) mma_16816_zc(t[0], af, b0, b1);
+                  else mma_16816(t[0], af, b0, b1);
+                }
+              }
+              float(&ac)[NT][4] = hb ? acc2 : acc;
+#pragma unroll
+              for (int j = 0; j < NT; ++j) {
+                ac[j][0] = fmaf(s_lo, t[j][0], ac[j][0]);
+                ac[j][1] = fmaf(s_lo, t[j][1], ac[j][1]);
+                ac[j][2] = fmaf(s_hi, t[j][2], ac[j][2]);
+                ac[j][3] = fmaf(s_hi, t[j][3], ac[j][3]);
+              }
             }
           }
         };
@@ -447,7 +506,7 @@ static int num_sms() {
   return n;
 }
 
-template <int SRC, int STAGE, int NT>
+template <int WF, int SRC, int STAGE, int NT>
 static cudaError_t launch_mma_one(const GroupedArgs &a, int rows_total, int E, cudaStream_t s) {
   constexpr size_t kSmemMax = 227 * 1024;
   constexpr size_t kSmemHalf = 112 * 1024;  // two CTAs per SM below this
@@ -462,7 +521,7 @@ static cudaError_t launch_mma_one(const GroupedArgs &a, int rows_total, int E, c
   }
   const size_t smem = tma_smem_bytes(a.K, NT, nst);
   if (smem > kSmemMax) return cudaErrorInvalidValue;
-  cudaError_t err = cudaFuncSetAttribute(k_grouped_mma<SRC, STAGE, NT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+  cudaError_t err = cudaFuncSetAttribute(k_grouped_mma<WF, SRC, STAGE, NT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          (int)smem);
   if (err != cudaSuccess) return err;
   const int sms = num_sms();
@@ -471,30 +530,40 @@ static cudaError_t launch_mma_one(const GroupedArgs &a, int rows_total, int E, c
   g.n_blocks = rows_total / (16 * kConsumers);
   const int units_max = E * g.n_blocks;
   const int grid = std::max(1, std::min(sms * ctas_per_sm, units_max));
-  return launch_pdl(k_grouped_mma<SRC, STAGE, NT>, dim3(grid), dim3(kTmaThreads), smem, s, g, nst);
+  return launch_pdl(k_grouped_mma<WF, SRC, STAGE, NT>, dim3(grid), dim3(kTmaThreads), smem, s, g, nst);
 }
 
-template <int STAGE, int NT>
+template <int WF, int STAGE, int NT>
 static cudaError_t launch_mma_src(int src, const GroupedArgs &a, int rows_total, int E, cudaStream_t s) {
   if (STAGE == STAGE_DOWN) {
     switch (src) {
-      case SRC_H_F32: return launch_mma_one<SRC_H_F32, STAGE, NT>(a, rows_total, E, s);
-      case SRC_H_NVFP4: return launch_mma_one<SRC_H_NVFP4, STAGE, NT>(a, rows_total, E, s);
-      case SRC_H_MXFP8: return launch_mma_one<SRC_H_MXFP8, STAGE, NT>(a, rows_total, E, s);
+      case SRC_H_F32: return launch_mma_one<WF, SRC_H_F32, STAGE, NT>(a, rows_total, E, s);
+      case SRC_H_NVFP4:
+        if (WF == W_NVFP4) return launch_mma_one<W_NVFP4, SRC_H_NVFP4, STAGE, NT>(a, rows_total, E, s);
+        break;
+      case SRC_H_MXFP8: return launch_mma_one<WF, SRC_H_MXFP8, STAGE, NT>(a, rows_total, E, s);
     }
   } else if (src == SRC_X16) {
-    return launch_mma_one<SRC_X16, STAGE, NT>(a, rows_total, E, s);
+    return launch_mma_one<WF, SRC_X16, STAGE, NT>(a, rows_total, E, s);
   }
   return cudaErrorInvalidValue;
 }
 
-template <int NT>
+template <int WF, int NT>
 static cudaError_t launch_mma_nt(int src, int stage, const GroupedArgs &a, int rows_total, int E, cudaStream_t s) {
   switch (stage) {
-    case STAGE_GATED: return launch_mma_src<STAGE_GATED, NT>(src, a, rows_total, E, s);
-    case STAGE_RELU2: return launch_mma_src<STAGE_RELU2, NT>(src, a, rows_total, E, s);
-    case STAGE_DOWN: return launch_mma_src<STAGE_DOWN, NT>(src, a, rows_total, E, s);
+    case STAGE_GATED: return launch_mma_src<WF, STAGE_GATED, NT>(src, a, rows_total, E, s);
+    case STAGE_RELU2: return launch_mma_src<WF, STAGE_RELU2, NT>(src, a, rows_total, E, s);
+    case STAGE_DOWN: return launch_mma_src<WF, STAGE_DOWN, NT>(src, a, rows_total, E, s);
   }
+  return cudaErrorInvalidValue;
+}
+
+template <int WF>
+static cudaError_t launch_mma_wf(int src, int stage, const GroupedArgs &a, int rows_total, int E, int ntok,
+                                 cudaStream_t s) {
+  if (ntok == 16) return launch_mma_nt<WF, 2>(src, stage, a, rows_total, E, s);
+  if (ntok == 8) return launch_mma_nt<WF, 1>(src, stage, a, rows_total, E, s);
   return cudaErrorInvalidValue;
 }
 
@@ -505,11 +574,11 @@ int mma_tokens_per_pass(int H, int I, bool wide) {
 
 // rows_total: rows of the weight matrix of this stage (2I gated, I for ReLU^2, H down).
 // ntok: tokens per pass (8 or 16, from mma_tokens_per_pass; must match routing's).
-cudaError_t launch_grouped_mma(int src, int stage, const GroupedArgs &a, int rows_total, int E, int ntok,
+cudaError_t launch_grouped_mma(int wfmt, int src, int stage, const GroupedArgs &a, int rows_total, int E, int ntok,
                                cudaStream_t s) {
   if (rows_total % (16 * kConsumers) != 0 || a.K % 64 != 0) return cudaErrorInvalidValue;
-  if (ntok == 16) return launch_mma_nt<2>(src, stage, a, rows_total, E, s);
-  if (ntok == 8) return launch_mma_nt<1>(src, stage, a, rows_total, E, s);
+  if (wfmt == W_NVFP4) return launch_mma_wf<W_NVFP4>(src, stage, a, rows_total, E, ntok, s);
+  if (wfmt == W_MXFP4) return launch_mma_wf<W_MXFP4>(src, stage, a, rows_total, E, ntok, s);
   return cudaErrorInvalidValue;
 }
 

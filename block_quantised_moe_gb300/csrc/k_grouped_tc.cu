@@ -48,7 +48,6 @@ constexpr int kTcBLag = 4;                   // cp.async stages a B thread keeps
 constexpr int kTcRingBytes = kTcAStages * kTcAStageBytes + kTcBStages * kTcBBytes;
 constexpr int kTcAccCols = kTcMB * kTcN;     // TMEM columns per accumulator buffer
 constexpr int kTcTmemCols = 2 * kTcAccCols;  // double buffered
-constexpr int kTcStepBytes = 4608;           // packed NVFP4: one 64-K step of a 128-row block
 constexpr int kTcAChunks = kTcMB * 8 * 32 / (kTcAWarps * 32);  // fragment chunks per A thread per k-block
 constexpr int kTcBRows = kTcN * 8 / (kTcBWarps * 32);          // 16-byte chunks per B thread per k-block
 
@@ -139,8 +138,8 @@ struct TcCursor {
 
 // ------------------------------------------------------------------ kernel
 
-// WF: W_NVFP4 (packed 128-row blocks, FP16 operands) or W_MXFP4 (row-major
-// checkpoint layout, BF16 operands: E2M1 * 2^X is exact in BF16 for any E8M0 X).
+// WF: W_NVFP4 (FP16 operands) or W_MXFP4 (BF16 operands: E2M1 * 2^X is exact in
+// BF16 for any E8M0 X); both read the packed fragment layout.
 template <int STAGE, int WF>
 __global__ void __launch_bounds__(kTcThreads, 1) k_grouped_tc(const GroupedArgs a) {
   extern __shared__ uint8_t smem_raw[];
@@ -201,87 +200,13 @@ __global__ void __launch_bounds__(kTcThreads, 1) k_grouped_tc(const GroupedArgs 
   if (w0 < W) cur.seek(a, w0, nbp);
   bool ok = true;
 
-  if (WF == W_MXFP4 && warp >= kTcEpiWarps && warp < kTcEpiWarps + kTcAWarps) {
-    // ---------------------------------------------- A producers (MXFP4, BF16)
-    // One weight row per thread per k-block: 32 code bytes and 2 E8M0 scales,
-    // decoded to BF16 (E2M1 * 2^X, exact) and written as 8 swizzled 16-byte chunks.
-    const int t = threadIdx.x - kTcEpiWarps * 32;  // row of the item's 256
-    const int blk_l = t >> 7, m = t & 127;
-    const bool gated = STAGE == STAGE_GATED;
-    int slot = 0;
-    uint32_t phase = 0;
-    uint4 c0, c1, n0, n1;
-    uint32_t sc = 0, nsc = 0;
-    auto load = [&](const TcItem &it, int kb, uint4 &d0, uint4 &d1, uint32_t &ds) {
-      const int blk = 2 * it.bp + blk_l;
-      const int64_t row = gated ? (m & 15) < 8 ? (int64_t)(8 * blk + (m >> 4)) * 8 + (m & 15)
-                                             : (int64_t)a.I + (int64_t)(8 * blk + (m >> 4)) * 8 + (m & 15) - 8
-                                : (int64_t)blk * 128 + m;
-      const uint4 *cp = reinterpret_cast<const uint4 *>(a.codes + (size_t)it.e * a.codes_expert + row * (K / 2) + kb * 32);
-      d0 = __ldg(cp);
-      d1 = __ldg(cp + 1);
-      const uint8_t *sp = a.scales + (size_t)it.e * a.scales_expert + row * (K / 32) + kb * 2;
-      ds = (uint32_t)__ldg(sp) | ((uint32_t)__ldg(sp + 1) << 8);
-    };
-    TcCursor pcur = cur;
-    int pw = w0, pkb = 0;
-    TcItem pit;
-    if (pw < W) {
-      pit = pcur.at(a, pw, nbp);
-      load(pit, 0, n0, n1, nsc);
-    }
-    for (int w = w0; w < W && ok; w += wstep) {
-      for (int kb = 0; kb < nk; ++kb) {
-        c0 = n0;
-        c1 = n1;
-        sc = nsc;
-        if (++pkb == nk) {
-          pkb = 0;
-          pw += wstep;
-          if (pw < W) pit = pcur.at(a, pw, nbp);
-        }
-        if (pw < W) load(pit, pkb, n0, n1, nsc);
-        if (!mbar_wait(aempty0 + 8u * slot, phase ^ 1u)) {
-          ok = false;
-          break;
-        }
-        uint8_t *tileA = base + (size_t)slot * kTcAStageBytes + blk_l * kTcABytes;
-        const uint32_t words[8] = {c0.x, c0.y, c0.z, c0.w, c1.x, c1.y, c1.z, c1.w};
-#pragma unroll
-        for (int h = 0; h < 2; ++h) {  // two 32-element MX blocks
-          const float p2 = e8m0_to_f32((sc >> (8 * h)) & 0xFFu);
-#pragma unroll
-          for (int q = 0; q < 2; ++q) {  // 16 elements -> 2 chunks of 8
-            uint32_t out[8];
-#pragma unroll
-            for (int wq = 0; wq < 2; ++wq) {
-              float v[8];
-              e2m1x8_to_f32(words[4 * h + 2 * q + wq], v);
-#pragma unroll
-              for (int i = 0; i < 4; ++i) {
-                __nv_bfloat162 b2 = __floats2bfloat162_rn(v[2 * i] * p2, v[2 * i + 1] * p2);
-                out[4 * wq + i] = *reinterpret_cast<uint32_t *>(&b2);
-              }
-            }
-#pragma unroll
-            for (int cc = 0; cc < 2; ++cc) {
-              const int c = 4 * h + 2 * q + cc;  // 16-byte chunk of the 128-byte row
-              *reinterpret_cast<uint4 *>(tileA + (m >> 3) * 1024 + (m & 7) * 128 + (((c ^ m) & 7) << 4)) =
-                  make_uint4(out[4 * cc], out[4 * cc + 1], out[4 * cc + 2], out[4 * cc + 3]);
-            }
-          }
-        }
-        fence_async_smem();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(afull0 + 8u * slot);
-        if (++slot == kTcAStages) {
-          slot = 0;
-          phase ^= 1u;
-        }
-      }
-    }
-  } else if (WF == W_NVFP4 && warp >= kTcEpiWarps && warp < kTcEpiWarps + kTcAWarps) {
-    // ---------------------------------------------- A producers (NVFP4, FP16)
+  if (warp >= kTcEpiWarps && warp < kTcEpiWarps + kTcAWarps) {
+    // ------------------------------------------------------ A producers
+    // The packed fragment chunks (16 code bytes per lane, the lane group's block
+    // scales) of two 128-row blocks, dequantised to 16-bit values and written
+    // at their slot positions in the swizzled tile: NVFP4 as FP16 (E2M1 x E4M3
+    // is exact), MXFP4 as BF16 (E2M1 x 2^X is exact for every E8M0 X).
+    constexpr int SB = WF == W_NVFP4 ? 4608 : 4352;  // bytes of one 64-K step of a block
     const int t = threadIdx.x - kTcEpiWarps * 32;  // 0..kTcAWarps*32-1
     int slot = 0;
     uint32_t phase = 0;
@@ -295,9 +220,10 @@ __global__ void __launch_bounds__(kTcThreads, 1) k_grouped_tc(const GroupedArgs 
       for (int i = 0; i < kTcAChunks; ++i) {
         const int c = t + kTcAWarps * 32 * i;
         const int blk = 2 * it.bp + (c >> 8), tile = (c >> 5) & 7, ln = c & 31;
-        const uint8_t *step = ebase + ((size_t)blk * nk + kb) * kTcStepBytes;
+        const uint8_t *step = ebase + ((size_t)blk * nk + kb) * SB;
         c4[i] = __ldg(reinterpret_cast<const uint4 *>(step + tile * 512 + ln * 16));
-        s4[i] = __ldg(reinterpret_cast<const uint2 *>(step + 4096 + tile * 64 + (ln >> 2) * 8));
+        if (WF == W_NVFP4) s4[i] = __ldg(reinterpret_cast<const uint2 *>(step + 4096 + tile * 64 + (ln >> 2) * 8));
+        else s4[i] = make_uint2(__ldg(reinterpret_cast<const uint32_t *>(step + 4096 + tile * 32 + (ln >> 2) * 4)), 0u);
       }
     };
     TcCursor pcur = cur;  // cursor for the prefetch (runs one k-block ahead)
@@ -333,20 +259,46 @@ __global__ void __launch_bounds__(kTcThreads, 1) k_grouped_tc(const GroupedArgs 
           const int g = ln >> 2, c4 = ln & 3;
           const int r0 = 16 * tile + g, r1 = r0 + 8;
           const uint32_t cw[4] = {cch[i].x, cch[i].y, cch[i].z, cch[i].w};
-          uint32_t sp[4];
-          e4m3x4_to_f16x2x2(sch[i].x, sp[0], sp[1]);
-          e4m3x4_to_f16x2x2(sch[i].y, sp[2], sp[3]);
+          uint32_t o[4][4];  // 16-bit pairs of mma j: (r0, k), (r1, k), (r0, k + 8), (r1, k + 8)
+          if (WF == W_NVFP4) {
+            uint32_t sp[4];
+            e4m3x4_to_f16x2x2(sch[i].x, sp[0], sp[1]);
+            e4m3x4_to_f16x2x2(sch[i].y, sp[2], sp[3]);
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+              // scale pairs (block 2(j>>1), block 2(j>>1)+1) of rows r0 and r1, as f16x2
+              const uint32_t s_lo = sp[2 * (j >> 1)], s_hi = sp[2 * (j >> 1) + 1];
+              uint32_t af[4];
+              e2m1x8_to_f16x2x4(cw[j], af);
+              o[j][0] = hmul2(af[0], s_lo);
+              o[j][1] = hmul2(af[1], s_hi);
+              o[j][2] = hmul2(af[2], s_lo);
+              o[j][3] = hmul2(af[3], s_hi);
+            }
+          } else {
+            const uint32_t sw = sch[i].x;  // (r0 block 0, r0 block 1, r1 block 0, r1 block 1)
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+              const float s_lo = e8m0_to_f32((sw >> (8 * (j >> 1))) & 0xFFu);
+              const float s_hi = e8m0_to_f32((sw >> (16 + 8 * (j >> 1))) & 0xFFu);
+              uint32_t af[4];
+              e2m1x8_to_f16x2x4(cw[j], af);
+#pragma unroll
+              for (int q = 0; q < 4; ++q) {
+                const float2 v = __half22float2(*reinterpret_cast<const __half2 *>(&af[q]));
+                const float sc = (q & 1) ? s_hi : s_lo;
+                __nv_bfloat162 b2 = __floats2bfloat162_rn(v.x * sc, v.y * sc);
+                o[j][q] = *reinterpret_cast<uint32_t *>(&b2);
+              }
+            }
+          }
 #pragma unroll
           for (int j = 0; j < 4; ++j) {
-            // scale pairs (block 2(j>>1), block 2(j>>1)+1) of rows r0 and r1, as f16x2
-            const uint32_t s_lo = sp[2 * (j >> 1)], s_hi = sp[2 * (j >> 1) + 1];
-            uint32_t af[4];
-            e2m1x8_to_f16x2x4(cw[j], af);
             const int k = 16 * j + 2 * c4;
-            *reinterpret_cast<uint32_t *>(tileA + sw128_elem(r0, k)) = hmul2(af[0], s_lo);
-            *reinterpret_cast<uint32_t *>(tileA + sw128_elem(r1, k)) = hmul2(af[1], s_hi);
-            *reinterpret_cast<uint32_t *>(tileA + sw128_elem(r0, k + 8)) = hmul2(af[2], s_lo);
-            *reinterpret_cast<uint32_t *>(tileA + sw128_elem(r1, k + 8)) = hmul2(af[3], s_hi);
+            *reinterpret_cast<uint32_t *>(tileA + sw128_elem(r0, k)) = o[j][0];
+            *reinterpret_cast<uint32_t *>(tileA + sw128_elem(r1, k)) = o[j][1];
+            *reinterpret_cast<uint32_t *>(tileA + sw128_elem(r0, k + 8)) = o[j][2];
+            *reinterpret_cast<uint32_t *>(tileA + sw128_elem(r1, k + 8)) = o[j][3];
           }
         }
         fence_async_smem();
@@ -606,12 +558,8 @@ __global__ void __launch_bounds__(256) k_stage_h16(const void *__restrict__ act,
   pdl_wait();
   const int64_t live = rows_dev == nullptr || rows < (int64_t)*rows_dev ? rows : (int64_t)*rows_dev;
   for (int64_t row = (int64_t)blockIdx.x * 8 + (threadIdx.x >> 5); row < live; row += (int64_t)gridDim.x * 8) {
-    if (OUT_BF16) {  // BF16 rows, no factor (the MXFP4 path's BF16 operands)
-      for (int k = lane * 8; k < K; k += 256) {
-        float v[8];
-        src_load8<SRC>(act, act_scales, row, k, K, v);
-        *reinterpret_cast<uint4 *>(h16 + row * K + k) = to_bf16x8(v);
-      }
+    if (OUT_BF16) {  // BF16 slot-order rows, no factor (the MXFP4 path's BF16 operands)
+      stage_row_slots<SRC, true>(act, act_scales, row, K, 1.f, h16 + row * K, lane, 32);
       continue;
     }
     float f;
@@ -642,6 +590,7 @@ cudaError_t launch_stage_h16(int src, const void *act, const uint8_t *act_scales
   const int grid = (int)std::min<int64_t>((rows + 7) / 8, 152 * 16);
   if (out_bf16) {
     switch (src) {
+      case SRC_X_BF16: return launch_pdl(k_stage_h16<SRC_X_BF16, true>, dim3(grid), dim3(256), 0, s, act, act_scales, act_g, K, rows, rows_dev, h16, fac);
       case SRC_H_F32: return launch_pdl(k_stage_h16<SRC_H_F32, true>, dim3(grid), dim3(256), 0, s, act, act_scales, act_g, K, rows, rows_dev, h16, fac);
       case SRC_H_MXFP8: return launch_pdl(k_stage_h16<SRC_H_MXFP8, true>, dim3(grid), dim3(256), 0, s, act, act_scales, act_g, K, rows, rows_dev, h16, fac);
       default: return cudaErrorInvalidValue;

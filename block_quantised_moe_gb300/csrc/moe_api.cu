@@ -94,19 +94,9 @@ moe_status moe_plan_weights(const moe_weight_desc *d, moe_weight_plan *out, size
   L.act = d->act;
   L.bs = d->wfmt == MOE_W_NVFP4 ? 16 : 32;
   L.n13 = d->act == MOE_ACT_SILU_GATED ? 2 * L.I : L.I;
-  L.layout = d->wfmt == MOE_W_NVFP4 ? LAYOUT_MMA16x64 : LAYOUT_ROWMAJOR;
-  L.off_c13 = 0;
-  if (L.layout == LAYOUT_MMA16x64) {  // codes and scales interleaved per block and K step
-    L.off_s13 = align_up(L.off_c13 + (size_t)L.E * L.blk13_expert());
-    L.off_c2 = L.off_s13;
-    L.off_s2 = align_up(L.off_c2 + (size_t)L.E * L.blk2_expert());
-    L.off_g = L.off_s2;
-  } else {
-    L.off_s13 = align_up(L.off_c13 + (size_t)L.E * L.c13_expert());
-    L.off_c2 = align_up(L.off_s13 + (size_t)L.E * L.s13_expert());
-    L.off_s2 = align_up(L.off_c2 + (size_t)L.E * L.c2_expert());
-    L.off_g = align_up(L.off_s2 + (size_t)L.E * L.s2_expert());
-  }
+  L.off_c13 = 0;  // codes and scales interleaved per 128-row block and 64-K step
+  L.off_c2 = align_up(L.off_c13 + (size_t)L.E * L.blk13_expert());
+  L.off_g = align_up(L.off_c2 + (size_t)L.E * L.blk2_expert());
   L.total = align_up(L.off_g + (size_t)L.E * 4 * sizeof(float));
   moe_weight_plan p = new (std::nothrow) moe_weight_plan_s{L};
   if (!p) return MOE_ERR_CAPACITY;
@@ -140,7 +130,7 @@ moe_status moe_is_supported(const moe_caps *c) {
   // MXFP4 weights with BF16 or MXFP8 activations.
   if (c->wplan->L.wfmt == MOE_W_MXFP4 && c->afmt == MOE_A_NVFP4) return MOE_ERR_UNSUPPORTED;
   // The tensor-core kernel works on 128-row blocks of each weight matrix.
-  if (c->wplan->L.layout == LAYOUT_MMA16x64 && c->wplan->L.n13 % 128 != 0) return MOE_ERR_UNSUPPORTED;
+  if (c->wplan->L.n13 % 128 != 0) return MOE_ERR_UNSUPPORTED;
   return MOE_OK;
 }
 
@@ -192,28 +182,19 @@ moe_status moe_plan(const moe_caps *c, moe_plan_t *out, size_t *scratch_bytes, i
     S.hq_codes = take((size_t)S.cap_sorted * L.I);
     S.hq_scales = take((size_t)S.cap_sorted * L.I / 32);
   }
-  if (L.layout == LAYOUT_MMA16x64) {
-    S.x16 = take(2 * (size_t)T * L.H);
-    S.xfac = take(4 * (size_t)T);
-    S.hamax = take(4 * (size_t)S.cap_sorted);
-    // Plans for batches of 1024+ (token, slot) pairs send experts with at least
-    // kLargeMin pairs to the tcgen05 kernel (dense tiles of 128 tokens).
-    P.tc_on = Pmax >= 1024 && tc_supported(L.n13, L.H) && tc_supported(L.H, L.I);
-    if (P.tc_on) {
-      P.large_min = kLargeMin;
-      S.h16 = take(2 * (size_t)S.cap_sorted * L.I);
-      S.h16fac = take(4 * (size_t)S.cap_sorted);
-    }
-  } else if (L.wfmt == MOE_W_MXFP4) {
-    // MXFP4 experts with at least kLargeMin pairs run on the tcgen05 kernel with
-    // BF16 operands (E2M1 * 2^X and E4M3 * 2^X are exact in BF16); the rest stay
-    // on the CUDA-core kernel.
-    P.tc_on = Pmax >= 1024 && tc_supported(L.n13, L.H) && tc_supported(L.H, L.I);
-    if (P.tc_on) {
-      P.large_min = kLargeMin;
-      if (P.afmt == MOE_A_MXFP8) S.x16 = take(2 * (size_t)T * L.H);
-      S.h16 = take(2 * (size_t)S.cap_sorted * L.I);
-    }
+  S.x16 = take(2 * (size_t)T * L.H);
+  S.xfac = take(4 * (size_t)T);
+  S.hamax = take(4 * (size_t)S.cap_sorted);
+  // Plans for batches of 1024+ (token, slot) pairs send experts with at least
+  // kLargeMin pairs to the tcgen05 kernel (dense tiles of 128 tokens): FP16
+  // operands with row factors for NVFP4, BF16 operands for MXFP4 (E2M1 * 2^X and
+  // E4M3 * 2^X are exact in BF16, not in FP16).
+  P.tc_on = Pmax >= 1024 && tc_supported(L.n13, L.H) && tc_supported(L.H, L.I);
+  if (P.tc_on) {
+    P.large_min = kLargeMin;
+    if (L.wfmt == MOE_W_MXFP4) S.xb16 = take(2 * (size_t)T * L.H);
+    S.h16 = take(2 * (size_t)S.cap_sorted * L.I);
+    if (L.wfmt == MOE_W_NVFP4) S.h16fac = take(4 * (size_t)S.cap_sorted);
   }
   S.part = take(4 * (size_t)S.cap_sorted * L.H);
   S.total = o;
@@ -299,10 +280,9 @@ static moe_status run_forward(moe_binding b, cudaStream_t stream, cudaEvent_t *e
   int32_t *large_tiles = at<int32_t>(sc, S.large_tiles);
   // With BF16 activations on the tensor-core path, extra CTAs of the routing
   // launch stage x as FP16 rows and clear the per-pair |h| maxima.
-  const bool mma_layout = L.layout == LAYOUT_MMA16x64;
   RouteStaging stg{static_cast<const __nv_bfloat16 *>(b->x), T, H, at<__half>(sc, S.x16), at<float>(sc, S.xfac),
                    at<float>(sc, S.hamax), S.cap_sorted};
-  const bool staged = mma_layout && P.afmt == MOE_A_BF16;
+  const bool staged = P.afmt == MOE_A_BF16;
   if ((err = launch_route(b->ids, T * K, E, P.pad, ntok, P.large_min, 128, counts, offsets, sorted, pair_pos, active,
                           passes, large, large_tiles, status, staged ? &stg : nullptr, stream)) != cudaSuccess)
     return MOE_ERR_CUDA;
@@ -340,45 +320,41 @@ static moe_status run_forward(moe_binding b, cudaStream_t stream, cudaEvent_t *e
     a.act_scales = at<uint8_t>(sc, S.xq_scales);
   }
   if (err != cudaSuccess) return MOE_ERR_CUDA;
-  const bool mma = mma_layout;
-  if (mma) {
-    // tensor-core path: x^ as FP16 rows + per-row factor; clears the per-pair |h| maxima
-    if (!staged) {
-      err = launch_stage_x16(src1, a.act, a.act_scales, a.act_g, T, H, at<__half>(sc, S.x16), at<float>(sc, S.xfac),
-                             at<float>(sc, S.hamax), S.cap_sorted, stream);
-      if (err != cudaSuccess) return MOE_ERR_CUDA;
-    }
-    src1 = SRC_X16;
-    a.act = at<__half>(sc, S.x16);
-    a.act_scales = nullptr;
-    a.act_g = at<float>(sc, S.xfac);
-    a.out_amax = P.afmt == MOE_A_BF16 ? at<float>(sc, S.hamax) : nullptr;
+  const bool nv = L.wfmt == MOE_W_NVFP4;
+  // Staged B operand of the register-dequant kernel: x^ as FP16 slot-order rows
+  // + per-row factor (done by the routing launch for BF16 x); also clears the
+  // per-pair |h| maxima.
+  if (!staged) {
+    err = launch_stage_x16(src1, a.act, a.act_scales, a.act_g, T, H, at<__half>(sc, S.x16), at<float>(sc, S.xfac),
+                           at<float>(sc, S.hamax), S.cap_sorted, stream);
+    if (err != cudaSuccess) return MOE_ERR_CUDA;
   }
+  const void *x_src = a.act;  // BF16 x or x^ codes, for the MXFP4 tcgen05 staging
+  const uint8_t *x_src_scales = a.act_scales;
+  a.act = at<__half>(sc, S.x16);
+  a.act_scales = nullptr;
+  a.act_g = at<float>(sc, S.xfac);
+  a.out_amax = P.afmt == MOE_A_BF16 ? at<float>(sc, S.hamax) : nullptr;
 
   // GEMM1 + activation -> h
   if (mark(MOE_STAGE_GEMM1) != cudaSuccess) return MOE_ERR_CUDA;
   a.codes = b->packed + L.off_c13;
-  a.scales = b->packed + L.off_s13;
-  a.codes_expert = mma ? L.blk13_expert() : L.c13_expert();
-  a.scales_expert = L.s13_expert();
+  a.codes_expert = L.blk13_expert();
   a.K = H;
   a.n_rows = I;
   a.out = h;
   const int stage1 = L.act == MOE_ACT_SILU_GATED ? STAGE_GATED : STAGE_RELU2;
-  a.tc_min_pairs = P.tc_on ? P.large_min : 0;
-  if (!mma && P.tc_on && P.afmt == MOE_A_MXFP8) {  // x^ as BF16 rows for the tcgen05 kernel
-    err = launch_stage_h16(SRC_H_MXFP8, a.act, a.act_scales, nullptr, H, T, nullptr, at<__half>(sc, S.x16), nullptr,
-                           true, stream);
+  if (!nv && P.tc_on) {  // MXFP4 tcgen05 operands: x or x^ as BF16 slot-order rows, factor 1
+    err = launch_stage_h16(P.afmt == MOE_A_MXFP8 ? SRC_H_MXFP8 : SRC_X_BF16, x_src, x_src_scales, nullptr, H, T,
+                           nullptr, at<__half>(sc, S.xb16), nullptr, true, stream);
     if (err != cudaSuccess) return MOE_ERR_CUDA;
   }
-  err = mma ? launch_grouped_mma(src1, stage1, a, L.n13, E, ntok, stream)
-            : launch_grouped_cc(L.wfmt, src1, stage1, a, E, stream);
+  err = launch_grouped_mma(L.wfmt, SRC_X16, stage1, a, L.n13, E, ntok, stream);
   if (err == cudaSuccess && P.tc_on) {
     GroupedArgs t = a;
     t.act_by_token = 1;
-    if (!mma) {  // MXFP4: BF16 rows of x (BF16 activations) or of x^ (MXFP8), factor 1
-      t.act = P.afmt == MOE_A_MXFP8 ? static_cast<const void *>(at<__half>(sc, S.x16)) : b->x;
-      t.act_scales = nullptr;
+    if (!nv) {
+      t.act = at<__half>(sc, S.xb16);
       t.act_g = nullptr;
     }
     err = launch_grouped_tc(stage1, L.wfmt, t, L.n13, E, stream);
@@ -391,7 +367,7 @@ static moe_status run_forward(moe_binding b, cudaStream_t stream, cudaEvent_t *e
   int src2 = SRC_H_F32;
   a.act = h;
   a.act_scales = nullptr;
-  a.act_g = mma ? at<float>(sc, S.hamax) : nullptr;
+  a.act_g = at<float>(sc, S.hamax);
   if (P.afmt == MOE_A_NVFP4) {
     err = launch_quant_rows_nvfp4(h, false, S.cap_sorted, I, at<uint8_t>(sc, S.hq_codes),
                                   at<uint8_t>(sc, S.hq_scales), at<float>(sc, S.hq_g), offsets + E, stream);
@@ -405,30 +381,28 @@ static moe_status run_forward(moe_binding b, cudaStream_t stream, cudaEvent_t *e
     src2 = SRC_H_MXFP8;
     a.act = at<uint8_t>(sc, S.hq_codes);
     a.act_scales = at<uint8_t>(sc, S.hq_scales);
+    a.act_g = nullptr;
   }
   if (err != cudaSuccess) return MOE_ERR_CUDA;
 
   // GEMM2 * topk_weight -> partials, then the ordered combine
-  if (P.tc_on) {  // 16-bit rows of h (or of its re-quantised codes) for the tcgen05 GEMM2
+  if (P.tc_on) {  // 16-bit slot-order rows of h (or of its re-quantised codes) for the tcgen05 GEMM2
     err = launch_stage_h16(src2, a.act, a.act_scales, a.act_g, I, S.cap_sorted, offsets + E, at<__half>(sc, S.h16),
-                           mma ? at<float>(sc, S.h16fac) : nullptr, !mma, stream);
+                           nv ? at<float>(sc, S.h16fac) : nullptr, !nv, stream);
     if (err != cudaSuccess) return MOE_ERR_CUDA;
   }
   a.codes = b->packed + L.off_c2;
-  a.scales = b->packed + L.off_s2;
-  a.codes_expert = mma ? L.blk2_expert() : L.c2_expert();
-  a.scales_expert = L.s2_expert();
+  a.codes_expert = L.blk2_expert();
   a.K = I;
   a.n_rows = H;
   a.out = part;
   if (mark(MOE_STAGE_GEMM2) != cudaSuccess) return MOE_ERR_CUDA;
-  err = mma ? launch_grouped_mma(src2, STAGE_DOWN, a, H, E, ntok, stream)
-            : launch_grouped_cc(L.wfmt, src2, STAGE_DOWN, a, E, stream);
+  err = launch_grouped_mma(L.wfmt, src2, STAGE_DOWN, a, H, E, ntok, stream);
   if (err == cudaSuccess && P.tc_on) {
     GroupedArgs t = a;
     t.act = at<__half>(sc, S.h16);
     t.act_scales = nullptr;
-    t.act_g = mma ? at<float>(sc, S.h16fac) : nullptr;
+    t.act_g = nv ? at<float>(sc, S.h16fac) : nullptr;
     t.act_by_token = 0;
     err = launch_grouped_tc(STAGE_DOWN, L.wfmt, t, H, E, stream);
   }

@@ -42,7 +42,9 @@
  * on the device (out-of-range expert ids, which are dropped) are recorded in a
  * status word inside scratch and read back with moe_device_status.
  *
- * Shapes.  hidden must be a multiple of 128 and intermediate a multiple of 64.
+ * Shapes.  hidden must be a multiple of 128 and intermediate a multiple of 64;
+ * moe_is_supported also requires the rows of W13 (2I gated, I for ReLU^2) to be
+ * a multiple of 128 (the tensor-core kernels work on 128-row blocks).
  * All device pointers must be 16-byte aligned.
  */
 #ifndef BQMOE_MOE_H
