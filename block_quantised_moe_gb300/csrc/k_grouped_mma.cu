@@ -510,10 +510,12 @@ template <int WF, int SRC, int STAGE, int NT>
 static cudaError_t launch_mma_one(const GroupedArgs &a, int rows_total, int E, cudaStream_t s) {
   constexpr size_t kSmemMax = 227 * 1024;
   constexpr size_t kSmemHalf = 112 * 1024;  // two CTAs per SM below this
-  // Prefer two CTAs per SM (16 consumer warps) with a 4-stage ring each; else one
-  // CTA with the deepest ring that fits.  (Three CTAs with 2-stage rings measured
-  // slower at every decode batch size.)
+  // Prefer two CTAs per SM (16 consumer warps) with the deepest ring of up to 4
+  // stages that still fits twice (at least 2 stages: 37 KB in flight per CTA);
+  // else one CTA with the deepest ring that fits.  (Three CTAs with 2-stage
+  // rings measured slower at every decode batch size.)
   int ctas_per_sm = 2, nst = 4;
+  while (nst > 2 && tma_smem_bytes(a.K, NT, nst) > kSmemHalf) --nst;
   if (tma_smem_bytes(a.K, NT, nst) > kSmemHalf) {
     ctas_per_sm = 1;
     nst = kMaxStages;
