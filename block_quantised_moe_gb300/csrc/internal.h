@@ -120,13 +120,14 @@ cudaError_t launch_combine(const float *part, int H, const int32_t *pair_pos, in
                            cudaStream_t s);
 
 // Quantisers.  `rows_dev`, when non-null, is a device int with the number of
-// rows that are live; rows at or beyond it are skipped.
+// rows that are live; rows at or beyond it are skipped, and so are rows r with
+// row_live[r] < 0 when row_live (the expert-sorted pair list) is non-null.
 cudaError_t launch_quant_rows_nvfp4(const void *src, bool src_bf16, int64_t rows, int64_t cols,
                                     uint8_t *codes, uint8_t *scales, float *g, const int32_t *rows_dev,
-                                    cudaStream_t s);
+                                    const int32_t *row_live, cudaStream_t s);
 cudaError_t launch_quant_blocks(int qfmt, const void *src, bool src_bf16, int64_t rows, int64_t cols,
                                 int64_t rows_per_global, const float *g, uint8_t *codes, uint8_t *scales,
-                                const int32_t *rows_dev, cudaStream_t s);
+                                const int32_t *rows_dev, const int32_t *row_live, cudaStream_t s);
 cudaError_t launch_amax_tensor(const void *src, bool src_bf16, int64_t batch, int64_t elems, float *amax,
                                cudaStream_t s);
 cudaError_t launch_amax_to_global(float *g, int64_t n, cudaStream_t s);

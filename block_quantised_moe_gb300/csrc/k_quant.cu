@@ -112,12 +112,14 @@ __device__ __forceinline__ float block_max(float v, float *red) {
 template <bool BF16>
 __global__ void __launch_bounds__(kQThreads)
 k_quant_rows_nvfp4(const void *__restrict__ src, int64_t cols, uint8_t *__restrict__ codes,
-                   uint8_t *__restrict__ scales, float *__restrict__ g_out, const int32_t *__restrict__ rows_dev) {
+                   uint8_t *__restrict__ scales, float *__restrict__ g_out, const int32_t *__restrict__ rows_dev,
+                   const int32_t *__restrict__ row_live) {
   __shared__ float red[32];
   pdl_trigger();
   pdl_wait();
   const int64_t row = blockIdx.x;
   if (rows_dev != nullptr && row >= *rows_dev) return;
+  if (row_live != nullptr && row_live[row] < 0) return;  // a padding slot of the expert-sorted list
   const int64_t base = row * cols;
   float m = 0.f;
   for (int64_t j = (int64_t)threadIdx.x * 8; j < cols; j += kQThreads * 8) {
@@ -147,7 +149,7 @@ template <int QF, bool BF16>
 __global__ void __launch_bounds__(kQThreads)
 k_quant_blocks(const void *__restrict__ src, int64_t rows, int64_t cols, int64_t rows_per_global,
                const float *__restrict__ g, uint8_t *__restrict__ codes, uint8_t *__restrict__ scales,
-               const int32_t *__restrict__ rows_dev) {
+               const int32_t *__restrict__ rows_dev, const int32_t *__restrict__ row_live) {
   constexpr int bs = QF == Q_NVFP4 ? 16 : 32;
   pdl_trigger();
   pdl_wait();
@@ -156,6 +158,7 @@ k_quant_blocks(const void *__restrict__ src, int64_t rows, int64_t cols, int64_t
   for (int64_t i = (int64_t)blockIdx.x * kQThreads + threadIdx.x; i < live_rows * nb;
        i += (int64_t)gridDim.x * kQThreads) {
     const int64_t row = i / nb, b = i % nb;
+    if (row_live != nullptr && row_live[row] < 0) continue;  // a padding slot of the expert-sorted list
     const int64_t e0 = row * cols + b * bs;
     float x[bs];
 #pragma unroll
@@ -216,25 +219,26 @@ static int grid_for(int64_t work, int per_cta) {
 }
 
 cudaError_t launch_quant_rows_nvfp4(const void *src, bool src_bf16, int64_t rows, int64_t cols, uint8_t *codes,
-                                    uint8_t *scales, float *g, const int32_t *rows_dev, cudaStream_t s) {
+                                    uint8_t *scales, float *g, const int32_t *rows_dev, const int32_t *row_live,
+                                    cudaStream_t s) {
   if (rows <= 0) return cudaSuccess;
   if (rows > 0x7FFFFFFF) return cudaErrorInvalidValue;
   if (src_bf16)
     return launch_pdl(k_quant_rows_nvfp4<true>, dim3((unsigned)rows), dim3(kQThreads), 0, s, src, cols, codes, scales,
-                      g, rows_dev);
+                      g, rows_dev, row_live);
   return launch_pdl(k_quant_rows_nvfp4<false>, dim3((unsigned)rows), dim3(kQThreads), 0, s, src, cols, codes, scales, g,
-                    rows_dev);
+                    rows_dev, row_live);
 }
 
 cudaError_t launch_quant_blocks(int qfmt, const void *src, bool src_bf16, int64_t rows, int64_t cols,
                                 int64_t rows_per_global, const float *g, uint8_t *codes, uint8_t *scales,
-                                const int32_t *rows_dev, cudaStream_t s) {
+                                const int32_t *rows_dev, const int32_t *row_live, cudaStream_t s) {
   if (rows <= 0) return cudaSuccess;
   const int bs = qfmt == Q_NVFP4 ? 16 : 32;
   const int grid = grid_for(rows * (cols / bs), kQThreads);
 #define QB(QF, B) \
   return launch_pdl(k_quant_blocks<QF, B>, dim3(grid), dim3(kQThreads), 0, s, src, rows, cols, rows_per_global, g, \
-                    codes, scales, rows_dev)
+                    codes, scales, rows_dev, row_live)
   if (qfmt == Q_NVFP4) { if (src_bf16) QB(Q_NVFP4, true); else QB(Q_NVFP4, false); }
   else if (qfmt == Q_MXFP4) { if (src_bf16) QB(Q_MXFP4, true); else QB(Q_MXFP4, false); }
   else if (qfmt == Q_MXFP8) { if (src_bf16) QB(Q_MXFP8, true); else QB(Q_MXFP8, false); }

@@ -307,14 +307,14 @@ static moe_status run_forward(moe_binding b, cudaStream_t stream, cudaEvent_t *e
   a.act = b->x;
   if (P.afmt == MOE_A_NVFP4) {
     err = launch_quant_rows_nvfp4(b->x, true, T, H, at<uint8_t>(sc, S.xq_codes), at<uint8_t>(sc, S.xq_scales),
-                                  at<float>(sc, S.xq_g), nullptr, stream);
+                                  at<float>(sc, S.xq_g), nullptr, nullptr, stream);
     src1 = SRC_X_NVFP4;
     a.act = at<uint8_t>(sc, S.xq_codes);
     a.act_scales = at<uint8_t>(sc, S.xq_scales);
     a.act_g = at<float>(sc, S.xq_g);
   } else if (P.afmt == MOE_A_MXFP8) {
     err = launch_quant_blocks(Q_MXFP8, b->x, true, T, H, 1, nullptr, at<uint8_t>(sc, S.xq_codes),
-                              at<uint8_t>(sc, S.xq_scales), nullptr, stream);
+                              at<uint8_t>(sc, S.xq_scales), nullptr, nullptr, stream);
     src1 = SRC_X_MXFP8;
     a.act = at<uint8_t>(sc, S.xq_codes);
     a.act_scales = at<uint8_t>(sc, S.xq_scales);
@@ -370,14 +370,14 @@ static moe_status run_forward(moe_binding b, cudaStream_t stream, cudaEvent_t *e
   a.act_g = at<float>(sc, S.hamax);
   if (P.afmt == MOE_A_NVFP4) {
     err = launch_quant_rows_nvfp4(h, false, S.cap_sorted, I, at<uint8_t>(sc, S.hq_codes),
-                                  at<uint8_t>(sc, S.hq_scales), at<float>(sc, S.hq_g), offsets + E, stream);
+                                  at<uint8_t>(sc, S.hq_scales), at<float>(sc, S.hq_g), offsets + E, sorted, stream);
     src2 = SRC_H_NVFP4;
     a.act = at<uint8_t>(sc, S.hq_codes);
     a.act_scales = at<uint8_t>(sc, S.hq_scales);
     a.act_g = at<float>(sc, S.hq_g);
   } else if (P.afmt == MOE_A_MXFP8) {
     err = launch_quant_blocks(Q_MXFP8, h, false, S.cap_sorted, I, 1, nullptr, at<uint8_t>(sc, S.hq_codes),
-                              at<uint8_t>(sc, S.hq_scales), offsets + E, stream);
+                              at<uint8_t>(sc, S.hq_scales), offsets + E, sorted, stream);
     src2 = SRC_H_MXFP8;
     a.act = at<uint8_t>(sc, S.hq_codes);
     a.act_scales = at<uint8_t>(sc, S.hq_scales);
@@ -498,20 +498,21 @@ moe_status moe_quantize(int32_t qfmt, int32_t gmode, int32_t src_bf16, const voi
     if (cols % 16 || !global || !aligned(global, 4)) return MOE_ERR_INVALID_ARG;
     if (gmode == MOE_G_PER_ROW) {
       err = launch_quant_rows_nvfp4(src, bf, batch * rows, cols, static_cast<uint8_t *>(codes),
-                                    static_cast<uint8_t *>(scales), global, nullptr, stream);
+                                    static_cast<uint8_t *>(scales), global, nullptr, nullptr, stream);
     } else if (gmode == MOE_G_PER_TENSOR) {
       err = launch_amax_tensor(src, bf, batch, rows * cols, global, stream);
       if (err == cudaSuccess) err = launch_amax_to_global(global, batch, stream);
       if (err == cudaSuccess)
         err = launch_quant_blocks(Q_NVFP4, src, bf, batch * rows, cols, rows, global, static_cast<uint8_t *>(codes),
-                                  static_cast<uint8_t *>(scales), nullptr, stream);
+                                  static_cast<uint8_t *>(scales), nullptr, nullptr, stream);
     } else {
       return MOE_ERR_INVALID_ARG;
     }
   } else {
     if (cols % 32 || gmode != MOE_G_NONE || global) return MOE_ERR_INVALID_ARG;
     err = launch_quant_blocks(qfmt == MOE_Q_MXFP4 ? Q_MXFP4 : Q_MXFP8, src, bf, batch * rows, cols, 1, nullptr,
-                              static_cast<uint8_t *>(codes), static_cast<uint8_t *>(scales), nullptr, stream);
+                              static_cast<uint8_t *>(codes), static_cast<uint8_t *>(scales), nullptr, nullptr,
+                              stream);
   }
   return cuda_status(err);
 }
