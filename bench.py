@@ -287,7 +287,8 @@ def main():
     R = max(1, args.replicas)
     seed_base = 1000 * rank
     ck = layer.make_experts_gpu(E, H, I, cfg["wfmt"], cfg["act"], seed=0)
-    packed0 = layer.PackedLayer(ck, H, I)
+    # W4A4 layers also carry the FP4 tiles of the block-scaled tensor-core kernel
+    packed0 = layer.PackedLayer(ck, H, I, fp4_tiles=cfg["wfmt"] == "nvfp4" and afmt == "nvfp4")
     del ck
     packed = [packed0.packed] + [packed0.packed.clone() for _ in range(R - 1)]
     plan = layer.Plan(packed0, K, T, afmt)

@@ -27,6 +27,7 @@ MOE_OK, MOE_ERR_INVALID_ARG, MOE_ERR_UNSUPPORTED, MOE_ERR_CAPACITY = 0, 1, 2, 3
 MOE_ERR_SCRATCH_TOO_SMALL, MOE_ERR_CUDA, MOE_ERR_TIMEOUT = 4, 5, 6
 MOE_W_NVFP4, MOE_W_MXFP4 = 1, 2
 MOE_A_BF16, MOE_A_NVFP4, MOE_A_MXFP8 = 1, 2, 3
+MOE_WFLAG_FP4_TILES = 1
 MOE_ACT_SILU_GATED, MOE_ACT_RELU2 = 1, 2
 MOE_Q_NVFP4, MOE_Q_MXFP4, MOE_Q_MXFP8 = 1, 2, 3
 MOE_G_NONE, MOE_G_PER_TENSOR, MOE_G_PER_ROW = 0, 1, 2
@@ -48,7 +49,8 @@ EXPORTS = (
 
 class moe_weight_desc(ctypes.Structure):
     _fields_ = [("num_experts", ctypes.c_int32), ("hidden", ctypes.c_int32),
-                ("intermediate", ctypes.c_int32), ("wfmt", ctypes.c_int32), ("act", ctypes.c_int32)]
+                ("intermediate", ctypes.c_int32), ("wfmt", ctypes.c_int32), ("act", ctypes.c_int32),
+                ("flags", ctypes.c_int32)]
 
 
 class moe_caps(ctypes.Structure):
@@ -122,9 +124,9 @@ def _stream(s):
 # ------------------------------------------------------------------ calls
 
 
-def moe_plan_weights(num_experts, hidden, intermediate, wfmt, act):
-    """-> (weight plan handle, packed_bytes)."""
-    d = moe_weight_desc(num_experts, hidden, intermediate, WFMT.get(wfmt, wfmt), ACT.get(act, act))
+def moe_plan_weights(num_experts, hidden, intermediate, wfmt, act, flags=0):
+    """-> (weight plan handle, packed_bytes).  flags: MOE_WFLAG_* bits."""
+    d = moe_weight_desc(num_experts, hidden, intermediate, WFMT.get(wfmt, wfmt), ACT.get(act, act), flags)
     h, n = _vp(), _sz()
     _check(_lib.moe_plan_weights(ctypes.byref(d), ctypes.byref(h), ctypes.byref(n)), "moe_plan_weights")
     return h.value, n.value

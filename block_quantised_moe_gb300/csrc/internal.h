@@ -18,11 +18,20 @@ inline size_t align_up(size_t v, size_t a = kAlign) { return (v + a - 1) / a * a
 //        A-fragment order (see the packer)
 //   c2   W2 (H rows x I), same layout
 //   g    float [E][4] global scales (gate|w1, up, down, 1); all 1 for MXFP4
+//   t13, t2  (MOE_WFLAG_FP4_TILES, NVFP4) per expert, 128-row block and
+//        256-K block: a 16 KB 128-byte-swizzled tile of E2M1 codes, then the
+//        block scales of the block's 128 rows as 2 KB in tensor-memory order
+//        (see the packer)
 struct WeightLayout {
   int E = 0, H = 0, I = 0, wfmt = 0, act = 0;
   int bs = 16;   // elements per block scale (16 NVFP4, 32 MXFP4)
   int n13 = 0;   // rows of W13
-  size_t off_c13 = 0, off_c2 = 0, off_g = 0, total = 0;
+  bool fp4_tiles = false;
+  size_t off_c13 = 0, off_c2 = 0, off_g = 0, off_t13 = 0, off_t2 = 0, total = 0;
+  // FP4 tiles: bytes of one (128-row block, 256-K block) tile + its scales
+  static constexpr size_t kFp4TileBytes = 16384 + 2048;
+  size_t t13_expert() const { return (size_t)(n13 / 128) * (H / 256) * kFp4TileBytes; }
+  size_t t2_expert() const { return (size_t)(H / 128) * (I / 256) * kFp4TileBytes; }
   // bytes of one expert's W13 / W2 segment (codes + block scales)
   size_t blk13_expert() const { return (size_t)n13 * H / 2 + (size_t)n13 * H / bs; }
   size_t blk2_expert() const { return (size_t)H * I / 2 + (size_t)H * I / bs; }
@@ -109,6 +118,10 @@ cudaError_t launch_stage_x16(int src, const void *act, const uint8_t *act_scales
 // or MXFP4 weights (BF16 operands), both from the packed fragment layout.
 bool tc_supported(int rows_total, int K);
 cudaError_t launch_grouped_tc(int stage, int wfmt, const GroupedArgs &a, int rows_total, int E, cudaStream_t s);
+// Block-scaled FP4 tcgen05 kernel for NVFP4 weights with NVFP4 activations (the
+// weights' FP4 tiles; a.act / act_scales / act_g = the quantised activations).
+bool fp4_tc_supported(int rows_total, int K);
+cudaError_t launch_grouped_fp4(int stage, const GroupedArgs &a, int rows_total, cudaStream_t s);
 // h (or its re-quantised codes) as 16-bit rows for the tcgen05 GEMM2: FP16 with a
 // per-row factor, or BF16 with factor 1 (out_bf16; also MXFP8 x^ -> BF16 rows).
 // rows_dev (device, nullable) caps the rows actually converted.

@@ -177,6 +177,55 @@ __global__ void k_pack_mma_scales(const uint8_t *__restrict__ src, uint8_t *__re
   }
 }
 
+// FP4 tiles for the block-scaled tensor-core kernel (MOE_WFLAG_FP4_TILES).  For
+// every (expert, 128-row block, 256-K block): 16384 bytes of E2M1 codes, rows of
+// 128 bytes (K order as in the checkpoint) in the UMMA 128-byte-swizzled K-major
+// layout (16-byte chunk c of row r at (r/8)*1024 + (r%8)*128 + ((c ^ r) % 8)*16),
+// then 2048 bytes of E4M3 block scales as 32-bit words (four 16-element blocks
+// of one row and one 64-K step, first block in the low byte) ordered
+// [lane i][step t][column c] for row i + 32c: the order in which the tensor-
+// memory scale layout (32 lanes x 4 columns per 128 rows) is written.  Rows follow
+// the same 8 gate + 8 up interleave per 16-row tile as the fragment layout.
+constexpr int64_t kFp4Tile = 16384 + 2048;
+
+__global__ void k_pack_fp4_codes(const uint8_t *__restrict__ src, uint8_t *__restrict__ dst, int E, int rows, int K,
+                                 int gated, int I) {
+  const int nblk = rows / 128, nkb = K / 256;
+  const int64_t n = (int64_t)E * nblk * nkb * 128 * 8;  // 16-byte chunks
+  for (int64_t idx = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; idx < n; idx += (int64_t)gridDim.x * blockDim.x) {
+    const int c = (int)(idx & 7), r = (int)((idx >> 3) & 127);
+    int64_t t = idx >> 10;
+    const int kb = (int)(t % nkb);
+    t /= nkb;
+    const int blk = (int)(t % nblk);
+    const int64_t e = t / nblk;
+    const int64_t row = tile_src_row(blk * 8 + r / 16, r % 16, gated, I);
+    const uint4 v = *reinterpret_cast<const uint4 *>(src + (e * rows + row) * (K / 2) + (int64_t)kb * 128 + c * 16);
+    uint8_t *tile = dst + ((e * nblk + blk) * nkb + kb) * kFp4Tile;
+    *reinterpret_cast<uint4 *>(tile + (r >> 3) * 1024 + (r & 7) * 128 + (((c ^ r) & 7) << 4)) = v;
+  }
+}
+
+__global__ void k_pack_fp4_scales(const uint8_t *__restrict__ src, uint8_t *__restrict__ dst, int E, int rows, int K,
+                                  int gated, int I) {
+  const int nblk = rows / 128, nkb = K / 256;
+  const int64_t n = (int64_t)E * nblk * nkb * 512;  // 32-bit words
+  for (int64_t idx = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; idx < n; idx += (int64_t)gridDim.x * blockDim.x) {
+    const int w = (int)(idx & 511);
+    const int i = w >> 4, st = (w >> 2) & 3, c = w & 3;
+    int64_t t = idx >> 9;
+    const int kb = (int)(t % nkb);
+    t /= nkb;
+    const int blk = (int)(t % nblk);
+    const int64_t e = t / nblk;
+    const int r = i + 32 * c;
+    const int64_t row = tile_src_row(blk * 8 + r / 16, r % 16, gated, I);
+    const uint32_t v = *reinterpret_cast<const uint32_t *>(src + (e * rows + row) * (K / 16) + (int64_t)kb * 16 + st * 4);
+    uint8_t *tile = dst + ((e * nblk + blk) * nkb + kb) * kFp4Tile;
+    reinterpret_cast<uint32_t *>(tile + 16384)[w] = v;
+  }
+}
+
 static int pack_grid(int64_t n) { return (int)std::max<int64_t>(1, std::min<int64_t>((n + 255) / 256, 152 * 32)); }
 
 cudaError_t launch_pack(const WeightLayout &L, const void *w13_codes, const void *w13_scales, const float *w13_global,
@@ -195,6 +244,13 @@ cudaError_t launch_pack(const WeightLayout &L, const void *w13_codes, const void
   } else {
     k_pack_mma_scales<32><<<pack_grid(g13), 256, 0, s>>>(w13s, packed + L.off_c13, L.E, L.n13, L.H, gated, L.I);
     k_pack_mma_scales<32><<<pack_grid(g2), 256, 0, s>>>(w2s, packed + L.off_c2, L.E, L.H, L.I, 0, L.I);
+  }
+  if (L.fp4_tiles) {
+    const int64_t t13 = (int64_t)L.E * (L.n13 / 128) * (L.H / 256), t2 = (int64_t)L.E * (L.H / 128) * (L.I / 256);
+    k_pack_fp4_codes<<<pack_grid(t13 * 1024), 256, 0, s>>>(w13c, packed + L.off_t13, L.E, L.n13, L.H, gated, L.I);
+    k_pack_fp4_scales<<<pack_grid(t13 * 512), 256, 0, s>>>(w13s, packed + L.off_t13, L.E, L.n13, L.H, gated, L.I);
+    k_pack_fp4_codes<<<pack_grid(t2 * 1024), 256, 0, s>>>(w2c, packed + L.off_t2, L.E, L.H, L.I, 0, L.I);
+    k_pack_fp4_scales<<<pack_grid(t2 * 512), 256, 0, s>>>(w2s, packed + L.off_t2, L.E, L.H, L.I, 0, L.I);
   }
   cudaError_t err = cudaGetLastError();
   if (err != cudaSuccess) return err;

@@ -1,0 +1,422 @@
+// Grouped expert contractions with NVFP4 weights AND NVFP4 activations (W4A4)
+// on the block-scaled FP4 tensor-core MMA, for experts with many pairs
+// (prefill).
+//
+// moe.fused_moe's NVFP4-activation mode (b12x project page, section "What's in
+// here"; vLLM docs "b12x Linear and MoE Backends", "Supported Configurations"):
+// both operands stay E2M1 codes with E4M3 scales per 16 elements, so the MMA
+// takes them as they are -- `tcgen05.mma.cta_group::1.kind::mxf4nvf4
+// .block_scale.scale_vec::4X`, M=128 N=128 K=64, FP32 accumulation in TMEM:
+//
+//   D[128 weight rows x 128 tokens] += sum over 4 MMAs of (A * sA)(B * sB)^T per 256-K block
+//
+// * A: the weights' FP4 tiles (MOE_WFLAG_FP4_TILES): a 16 KB 128-byte-swizzled
+//   tile per 128-row block and 256-K block, one bulk copy; no dequantisation.
+// * B: 128 rows of the quantised activations (x^ per token for GEMM1, h^ per
+//   slot for GEMM2), gathered with cp.async into the same swizzled layout
+//   (zero-filled past the expert's last token).
+// * Scale factors: the weight tile's scale words ride in the same bulk copy as
+//   its codes, the activation rows' scale bytes in the same gather as theirs;
+//   four warps, one per TMEM lane quadrant, move them from shared memory into
+//   TMEM with tcgen05.st in the layout the MMA reads: 32 lanes x 4 columns per
+//   64-K step, lane i column c holding the four E4M3 scales of row i + 32c, the
+//   same in every quadrant.
+// * Epilogue: D x the weights' FP32 global x the row's FP32 activation global,
+//   then SiLU(g)*u or ReLU^2 (GEMM1) or the topk_weight (GEMM2).
+// Every wait is a bounded mbarrier wait; a timeout sets the status flag, and
+// the MMA warp drains its MMAs before TMEM is released.
+#include <algorithm>
+
+#include "common.cuh"
+#include "internal.h"
+#include "launch.h"
+#include "sync.cuh"
+#include "tcgen05.cuh"
+
+namespace bqmoe {
+
+constexpr int kF4EpiWarps = 4;                       // warps 0-3: epilogue
+constexpr int kF4SfWarp0 = 4;                        // warps 4-7: scale factors into TMEM
+constexpr int kF4BWarp0 = 8, kF4BWarps = 4;          // warps 8-11: activation gather
+constexpr int kF4AWarp = 12;                         // weight tile bulk copies
+constexpr int kF4MmaWarp = 13;                       // MMA issue
+constexpr int kF4Threads = (kF4MmaWarp + 1) * 32;
+constexpr int kF4N = 128;                            // tokens per tile
+constexpr int kF4TileBytes = 16384;                  // 128 rows x 256 K of E2M1
+constexpr int kF4SfBytes = 2048;                     // their scales (weights: packed tile; activations: gathered)
+constexpr int kF4StageBytes = kF4TileBytes + kF4SfBytes;  // one operand's ring stage (a multiple of 1024)
+constexpr int kF4Stages = 6;                         // A, B and scale-factor ring depth
+constexpr int kF4BLag = 4;                           // cp.async stages a B thread keeps in flight
+constexpr int kF4RingBytes = 2 * kF4Stages * kF4StageBytes;
+constexpr int kF4AccCols = kF4N;                     // TMEM columns per accumulator (FP32, N tokens)
+constexpr int kF4SfCol0 = 2 * kF4AccCols;            // scale-factor stages after the two accumulators
+constexpr int kF4SfCols = 32;                        // per stage: A 16 + B 16 (4 K steps x 4 columns)
+constexpr int kF4TmemCols = 512;
+constexpr int kF4BRows = kF4N * 8 / (kF4BWarps * 32);  // 16-byte code chunks per B thread per k-block
+static_assert(kF4StageBytes % 1024 == 0, "swizzled tiles need 1024-byte aligned stages");
+static_assert(kF4SfCol0 + kF4Stages * kF4SfCols <= kF4TmemCols, "TMEM budget");
+
+// Instruction descriptor of kind::mxf4nvf4: A and B E2M1 (format 1), K-major,
+// N >> 3 at bit 17, UE4M3 scales (bit 23 = 0), M >> 4 at bit 24, K = 64.
+constexpr uint32_t kF4Idesc = (1u << 7) | (1u << 10) | ((uint32_t)(kF4N >> 3) << 17) | ((uint32_t)(128 >> 4) << 24);
+
+__device__ __forceinline__ void tc_mma_fp4(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t sfa,
+                                           uint32_t sfb, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %6, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::mxf4nvf4.block_scale.scale_vec::4X [%0], %1, %2, %3, [%4], [%5], p;\n\t}" ::"r"(
+          d_tmem),
+      "l"(adesc), "l"(bdesc), "r"(kF4Idesc), "r"(sfa), "r"(sfb), "r"(accumulate));
+}
+
+template <int STAGE>
+__global__ void __launch_bounds__(kF4Threads, 1) k_grouped_fp4(const GroupedArgs a) {
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw_s = (uint32_t)__cvta_generic_to_shared(smem_raw);
+  const uint32_t base_s = (raw_s + 1023u) & ~1023u;  // swizzled tiles need 1024-byte alignment
+  uint8_t *base = smem_raw + (base_s - raw_s);
+  const uint32_t ringA = base_s, ringB = base_s + kF4Stages * kF4StageBytes;
+  uint64_t *bars = reinterpret_cast<uint64_t *>(base + kF4RingBytes);
+  constexpr int kBars = 6 * kF4Stages + 4 + 1;
+  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + kBars);
+  const uint32_t afull0 = (uint32_t)__cvta_generic_to_shared(bars);
+  const uint32_t aempty0 = afull0 + 8u * kF4Stages;
+  const uint32_t bfull0 = aempty0 + 8u * kF4Stages;
+  const uint32_t bempty0 = bfull0 + 8u * kF4Stages;
+  const uint32_t sfull0 = bempty0 + 8u * kF4Stages;
+  const uint32_t sempty0 = sfull0 + 8u * kF4Stages;
+  const uint32_t tfull0 = sempty0 + 8u * kF4Stages;  // 2
+  const uint32_t tempty0 = tfull0 + 16u;              // 2
+  const uint32_t drain = tempty0 + 16u;               // 1
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  pdl_trigger();
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < kF4Stages; ++i) {
+      mbar_init(afull0 + 8u * i, 1);
+      mbar_init(aempty0 + 8u * i, 1);
+      mbar_init(bfull0 + 8u * i, kF4BWarps);
+      mbar_init(bempty0 + 8u * i, 1);
+      mbar_init(sfull0 + 8u * i, 4);
+      mbar_init(sempty0 + 8u * i, 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(tfull0 + 8u * b, 1);
+      mbar_init(tempty0 + 8u * b, kF4EpiWarps);
+    }
+    mbar_init(drain, 1);
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+  if (warp == kF4MmaWarp) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                     (uint32_t)__cvta_generic_to_shared(tmem_slot)),
+                 "n"(kF4TmemCols));
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;");
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+
+  const int K = a.K;
+  const int nkb = K / 256;
+  const int nblk = a.n_blocks;
+  const int n_large = a.large[0];
+  const int W = n_large > 0 ? a.large_tiles[n_large] * nblk : 0;
+  // Items (large expert, 128-token tile, 128-row block) dealt round-robin, so
+  // that neighbouring CTAs share token tiles and weight blocks in L2.
+  const int w0 = blockIdx.x, wstep = gridDim.x;
+  TcCursor cur;
+  if (w0 < W) cur.seek(a, w0, nblk);
+  bool ok = true;
+  const bool by_token = a.act_by_token != 0;
+
+  if (warp == kF4AWarp) {
+    // ------------------------------------------------------ weight tiles
+    if (lane == 0) {
+      int slot = 0;
+      uint32_t phase = 0;
+      uint32_t issued = 0, issued_parity = 0;
+      for (int w = w0; w < W && ok; w += wstep) {
+        const TcItem it = cur.at(a, w, nblk);
+        const uint8_t *tiles = a.codes + (size_t)it.e * a.codes_expert + (size_t)it.bp * nkb * (kF4TileBytes + kF4SfBytes);
+        for (int kb = 0; kb < nkb; ++kb) {
+          if (!mbar_wait(aempty0 + 8u * slot, phase ^ 1u)) {
+            ok = false;
+            break;
+          }
+          // the tile's codes and, right after them, its scale words in TMEM order
+          mbar_expect_tx(afull0 + 8u * slot, kF4StageBytes);
+          bulk_g2s(ringA + (uint32_t)slot * kF4StageBytes, tiles + (size_t)kb * kF4StageBytes, kF4StageBytes,
+                   afull0 + 8u * slot);
+          issued |= 1u << slot;
+          issued_parity = (issued_parity & ~(1u << slot)) | (phase << slot);
+          if (++slot == kF4Stages) {
+            slot = 0;
+            phase ^= 1u;
+          }
+        }
+      }
+      // Never leave with a copy in flight into this CTA's shared memory.
+      for (int i = 0; i < kF4Stages; ++i)
+        if (issued & (1u << i)) mbar_wait(afull0 + 8u * i, (issued_parity >> i) & 1u);
+    }
+    __syncwarp();
+  } else if (warp >= kF4BWarp0 && warp < kF4BWarp0 + kF4BWarps) {
+    // ------------------------------------------------------ activation gather
+    const int t = threadIdx.x - kF4BWarp0 * 32;
+    const int cc = t & 7;                          // 16-byte chunk of the 128-byte row
+    constexpr int kRowStep = kF4BWarps * 32 / 8;   // rows between a thread's chunks
+    int slot = 0, issued = 0;
+    uint32_t phase = 0;
+    const uint8_t *act = reinterpret_cast<const uint8_t *>(a.act);
+    pdl_wait();  // the quantised activations come from the preceding kernel
+    for (int w = w0; w < W && ok; w += wstep) {
+      const TcItem it = cur.at(a, w, nblk);
+      int rid[kF4BRows];
+#pragma unroll
+      for (int i = 0; i < kF4BRows; ++i) {
+        const int r = (t >> 3) + kRowStep * i;
+        const int s = it.s0 + r;
+        rid[i] = r < it.ntok ? (by_token ? a.sorted_pair[s] / a.top_k : s) : -1;
+      }
+      for (int kb = 0; kb < nkb; ++kb) {
+        if (!mbar_wait(bempty0 + 8u * slot, phase ^ 1u)) {
+          ok = false;
+          break;
+        }
+        const uint32_t stB = ringB + (uint32_t)slot * kF4StageBytes;
+#pragma unroll
+        for (int i = 0; i < kF4BRows; ++i) {
+          const int r = (t >> 3) + kRowStep * i;
+          const uint32_t dst = stB + (uint32_t)((r >> 3) * 1024 + (r & 7) * 128 + (((cc ^ r) & 7) << 4));
+          const uint8_t *src = act + (int64_t)(rid[i] < 0 ? 0 : rid[i]) * (K / 2) + kb * 128 + cc * 16;
+          cp_async16(dst, src, rid[i] >= 0);
+        }
+        // the 16 scale bytes of token row t of this 256-K block (rows past the tile's tokens: zero)
+        if (t < kF4N) {
+          const int s = it.s0 + t;
+          const int64_t rs = t < it.ntok ? (by_token ? a.sorted_pair[s] / a.top_k : s) : -1;
+          cp_async16(stB + kF4TileBytes + t * 16, a.act_scales + (rs < 0 ? 0 : rs) * (K / 16) + kb * 16, rs >= 0);
+        }
+        cp_async_commit();
+        ++issued;
+        if (issued > kF4BLag) {  // the stage issued kF4BLag steps ago has landed
+          cp_async_wait_group<kF4BLag>();
+          fence_async_smem();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(bfull0 + 8u * ((slot + kF4Stages - kF4BLag) % kF4Stages));
+        }
+        if (++slot == kF4Stages) {
+          slot = 0;
+          phase ^= 1u;
+        }
+      }
+    }
+    cp_async_wait_group<0>();
+    fence_async_smem();
+    __syncwarp();
+    if (ok && lane == 0) {
+      for (int back = issued < kF4BLag ? issued : kF4BLag; back >= 1; --back)
+        mbar_arrive(bfull0 + 8u * ((slot + kF4Stages - back) % kF4Stages));
+    }
+  } else if (warp >= kF4SfWarp0 && warp < kF4SfWarp0 + 4) {
+    // ------------------------------------------------------ scale factors -> TMEM
+    // Warp 4 + q writes lane quadrant q; every quadrant gets the same words:
+    // the weight tile's 16 words of this lane (copied with the codes, already in
+    // [step][column] order) and the 16 scale bytes of token rows lane + 32c
+    // (gathered with the activation codes).
+    const int q = warp - kF4SfWarp0;
+    const uint32_t lane_base = (uint32_t)(q * 32) << 16;
+    int slot = 0;
+    uint32_t phase = 0;
+    for (int w = w0; w < W && ok; w += wstep) {
+      for (int kb = 0; kb < nkb; ++kb) {
+        if (!mbar_wait(sempty0 + 8u * slot, phase ^ 1u) || !mbar_wait(afull0 + 8u * slot, phase) ||
+            !mbar_wait(bfull0 + 8u * slot, phase)) {
+          ok = false;
+          break;
+        }
+        const uint4 *sfa = reinterpret_cast<const uint4 *>(base + slot * kF4StageBytes + kF4TileBytes) + lane * 4;
+        const uint8_t *sfb = base + (kF4Stages + slot) * kF4StageBytes + kF4TileBytes;
+        uint32_t ra[16], rb[16];
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          const uint4 v = sfa[j];
+          ra[4 * j + 0] = v.x;
+          ra[4 * j + 1] = v.y;
+          ra[4 * j + 2] = v.z;
+          ra[4 * j + 3] = v.w;
+        }
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+          const uint4 v = *reinterpret_cast<const uint4 *>(sfb + (lane + 32 * c) * 16);
+          rb[0 * 4 + c] = v.x;
+          rb[1 * 4 + c] = v.y;
+          rb[2 * 4 + c] = v.z;
+          rb[3 * 4 + c] = v.w;
+        }
+        tc_fence_after();
+        const uint32_t col = tmem + lane_base + (uint32_t)(kF4SfCol0 + slot * kF4SfCols);
+        tc_st16(col, ra);
+        tc_st16(col + 16, rb);
+        tc_wait_st();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(sfull0 + 8u * slot);
+        if (++slot == kF4Stages) {
+          slot = 0;
+          phase ^= 1u;
+        }
+      }
+    }
+  } else if (warp == kF4MmaWarp) {
+    // ------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      int sa = 0, li = 0;
+      uint32_t pa = 0;
+      bool any = false;
+      for (int w = w0; w < W && ok; w += wstep, ++li) {
+        const int b = li & 1;
+        if (!mbar_wait(tempty0 + 8u * b, ((li >> 1) & 1) ^ 1u)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const uint32_t d = tmem + (uint32_t)(b * kF4AccCols);
+        for (int kb = 0; kb < nkb; ++kb) {
+          // A, B and scale-factor rings advance together
+          if (!mbar_wait(afull0 + 8u * sa, pa) || !mbar_wait(bfull0 + 8u * sa, pa) || !mbar_wait(sfull0 + 8u * sa, pa)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint64_t da = umma_desc_sw128(ringA + (uint32_t)sa * kF4StageBytes);
+          const uint64_t db = umma_desc_sw128(ringB + (uint32_t)sa * kF4StageBytes);
+          const uint32_t sf = tmem + (uint32_t)(kF4SfCol0 + sa * kF4SfCols);
+#pragma unroll
+          for (int j = 0; j < 4; ++j)  // K = 64 per MMA: 32 bytes of each operand row
+            tc_mma_fp4(d, da + 2u * j, db + 2u * j, sf + 4u * j, sf + 16u + 4u * j, (kb > 0 || j > 0) ? 1u : 0u);
+          tc_commit(aempty0 + 8u * sa);
+          tc_commit(bempty0 + 8u * sa);
+          tc_commit(sempty0 + 8u * sa);
+          any = true;
+          if (++sa == kF4Stages) {
+            sa = 0;
+            pa ^= 1u;
+          }
+        }
+        if (!ok) break;
+        tc_commit(tfull0 + 8u * b);
+      }
+      if (any) {  // all issued MMAs complete before TMEM can be released
+        tc_commit(drain);
+        mbar_wait(drain, 0);
+      }
+    }
+    __syncwarp();
+  } else {
+    // ------------------------------------------------------ epilogue
+    const int m = warp * 32 + lane;  // accumulator row = TMEM lane
+    pdl_wait();                      // activation globals come from the preceding kernel
+    int li = 0;
+    for (int w = w0; w < W && ok; w += wstep, ++li) {
+      const TcItem it = cur.at(a, w, nblk);
+      const int b = li & 1;
+      const float *gl = a.globals + 4 * it.e;
+      // Per column (one per lane and 32-column chunk, broadcast with shuffles):
+      // the activation row's FP32 global and, for the down projection, the
+      // topk weight -- loaded before the accumulator is ready.
+      float f_l[kF4N / 32], w_l[kF4N / 32];
+      {
+        int p_l[kF4N / 32];
+#pragma unroll
+        for (int ch = 0; ch < kF4N / 32; ++ch) {
+          const int nl = 32 * ch + lane;
+          p_l[ch] = nl < it.ntok ? a.sorted_pair[it.s0 + nl] : -1;
+        }
+#pragma unroll
+        for (int ch = 0; ch < kF4N / 32; ++ch) {
+          const int nl = 32 * ch + lane;
+          f_l[ch] = 0.f;
+          w_l[ch] = 0.f;
+          if (p_l[ch] >= 0) {
+            f_l[ch] = a.act_g[by_token ? (int64_t)(p_l[ch] / a.top_k) : (int64_t)(it.s0 + nl)];
+            if (STAGE == STAGE_DOWN) w_l[ch] = a.topk_weights[p_l[ch]] * gl[2];
+          }
+        }
+      }
+      if (!mbar_wait(tfull0 + 8u * b, (li >> 1) & 1)) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+      const int blk = it.bp;
+      const int tile = 8 * blk + (m >> 4), rr = m & 15;
+#pragma unroll
+      for (int ch = 0; ch < kF4N / 32; ++ch) {
+        const int c0 = 32 * ch;
+        uint32_t raw[32];
+        tc_ld32(tmem + ((uint32_t)(warp * 32) << 16) + (uint32_t)(b * kF4AccCols + c0), raw);
+#pragma unroll
+        for (int j = 0; j < 32; ++j) {
+          const int n = c0 + j;
+          const bool live = n < it.ntok;
+          const int s = it.s0 + n;
+          const float v = __uint_as_float(raw[j]) * __shfl_sync(0xffffffffu, f_l[ch], j);
+          if (STAGE == STAGE_GATED) {
+            const float up = __shfl_down_sync(0xffffffffu, v, 8);
+            if (rr < 8 && live) a.out[(size_t)s * a.n_rows + tile * 8 + rr] = silu_f32(v * gl[0]) * (up * gl[1]);
+          } else if (STAGE == STAGE_RELU2) {
+            const float r = fmaxf(v * gl[0], 0.f);
+            if (live) a.out[(size_t)s * a.n_rows + tile * 16 + rr] = r * r;
+          } else {
+            const float wt = __shfl_sync(0xffffffffu, w_l[ch], j);
+            if (live) a.out[(size_t)s * a.n_rows + blk * 128 + m] = wt * v;
+          }
+        }
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(tempty0 + 8u * b);
+    }
+  }
+
+  if (!ok && lane == 0) atomicOr(&a.status[ST_FLAGS], ST_FLAG_TIMEOUT);
+  pdl_wait();  // completion implies the predecessor's (a no-op for threads that already waited)
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == kF4MmaWarp)
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "n"(kF4TmemCols));
+}
+
+static size_t fp4_smem_bytes() { return (size_t)kF4RingBytes + 1024 + 8 * (6 * kF4Stages + 5) + 16; }
+static_assert(kF4RingBytes + 1024 + 8 * (6 * kF4Stages + 5) + 16 <= 227 * 1024, "shared memory budget");
+
+bool fp4_tc_supported(int rows_total, int K) { return rows_total % 128 == 0 && K % 256 == 0; }
+
+template <int STAGE>
+static cudaError_t launch_fp4_one(const GroupedArgs &a, int rows_total, cudaStream_t s) {
+  const size_t smem = fp4_smem_bytes();
+  cudaError_t err = cudaFuncSetAttribute(k_grouped_fp4<STAGE>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (err != cudaSuccess) return err;
+  int dev = 0, sms = 0;
+  if ((err = cudaGetDevice(&dev)) != cudaSuccess) return err;
+  if ((err = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) return err;
+  GroupedArgs g = a;
+  g.n_blocks = rows_total / 128;
+  return launch_pdl(k_grouped_fp4<STAGE>, dim3(sms), dim3(kF4Threads), smem, s, g);
+}
+
+cudaError_t launch_grouped_fp4(int stage, const GroupedArgs &a, int rows_total, cudaStream_t s) {
+  if (!fp4_tc_supported(rows_total, a.K)) return cudaErrorInvalidValue;
+  switch (stage) {
+    case STAGE_GATED: return launch_fp4_one<STAGE_GATED>(a, rows_total, s);
+    case STAGE_RELU2: return launch_fp4_one<STAGE_RELU2>(a, rows_total, s);
+    case STAGE_DOWN: return launch_fp4_one<STAGE_DOWN>(a, rows_total, s);
+  }
+  return cudaErrorInvalidValue;
+}
+
+}  // namespace bqmoe

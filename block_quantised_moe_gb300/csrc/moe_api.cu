@@ -23,6 +23,7 @@ struct moe_plan_s {
   WeightLayout L;
   int K = 0, max_tokens = 0, afmt = 0, pad = 16;
   bool tc_on = false;  // experts with >= large_min pairs run on the tcgen05 kernel
+  bool fp4_on = false; // ... on the block-scaled FP4 kernel (W4A4 with the weights' FP4 tiles)
   int large_min = 0x7FFFFFFF;
   ScratchLayout S;
 };
@@ -85,6 +86,7 @@ moe_status moe_plan_weights(const moe_weight_desc *d, moe_weight_plan *out, size
   if (d->num_experts < 1 || d->hidden <= 0 || d->intermediate <= 0) return MOE_ERR_INVALID_ARG;
   if (d->wfmt != MOE_W_NVFP4 && d->wfmt != MOE_W_MXFP4) return MOE_ERR_INVALID_ARG;
   if (d->act != MOE_ACT_SILU_GATED && d->act != MOE_ACT_RELU2) return MOE_ERR_INVALID_ARG;
+  if (d->flags & ~MOE_WFLAG_FP4_TILES) return MOE_ERR_INVALID_ARG;
   if (d->num_experts > kMaxExperts || d->hidden % 128 || d->intermediate % 64) return MOE_ERR_UNSUPPORTED;
   WeightLayout L;
   L.E = d->num_experts;
@@ -97,7 +99,14 @@ moe_status moe_plan_weights(const moe_weight_desc *d, moe_weight_plan *out, size
   L.off_c13 = 0;  // codes and scales interleaved per 128-row block and 64-K step
   L.off_c2 = align_up(L.off_c13 + (size_t)L.E * L.blk13_expert());
   L.off_g = align_up(L.off_c2 + (size_t)L.E * L.blk2_expert());
-  L.total = align_up(L.off_g + (size_t)L.E * 4 * sizeof(float));
+  L.off_t13 = L.off_t2 = align_up(L.off_g + (size_t)L.E * 4 * sizeof(float));
+  if (d->flags & MOE_WFLAG_FP4_TILES) {
+    if (d->wfmt != MOE_W_NVFP4) return MOE_ERR_UNSUPPORTED;
+    L.fp4_tiles = L.n13 % 128 == 0 && L.H % 256 == 0 && L.I % 256 == 0;
+    if (!L.fp4_tiles) return MOE_ERR_UNSUPPORTED;
+    L.off_t2 = align_up(L.off_t13 + (size_t)L.E * L.t13_expert());
+  }
+  L.total = L.fp4_tiles ? align_up(L.off_t2 + (size_t)L.E * L.t2_expert()) : L.off_t13;
   moe_weight_plan p = new (std::nothrow) moe_weight_plan_s{L};
   if (!p) return MOE_ERR_CAPACITY;
   *out = p;
@@ -192,9 +201,13 @@ moe_status moe_plan(const moe_caps *c, moe_plan_t *out, size_t *scratch_bytes, i
   P.tc_on = Pmax >= 1024 && tc_supported(L.n13, L.H) && tc_supported(L.H, L.I);
   if (P.tc_on) {
     P.large_min = kLargeMin;
-    if (L.wfmt == MOE_W_MXFP4) S.xb16 = take(2 * (size_t)T * L.H);
-    S.h16 = take(2 * (size_t)S.cap_sorted * L.I);
-    if (L.wfmt == MOE_W_NVFP4) S.h16fac = take(4 * (size_t)S.cap_sorted);
+    // W4A4 with FP4 tiles: both operands go to the block-scaled FP4 MMA as codes.
+    P.fp4_on = P.afmt == MOE_A_NVFP4 && L.fp4_tiles && fp4_tc_supported(L.n13, L.H) && fp4_tc_supported(L.H, L.I);
+    if (!P.fp4_on) {
+      if (L.wfmt == MOE_W_MXFP4) S.xb16 = take(2 * (size_t)T * L.H);
+      S.h16 = take(2 * (size_t)S.cap_sorted * L.I);
+      if (L.wfmt == MOE_W_NVFP4) S.h16fac = take(4 * (size_t)S.cap_sorted);
+    }
   }
   S.part = take(4 * (size_t)S.cap_sorted * L.H);
   S.total = o;
@@ -353,11 +366,21 @@ static moe_status run_forward(moe_binding b, cudaStream_t stream, cudaEvent_t *e
   if (err == cudaSuccess && P.tc_on) {
     GroupedArgs t = a;
     t.act_by_token = 1;
-    if (!nv) {
-      t.act = at<__half>(sc, S.xb16);
-      t.act_g = nullptr;
+    if (P.fp4_on) {
+      t.codes = b->packed + L.off_t13;
+      t.codes_expert = L.t13_expert();
+      t.act = x_src;
+      t.act_scales = x_src_scales;
+      t.act_g = at<float>(sc, S.xq_g);
+      t.out_amax = nullptr;
+      err = launch_grouped_fp4(stage1, t, L.n13, stream);
+    } else {
+      if (!nv) {
+        t.act = at<__half>(sc, S.xb16);
+        t.act_g = nullptr;
+      }
+      err = launch_grouped_tc(stage1, L.wfmt, t, L.n13, E, stream);
     }
-    err = launch_grouped_tc(stage1, L.wfmt, t, L.n13, E, stream);
   }
   a.out_amax = nullptr;
   if (err != cudaSuccess) return MOE_ERR_CUDA;
@@ -386,7 +409,7 @@ static moe_status run_forward(moe_binding b, cudaStream_t stream, cudaEvent_t *e
   if (err != cudaSuccess) return MOE_ERR_CUDA;
 
   // GEMM2 * topk_weight -> partials, then the ordered combine
-  if (P.tc_on) {  // 16-bit slot-order rows of h (or of its re-quantised codes) for the tcgen05 GEMM2
+  if (P.tc_on && !P.fp4_on) {  // 16-bit slot-order rows of h (or of its re-quantised codes) for the tcgen05 GEMM2
     err = launch_stage_h16(src2, a.act, a.act_scales, a.act_g, I, S.cap_sorted, offsets + E, at<__half>(sc, S.h16),
                            nv ? at<float>(sc, S.h16fac) : nullptr, !nv, stream);
     if (err != cudaSuccess) return MOE_ERR_CUDA;
@@ -398,7 +421,13 @@ static moe_status run_forward(moe_binding b, cudaStream_t stream, cudaEvent_t *e
   a.out = part;
   if (mark(MOE_STAGE_GEMM2) != cudaSuccess) return MOE_ERR_CUDA;
   err = launch_grouped_mma(L.wfmt, src2, STAGE_DOWN, a, H, E, ntok, stream);
-  if (err == cudaSuccess && P.tc_on) {
+  if (err == cudaSuccess && P.tc_on && P.fp4_on) {
+    GroupedArgs t = a;  // h^ codes, scales and per-slot globals
+    t.codes = b->packed + L.off_t2;
+    t.codes_expert = L.t2_expert();
+    t.act_by_token = 0;
+    err = launch_grouped_fp4(STAGE_DOWN, t, H, stream);
+  } else if (err == cudaSuccess && P.tc_on) {
     GroupedArgs t = a;
     t.act = at<__half>(sc, S.h16);
     t.act_scales = nullptr;

@@ -79,10 +79,11 @@ def make_experts_gpu(E, H, I, wfmt, act, seed=0, device="cuda", gen_device=None)
 class PackedLayer:
     """Packed experts of one layer (moe_plan_weights + moe_prepare_weights)."""
 
-    def __init__(self, ck: CheckpointExperts, hidden: int, intermediate: int):
+    def __init__(self, ck: CheckpointExperts, hidden: int, intermediate: int, fp4_tiles: bool = False):
         self.wfmt, self.act = ck.wfmt, ck.act
         self.E, self.H, self.I = ck.num_experts, hidden, intermediate
-        self.wplan, nbytes = abi.moe_plan_weights(self.E, hidden, intermediate, ck.wfmt, ck.act)
+        flags = abi.MOE_WFLAG_FP4_TILES if fp4_tiles else 0
+        self.wplan, nbytes = abi.moe_plan_weights(self.E, hidden, intermediate, ck.wfmt, ck.act, flags)
         dev = ck.w13_codes.device
         self.packed = torch.empty(nbytes, dtype=torch.uint8, device=dev)
         abi.moe_prepare_weights(self.wplan, ck.w13_codes, ck.w13_scales, ck.w13_global, ck.w2_codes,

@@ -89,12 +89,22 @@ enum { MOE_A_BF16 = 1, MOE_A_NVFP4 = 2, MOE_A_MXFP8 = 3 };
 /* Expert activation. */
 enum { MOE_ACT_SILU_GATED = 1, MOE_ACT_RELU2 = 2 };
 
+/* Weight packing flags (moe_weight_desc.flags).
+ * MOE_WFLAG_FP4_TILES: NVFP4 only.  Also store every 128-row x 256-K block of
+ * W13 and W2 as a 128-byte-swizzled tile of E2M1 codes plus its E4M3 scales
+ * arranged for tensor memory, which the prefill kernel feeds straight to the
+ * block-scaled FP4 tensor-core MMA when the activations are NVFP4 (W4A4; b12x
+ * project page, "What's in here": NVFP4 activations).  Costs another 0.5625
+ * bytes per weight element.  Without it W4A4 prefill dequantises to FP16. */
+enum { MOE_WFLAG_FP4_TILES = 1 };
+
 typedef struct moe_weight_desc {
   int32_t num_experts;   /* E, 1..512                         */
   int32_t hidden;        /* H, multiple of 128                */
   int32_t intermediate;  /* I, multiple of 64                 */
   int32_t wfmt;          /* MOE_W_*                           */
   int32_t act;           /* MOE_ACT_*                         */
+  int32_t flags;         /* MOE_WFLAG_* bits, 0 for none      */
 } moe_weight_desc;
 
 typedef struct moe_weight_plan_s *moe_weight_plan;

@@ -27,13 +27,13 @@ def lib():
 _LAYERS = {}
 
 
-def gpu_layer(lib, E, H, I, wfmt, act, seed=0):
+def gpu_layer(lib, E, H, I, wfmt, act, seed=0, fp4_tiles=False):
     abi, layer = lib
-    key = (E, H, I, wfmt, act, seed)
+    key = (E, H, I, wfmt, act, seed, fp4_tiles)
     if key not in _LAYERS:
         ck = layer.make_experts_gpu(E, H, I, wfmt, act, seed=seed)
         _LAYERS.clear()  # keep at most one large layer resident
-        _LAYERS[key] = (ck, layer.PackedLayer(ck, H, I))
+        _LAYERS[key] = (ck, layer.PackedLayer(ck, H, I, fp4_tiles=fp4_tiles))
     return _LAYERS[key]
 
 
@@ -113,10 +113,12 @@ def test_decode_zipf_e256_h7168(lib, T):
     tl.check_close(out.float().cpu().numpy()[toks], y_ref, f"zipf T={T}")
 
 
-@pytest.mark.parametrize("name", ["prefill_w4a16_e256_h7168_i2048_k8", "prefill_w4a4_e256_h7168_i2048_k8"])
-def test_prefill_e256_h7168(lib, name):
+@pytest.mark.parametrize("name,fp4_tiles", [("prefill_w4a16_e256_h7168_i2048_k8", False),
+                                            ("prefill_w4a4_e256_h7168_i2048_k8", False),
+                                            ("prefill_w4a4_e256_h7168_i2048_k8", True)])
+def test_prefill_e256_h7168(lib, name, fp4_tiles):
     cfg = cfg_of(name)
-    ck, packed = gpu_layer(lib, cfg["E"], cfg["H"], cfg["I"], cfg["wfmt"], cfg["act"])
+    ck, packed = gpu_layer(lib, cfg["E"], cfg["H"], cfg["I"], cfg["wfmt"], cfg["act"], fp4_tiles=fp4_tiles)
     T = cfg["tokens"][0]
     x, ids, w = tl.make_inputs(cfg, T)
     out, _, _ = run(lib, packed, x, ids, w, cfg["K"], cfg["afmt"])
@@ -145,6 +147,19 @@ def test_tcgen05_path_small_layer(lib, wfmt, act, afmt, T):
     out, _, _ = run(lib, packed, x, ids, w, K, afmt)
     y_ref = tl.oracle_forward(ck, H, I, x, ids, w, afmt)
     tl.check_close(out.float().cpu().numpy(), y_ref, f"tcgen05 {wfmt}/{act}/{afmt} T={T}")
+
+
+@pytest.mark.parametrize("act", ["silu", "relu2"])
+@pytest.mark.parametrize("T", [512, 700])
+def test_block_scaled_fp4_path_small_layer(lib, act, T):
+    # W4A4 with the weights' FP4 tiles: experts with 32+ pairs run on the
+    # kind::mxf4nvf4 kernel, both operands as E2M1 codes with E4M3 block scales
+    cfg = dict(cfg_of("tiny_e8_h256_i512_k2"))
+    E, H, I, K = cfg["E"], cfg["H"], cfg["I"], cfg["K"]
+    ck, packed = gpu_layer(lib, E, H, I, "nvfp4", act, fp4_tiles=True)
+    x, ids, w = tl.make_inputs(cfg, T, seed=T)
+    out, _, _ = run(lib, packed, x, ids, w, K, "nvfp4")
+    tl.check_close(out.float().cpu().numpy(), tl.oracle_forward(ck, H, I, x, ids, w, "nvfp4"), f"fp4 {act} T={T}")
 
 
 @pytest.mark.parametrize("wfmt,act,afmt", [("nvfp4", "silu", "bf16"), ("mxfp4", "relu2", "mxfp8")])
