@@ -115,7 +115,10 @@ __device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;"
 
 // --------------------------------------------------------------- misc
 
-__device__ __forceinline__ float silu_f32(float a) { return a * (1.0f / (1.0f + expf(-a))); }
+// SiLU(a) = a * sigmoid(a), with the hardware exponential and approximate
+// division (relative error ~1e-6, far inside the output tolerance); large
+// negative a gives exp(-a) = inf and a zero sigmoid.
+__device__ __forceinline__ float silu_f32(float a) { return a * __fdividef(1.0f, 1.0f + __expf(-a)); }
 
 __device__ __forceinline__ float warp_max(float v) {
 #pragma unroll

@@ -48,6 +48,7 @@ struct ScratchLayout {
   size_t x16 = 0, xfac = 0, hamax = 0;  // tensor-core path: FP16 x, its factors, per-pair max |h|
   size_t h16 = 0, h16fac = 0;           // tcgen05 path: 16-bit h rows (and their FP16 factors)
   size_t xb16 = 0;                      // tcgen05 path, MXFP4: BF16 slot-order x rows
+  size_t xt = 0, ht = 0;                // FP4 path: x^ / h^ as slot-major 128-row tiles (codes + scales)
   size_t part = 0, total = 0;
 };
 
@@ -135,9 +136,13 @@ cudaError_t launch_combine(const float *part, int H, const int32_t *pair_pos, in
 // Quantisers.  `rows_dev`, when non-null, is a device int with the number of
 // rows that are live; rows at or beyond it are skipped, and so are rows r with
 // row_live[r] < 0 when row_live (the expert-sorted pair list) is non-null.
+// With `tiles` (cols a multiple of 256) the codes and scales also go to the
+// slot-major FP4 tiles of the block-scaled kernel: token row r to the slots
+// tile_slots[r * top_k + k] (top_k > 0), or row r to slot r (top_k == 0).
 cudaError_t launch_quant_rows_nvfp4(const void *src, bool src_bf16, int64_t rows, int64_t cols,
                                     uint8_t *codes, uint8_t *scales, float *g, const int32_t *rows_dev,
-                                    const int32_t *row_live, cudaStream_t s);
+                                    const int32_t *row_live, cudaStream_t s, uint8_t *tiles = nullptr,
+                                    const int32_t *tile_slots = nullptr, int top_k = 0);
 cudaError_t launch_quant_blocks(int qfmt, const void *src, bool src_bf16, int64_t rows, int64_t cols,
                                 int64_t rows_per_global, const float *g, uint8_t *codes, uint8_t *scales,
                                 const int32_t *rows_dev, const int32_t *row_live, cudaStream_t s);

@@ -12,11 +12,13 @@
 //
 // * A: the weights' FP4 tiles (MOE_WFLAG_FP4_TILES): a 16 KB 128-byte-swizzled
 //   tile per 128-row block and 256-K block, one bulk copy; no dequantisation.
-// * B: 128 rows of the quantised activations (x^ per token for GEMM1, h^ per
-//   slot for GEMM2), gathered with cp.async into the same swizzled layout
-//   (zero-filled past the expert's last token).
+// * B: the quantised activations of the item's 128 slots (x^ of each slot's
+//   token for GEMM1, h^ for GEMM2), which the row quantiser writes as slot-major
+//   tiles in the same swizzled layout (16 KB of codes + 2 KB of scales per
+//   256-K block): one bulk copy, like A.  Slots past the expert's last pair hold
+//   stale values that only reach accumulator columns that are never read.
 // * Scale factors: the weight tile's scale words ride in the same bulk copy as
-//   its codes, the activation rows' scale bytes in the same gather as theirs;
+//   its codes, the activation rows' scale bytes in the same copy as theirs;
 //   four warps, one per TMEM lane quadrant, move them from shared memory into
 //   TMEM with tcgen05.st in the layout the MMA reads: 32 lanes x 4 columns per
 //   64-K step, lane i column c holding the four E4M3 scales of row i + 32c, the
@@ -35,24 +37,22 @@
 
 namespace bqmoe {
 
-constexpr int kF4EpiWarps = 4;                       // warps 0-3: epilogue
-constexpr int kF4SfWarp0 = 4;                        // warps 4-7: scale factors into TMEM
-constexpr int kF4BWarp0 = 8, kF4BWarps = 4;          // warps 8-11: activation gather
-constexpr int kF4AWarp = 12;                         // weight tile bulk copies
-constexpr int kF4MmaWarp = 13;                       // MMA issue
+constexpr int kF4EpiWarps = 8;                       // warps 0-7: epilogue (lane quadrant w % 4, column half w / 4)
+constexpr int kF4SfWarp0 = 8;                        // warps 8-11: scale factors into TMEM
+constexpr int kF4BWarp = 12;                         // activation tile bulk copies
+constexpr int kF4AWarp = 13;                         // weight tile bulk copies
+constexpr int kF4MmaWarp = 14;                       // MMA issue
 constexpr int kF4Threads = (kF4MmaWarp + 1) * 32;
 constexpr int kF4N = 128;                            // tokens per tile
 constexpr int kF4TileBytes = 16384;                  // 128 rows x 256 K of E2M1
 constexpr int kF4SfBytes = 2048;                     // their scales (weights: packed tile; activations: gathered)
 constexpr int kF4StageBytes = kF4TileBytes + kF4SfBytes;  // one operand's ring stage (a multiple of 1024)
 constexpr int kF4Stages = 6;                         // A, B and scale-factor ring depth
-constexpr int kF4BLag = 4;                           // cp.async stages a B thread keeps in flight
 constexpr int kF4RingBytes = 2 * kF4Stages * kF4StageBytes;
 constexpr int kF4AccCols = kF4N;                     // TMEM columns per accumulator (FP32, N tokens)
 constexpr int kF4SfCol0 = 2 * kF4AccCols;            // scale-factor stages after the two accumulators
 constexpr int kF4SfCols = 32;                        // per stage: A 16 + B 16 (4 K steps x 4 columns)
 constexpr int kF4TmemCols = 512;
-constexpr int kF4BRows = kF4N * 8 / (kF4BWarps * 32);  // 16-byte code chunks per B thread per k-block
 static_assert(kF4StageBytes % 1024 == 0, "swizzled tiles need 1024-byte aligned stages");
 static_assert(kF4SfCol0 + kF4Stages * kF4SfCols <= kF4TmemCols, "TMEM budget");
 
@@ -95,7 +95,7 @@ __global__ void __launch_bounds__(kF4Threads, 1) k_grouped_fp4(const GroupedArgs
     for (int i = 0; i < kF4Stages; ++i) {
       mbar_init(afull0 + 8u * i, 1);
       mbar_init(aempty0 + 8u * i, 1);
-      mbar_init(bfull0 + 8u * i, kF4BWarps);
+      mbar_init(bfull0 + 8u * i, 1);
       mbar_init(bempty0 + 8u * i, 1);
       mbar_init(sfull0 + 8u * i, 4);
       mbar_init(sempty0 + 8u * i, 1);
@@ -162,67 +162,43 @@ __global__ void __launch_bounds__(kF4Threads, 1) k_grouped_fp4(const GroupedArgs
         if (issued & (1u << i)) mbar_wait(afull0 + 8u * i, (issued_parity >> i) & 1u);
     }
     __syncwarp();
-  } else if (warp >= kF4BWarp0 && warp < kF4BWarp0 + kF4BWarps) {
-    // ------------------------------------------------------ activation gather
-    const int t = threadIdx.x - kF4BWarp0 * 32;
-    const int cc = t & 7;                          // 16-byte chunk of the 128-byte row
-    constexpr int kRowStep = kF4BWarps * 32 / 8;   // rows between a thread's chunks
-    int slot = 0, issued = 0;
-    uint32_t phase = 0;
-    const uint8_t *act = reinterpret_cast<const uint8_t *>(a.act);
-    pdl_wait();  // the quantised activations come from the preceding kernel
-    for (int w = w0; w < W && ok; w += wstep) {
-      const TcItem it = cur.at(a, w, nblk);
-      int rid[kF4BRows];
-#pragma unroll
-      for (int i = 0; i < kF4BRows; ++i) {
-        const int r = (t >> 3) + kRowStep * i;
-        const int s = it.s0 + r;
-        rid[i] = r < it.ntok ? (by_token ? a.sorted_pair[s] / a.top_k : s) : -1;
-      }
-      for (int kb = 0; kb < nkb; ++kb) {
-        if (!mbar_wait(bempty0 + 8u * slot, phase ^ 1u)) {
-          ok = false;
-          break;
-        }
-        const uint32_t stB = ringB + (uint32_t)slot * kF4StageBytes;
-#pragma unroll
-        for (int i = 0; i < kF4BRows; ++i) {
-          const int r = (t >> 3) + kRowStep * i;
-          const uint32_t dst = stB + (uint32_t)((r >> 3) * 1024 + (r & 7) * 128 + (((cc ^ r) & 7) << 4));
-          const uint8_t *src = act + (int64_t)(rid[i] < 0 ? 0 : rid[i]) * (K / 2) + kb * 128 + cc * 16;
-          cp_async16(dst, src, rid[i] >= 0);
-        }
-        // the 16 scale bytes of token row t of this 256-K block (rows past the tile's tokens: zero)
-        if (t < kF4N) {
-          const int s = it.s0 + t;
-          const int64_t rs = t < it.ntok ? (by_token ? a.sorted_pair[s] / a.top_k : s) : -1;
-          cp_async16(stB + kF4TileBytes + t * 16, a.act_scales + (rs < 0 ? 0 : rs) * (K / 16) + kb * 16, rs >= 0);
-        }
-        cp_async_commit();
-        ++issued;
-        if (issued > kF4BLag) {  // the stage issued kF4BLag steps ago has landed
-          cp_async_wait_group<kF4BLag>();
-          fence_async_smem();
-          __syncwarp();
-          if (lane == 0) mbar_arrive(bfull0 + 8u * ((slot + kF4Stages - kF4BLag) % kF4Stages));
-        }
-        if (++slot == kF4Stages) {
-          slot = 0;
-          phase ^= 1u;
+  } else if (warp == kF4BWarp) {
+    // ------------------------------------------------------ activation tiles
+    // The activation rows of an item's 128 slots are one slot-major tile per
+    // 256-K block (written by the row quantiser; expert groups are padded to
+    // 128 slots, so a tile never straddles two experts): one bulk copy each.
+    if (lane == 0) {
+      int slot = 0;
+      uint32_t phase = 0;
+      uint32_t issued = 0, issued_parity = 0;
+      const uint8_t *act = reinterpret_cast<const uint8_t *>(a.act);
+      pdl_wait();  // the activation tiles come from the preceding kernel
+      for (int w = w0; w < W && ok; w += wstep) {
+        const TcItem it = cur.at(a, w, nblk);
+        const uint8_t *tiles = act + (size_t)(it.s0 / kF4N) * nkb * kF4StageBytes;
+        for (int kb = 0; kb < nkb; ++kb) {
+          if (!mbar_wait(bempty0 + 8u * slot, phase ^ 1u)) {
+            ok = false;
+            break;
+          }
+          mbar_expect_tx(bfull0 + 8u * slot, kF4StageBytes);
+          bulk_g2s(ringB + (uint32_t)slot * kF4StageBytes, tiles + (size_t)kb * kF4StageBytes, kF4StageBytes,
+                   bfull0 + 8u * slot);
+          issued |= 1u << slot;
+          issued_parity = (issued_parity & ~(1u << slot)) | (phase << slot);
+          if (++slot == kF4Stages) {
+            slot = 0;
+            phase ^= 1u;
+          }
         }
       }
+      for (int i = 0; i < kF4Stages; ++i)
+        if (issued & (1u << i)) mbar_wait(bfull0 + 8u * i, (issued_parity >> i) & 1u);
     }
-    cp_async_wait_group<0>();
-    fence_async_smem();
     __syncwarp();
-    if (ok && lane == 0) {
-      for (int back = issued < kF4BLag ? issued : kF4BLag; back >= 1; --back)
-        mbar_arrive(bfull0 + 8u * ((slot + kF4Stages - back) % kF4Stages));
-    }
   } else if (warp >= kF4SfWarp0 && warp < kF4SfWarp0 + 4) {
     // ------------------------------------------------------ scale factors -> TMEM
-    // Warp 4 + q writes lane quadrant q; every quadrant gets the same words:
+    // Warp 8 + q writes lane quadrant q; every quadrant gets the same words:
     // the weight tile's 16 words of this lane (copied with the codes, already in
     // [step][column] order) and the 16 scale bytes of token rows lane + 32c
     // (gathered with the activation codes).
@@ -317,7 +293,9 @@ __global__ void __launch_bounds__(kF4Threads, 1) k_grouped_fp4(const GroupedArgs
     __syncwarp();
   } else {
     // ------------------------------------------------------ epilogue
-    const int m = warp * 32 + lane;  // accumulator row = TMEM lane
+    const int m = (warp & 3) * 32 + lane;  // accumulator row = TMEM lane
+    const int cbase = (warp >> 2) * (kF4N / 2);  // this warp's half of the 128 token columns
+    constexpr int kCh = kF4N / 2 / 32;
     pdl_wait();                      // activation globals come from the preceding kernel
     int li = 0;
     for (int w = w0; w < W && ok; w += wstep, ++li) {
@@ -327,17 +305,17 @@ __global__ void __launch_bounds__(kF4Threads, 1) k_grouped_fp4(const GroupedArgs
       // Per column (one per lane and 32-column chunk, broadcast with shuffles):
       // the activation row's FP32 global and, for the down projection, the
       // topk weight -- loaded before the accumulator is ready.
-      float f_l[kF4N / 32], w_l[kF4N / 32];
+      float f_l[kCh], w_l[kCh];
       {
-        int p_l[kF4N / 32];
+        int p_l[kCh];
 #pragma unroll
-        for (int ch = 0; ch < kF4N / 32; ++ch) {
-          const int nl = 32 * ch + lane;
+        for (int ch = 0; ch < kCh; ++ch) {
+          const int nl = cbase + 32 * ch + lane;
           p_l[ch] = nl < it.ntok ? a.sorted_pair[it.s0 + nl] : -1;
         }
 #pragma unroll
-        for (int ch = 0; ch < kF4N / 32; ++ch) {
-          const int nl = 32 * ch + lane;
+        for (int ch = 0; ch < kCh; ++ch) {
+          const int nl = cbase + 32 * ch + lane;
           f_l[ch] = 0.f;
           w_l[ch] = 0.f;
           if (p_l[ch] >= 0) {
@@ -354,10 +332,10 @@ __global__ void __launch_bounds__(kF4Threads, 1) k_grouped_fp4(const GroupedArgs
       const int blk = it.bp;
       const int tile = 8 * blk + (m >> 4), rr = m & 15;
 #pragma unroll
-      for (int ch = 0; ch < kF4N / 32; ++ch) {
-        const int c0 = 32 * ch;
+      for (int ch = 0; ch < kCh; ++ch) {
+        const int c0 = cbase + 32 * ch;
         uint32_t raw[32];
-        tc_ld32(tmem + ((uint32_t)(warp * 32) << 16) + (uint32_t)(b * kF4AccCols + c0), raw);
+        tc_ld32(tmem + ((uint32_t)((warp & 3) * 32) << 16) + (uint32_t)(b * kF4AccCols + c0), raw);
 #pragma unroll
         for (int j = 0; j < 32; ++j) {
           const int n = c0 + j;

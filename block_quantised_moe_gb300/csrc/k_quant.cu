@@ -108,12 +108,29 @@ __device__ __forceinline__ float block_max(float v, float *red) {
   return r;
 }
 
-// NVFP4 with one global per row: one CTA per row.
+// Position of 16-element block b of a row in a slot-major FP4 tile buffer
+// (128 slots x 256 K per 18432-byte tile: codes in the 128-byte-swizzled K-major
+// layout, then 16 scale bytes per slot row).
+__device__ __forceinline__ uint8_t *fp4_tile_codes(uint8_t *tiles, int64_t slot, int64_t b, int nkb) {
+  const int64_t kb = b >> 4, r = slot & 127;
+  uint8_t *tile = tiles + ((slot >> 7) * nkb + kb) * 18432;
+  const int c = (int)((b & 15) >> 1);  // 16-byte chunk of the 128-byte row
+  return tile + (r >> 3) * 1024 + (r & 7) * 128 + (((c ^ (int)r) & 7) << 4) + 8 * (b & 1);
+}
+__device__ __forceinline__ uint8_t *fp4_tile_scale(uint8_t *tiles, int64_t slot, int64_t b, int nkb) {
+  return tiles + ((slot >> 7) * nkb + (b >> 4)) * 18432 + 16384 + (slot & 127) * 16 + (b & 15);
+}
+
+// NVFP4 with one global per row: one CTA per row.  With `tiles` the row's codes
+// and scales also go to the slot-major FP4 tiles of the block-scaled kernel:
+// a token row (tile_slots = pair_pos, top_k > 0) to each of its valid slots, a
+// slot row (top_k == 0) to its own slot.
 template <bool BF16>
 __global__ void __launch_bounds__(kQThreads)
 k_quant_rows_nvfp4(const void *__restrict__ src, int64_t cols, uint8_t *__restrict__ codes,
                    uint8_t *__restrict__ scales, float *__restrict__ g_out, const int32_t *__restrict__ rows_dev,
-                   const int32_t *__restrict__ row_live) {
+                   const int32_t *__restrict__ row_live, uint8_t *__restrict__ tiles,
+                   const int32_t *__restrict__ tile_slots, int top_k) {
   __shared__ float red[32];
   pdl_trigger();
   pdl_wait();
@@ -141,6 +158,15 @@ k_quant_rows_nvfp4(const void *__restrict__ src, int64_t cols, uint8_t *__restri
     nvfp4_block(x, g, c, s);
     *reinterpret_cast<uint2 *>(codes + (base + b * 16) / 2) = c;
     scales[row * (cols / 16) + b] = (uint8_t)s;
+    if (tiles != nullptr) {
+      const int nkb = (int)(cols / 256);
+      for (int k = 0; k < (top_k > 0 ? top_k : 1); ++k) {
+        const int64_t slot = top_k > 0 ? (int64_t)tile_slots[row * top_k + k] : row;
+        if (slot < 0) continue;
+        *reinterpret_cast<uint2 *>(fp4_tile_codes(tiles, slot, b, nkb)) = c;
+        *fp4_tile_scale(tiles, slot, b, nkb) = (uint8_t)s;
+      }
+    }
   }
 }
 
@@ -220,14 +246,15 @@ static int grid_for(int64_t work, int per_cta) {
 
 cudaError_t launch_quant_rows_nvfp4(const void *src, bool src_bf16, int64_t rows, int64_t cols, uint8_t *codes,
                                     uint8_t *scales, float *g, const int32_t *rows_dev, const int32_t *row_live,
-                                    cudaStream_t s) {
+                                    cudaStream_t s, uint8_t *tiles, const int32_t *tile_slots, int top_k) {
   if (rows <= 0) return cudaSuccess;
   if (rows > 0x7FFFFFFF) return cudaErrorInvalidValue;
+  if (tiles != nullptr && cols % 256 != 0) return cudaErrorInvalidValue;
   if (src_bf16)
     return launch_pdl(k_quant_rows_nvfp4<true>, dim3((unsigned)rows), dim3(kQThreads), 0, s, src, cols, codes, scales,
-                      g, rows_dev, row_live);
+                      g, rows_dev, row_live, tiles, tile_slots, top_k);
   return launch_pdl(k_quant_rows_nvfp4<false>, dim3((unsigned)rows), dim3(kQThreads), 0, s, src, cols, codes, scales, g,
-                    rows_dev, row_live);
+                    rows_dev, row_live, tiles, tile_slots, top_k);
 }
 
 cudaError_t launch_quant_blocks(int qfmt, const void *src, bool src_bf16, int64_t rows, int64_t cols,

@@ -51,7 +51,8 @@ namespace {
 
 constexpr int kMaxExperts = 512;
 constexpr int kMaxTopK = 16;
-constexpr int kPad = 16;  // expert groups are padded to this many pairs
+constexpr int kPad = 16;        // expert groups are padded to this many pairs
+constexpr int kFp4Tile = 128;   // ... and to this many with the block-scaled FP4 kernel
 constexpr int kLargeMin = 32;  // pairs from which an expert runs on the tcgen05 kernel
 
 bool aligned(const void *p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
@@ -158,6 +159,17 @@ moe_status moe_plan(const moe_caps *c, moe_plan_t *out, size_t *scratch_bytes, i
   const int64_t Pmax = (int64_t)c->max_tokens * c->top_k;
   const int64_t T = c->max_tokens;
   ScratchLayout &S = P.S;
+  // Plans for batches of 1024+ (token, slot) pairs send experts with at least
+  // kLargeMin pairs to the tcgen05 kernels (dense tiles of 128 tokens): FP16
+  // operands with row factors for NVFP4, BF16 operands for MXFP4 (E2M1 * 2^X and
+  // E4M3 * 2^X are exact in BF16, not in FP16), and, for W4A4 with the weights'
+  // FP4 tiles, both operands as E2M1 codes on the block-scaled FP4 MMA.  The FP4
+  // kernel reads its activation rows as slot-major 128-row tiles, so its plans
+  // pad every expert's group to 128 slots.
+  P.tc_on = Pmax >= 1024 && tc_supported(L.n13, L.H) && tc_supported(L.H, L.I);
+  P.fp4_on = P.tc_on && P.afmt == MOE_A_NVFP4 && L.fp4_tiles && fp4_tc_supported(L.n13, L.H) &&
+             fp4_tc_supported(L.H, L.I);
+  if (P.fp4_on) P.pad = kFp4Tile;
   S.cap_sorted = round_up(Pmax + (int64_t)L.E * (P.pad - 1), P.pad);
   size_t o = 0;
   auto take = [&](size_t bytes) {
@@ -194,16 +206,13 @@ moe_status moe_plan(const moe_caps *c, moe_plan_t *out, size_t *scratch_bytes, i
   S.x16 = take(2 * (size_t)T * L.H);
   S.xfac = take(4 * (size_t)T);
   S.hamax = take(4 * (size_t)S.cap_sorted);
-  // Plans for batches of 1024+ (token, slot) pairs send experts with at least
-  // kLargeMin pairs to the tcgen05 kernel (dense tiles of 128 tokens): FP16
-  // operands with row factors for NVFP4, BF16 operands for MXFP4 (E2M1 * 2^X and
-  // E4M3 * 2^X are exact in BF16, not in FP16).
-  P.tc_on = Pmax >= 1024 && tc_supported(L.n13, L.H) && tc_supported(L.H, L.I);
   if (P.tc_on) {
     P.large_min = kLargeMin;
-    // W4A4 with FP4 tiles: both operands go to the block-scaled FP4 MMA as codes.
-    P.fp4_on = P.afmt == MOE_A_NVFP4 && L.fp4_tiles && fp4_tc_supported(L.n13, L.H) && fp4_tc_supported(L.H, L.I);
-    if (!P.fp4_on) {
+    if (P.fp4_on) {
+      // activation tiles: per 128 slots and 256-K block, 16 KB of codes + 2 KB of scales
+      S.xt = take((size_t)(S.cap_sorted / kFp4Tile) * (L.H / 256) * WeightLayout::kFp4TileBytes);
+      S.ht = take((size_t)(S.cap_sorted / kFp4Tile) * (L.I / 256) * WeightLayout::kFp4TileBytes);
+    } else {
       if (L.wfmt == MOE_W_MXFP4) S.xb16 = take(2 * (size_t)T * L.H);
       S.h16 = take(2 * (size_t)S.cap_sorted * L.I);
       if (L.wfmt == MOE_W_NVFP4) S.h16fac = take(4 * (size_t)S.cap_sorted);
@@ -320,7 +329,8 @@ static moe_status run_forward(moe_binding b, cudaStream_t stream, cudaEvent_t *e
   a.act = b->x;
   if (P.afmt == MOE_A_NVFP4) {
     err = launch_quant_rows_nvfp4(b->x, true, T, H, at<uint8_t>(sc, S.xq_codes), at<uint8_t>(sc, S.xq_scales),
-                                  at<float>(sc, S.xq_g), nullptr, nullptr, stream);
+                                  at<float>(sc, S.xq_g), nullptr, nullptr, stream,
+                                  P.fp4_on ? at<uint8_t>(sc, S.xt) : nullptr, pair_pos, K);
     src1 = SRC_X_NVFP4;
     a.act = at<uint8_t>(sc, S.xq_codes);
     a.act_scales = at<uint8_t>(sc, S.xq_scales);
@@ -369,8 +379,8 @@ static moe_status run_forward(moe_binding b, cudaStream_t stream, cudaEvent_t *e
     if (P.fp4_on) {
       t.codes = b->packed + L.off_t13;
       t.codes_expert = L.t13_expert();
-      t.act = x_src;
-      t.act_scales = x_src_scales;
+      t.act = at<uint8_t>(sc, S.xt);  // x^ as slot-major FP4 tiles; per-token globals
+      t.act_scales = nullptr;
       t.act_g = at<float>(sc, S.xq_g);
       t.out_amax = nullptr;
       err = launch_grouped_fp4(stage1, t, L.n13, stream);
@@ -393,7 +403,8 @@ static moe_status run_forward(moe_binding b, cudaStream_t stream, cudaEvent_t *e
   a.act_g = at<float>(sc, S.hamax);
   if (P.afmt == MOE_A_NVFP4) {
     err = launch_quant_rows_nvfp4(h, false, S.cap_sorted, I, at<uint8_t>(sc, S.hq_codes),
-                                  at<uint8_t>(sc, S.hq_scales), at<float>(sc, S.hq_g), offsets + E, sorted, stream);
+                                  at<uint8_t>(sc, S.hq_scales), at<float>(sc, S.hq_g), offsets + E, sorted, stream,
+                                  P.fp4_on ? at<uint8_t>(sc, S.ht) : nullptr, nullptr, 0);
     src2 = SRC_H_NVFP4;
     a.act = at<uint8_t>(sc, S.hq_codes);
     a.act_scales = at<uint8_t>(sc, S.hq_scales);
@@ -422,9 +433,11 @@ static moe_status run_forward(moe_binding b, cudaStream_t stream, cudaEvent_t *e
   if (mark(MOE_STAGE_GEMM2) != cudaSuccess) return MOE_ERR_CUDA;
   err = launch_grouped_mma(L.wfmt, src2, STAGE_DOWN, a, H, E, ntok, stream);
   if (err == cudaSuccess && P.tc_on && P.fp4_on) {
-    GroupedArgs t = a;  // h^ codes, scales and per-slot globals
+    GroupedArgs t = a;  // h^ as slot-major FP4 tiles; per-slot globals
     t.codes = b->packed + L.off_t2;
     t.codes_expert = L.t2_expert();
+    t.act = at<uint8_t>(sc, S.ht);
+    t.act_scales = nullptr;
     t.act_by_token = 0;
     err = launch_grouped_fp4(STAGE_DOWN, t, H, stream);
   } else if (err == cudaSuccess && P.tc_on) {
