@@ -44,6 +44,7 @@ EXPORTS = (
     "moe_status_str", "moe_plan_weights", "moe_prepare_weights", "moe_is_supported", "moe_plan",
     "moe_bind", "moe_run", "moe_run_timed", "moe_run_host", "moe_device_status", "moe_debug_routing", "moe_quantize",
     "moe_destroy_weight_plan", "moe_destroy_plan", "moe_destroy_binding", "moe_run_no_alloc", "moe_launch_count",
+    "moe_measure_mma_peak",
 )
 
 
@@ -70,6 +71,7 @@ _sig = {
     "moe_run": (_i32, [_vp, _vp]),
     "moe_run_timed": (_i32, [_vp, _vp, _P(_vp)]),
     "moe_launch_count": (_i32, [_vp, _P(_i32)]),
+    "moe_measure_mma_peak": (_i32, [_i32, _i32, _i32, _P(ctypes.c_float)]),
     "moe_run_host": (_i32, [_vp, _vp, _vp, _vp, _vp, _vp]),
     "moe_device_status": (_i32, [_vp, _vp, _P(_i32)]),
     "moe_debug_routing": (_i32, [_vp, _vp, _P(_i32), _P(_i32), _P(_i32), _P(_i32), _i32]),
@@ -172,6 +174,16 @@ def moe_run_timed(binding, events, stream=None):
     """``events``: MOE_NUM_STAGES+1 raw cudaEvent_t handles (ints) created with timing enabled."""
     arr = (_vp * (MOE_NUM_STAGES + 1))(*events)
     _check(_lib.moe_run_timed(binding, _stream(stream), arr), "moe_run_timed")
+
+
+MOE_PEAK_F16, MOE_PEAK_FP4 = 0, 1
+
+
+def moe_measure_mma_peak(kind, n, iters=20000):
+    """Back-to-back tcgen05.mma issue rate (TFLOP/s) for kind MOE_PEAK_F16 / MOE_PEAK_FP4."""
+    t = ctypes.c_float(0)
+    _check(_lib.moe_measure_mma_peak(kind, n, iters, ctypes.byref(t)), "moe_measure_mma_peak")
+    return t.value
 
 
 def moe_launch_count(binding):

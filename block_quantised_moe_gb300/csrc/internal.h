@@ -43,6 +43,7 @@ struct WeightLayout {
 struct ScratchLayout {
   int64_t cap_sorted = 0;  // rows of the padded, expert-sorted pair list
   size_t status = 0, counts = 0, offsets = 0, sorted = 0, pair_pos = 0, active = 0, passes = 0, large = 0, large_tiles = 0;
+  size_t route_hist = 0;  // per-chunk expert counts of the chunked routing sort
   size_t xq_codes = 0, xq_scales = 0, xq_g = 0;
   size_t h = 0, hq_codes = 0, hq_scales = 0, hq_g = 0;
   size_t x16 = 0, xfac = 0, hamax = 0;  // tensor-core path: FP16 x, its factors, per-pair max |h|
@@ -84,7 +85,14 @@ struct GroupedArgs {
   const float *topk_weights;
   // output: h [cap][I] (GEMM1) or partials [cap][H] (GEMM2)
   float *out;
+  int out_bf16;  // GEMM2: the partials are BF16 (out reinterpreted), else FP32
 };
+
+// A GEMM2 partial (topk_weight x g_down x W2 h) into the FP32 or BF16 partial array.
+__device__ __forceinline__ void store_partial(const GroupedArgs &a, size_t idx, float v) {
+  if (a.out_bf16) reinterpret_cast<__nv_bfloat16 *>(a.out)[idx] = __float2bfloat16_rn(v);
+  else a.out[idx] = v;
+}
 
 // Optional staging done by extra CTAs of the routing launch: BF16 x [T][H] ->
 // FP16 rows + per-row factor, and clearing of `zero` (zero_n floats).
@@ -98,9 +106,12 @@ struct RouteStaging {
 
 // ntok: tokens per pass of the register-dequant kernel; experts with at least
 // large_min pairs go to the tcgen05 kernel in tiles of large_tile tokens.
+// Above 1024 pairs the sort runs in route_chunks(P) chunks and needs
+// chunk_hist: route_chunks(P) * (E + 1) ints of scratch.
+int route_chunks(int P);
 cudaError_t launch_route(const int32_t *ids, int P, int E, int pad, int ntok, int large_min, int large_tile,
                          int32_t *counts, int32_t *offsets, int32_t *sorted_pair, int32_t *pair_pos, int32_t *active,
-                         int32_t *passes, int32_t *large, int32_t *large_tiles, int32_t *status,
+                         int32_t *passes, int32_t *large, int32_t *large_tiles, int32_t *status, int32_t *chunk_hist,
                          const RouteStaging *stg, cudaStream_t s);
 
 // Register-dequant tensor-core grouped kernel (experts with few pairs), NVFP4 or
@@ -130,8 +141,9 @@ cudaError_t launch_stage_h16(int src, const void *act, const uint8_t *act_scales
                              int64_t rows, const int32_t *rows_dev, __half *h16, float *fac, bool out_bf16,
                              cudaStream_t s);
 
-cudaError_t launch_combine(const float *part, int H, const int32_t *pair_pos, int T, int K, void *out_bf16,
-                           cudaStream_t s);
+// Ordered per-token sum of the partials (FP32, or BF16 when part_bf16).
+cudaError_t launch_combine(const void *part, bool part_bf16, int H, const int32_t *pair_pos, int T, int K,
+                           void *out_bf16, cudaStream_t s);
 
 // Quantisers.  `rows_dev`, when non-null, is a device int with the number of
 // rows that are live; rows at or beyond it are skipped, and so are rows r with

@@ -19,45 +19,94 @@ namespace bqmoe {
 constexpr int kCombThreads = 128;
 constexpr int kMaxK = 16;
 
-__global__ void __launch_bounds__(kCombThreads)
-k_combine(const float *__restrict__ part, int H, const int32_t *__restrict__ pair_pos, int K,
-          __nv_bfloat16 *__restrict__ out) {
-  pdl_trigger();
-  // pair_pos is a routing output (complete before this kernel started): read and
-  // sort it while the preceding GEMM finishes.
-  const int t = blockIdx.y;
-  int pos[kMaxK];
-  int n = 0;
-  for (int k = 0; k < K; ++k) {
-    const int p = pair_pos[(size_t)t * K + k];
-    if (p < 0) continue;
-    int j = n++;
-    while (j > 0 && pos[j - 1] > p) { pos[j] = pos[j - 1]; --j; }
-    pos[j] = p;
-  }
-  pdl_wait();
-  const int c = (blockIdx.x * kCombThreads + threadIdx.x) * 4;
-  if (c >= H) return;
-  float4 v[kMaxK];
+// Eight consecutive partials as FP32 (one 16-byte BF16 load, or two FP32 ones).
+template <bool BF16>
+__device__ __forceinline__ void load_part8(const void *part, size_t idx, float (&v)[8]) {
+  if (BF16) {
+    const uint4 r = __ldcs(reinterpret_cast<const uint4 *>(reinterpret_cast<const __nv_bfloat16 *>(part) + idx));
+    const uint32_t w[4] = {r.x, r.y, r.z, r.w};
 #pragma unroll
-  for (int i = 0; i < kMaxK; ++i)  // all loads in flight before the ordered sum
-    if (i < n) v[i] = __ldcs(reinterpret_cast<const float4 *>(part + (size_t)pos[i] * H + c));
-  float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll
-  for (int i = 0; i < kMaxK; ++i)
-    if (i < n) {
-      acc.x += v[i].x; acc.y += v[i].y; acc.z += v[i].z; acc.w += v[i].w;
+    for (int i = 0; i < 4; ++i) {
+      v[2 * i] = __uint_as_float(w[i] << 16);
+      v[2 * i + 1] = __uint_as_float(w[i] & 0xFFFF0000u);
     }
-  __align__(8) __nv_bfloat162 o[2] = {__floats2bfloat162_rn(acc.x, acc.y), __floats2bfloat162_rn(acc.z, acc.w)};
-  *reinterpret_cast<uint2 *>(out + (size_t)t * H + c) = *reinterpret_cast<const uint2 *>(o);
+  } else {
+    const float4 a = __ldcs(reinterpret_cast<const float4 *>(reinterpret_cast<const float *>(part) + idx));
+    const float4 b = __ldcs(reinterpret_cast<const float4 *>(reinterpret_cast<const float *>(part) + idx) + 1);
+    v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w; v[4] = b.x; v[5] = b.y; v[6] = b.z; v[7] = b.w;
+  }
 }
 
-cudaError_t launch_combine(const float *part, int H, const int32_t *pair_pos, int T, int K, void *out,
+// Grid (column chunks of 8 * kCombThreads, token groups); each block loops over
+// tokens blockIdx.y, blockIdx.y + gridDim.y, ... (one resident wave; a block per
+// token made the kernel bound by block launches at large T).  The next token's
+// pair_pos row is fetched while the current token's partials load.
+template <bool BF16>
+__global__ void __launch_bounds__(kCombThreads)
+k_combine(const void *__restrict__ part, int H, const int32_t *__restrict__ pair_pos, int T, int K,
+          __nv_bfloat16 *__restrict__ out) {
+  pdl_trigger();
+  pdl_wait();
+  const int c = (blockIdx.x * kCombThreads + threadIdx.x) * 8;
+  if (c >= H) return;
+  int ids[kMaxK];  // pair_pos row of the block's next token, fetched one token ahead
+#pragma unroll
+  for (int k = 0; k < kMaxK; ++k) ids[k] = (k < K && blockIdx.y < T) ? __ldg(pair_pos + (size_t)blockIdx.y * K + k) : -1;
+  for (int t = blockIdx.y; t < T; t += gridDim.y) {
+    int pos[kMaxK];
+    int n = 0;
+#pragma unroll
+    for (int k = 0; k < kMaxK; ++k) {
+      const int p = ids[k];
+      if (p < 0) continue;
+      int j = n++;
+      while (j > 0 && pos[j - 1] > p) { pos[j] = pos[j - 1]; --j; }
+      pos[j] = p;
+    }
+    const int tn = t + gridDim.y;
+#pragma unroll
+    for (int k = 0; k < kMaxK; ++k) ids[k] = (k < K && tn < T) ? __ldg(pair_pos + (size_t)tn * K + k) : -1;
+    // ordered sum in chunks of 8 partials (the chunk's loads all in flight first)
+    float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+    for (int i0 = 0; i0 < n; i0 += 8) {
+      float v[8][8];
+#pragma unroll
+      for (int i = 0; i < 8; ++i)
+        if (i0 + i < n) load_part8<BF16>(part, (size_t)pos[i0 + i] * H + c, v[i]);
+#pragma unroll
+      for (int i = 0; i < 8; ++i)
+        if (i0 + i < n) {
+#pragma unroll
+          for (int e = 0; e < 8; ++e) acc[e] += v[i][e];
+        }
+    }
+    __align__(16) __nv_bfloat162 o[4];
+#pragma unroll
+    for (int e = 0; e < 4; ++e) o[e] = __floats2bfloat162_rn(acc[2 * e], acc[2 * e + 1]);
+    *reinterpret_cast<uint4 *>(out + (size_t)t * H + c) = *reinterpret_cast<const uint4 *>(o);
+  }
+}
+
+cudaError_t launch_combine(const void *part, bool part_bf16, int H, const int32_t *pair_pos, int T, int K, void *out,
                            cudaStream_t s) {
   if (T <= 0) return cudaSuccess;
-  if (K > kMaxK) return cudaErrorInvalidValue;
-  const int gx = (H + kCombThreads * 4 - 1) / (kCombThreads * 4);
-  return launch_pdl(k_combine, dim3(gx, T), dim3(kCombThreads), 0, s, part, H, pair_pos, K,
+  if (K > kMaxK || H % 8) return cudaErrorInvalidValue;
+  // one resident wave of blocks, each looping over its tokens
+  static int sms = 0, occ[2] = {0, 0};
+  if (!sms) {
+    int dev = 0, n = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
+        cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ[0], k_combine<false>, kCombThreads, 0) != cudaSuccess ||
+        cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ[1], k_combine<true>, kCombThreads, 0) != cudaSuccess)
+      return cudaErrorUnknown;
+    sms = n;
+  }
+  const int gx = (H + kCombThreads * 8 - 1) / (kCombThreads * 8);
+  const int gy = std::max(1, std::min(T, sms * std::max(1, occ[part_bf16 ? 1 : 0]) / gx));
+  if (part_bf16)
+    return launch_pdl(k_combine<true>, dim3(gx, gy), dim3(kCombThreads), 0, s, part, H, pair_pos, T, K,
+                      reinterpret_cast<__nv_bfloat16 *>(out));
+  return launch_pdl(k_combine<false>, dim3(gx, gy), dim3(kCombThreads), 0, s, part, H, pair_pos, T, K,
                     reinterpret_cast<__nv_bfloat16 *>(out));
 }
 

@@ -350,7 +350,7 @@ __global__ void __launch_bounds__(kF4Threads, 1) k_grouped_fp4(const GroupedArgs
             if (live) a.out[(size_t)s * a.n_rows + tile * 16 + rr] = r * r;
           } else {
             const float wt = __shfl_sync(0xffffffffu, w_l[ch], j);
-            if (live) a.out[(size_t)s * a.n_rows + blk * 128 + m] = wt * v;
+            if (live) store_partial(a, (size_t)s * a.n_rows + blk * 128 + m, wt * v);
           }
         }
       }

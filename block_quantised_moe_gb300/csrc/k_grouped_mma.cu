@@ -477,8 +477,8 @@ __global__ void __maxnreg__(kMmaMaxRegs) k_grouped_mma(const GroupedArgs a, int 
             hmax = fmaxf(v0 * v0, v1 * v1);
           } else if (live) {
             const float wt = a.topk_weights[a.sorted_pair[s]] * gl[2];
-            a.out[(size_t)s * a.n_rows + tile * 16 + r] = wt * lo;
-            a.out[(size_t)s * a.n_rows + tile * 16 + r + 8] = wt * hi;
+            store_partial(a, (size_t)s * a.n_rows + tile * 16 + r, wt * lo);
+            store_partial(a, (size_t)s * a.n_rows + tile * 16 + r + 8, wt * hi);
           }
           if (STAGE != STAGE_DOWN && a.out_amax != nullptr) {
             // max over the 8 lanes holding this token, then one atomic per warp; a max of

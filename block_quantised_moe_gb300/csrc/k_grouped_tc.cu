@@ -385,7 +385,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) k_grouped_tc(const GroupedArgs 
               hv[j] = r * r;
             } else {
               const float wt = __shfl_sync(0xffffffffu, w_l, j);
-              if (live) a.out[(size_t)s * a.n_rows + blk * 128 + m] = wt * v;
+              if (live) store_partial(a, (size_t)s * a.n_rows + blk * 128 + m, wt * v);
             }
           }
           if (STAGE != STAGE_DOWN && a.out_amax != nullptr) {

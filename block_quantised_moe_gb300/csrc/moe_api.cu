@@ -186,6 +186,7 @@ moe_status moe_plan(const moe_caps *c, moe_plan_t *out, size_t *scratch_bytes, i
   S.passes = take(4 * (size_t)(L.E + 1));
   S.large = take(4 * (size_t)(L.E + 1));
   S.large_tiles = take(4 * (size_t)(L.E + 1));
+  S.route_hist = take(4 * (size_t)route_chunks((int)Pmax) * (L.E + 1));
   if (P.afmt == MOE_A_NVFP4) {
     S.xq_codes = take((size_t)T * L.H / 2);
     S.xq_scales = take((size_t)T * L.H / 16);
@@ -218,7 +219,9 @@ moe_status moe_plan(const moe_caps *c, moe_plan_t *out, size_t *scratch_bytes, i
       if (L.wfmt == MOE_W_NVFP4) S.h16fac = take(4 * (size_t)S.cap_sorted);
     }
   }
-  S.part = take(4 * (size_t)S.cap_sorted * L.H);
+  // GEMM2 partials: BF16 when the tcgen05 kernels run (many tokens: the partials'
+  // write + read dominate the non-GEMM traffic), FP32 otherwise.
+  S.part = take((P.tc_on ? 2 : 4) * (size_t)S.cap_sorted * L.H);
   S.total = o;
   moe_plan_t p = new (std::nothrow) moe_plan_s(P);
   if (!p) return MOE_ERR_CAPACITY;
@@ -306,7 +309,8 @@ static moe_status run_forward(moe_binding b, cudaStream_t stream, cudaEvent_t *e
                    at<float>(sc, S.hamax), S.cap_sorted};
   const bool staged = P.afmt == MOE_A_BF16;
   if ((err = launch_route(b->ids, T * K, E, P.pad, ntok, P.large_min, 128, counts, offsets, sorted, pair_pos, active,
-                          passes, large, large_tiles, status, staged ? &stg : nullptr, stream)) != cudaSuccess)
+                          passes, large, large_tiles, status, at<int32_t>(sc, S.route_hist), staged ? &stg : nullptr,
+                          stream)) != cudaSuccess)
     return MOE_ERR_CUDA;
 
   GroupedArgs a{};
@@ -430,6 +434,7 @@ static moe_status run_forward(moe_binding b, cudaStream_t stream, cudaEvent_t *e
   a.K = I;
   a.n_rows = H;
   a.out = part;
+  a.out_bf16 = P.tc_on ? 1 : 0;
   if (mark(MOE_STAGE_GEMM2) != cudaSuccess) return MOE_ERR_CUDA;
   err = launch_grouped_mma(L.wfmt, src2, STAGE_DOWN, a, H, E, ntok, stream);
   if (err == cudaSuccess && P.tc_on && P.fp4_on) {
@@ -450,7 +455,7 @@ static moe_status run_forward(moe_binding b, cudaStream_t stream, cudaEvent_t *e
   }
   if (err != cudaSuccess) return MOE_ERR_CUDA;
   if (mark(MOE_STAGE_COMBINE) != cudaSuccess) return MOE_ERR_CUDA;
-  if ((err = launch_combine(part, H, pair_pos, T, K, b->out, stream)) != cudaSuccess) return MOE_ERR_CUDA;
+  if ((err = launch_combine(part, P.tc_on, H, pair_pos, T, K, b->out, stream)) != cudaSuccess) return MOE_ERR_CUDA;
   if (mark(MOE_NUM_STAGES) != cudaSuccess) return MOE_ERR_CUDA;
   return MOE_OK;
 }

@@ -297,6 +297,17 @@ MOE_API void moe_destroy_weight_plan(moe_weight_plan p);
 MOE_API void moe_destroy_plan(moe_plan_t p);
 MOE_API void moe_destroy_binding(moe_binding b);
 
+/* ------------------------------------------------------- measurement ---- */
+
+/* Issue rate of back-to-back tensor-core MMAs on this device, in TFLOP/s: one
+ * CTA per SM issuing `iters` x 4 tcgen05.mma (M=128, N = n in {128, 256}) from
+ * fixed shared-memory operands.  kind: MOE_PEAK_F16 (kind::f16, K=16) or
+ * MOE_PEAK_FP4 (kind::mxf4nvf4 block_scale scale_vec::4X, K=64).  The roofline
+ * denominator of the prefill kernels (no counterpart on the pages).  Allocates
+ * 16 bytes of device memory and two events, synchronises the device. */
+enum { MOE_PEAK_F16 = 0, MOE_PEAK_FP4 = 1 };
+MOE_API moe_status moe_measure_mma_peak(int32_t kind, int32_t n, int32_t iters, float *tflops);
+
 #ifdef __cplusplus
 }
 #endif

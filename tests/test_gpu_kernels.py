@@ -77,7 +77,8 @@ def test_quantiser_bit_exact(lib, mode, src_dtype):
 # ------------------------------------------------------------------ routing
 
 @pytest.mark.parametrize("T,K,E", [(1, 8, 128), (16, 2, 8), (64, 8, 128), (128, 8, 256), (341, 3, 512),
-                                   (129, 8, 64), (8192, 8, 256), (3000, 4, 512), (1, 1, 1)])
+                                   (129, 8, 64), (8192, 8, 256), (3000, 4, 512), (1, 1, 1), (1025, 1, 1),
+                                   (600, 4, 3)])
 def test_routing_bit_exact(lib, T, K, E):
     from oracle import routing
     abi, layer = lib
