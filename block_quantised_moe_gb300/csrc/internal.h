@@ -10,6 +10,9 @@
 namespace bqmoe {
 
 constexpr size_t kAlign = 256;
+// Work counters per grouped launch of the register-dequant kernel (one per CTA
+// group; zeroed by the routing kernel at the start of every forward).
+constexpr int kWorkSlots = 512;
 inline size_t align_up(size_t v, size_t a = kAlign) { return (v + a - 1) / a * a; }
 
 // Packed expert buffer written by the packer, segments on 256-byte boundaries:
@@ -44,6 +47,7 @@ struct ScratchLayout {
   int64_t cap_sorted = 0;  // rows of the padded, expert-sorted pair list
   size_t status = 0, counts = 0, offsets = 0, sorted = 0, pair_pos = 0, active = 0, passes = 0, large = 0, large_tiles = 0;
   size_t route_hist = 0;  // per-chunk expert counts of the chunked routing sort
+  size_t work = 0;        // 2 x kWorkSlots work counters of the register-dequant kernel (GEMM1, GEMM2)
   size_t xq_codes = 0, xq_scales = 0, xq_g = 0;
   size_t h = 0, hq_codes = 0, hq_scales = 0, hq_g = 0;
   size_t x16 = 0, xfac = 0, hamax = 0;  // tensor-core path: FP16 x, its factors, per-pair max |h|
@@ -81,6 +85,7 @@ struct GroupedArgs {
   const int32_t *large_tiles;  // [i] = 128-token tiles of large experts before i (prefix)
   int act_by_token;            // tcgen05 kernel: B rows indexed by token (GEMM1) or by slot (GEMM2)
   int32_t *status;        // device status word (timeout flag)
+  int32_t *work;          // register-dequant kernel: kWorkSlots zeroed item counters
   int top_k;
   const float *topk_weights;
   // output: h [cap][I] (GEMM1) or partials [cap][H] (GEMM2)
@@ -112,7 +117,7 @@ int route_chunks(int P);
 cudaError_t launch_route(const int32_t *ids, int P, int E, int pad, int ntok, int large_min, int large_tile,
                          int32_t *counts, int32_t *offsets, int32_t *sorted_pair, int32_t *pair_pos, int32_t *active,
                          int32_t *passes, int32_t *large, int32_t *large_tiles, int32_t *status, int32_t *chunk_hist,
-                         const RouteStaging *stg, cudaStream_t s);
+                         int32_t *work, int work_n, const RouteStaging *stg, cudaStream_t s);
 
 // Register-dequant tensor-core grouped kernel (experts with few pairs), NVFP4 or
 // MXFP4 weights (wfmt); rows_total = rows of the stage's weight matrix (2I gated,

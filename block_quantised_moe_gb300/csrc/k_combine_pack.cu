@@ -232,8 +232,9 @@ __global__ void k_pack_mma_scales(const uint8_t *__restrict__ src, uint8_t *__re
 // layout (16-byte chunk c of row r at (r/8)*1024 + (r%8)*128 + ((c ^ r) % 8)*16),
 // then 2048 bytes of E4M3 block scales as 32-bit words (four 16-element blocks
 // of one row and one 64-K step, first block in the low byte) ordered
-// [lane i][step t][column c] for row i + 32c: the order in which the tensor-
-// memory scale layout (32 lanes x 4 columns per 128 rows) is written.  Rows follow
+// [step t][lane i][column c] for row i + 32c: per 64-K step one 512-byte block
+// in the tensor-memory scale layout (32 lanes x 4 columns per 128 rows), which
+// the MMA copies into TMEM as it is.  Rows follow
 // the same 8 gate + 8 up interleave per 16-row tile as the fragment layout.
 constexpr int64_t kFp4Tile = 16384 + 2048;
 
@@ -261,7 +262,7 @@ __global__ void k_pack_fp4_scales(const uint8_t *__restrict__ src, uint8_t *__re
   const int64_t n = (int64_t)E * nblk * nkb * 512;  // 32-bit words
   for (int64_t idx = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; idx < n; idx += (int64_t)gridDim.x * blockDim.x) {
     const int w = (int)(idx & 511);
-    const int i = w >> 4, st = (w >> 2) & 3, c = w & 3;
+    const int st = w >> 7, i = (w >> 2) & 31, c = w & 3;
     int64_t t = idx >> 9;
     const int kb = (int)(t % nkb);
     t /= nkb;

@@ -17,12 +17,15 @@
 //   tiles in the same swizzled layout (16 KB of codes + 2 KB of scales per
 //   256-K block): one bulk copy, like A.  Slots past the expert's last pair hold
 //   stale values that only reach accumulator columns that are never read.
-// * Scale factors: the weight tile's scale words ride in the same bulk copy as
-//   its codes, the activation rows' scale bytes in the same copy as theirs;
-//   four warps, one per TMEM lane quadrant, move them from shared memory into
-//   TMEM with tcgen05.st in the layout the MMA reads: 32 lanes x 4 columns per
-//   64-K step, lane i column c holding the four E4M3 scales of row i + 32c, the
-//   same in every quadrant.
+// * Scale factors: both tiles end in their rows' E4M3 scales as four 512-byte
+//   blocks, one per 64-K step, already in the order the MMA reads them from
+//   TMEM (32 lanes x 4 columns, lane i column c = the four scales of row
+//   i + 32c); they ride in the same bulk copies as the codes.  Four warps, one
+//   per TMEM lane quadrant, move them into TMEM with tcgen05.st (the MMA reads
+//   the same words in every quadrant); each lane reads 16 consecutive bytes per
+//   block, so the shared-memory loads are free of bank conflicts.  (Issuing
+//   the moves as tcgen05.cp from the MMA thread puts them in the MMA's own
+//   in-order pipe, between the MMAs, and measured slower.)
 // * Epilogue: D x the weights' FP32 global x the row's FP32 activation global,
 //   then SiLU(g)*u or ReLU^2 (GEMM1) or the topk_weight (GEMM2).
 // Every wait is a bounded mbarrier wait; a timeout sets the status flag, and
@@ -45,7 +48,7 @@ constexpr int kF4MmaWarp = 14;                       // MMA issue
 constexpr int kF4Threads = (kF4MmaWarp + 1) * 32;
 constexpr int kF4N = 128;                            // tokens per tile
 constexpr int kF4TileBytes = 16384;                  // 128 rows x 256 K of E2M1
-constexpr int kF4SfBytes = 2048;                     // their scales (weights: packed tile; activations: gathered)
+constexpr int kF4SfBytes = 2048;                     // their scales: 4 K steps x 512 bytes in TMEM order
 constexpr int kF4StageBytes = kF4TileBytes + kF4SfBytes;  // one operand's ring stage (a multiple of 1024)
 constexpr int kF4Stages = 6;                         // A, B and scale-factor ring depth
 constexpr int kF4RingBytes = 2 * kF4Stages * kF4StageBytes;
@@ -199,9 +202,8 @@ __global__ void __launch_bounds__(kF4Threads, 1) k_grouped_fp4(const GroupedArgs
   } else if (warp >= kF4SfWarp0 && warp < kF4SfWarp0 + 4) {
     // ------------------------------------------------------ scale factors -> TMEM
     // Warp 8 + q writes lane quadrant q; every quadrant gets the same words:
-    // the weight tile's 16 words of this lane (copied with the codes, already in
-    // [step][column] order) and the 16 scale bytes of token rows lane + 32c
-    // (gathered with the activation codes).
+    // per 64-K step t, this lane's 16 bytes of the weight tile's and of the
+    // activation tile's scale blocks.
     const int q = warp - kF4SfWarp0;
     const uint32_t lane_base = (uint32_t)(q * 32) << 16;
     int slot = 0;
@@ -213,24 +215,15 @@ __global__ void __launch_bounds__(kF4Threads, 1) k_grouped_fp4(const GroupedArgs
           ok = false;
           break;
         }
-        const uint4 *sfa = reinterpret_cast<const uint4 *>(base + slot * kF4StageBytes + kF4TileBytes) + lane * 4;
-        const uint8_t *sfb = base + (kF4Stages + slot) * kF4StageBytes + kF4TileBytes;
+        const uint8_t *sfa = base + slot * kF4StageBytes + kF4TileBytes + lane * 16;
+        const uint8_t *sfb = base + (kF4Stages + slot) * kF4StageBytes + kF4TileBytes + lane * 16;
         uint32_t ra[16], rb[16];
 #pragma unroll
-        for (int j = 0; j < 4; ++j) {
-          const uint4 v = sfa[j];
-          ra[4 * j + 0] = v.x;
-          ra[4 * j + 1] = v.y;
-          ra[4 * j + 2] = v.z;
-          ra[4 * j + 3] = v.w;
-        }
-#pragma unroll
-        for (int c = 0; c < 4; ++c) {
-          const uint4 v = *reinterpret_cast<const uint4 *>(sfb + (lane + 32 * c) * 16);
-          rb[0 * 4 + c] = v.x;
-          rb[1 * 4 + c] = v.y;
-          rb[2 * 4 + c] = v.z;
-          rb[3 * 4 + c] = v.w;
+        for (int t = 0; t < 4; ++t) {
+          const uint4 va = *reinterpret_cast<const uint4 *>(sfa + 512 * t);
+          const uint4 vb = *reinterpret_cast<const uint4 *>(sfb + 512 * t);
+          ra[4 * t + 0] = va.x; ra[4 * t + 1] = va.y; ra[4 * t + 2] = va.z; ra[4 * t + 3] = va.w;
+          rb[4 * t + 0] = vb.x; rb[4 * t + 1] = vb.y; rb[4 * t + 2] = vb.z; rb[4 * t + 3] = vb.w;
         }
         tc_fence_after();
         const uint32_t col = tmem + lane_base + (uint32_t)(kF4SfCol0 + slot * kF4SfCols);

@@ -134,6 +134,7 @@ constexpr int kStepBytes = 4608;
 constexpr int kSPS = 4;           // K steps per ring stage
 constexpr int kStageBytes = kStepBytes * kSPS;
 constexpr int kMaxStages = 8;
+constexpr int kQueue = 8;         // item ids handed from the producer to the consumers
 // Two 9-warp CTAs per SM put five warps on some SM sub-partitions, whose
 // register files hold 16K registers each: 5 x 32 x 96 <= 16384.
 constexpr int kMmaMaxRegs = 96;
@@ -182,7 +183,7 @@ struct ItemCursor {
 };
 
 template <int WF, int SRC, int STAGE, int NT>
-__global__ void __maxnreg__(kMmaMaxRegs) k_grouped_mma(const GroupedArgs a, int nst) {
+__global__ void __maxnreg__(kMmaMaxRegs) k_grouped_mma(const GroupedArgs a, int nst, int ngroups) {
   extern __shared__ __align__(1024) uint8_t smem[];
   constexpr int NTOK = 8 * NT;
   const int K = a.K;
@@ -191,11 +192,15 @@ __global__ void __maxnreg__(kMmaMaxRegs) k_grouped_mma(const GroupedArgs a, int 
   __half *xs = reinterpret_cast<__half *>(smem + (size_t)nst * kStageBytes);
   float *fac = reinterpret_cast<float *>(reinterpret_cast<uint8_t *>(xs) + (size_t)NTOK * pitch);
   int64_t *rows = reinterpret_cast<int64_t *>(fac + NTOK);
-  uint64_t *bars = reinterpret_cast<uint64_t *>(rows + NTOK);  // full[nst], empty[nst], consumer barrier
+  float *wts = reinterpret_cast<float *>(rows + NTOK);  // GEMM2: topk weight x down global per staged token
+  // full[nst], empty[nst], consumer barrier, item queue full[kQueue] / empty[kQueue]
+  uint64_t *bars = reinterpret_cast<uint64_t *>(wts + NTOK);
+  volatile int *qitem = reinterpret_cast<volatile int *>(bars + 2 * nst + 1 + 2 * kQueue);
   const uint32_t ring_s = (uint32_t)__cvta_generic_to_shared(ring);
   const uint32_t full0 = (uint32_t)__cvta_generic_to_shared(bars);
   const uint32_t empty0 = full0 + 8u * nst;
   const uint32_t cbar = empty0 + 8u * nst;
+  const uint32_t qfull0 = cbar + 8u, qempty0 = qfull0 + 8u * kQueue;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   pdl_trigger();
@@ -205,6 +210,10 @@ __global__ void __maxnreg__(kMmaMaxRegs) k_grouped_mma(const GroupedArgs a, int 
       mbar_init(empty0 + 8u * i, kConsumers);
     }
     mbar_init(cbar, kConsumers);
+    for (int i = 0; i < kQueue; ++i) {
+      mbar_init(qfull0 + 8u * i, 1);
+      mbar_init(qempty0 + 8u * i, kConsumers);
+    }
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
   __syncthreads();
@@ -213,8 +222,15 @@ __global__ void __maxnreg__(kMmaMaxRegs) k_grouped_mma(const GroupedArgs a, int 
   const int nblk = a.n_blocks;
   const int n_active = a.active[0];
   const int W = n_active > 0 ? a.passes[n_active] * nblk : 0;
-  const int u0 = (int)((int64_t)blockIdx.x * W / gridDim.x);
-  const int u1 = (int)((int64_t)(blockIdx.x + 1) * W / gridDim.x);
+  // CTA group g = blockIdx % ngroups (the CTAs that share an SM when the grid
+  // is ctas-per-SM x SMs) owns the contiguous items [u0, u1) and its CTAs take
+  // them one at a time from the group's counter, so a CTA the warp scheduler
+  // serves less simply takes fewer items; neighbouring items share staged
+  // activations.
+  const int grp = (int)blockIdx.x % ngroups;
+  const int u0 = (int)((int64_t)grp * W / ngroups);
+  const int u1 = (int)((int64_t)(grp + 1) * W / ngroups);
+  int32_t *const ctr = a.work + grp;
   const int stages_per_pass = (nsteps + kSPS - 1) / kSPS;
   ItemCursor cur;
   if (u0 < u1) cur.seek(a, u0, nblk);
@@ -226,27 +242,48 @@ __global__ void __maxnreg__(kMmaMaxRegs) k_grouped_mma(const GroupedArgs a, int 
       uint32_t phase = 0;
       uint32_t issued = 0, issued_parity = 0;  // per-slot: has a copy, parity of its last phase
       bool ok = true;
-      for (int u = u0; u < u1 && ok; ++u) {
+      int q = 0;
+      uint32_t qph = 0;
+      // the CTA's first item is its rank in the group (no atomic on the way to
+      // the first copy); later ones come from the counter, past those
+      const int rank = (int)blockIdx.x / ngroups;
+      const int in_grp = ((int)gridDim.x - 1 - grp) / ngroups + 1;
+      int u = u0 + rank;
+      for (;;) {
+        if (u >= u1) u = -1;
+        // hand the item to the consumers (-1: no more)
+        if (!mbar_wait(qempty0 + 8u * q, qph ^ 1u)) {
+          ok = false;
+          break;
+        }
+        qitem[q] = u;
+        mbar_arrive(qfull0 + 8u * q);
+        if (++q == kQueue) {
+          q = 0;
+          qph ^= 1u;
+        }
+        if (u < 0) break;
+        const int un = u0 + in_grp + atomicAdd(ctr, 1);  // the next item, fetched while this one streams
         const Item w = cur.at(a, u, nblk);
         const uint8_t *base = a.codes + (size_t)w.e * a.codes_expert + (size_t)w.blk * nsteps * step_bytes<WF>();
-        {
-          for (int st = 0; st < stages_per_pass; ++st) {
-            if (!mbar_wait(empty0 + 8u * slot, phase ^ 1u)) {
-              ok = false;
-              break;
-            }
-            const uint32_t bytes = (uint32_t)min(kSPS, nsteps - st * kSPS) * step_bytes<WF>();
-            mbar_expect_tx(full0 + 8u * slot, bytes);
-            bulk_g2s(ring_s + (uint32_t)slot * kStageBytes, base + (size_t)st * kSPS * step_bytes<WF>(), bytes,
-                     full0 + 8u * slot);
-            issued |= 1u << slot;
-            issued_parity = (issued_parity & ~(1u << slot)) | (phase << slot);
-            if (++slot == nst) {
-              slot = 0;
-              phase ^= 1u;
-            }
+        for (int st = 0; st < stages_per_pass; ++st) {
+          if (!mbar_wait(empty0 + 8u * slot, phase ^ 1u)) {
+            ok = false;
+            break;
+          }
+          const uint32_t bytes = (uint32_t)min(kSPS, nsteps - st * kSPS) * step_bytes<WF>();
+          mbar_expect_tx(full0 + 8u * slot, bytes);
+          bulk_g2s(ring_s + (uint32_t)slot * kStageBytes, base + (size_t)st * kSPS * step_bytes<WF>(), bytes,
+                   full0 + 8u * slot);
+          issued |= 1u << slot;
+          issued_parity = (issued_parity & ~(1u << slot)) | (phase << slot);
+          if (++slot == nst) {
+            slot = 0;
+            phase ^= 1u;
           }
         }
+        if (!ok) break;
+        u = un;
       }
       if (!ok) atomicOr(&a.status[ST_FLAGS], ST_FLAG_TIMEOUT);
       // Never leave with a copy in flight into this CTA's shared memory.
@@ -272,10 +309,25 @@ __global__ void __maxnreg__(kMmaMaxRegs) k_grouped_mma(const GroupedArgs a, int 
   bool ok = true;
   pdl_wait();  // activations / h come from the preceding kernels
 
-  for (int u = u0; u < u1 && ok; ++u) {
+  int q = 0;
+  uint32_t qph = 0;
+  while (ok) {
+    if (!mbar_wait(qfull0 + 8u * q, qph)) {
+      ok = false;
+      break;
+    }
+    const int u = qitem[q];
+    __syncwarp();
+    if (lane == 0) mbar_arrive(qempty0 + 8u * q);
+    if (++q == kQueue) {
+      q = 0;
+      qph ^= 1u;
+    }
+    if (u < 0) break;
     const Item w = cur.at(a, u, nblk);
     const int tile = w.blk * kConsumers + warp;  // 16-row tile of this warp
-    const float *gl = a.globals + 4 * w.e;
+    // the expert's globals, loaded while the item's K loop runs
+    const float gl0 = a.globals[4 * w.e], gl1 = a.globals[4 * w.e + 1];
     {
       const int pass = w.pass;
       const int s0 = w.off + pass * NTOK;
@@ -288,11 +340,15 @@ __global__ void __maxnreg__(kMmaMaxRegs) k_grouped_mma(const GroupedArgs a, int 
         }
         if (threadIdx.x < NTOK) {
           int64_t rid = -1;
+          float wt = 0.f;
           if ((int)threadIdx.x < ntok) {
             const int s = s0 + threadIdx.x;
-            rid = by_token ? (int64_t)(a.sorted_pair[s] / a.top_k) : (int64_t)s;
+            const int p = a.sorted_pair[s];
+            rid = by_token ? (int64_t)(p / a.top_k) : (int64_t)s;
+            if (STAGE == STAGE_DOWN) wt = a.topk_weights[p] * a.globals[4 * w.e + 2];
           }
           rows[threadIdx.x] = rid;
+          wts[threadIdx.x] = wt;  // the epilogue reads it from shared memory
         }
         if (!consumer_sync(cbar, cphase)) {
           ok = false;
@@ -465,18 +521,18 @@ __global__ void __maxnreg__(kMmaMaxRegs) k_grouped_mma(const GroupedArgs a, int 
           const float lo = acc[j][c] * f, hi = acc[j][2 + c] * f;
           float hmax = 0.f;
           if (STAGE == STAGE_GATED) {
-            const float h = silu_f32(lo * gl[0]) * (hi * gl[1]);
+            const float h = silu_f32(lo * gl0) * (hi * gl1);
             if (live) a.out[(size_t)s * a.n_rows + tile * 8 + r] = h;
             hmax = fabsf(h);
           } else if (STAGE == STAGE_RELU2) {
-            const float v0 = fmaxf(lo * gl[0], 0.f), v1 = fmaxf(hi * gl[0], 0.f);
+            const float v0 = fmaxf(lo * gl0, 0.f), v1 = fmaxf(hi * gl0, 0.f);
             if (live) {
               a.out[(size_t)s * a.n_rows + tile * 16 + r] = v0 * v0;
               a.out[(size_t)s * a.n_rows + tile * 16 + r + 8] = v1 * v1;
             }
             hmax = fmaxf(v0 * v0, v1 * v1);
           } else if (live) {
-            const float wt = a.topk_weights[a.sorted_pair[s]] * gl[2];
+            const float wt = wts[n];
             store_partial(a, (size_t)s * a.n_rows + tile * 16 + r, wt * lo);
             store_partial(a, (size_t)s * a.n_rows + tile * 16 + r + 8, wt * hi);
           }
@@ -496,7 +552,8 @@ __global__ void __maxnreg__(kMmaMaxRegs) k_grouped_mma(const GroupedArgs a, int 
 }
 
 static size_t tma_smem_bytes(int K, int NT, int nst) {
-  return (size_t)nst * kStageBytes + (size_t)8 * NT * (2 * K + 16) + 8 * NT * (4 + 8) + 16 * (size_t)nst + 8;
+  return (size_t)nst * kStageBytes + (size_t)8 * NT * (2 * K + 16) + 8 * NT * (4 + 8 + 4) + 16 * (size_t)nst + 8 +
+         (16 + 4) * kQueue;
 }
 
 static int num_sms() {
@@ -532,7 +589,10 @@ static cudaError_t launch_mma_one(const GroupedArgs &a, int rows_total, int E, c
   g.n_blocks = rows_total / (16 * kConsumers);
   const int units_max = E * g.n_blocks;
   const int grid = std::max(1, std::min(sms * ctas_per_sm, units_max));
-  return launch_pdl(k_grouped_mma<WF, SRC, STAGE, NT>, dim3(grid), dim3(kTmaThreads), smem, s, g, nst);
+  // groups of ctas_per_sm CTAs share an item range (blockIdx b, b + ngroups, ...)
+  const int ngroups = (grid + ctas_per_sm - 1) / ctas_per_sm;
+  if (a.work == nullptr || ngroups > kWorkSlots) return cudaErrorInvalidValue;
+  return launch_pdl(k_grouped_mma<WF, SRC, STAGE, NT>, dim3(grid), dim3(kTmaThreads), smem, s, g, nst, ngroups);
 }
 
 template <int WF, int STAGE, int NT>

@@ -110,7 +110,9 @@ __device__ __forceinline__ float block_max(float v, float *red) {
 
 // Position of 16-element block b of a row in a slot-major FP4 tile buffer
 // (128 slots x 256 K per 18432-byte tile: codes in the 128-byte-swizzled K-major
-// layout, then 16 scale bytes per slot row).
+// layout, then the slots' scales as four 512-byte blocks, one per 64-K step, in
+// the tensor-memory scale layout: lane slot % 32, column slot / 32 % 4, the four
+// blocks of the step in the column's four bytes).
 __device__ __forceinline__ uint8_t *fp4_tile_codes(uint8_t *tiles, int64_t slot, int64_t b, int nkb) {
   const int64_t kb = b >> 4, r = slot & 127;
   uint8_t *tile = tiles + ((slot >> 7) * nkb + kb) * 18432;
@@ -118,7 +120,9 @@ __device__ __forceinline__ uint8_t *fp4_tile_codes(uint8_t *tiles, int64_t slot,
   return tile + (r >> 3) * 1024 + (r & 7) * 128 + (((c ^ (int)r) & 7) << 4) + 8 * (b & 1);
 }
 __device__ __forceinline__ uint8_t *fp4_tile_scale(uint8_t *tiles, int64_t slot, int64_t b, int nkb) {
-  return tiles + ((slot >> 7) * nkb + (b >> 4)) * 18432 + 16384 + (slot & 127) * 16 + (b & 15);
+  // 64-K step (b & 15) >> 2, TMEM lane slot & 31, column (slot & 127) >> 5, byte b & 3
+  const int r = (int)(slot & 127), j = (int)(b & 15);
+  return tiles + ((slot >> 7) * nkb + (b >> 4)) * 18432 + 16384 + (j >> 2) * 512 + (r & 31) * 16 + (r >> 5) * 4 + (j & 3);
 }
 
 // NVFP4 with one global per row: one CTA per row.  With `tiles` the row's codes
@@ -160,11 +164,17 @@ k_quant_rows_nvfp4(const void *__restrict__ src, int64_t cols, uint8_t *__restri
     scales[row * (cols / 16) + b] = (uint8_t)s;
     if (tiles != nullptr) {
       const int nkb = (int)(cols / 256);
+      // Lanes 4i..4i+3 hold the four blocks of one 64-K step (cols / 16 is a
+      // multiple of 16, so the group is all active): one 32-bit scale store.
+      const unsigned grp = 0xFu << (threadIdx.x & 28);
+      const uint32_t s1 = __shfl_down_sync(grp, s, 1, 4), s2 = __shfl_down_sync(grp, s, 2, 4),
+                     s3 = __shfl_down_sync(grp, s, 3, 4);
+      const uint32_t s4 = (s & 0xFFu) | (s1 & 0xFFu) << 8 | (s2 & 0xFFu) << 16 | (s3 & 0xFFu) << 24;
       for (int k = 0; k < (top_k > 0 ? top_k : 1); ++k) {
         const int64_t slot = top_k > 0 ? (int64_t)tile_slots[row * top_k + k] : row;
         if (slot < 0) continue;
         *reinterpret_cast<uint2 *>(fp4_tile_codes(tiles, slot, b, nkb)) = c;
-        *fp4_tile_scale(tiles, slot, b, nkb) = (uint8_t)s;
+        if ((b & 3) == 0) *reinterpret_cast<uint32_t *>(fp4_tile_scale(tiles, slot, b, nkb)) = s4;
       }
     }
   }

@@ -159,6 +159,8 @@ __device__ __forceinline__ void write_status(int32_t *status, int dropped) {
 
 struct RouteOut {
   int32_t *counts, *offsets, *sorted_pair, *pair_pos, *active, *passes, *large, *large_tiles, *status;
+  int32_t *work;  // work_n counters of the grouped kernels, zeroed here
+  int work_n;
 };
 
 // Both routing launches go out with programmatic dependent launch so that their
@@ -201,6 +203,7 @@ k_route_one(const int32_t *__restrict__ ids, int P, int E, int pad, int ntok, in
     o.pair_pos[tid] = -1;
   }
   if (tid == 0) write_status(o.status, dropped);
+  for (int i = tid; i < o.work_n; i += kRouteThreads) o.work[i] = 0;
 }
 
 // P > kRouteThreads, first launch: CTA c < nchunk ranks chunk c, writing
@@ -280,6 +283,7 @@ k_route_scatter(const int32_t *__restrict__ ids, int P, int E, int pad, int ntok
     for (int e = tid; e <= E; e += kRouteThreads) o.offsets[e] = base[e];
     for (int e = tid; e < E; e += kRouteThreads) o.counts[e] = tot[e];
     if (tid == 0) write_status(o.status, tot[E]);
+    for (int i = tid; i < o.work_n; i += kRouteThreads) o.work[i] = 0;
   }
   for (int e = c + nchunk * warp; e < E; e += nchunk * kRouteWarps)
     for (int j = base[e] + tot[e] + lane; j < base[e + 1]; j += 32) o.sorted_pair[j] = -1;
@@ -299,9 +303,9 @@ int route_chunks(int P) { return P <= kRouteThreads ? 0 : (P + kRouteThreads - 1
 cudaError_t launch_route(const int32_t *ids, int P, int E, int pad, int ntok, int large_min, int large_tile,
                          int32_t *counts, int32_t *offsets, int32_t *sorted_pair, int32_t *pair_pos, int32_t *active,
                          int32_t *passes, int32_t *large, int32_t *large_tiles, int32_t *status, int32_t *chunk_hist,
-                         const RouteStaging *stg, cudaStream_t s) {
+                         int32_t *work, int work_n, const RouteStaging *stg, cudaStream_t s) {
   if (E > kMaxExperts || E < 1) return cudaErrorInvalidValue;
-  const RouteOut o{counts, offsets, sorted_pair, pair_pos, active, passes, large, large_tiles, status};
+  const RouteOut o{counts, offsets, sorted_pair, pair_pos, active, passes, large, large_tiles, status, work, work_n};
   const RouteStaging st = stg ? *stg : RouteStaging{nullptr, 0, 0, nullptr, nullptr, nullptr, 0};
   const int T = stg ? stg->T : 0;
   const int nchunk = route_chunks(P);

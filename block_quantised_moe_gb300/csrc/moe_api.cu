@@ -187,6 +187,7 @@ moe_status moe_plan(const moe_caps *c, moe_plan_t *out, size_t *scratch_bytes, i
   S.large = take(4 * (size_t)(L.E + 1));
   S.large_tiles = take(4 * (size_t)(L.E + 1));
   S.route_hist = take(4 * (size_t)route_chunks((int)Pmax) * (L.E + 1));
+  S.work = take(4 * 2 * (size_t)kWorkSlots);
   if (P.afmt == MOE_A_NVFP4) {
     S.xq_codes = take((size_t)T * L.H / 2);
     S.xq_scales = take((size_t)T * L.H / 16);
@@ -309,7 +310,8 @@ static moe_status run_forward(moe_binding b, cudaStream_t stream, cudaEvent_t *e
                    at<float>(sc, S.hamax), S.cap_sorted};
   const bool staged = P.afmt == MOE_A_BF16;
   if ((err = launch_route(b->ids, T * K, E, P.pad, ntok, P.large_min, 128, counts, offsets, sorted, pair_pos, active,
-                          passes, large, large_tiles, status, at<int32_t>(sc, S.route_hist), staged ? &stg : nullptr,
+                          passes, large, large_tiles, status, at<int32_t>(sc, S.route_hist), at<int32_t>(sc, S.work),
+                          2 * kWorkSlots, staged ? &stg : nullptr,
                           stream)) != cudaSuccess)
     return MOE_ERR_CUDA;
 
@@ -376,6 +378,7 @@ static moe_status run_forward(moe_binding b, cudaStream_t stream, cudaEvent_t *e
                            nullptr, at<__half>(sc, S.xb16), nullptr, true, stream);
     if (err != cudaSuccess) return MOE_ERR_CUDA;
   }
+  a.work = at<int32_t>(sc, S.work);
   err = launch_grouped_mma(L.wfmt, SRC_X16, stage1, a, L.n13, E, ntok, stream);
   if (err == cudaSuccess && P.tc_on) {
     GroupedArgs t = a;
@@ -436,6 +439,7 @@ static moe_status run_forward(moe_binding b, cudaStream_t stream, cudaEvent_t *e
   a.out = part;
   a.out_bf16 = P.tc_on ? 1 : 0;
   if (mark(MOE_STAGE_GEMM2) != cudaSuccess) return MOE_ERR_CUDA;
+  a.work = at<int32_t>(sc, S.work) + kWorkSlots;
   err = launch_grouped_mma(L.wfmt, src2, STAGE_DOWN, a, H, E, ntok, stream);
   if (err == cudaSuccess && P.tc_on && P.fp4_on) {
     GroupedArgs t = a;  // h^ as slot-major FP4 tiles; per-slot globals
