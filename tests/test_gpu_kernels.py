@@ -165,6 +165,28 @@ def test_dropped_ids_are_reported_and_skipped(lib, decode_layer):
     tl.check_close(out.float().cpu().numpy(), y_ref, "dropped ids")
 
 
+def test_fully_dropped_token_and_duplicate_ids(lib, decode_layer):
+    # A token whose every id is out of range gets an exact zero row (the output
+    # starts as NaN), and a token routed twice to one expert counts both pairs.
+    abi, layer = lib
+    cfg, ck, packed = decode_layer
+    K = cfg["K"]
+    x, ids, w = tl.make_inputs(cfg, 16)
+    ids2 = ids.clone()
+    ids2[2, :] = -1
+    ids2[9, 1] = ids2[9, 0]
+    plan = layer.Plan(packed, K, 16, "bf16")
+    out = torch.full((16, cfg["H"]), float("nan"), dtype=torch.bfloat16, device="cuda")
+    b = plan.bind(x, ids2, w, out)
+    b.run()
+    torch.cuda.synchronize()
+    rc, st = b.device_status()
+    assert rc == abi.MOE_OK and st[1] == K
+    assert torch.equal(out[2], torch.zeros_like(out[2]))
+    y_ref = tl.oracle_forward(ck, cfg["H"], cfg["I"], x, ids2, w, "bf16")
+    tl.check_close(out.float().cpu().numpy(), y_ref, "dropped token, duplicate ids")
+
+
 def test_zero_weights_and_zero_tokens(lib, decode_layer):
     _, layer = lib
     cfg, ck, packed = decode_layer
