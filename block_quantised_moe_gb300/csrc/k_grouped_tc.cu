@@ -46,6 +46,7 @@ constexpr int kTcAStageBytes = kTcMB * kTcABytes;
 constexpr int kTcAStages = 3;                // dequantised A tiles
 constexpr int kTcBStages = 6;                // gathered activation tiles
 constexpr int kTcBLag = 4;                   // cp.async stages a B thread keeps in flight
+constexpr int kTcAPrefetch = 3;              // k-blocks of packed A bytes an A thread keeps in flight
 constexpr int kTcRingBytes = kTcAStages * kTcAStageBytes + kTcBStages * kTcBBytes;
 constexpr int kTcAccCols = kTcMB * kTcN;     // TMEM columns per accumulator buffer
 constexpr int kTcTmemCols = 2 * kTcAccCols;  // double buffered
@@ -126,10 +127,10 @@ __global__ void __launch_bounds__(kTcThreads, 1) k_grouped_tc(const GroupedArgs 
     const int t = threadIdx.x - kTcEpiWarps * 32;  // 0..kTcAWarps*32-1
     int slot = 0;
     uint32_t phase = 0;
-    // Software pipeline: the chunks of the next k-block (possibly of the next
-    // item) are loaded while the current one is dequantised.
-    uint4 cch[kTcAChunks], nch[kTcAChunks];
-    uint2 sch[kTcAChunks], nsc[kTcAChunks];
+    // Software pipeline: the chunks of the next kTcAPrefetch k-blocks (possibly
+    // of the next items) are in flight while the current one is dequantised.
+    uint4 cch[kTcAChunks], pch[kTcAPrefetch][kTcAChunks];
+    uint2 sch[kTcAChunks], psc[kTcAPrefetch][kTcAChunks];
     auto load = [&](const TcItem &it, int kb, uint4 (&c4)[kTcAChunks], uint2 (&s4)[kTcAChunks]) {
       const uint8_t *ebase = a.codes + (size_t)it.e * a.codes_expert;
 #pragma unroll
@@ -142,26 +143,40 @@ __global__ void __launch_bounds__(kTcThreads, 1) k_grouped_tc(const GroupedArgs 
         else s4[i] = make_uint2(__ldg(reinterpret_cast<const uint32_t *>(step + 4096 + tile * 32 + (ln >> 2) * 4)), 0u);
       }
     };
-    TcCursor pcur = cur;  // cursor for the prefetch (runs one k-block ahead)
+    TcCursor pcur = cur;  // cursor of the prefetch (kTcAPrefetch k-blocks ahead)
     int pw = w0, pkb = 0;
+    bool pv = pw < W;
     TcItem pit;
-    if (pw < W) {
-      pit = pcur.at(a, pw, nbp);
-      load(pit, 0, nch, nsc);
+    if (pv) pit = pcur.at(a, pw, nbp);
+    auto advance = [&]() {
+      if (++pkb == nk) {
+        pkb = 0;
+        pw += wstep;
+        pv = pw < W;
+        if (pv) pit = pcur.at(a, pw, nbp);
+      }
+    };
+#pragma unroll
+    for (int d = 0; d < kTcAPrefetch; ++d) {
+      if (pv) load(pit, pkb, pch[d], psc[d]);
+      advance();
     }
     for (int w = w0; w < W && ok; w += wstep) {
       for (int kb = 0; kb < nk; ++kb) {
 #pragma unroll
         for (int i = 0; i < kTcAChunks; ++i) {
-          cch[i] = nch[i];
-          sch[i] = nsc[i];
+          cch[i] = pch[0][i];
+          sch[i] = psc[0][i];
         }
-        if (++pkb == nk) {
-          pkb = 0;
-          pw += wstep;
-          if (pw < W) pit = pcur.at(a, pw, nbp);
-        }
-        if (pw < W) load(pit, pkb, nch, nsc);
+#pragma unroll
+        for (int d = 0; d + 1 < kTcAPrefetch; ++d)
+#pragma unroll
+          for (int i = 0; i < kTcAChunks; ++i) {
+            pch[d][i] = pch[d + 1][i];
+            psc[d][i] = psc[d + 1][i];
+          }
+        if (pv) load(pit, pkb, pch[kTcAPrefetch - 1], psc[kTcAPrefetch - 1]);
+        advance();
         if (!mbar_wait(aempty0 + 8u * slot, phase ^ 1u)) {
           ok = false;
           break;
