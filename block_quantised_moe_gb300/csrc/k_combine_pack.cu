@@ -66,19 +66,39 @@ k_combine(const void *__restrict__ part, int H, const int32_t *__restrict__ pair
     const int tn = t + gridDim.y;
 #pragma unroll
     for (int k = 0; k < kMaxK; ++k) ids[k] = (k < K && tn < T) ? __ldg(pair_pos + (size_t)tn * K + k) : -1;
-    // ordered sum in chunks of 8 partials (the chunk's loads all in flight first)
+    // ordered sum in chunks of 8 partials (the chunk's loads all in flight first;
+    // BF16 partials stay packed until the sum, which halves their registers)
     float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
     for (int i0 = 0; i0 < n; i0 += 8) {
-      float v[8][8];
+      if (BF16) {
+        uint4 raw[8];
 #pragma unroll
-      for (int i = 0; i < 8; ++i)
-        if (i0 + i < n) load_part8<BF16>(part, (size_t)pos[i0 + i] * H + c, v[i]);
+        for (int i = 0; i < 8; ++i)
+          if (i0 + i < n)
+            raw[i] = __ldcs(reinterpret_cast<const uint4 *>(reinterpret_cast<const __nv_bfloat16 *>(part) +
+                                                            (size_t)pos[i0 + i] * H + c));
 #pragma unroll
-      for (int i = 0; i < 8; ++i)
-        if (i0 + i < n) {
+        for (int i = 0; i < 8; ++i)
+          if (i0 + i < n) {
+            const uint32_t w[4] = {raw[i].x, raw[i].y, raw[i].z, raw[i].w};
 #pragma unroll
-          for (int e = 0; e < 8; ++e) acc[e] += v[i][e];
-        }
+            for (int e = 0; e < 4; ++e) {
+              acc[2 * e] += __uint_as_float(w[e] << 16);
+              acc[2 * e + 1] += __uint_as_float(w[e] & 0xFFFF0000u);
+            }
+          }
+      } else {
+        float v[8][8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i)
+          if (i0 + i < n) load_part8<false>(part, (size_t)pos[i0 + i] * H + c, v[i]);
+#pragma unroll
+        for (int i = 0; i < 8; ++i)
+          if (i0 + i < n) {
+#pragma unroll
+            for (int e = 0; e < 8; ++e) acc[e] += v[i][e];
+          }
+      }
     }
     __align__(16) __nv_bfloat162 o[4];
 #pragma unroll

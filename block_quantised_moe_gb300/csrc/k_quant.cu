@@ -125,13 +125,74 @@ __device__ __forceinline__ uint8_t *fp4_tile_scale(uint8_t *tiles, int64_t slot,
   return tiles + ((slot >> 7) * nkb + (b >> 4)) * 18432 + 16384 + (j >> 2) * 512 + (r & 31) * 16 + (r >> 5) * 4 + (j & 3);
 }
 
-// NVFP4 with one global per row: one CTA per row.  With `tiles` the row's codes
+// NVFP4 with one global per row, rows up to 2048 wide: one warp per row over a
+// persistent grid (a CTA per row made the kernel bound by CTA launches at 65k
+// rows of 2048; wide rows keep a CTA each, below).  Pass 1 takes the
+// row's amax, pass 2 (re-reading the row, now in L1/L2) quantises 16-element
+// blocks, block b on lane b % 32, so loads and stores are coalesced.  With
+// `tiles` the row's codes and scales also go to the slot-major FP4 tiles of the
+// block-scaled kernel: a token row (tile_slots = pair_pos, top_k > 0) to each of
+// its valid slots, a slot row (top_k == 0) to its own slot.
+template <bool BF16>
+__global__ void __launch_bounds__(kQThreads)
+k_quant_rows_nvfp4(const void *__restrict__ src, int64_t rows, int64_t cols, uint8_t *__restrict__ codes,
+                   uint8_t *__restrict__ scales, float *__restrict__ g_out, const int32_t *__restrict__ rows_dev,
+                   const int32_t *__restrict__ row_live, uint8_t *__restrict__ tiles,
+                   const int32_t *__restrict__ tile_slots, int top_k) {
+  pdl_trigger();
+  pdl_wait();
+  const int lane = threadIdx.x & 31;
+  const int64_t live_rows = rows_dev != nullptr ? min(rows, (int64_t)*rows_dev) : rows;
+  const int64_t nwarps = (int64_t)gridDim.x * (kQThreads / 32);
+  const int64_t nb = cols / 16;
+  const int nkb = (int)(cols / 256);
+  for (int64_t row = (int64_t)blockIdx.x * (kQThreads / 32) + (threadIdx.x >> 5); row < live_rows; row += nwarps) {
+    if (row_live != nullptr && row_live[row] < 0) continue;  // a padding slot of the expert-sorted list
+    const int64_t base = row * cols;
+    float m = 0.f;
+    for (int64_t j = (int64_t)lane * 8; j < cols; j += 256) {
+      float v[8];
+      load8<BF16>(src, base + j, v);
+#pragma unroll
+      for (int i = 0; i < 8; ++i) m = fmaxf(m, fabsf(v[i]));
+    }
+    const float amax = warp_max(m);
+    const float g = __fdiv_rn(amax, 2688.0f);
+    if (lane == 0) g_out[row] = g;
+    for (int64_t b = lane; b < nb; b += 32) {
+      float x[16];
+      load8<BF16>(src, base + b * 16, *reinterpret_cast<float(*)[8]>(x));
+      load8<BF16>(src, base + b * 16 + 8, *reinterpret_cast<float(*)[8]>(x + 8));
+      uint2 c;
+      uint32_t sc;
+      nvfp4_block(x, g, c, sc);
+      *reinterpret_cast<uint2 *>(codes + (base + b * 16) / 2) = c;
+      scales[row * nb + b] = (uint8_t)sc;
+      if (tiles != nullptr) {
+        // Lanes 4i..4i+3 hold the four blocks of one 64-K step (nb is a multiple
+        // of 16, so the group is all active): one 32-bit scale store.
+        const unsigned grp = 0xFu << (lane & 28);
+        const uint32_t s1 = __shfl_down_sync(grp, sc, 1, 4), s2 = __shfl_down_sync(grp, sc, 2, 4),
+                       s3 = __shfl_down_sync(grp, sc, 3, 4);
+        const uint32_t s4 = (sc & 0xFFu) | (s1 & 0xFFu) << 8 | (s2 & 0xFFu) << 16 | (s3 & 0xFFu) << 24;
+        for (int k = 0; k < (top_k > 0 ? top_k : 1); ++k) {
+          const int64_t slot = top_k > 0 ? (int64_t)tile_slots[row * top_k + k] : row;
+          if (slot < 0) continue;
+          *reinterpret_cast<uint2 *>(fp4_tile_codes(tiles, slot, b, nkb)) = c;
+          if ((b & 3) == 0) *reinterpret_cast<uint32_t *>(fp4_tile_scale(tiles, slot, b, nkb)) = s4;
+        }
+      }
+    }
+  }
+}
+
+// NVFP4 with one global per row, one CTA per row (rows wider than 2048).  With `tiles` the row's codes
 // and scales also go to the slot-major FP4 tiles of the block-scaled kernel:
 // a token row (tile_slots = pair_pos, top_k > 0) to each of its valid slots, a
 // slot row (top_k == 0) to its own slot.
 template <bool BF16>
 __global__ void __launch_bounds__(kQThreads)
-k_quant_rows_nvfp4(const void *__restrict__ src, int64_t cols, uint8_t *__restrict__ codes,
+k_quant_rows_nvfp4_cta(const void *__restrict__ src, int64_t cols, uint8_t *__restrict__ codes,
                    uint8_t *__restrict__ scales, float *__restrict__ g_out, const int32_t *__restrict__ rows_dev,
                    const int32_t *__restrict__ row_live, uint8_t *__restrict__ tiles,
                    const int32_t *__restrict__ tile_slots, int top_k) {
@@ -260,10 +321,20 @@ cudaError_t launch_quant_rows_nvfp4(const void *src, bool src_bf16, int64_t rows
   if (rows <= 0) return cudaSuccess;
   if (rows > 0x7FFFFFFF) return cudaErrorInvalidValue;
   if (tiles != nullptr && cols % 256 != 0) return cudaErrorInvalidValue;
+  if (cols % 16 != 0) return cudaErrorInvalidValue;
+  if (cols > 2048) {  // a CTA per row
+    if (src_bf16)
+      return launch_pdl(k_quant_rows_nvfp4_cta<true>, dim3((unsigned)rows), dim3(kQThreads), 0, s, src, cols, codes,
+                        scales, g, rows_dev, row_live, tiles, tile_slots, top_k);
+    return launch_pdl(k_quant_rows_nvfp4_cta<false>, dim3((unsigned)rows), dim3(kQThreads), 0, s, src, cols, codes,
+                      scales, g, rows_dev, row_live, tiles, tile_slots, top_k);
+  }
+  // a warp per row; at most 8 CTAs of 8 warps per SM-sized share of the rows
+  const int grid = (int)std::max<int64_t>(1, std::min<int64_t>((rows + 7) / 8, 152 * 8));
   if (src_bf16)
-    return launch_pdl(k_quant_rows_nvfp4<true>, dim3((unsigned)rows), dim3(kQThreads), 0, s, src, cols, codes, scales,
-                      g, rows_dev, row_live, tiles, tile_slots, top_k);
-  return launch_pdl(k_quant_rows_nvfp4<false>, dim3((unsigned)rows), dim3(kQThreads), 0, s, src, cols, codes, scales, g,
+    return launch_pdl(k_quant_rows_nvfp4<true>, dim3(grid), dim3(kQThreads), 0, s, src, rows, cols, codes, scales, g,
+                      rows_dev, row_live, tiles, tile_slots, top_k);
+  return launch_pdl(k_quant_rows_nvfp4<false>, dim3(grid), dim3(kQThreads), 0, s, src, rows, cols, codes, scales, g,
                     rows_dev, row_live, tiles, tile_slots, top_k);
 }
 
