@@ -135,6 +135,7 @@ constexpr int kSPS = 4;           // K steps per ring stage
 constexpr int kStageBytes = kStepBytes * kSPS;
 constexpr int kMaxStages = 8;
 constexpr int kQueue = 8;         // item ids handed from the producer to the consumers
+constexpr int kQEntry = 8 + 2 * 16;  // ints per queue entry: unit, item fields, rows[16], weights[16]
 // Two 9-warp CTAs per SM put five warps on some SM sub-partitions, whose
 // register files hold 16K registers each: 5 x 32 x 96 <= 16384.
 constexpr int kMmaMaxRegs = 96;
@@ -195,6 +196,9 @@ __global__ void __maxnreg__(kMmaMaxRegs) k_grouped_mma(const GroupedArgs a, int 
   float *wts = reinterpret_cast<float *>(rows + NTOK);  // GEMM2: topk weight x down global per staged token
   // full[nst], empty[nst], consumer barrier, item queue full[kQueue] / empty[kQueue]
   uint64_t *bars = reinterpret_cast<uint64_t *>(wts + NTOK);
+  // item queue entries: unit id (-1: no more), then the item's expert, pass, row
+  // block, pair count and sorted offset (the producer has them, the consumers
+  // would otherwise re-read the routing arrays at every item)
   volatile int *qitem = reinterpret_cast<volatile int *>(bars + 2 * nst + 1 + 2 * kQueue);
   const uint32_t ring_s = (uint32_t)__cvta_generic_to_shared(ring);
   const uint32_t full0 = (uint32_t)__cvta_generic_to_shared(bars);
@@ -249,14 +253,45 @@ __global__ void __maxnreg__(kMmaMaxRegs) k_grouped_mma(const GroupedArgs a, int 
       const int rank = (int)blockIdx.x / ngroups;
       const int in_grp = ((int)gridDim.x - 1 - grp) / ngroups + 1;
       int u = u0 + rank;
+      int last_e = -1, last_pass = -1;
+      constexpr bool by_token_src = SRC == SRC_X16;
       for (;;) {
         if (u >= u1) u = -1;
+        Item w;
+        if (u >= 0) w = cur.at(a, u, nblk);
         // hand the item to the consumers (-1: no more)
         if (!mbar_wait(qempty0 + 8u * q, qph ^ 1u)) {
           ok = false;
           break;
         }
-        qitem[q] = u;
+        if (u >= 0) {
+          volatile int *qe = qitem + kQEntry * q;
+          qe[1] = w.e;
+          qe[2] = w.pass;
+          qe[3] = w.blk;
+          qe[4] = w.cnt;
+          qe[5] = w.off;
+          if (w.e != last_e || w.pass != last_pass) {
+            // the pass's activation rows (token or slot ids, -1 past the
+            // expert's pairs) and, for the down projection, topk_weight x g_down
+            const int s0 = w.off + w.pass * NTOK;
+            const int ntok = min(NTOK, w.off + w.cnt - s0);
+            int pr[NTOK];
+#pragma unroll
+            for (int n = 0; n < NTOK; ++n) pr[n] = n < ntok ? a.sorted_pair[s0 + n] : -1;
+            const float gd = STAGE == STAGE_DOWN ? a.globals[4 * w.e + 2] : 0.f;
+#pragma unroll
+            for (int n = 0; n < NTOK; ++n) {
+              qe[8 + n] = pr[n] < 0 ? -1 : (by_token_src ? pr[n] / a.top_k : s0 + n);
+              float wt = 0.f;
+              if (STAGE == STAGE_DOWN && pr[n] >= 0) wt = a.topk_weights[pr[n]] * gd;
+              reinterpret_cast<volatile float *>(qe)[8 + NTOK + n] = wt;
+            }
+            last_e = w.e;
+            last_pass = w.pass;
+          }
+        }
+        qitem[kQEntry * q] = u;
         mbar_arrive(qfull0 + 8u * q);
         if (++q == kQueue) {
           q = 0;
@@ -264,7 +299,6 @@ __global__ void __maxnreg__(kMmaMaxRegs) k_grouped_mma(const GroupedArgs a, int 
         }
         if (u < 0) break;
         const int un = u0 + in_grp + atomicAdd(ctr, 1);  // the next item, fetched while this one streams
-        const Item w = cur.at(a, u, nblk);
         const uint8_t *base = a.codes + (size_t)w.e * a.codes_expert + (size_t)w.blk * nsteps * step_bytes<WF>();
         for (int st = 0; st < stages_per_pass; ++st) {
           if (!mbar_wait(empty0 + 8u * slot, phase ^ 1u)) {
@@ -295,7 +329,6 @@ __global__ void __maxnreg__(kMmaMaxRegs) k_grouped_mma(const GroupedArgs a, int 
   }
 
   // ------------------------------------------------------------- consumers
-  constexpr bool by_token = SRC == SRC_X16;
   const uint32_t xs_base = (uint32_t)__cvta_generic_to_shared(xs);
   // ldmatrix row addresses: lanes 0-7 rows 0-7 at k, 8-15 rows 0-7 at k+8,
   // 16-23 rows 8-15 at k, 24-31 rows 8-15 at k+8.
@@ -316,15 +349,24 @@ __global__ void __maxnreg__(kMmaMaxRegs) k_grouped_mma(const GroupedArgs a, int 
       ok = false;
       break;
     }
-    const int u = qitem[q];
-    __syncwarp();
-    if (lane == 0) mbar_arrive(qempty0 + 8u * q);
+    const volatile int *qe = qitem + kQEntry * q;
+    const uint32_t qe_bar = qempty0 + 8u * q;
+    const int u = qe[0];
+    Item w;
+    w.e = qe[1];
+    w.pass = qe[2];
+    w.blk = qe[3];
+    w.cnt = qe[4];
+    w.off = qe[5];
     if (++q == kQueue) {
       q = 0;
       qph ^= 1u;
     }
-    if (u < 0) break;
-    const Item w = cur.at(a, u, nblk);
+    if (u < 0) {
+      __syncwarp();
+      if (lane == 0) mbar_arrive(qe_bar);
+      break;
+    }
     const int tile = w.blk * kConsumers + warp;  // 16-row tile of this warp
     // the expert's globals, loaded while the item's K loop runs
     const float gl0 = a.globals[4 * w.e], gl1 = a.globals[4 * w.e + 1];
@@ -338,17 +380,9 @@ __global__ void __maxnreg__(kMmaMaxRegs) k_grouped_mma(const GroupedArgs a, int 
           ok = false;
           break;
         }
-        if (threadIdx.x < NTOK) {
-          int64_t rid = -1;
-          float wt = 0.f;
-          if ((int)threadIdx.x < ntok) {
-            const int s = s0 + threadIdx.x;
-            const int p = a.sorted_pair[s];
-            rid = by_token ? (int64_t)(p / a.top_k) : (int64_t)s;
-            if (STAGE == STAGE_DOWN) wt = a.topk_weights[p] * a.globals[4 * w.e + 2];
-          }
-          rows[threadIdx.x] = rid;
-          wts[threadIdx.x] = wt;  // the epilogue reads it from shared memory
+        if (threadIdx.x < NTOK) {  // the rows and weights the producer looked up
+          rows[threadIdx.x] = qe[8 + threadIdx.x];
+          wts[threadIdx.x] = reinterpret_cast<const volatile float *>(qe)[8 + NTOK + threadIdx.x];
         }
         if (!consumer_sync(cbar, cphase)) {
           ok = false;
@@ -396,6 +430,8 @@ __global__ void __maxnreg__(kMmaMaxRegs) k_grouped_mma(const GroupedArgs a, int 
         staged_e = w.e;
         staged_pass = pass;
       }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(qe_bar);  // done with this queue entry
 
       // Two accumulator sets (even / odd k16 sub-steps) halve the dependent mma chain.
       float acc[NT][4], acc2[NT][4];
@@ -553,7 +589,7 @@ __global__ void __maxnreg__(kMmaMaxRegs) k_grouped_mma(const GroupedArgs a, int 
 
 static size_t tma_smem_bytes(int K, int NT, int nst) {
   return (size_t)nst * kStageBytes + (size_t)8 * NT * (2 * K + 16) + 8 * NT * (4 + 8 + 4) + 16 * (size_t)nst + 8 +
-         (16 + 4) * kQueue;
+         (16 + 4 * kQEntry) * kQueue;
 }
 
 static int num_sms() {
