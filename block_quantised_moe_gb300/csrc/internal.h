@@ -86,6 +86,7 @@ struct GroupedArgs {
   int act_by_token;            // tcgen05 kernel: B rows indexed by token (GEMM1) or by slot (GEMM2)
   int32_t *status;        // device status word (timeout flag)
   int32_t *work;          // register-dequant kernel: kWorkSlots zeroed item counters
+  int tiny;               // register-dequant kernel: at most E/8 pairs (one deep-ring CTA per SM)
   int top_k;
   const float *topk_weights;
   // output: h [cap][I] (GEMM1) or partials [cap][H] (GEMM2)

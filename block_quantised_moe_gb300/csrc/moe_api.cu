@@ -379,6 +379,7 @@ static moe_status run_forward(moe_binding b, cudaStream_t stream, cudaEvent_t *e
     if (err != cudaSuccess) return MOE_ERR_CUDA;
   }
   a.work = at<int32_t>(sc, S.work);
+  a.tiny = (int64_t)P.max_tokens * K * 8 <= E;
   err = launch_grouped_mma(L.wfmt, SRC_X16, stage1, a, L.n13, E, ntok, stream);
   if (err == cudaSuccess && P.tc_on) {
     GroupedArgs t = a;
