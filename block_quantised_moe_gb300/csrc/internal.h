@@ -13,6 +13,8 @@ constexpr size_t kAlign = 256;
 // Work counters per grouped launch of the register-dequant kernel (one per CTA
 // group; zeroed by the routing kernel at the start of every forward).
 constexpr int kWorkSlots = 512;
+// Largest expert count a layer may have (moe_plan_weights rejects more).
+constexpr int kMaxExperts = 512;
 inline size_t align_up(size_t v, size_t a = kAlign) { return (v + a - 1) / a * a; }
 
 // Packed expert buffer written by the packer, segments on 256-byte boundaries:
@@ -87,6 +89,7 @@ struct GroupedArgs {
   int32_t *status;        // device status word (timeout flag)
   int32_t *work;          // register-dequant kernel: kWorkSlots zeroed item counters
   int tiny;               // register-dequant kernel: at most E/8 pairs (one deep-ring CTA per SM)
+  int wait_first;         // register-dequant GEMM1: routing triggered early, wait before triggering
   int top_k;
   const float *topk_weights;
   // output: h [cap][I] (GEMM1) or partials [cap][H] (GEMM2)

@@ -46,12 +46,18 @@ __global__ void __launch_bounds__(kCombThreads)
 k_combine(const void *__restrict__ part, int H, const int32_t *__restrict__ pair_pos, int T, int K,
           __nv_bfloat16 *__restrict__ out) {
   pdl_trigger();
-  pdl_wait();
   const int c = (blockIdx.x * kCombThreads + threadIdx.x) * 8;
-  if (c >= H) return;
-  int ids[kMaxK];  // pair_pos row of the block's next token, fetched one token ahead
+  if (c >= H) {
+    pdl_wait();
+    return;
+  }
+  // pair_pos row of the block's next token, fetched one token ahead; routing
+  // output, complete when this kernel starts, so the first row is in flight
+  // while the partials are still being written
+  int ids[kMaxK];
 #pragma unroll
   for (int k = 0; k < kMaxK; ++k) ids[k] = (k < K && blockIdx.y < T) ? __ldg(pair_pos + (size_t)blockIdx.y * K + k) : -1;
+  pdl_wait();  // the partials come from the preceding kernel
   for (int t = blockIdx.y; t < T; t += gridDim.y) {
     int pos[kMaxK];
     int n = 0;

@@ -160,15 +160,20 @@ struct Item {
 
 struct ItemCursor {
   int i = 0;  // active-expert index of the current item
-  __device__ __forceinline__ void seek(const GroupedArgs &a, int w, int nblk) {
-    // smallest i with passes[i+1] * nblk > w (items only move forward)
-    int lo = 0, hi = a.active[0] - 1;
-    while (lo < hi) {
-      const int mid = (lo + hi) >> 1;
-      if (a.passes[mid + 1] * nblk > w) hi = mid;
-      else lo = mid + 1;
+  // Called by all 32 lanes of a warp.  i = the smallest i < n_active with
+  // passes[i+1] * nblk > w (else n_active - 1): passes is a non-decreasing
+  // prefix, so that is the number of entries at or below w, counted over the
+  // whole list in one round of independent loads (n_active <= kMaxExperts).
+  __device__ __forceinline__ void seek(const GroupedArgs &a, int w, int nblk, int n_active) {
+    const int lane = threadIdx.x & 31;
+    int cnt = 0;
+#pragma unroll
+    for (int j = 0; j < kMaxExperts / 32; ++j) {
+      const int e = lane + 32 * j;
+      if (e < n_active && a.passes[e + 1] * nblk <= w) ++cnt;
     }
-    i = lo;
+    cnt = __reduce_add_sync(0xffffffffu, cnt);
+    i = min(cnt, n_active - 1);
   }
   __device__ __forceinline__ Item at(const GroupedArgs &a, int w, int nblk) {
     while (a.passes[i + 1] * nblk <= w) ++i;
@@ -207,7 +212,15 @@ __global__ void __maxnreg__(kMmaMaxRegs) k_grouped_mma(const GroupedArgs a, int 
   const uint32_t qfull0 = cbar + 8u, qempty0 = qfull0 + 8u * kQueue;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  pdl_trigger();
+  // With BF16 x, routing stages the x rows and triggers its dependents on
+  // entry, and GEMM1 follows it directly: GEMM1 then waits before its first
+  // read of a routing output and triggers only after that wait, so every later
+  // kernel still starts after routing has completed.  Otherwise (GEMM2, or
+  // GEMM1 behind the activation quantisers, whose routing never triggered
+  // early) the kernel triggers on entry and the producer streams weights while
+  // the predecessor finishes.
+  const bool wait_first = SRC == SRC_X16 && a.wait_first;
+  if (!wait_first) pdl_trigger();
   if (threadIdx.x == 0) {
     for (int i = 0; i < nst; ++i) {
       mbar_init(full0 + 8u * i, 1);
@@ -221,6 +234,10 @@ __global__ void __maxnreg__(kMmaMaxRegs) k_grouped_mma(const GroupedArgs a, int 
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
   __syncthreads();
+  if (wait_first) {
+    pdl_wait();
+    pdl_trigger();
+  }
 
   const int nsteps = K / 64;
   const int nblk = a.n_blocks;
@@ -237,7 +254,7 @@ __global__ void __maxnreg__(kMmaMaxRegs) k_grouped_mma(const GroupedArgs a, int 
   int32_t *const ctr = a.work + grp;
   const int stages_per_pass = (nsteps + kSPS - 1) / kSPS;
   ItemCursor cur;
-  if (u0 < u1) cur.seek(a, u0, nblk);
+  if (u0 < u1) cur.seek(a, u0, nblk, n_active);
 
   if (warp == kConsumers) {
     // ------------------------------------------------------------ producer
@@ -419,7 +436,10 @@ __global__ void __maxnreg__(kMmaMaxRegs) k_grouped_mma(const GroupedArgs a, int 
             f = stage_factor(warp_max(m));
           }
           const float inv = SRC == SRC_H_NVFP4 ? 1.f : __frcp_rn(f);
-          stage_row_slots<SRC>(a.act, a.act_scales, rid, K, inv, reinterpret_cast<__half *>(dst), lane, 32);
+          if (WF == W_NVFP4 || NT == 1)  // (MXFP4 with 16-token passes would spill)
+            stage_row_slots_x2<SRC>(a.act, a.act_scales, rid, K, inv, reinterpret_cast<__half *>(dst), lane, 32);
+          else
+            stage_row_slots<SRC>(a.act, a.act_scales, rid, K, inv, reinterpret_cast<__half *>(dst), lane, 32);
           if (lane == 0) fac[j] = f;
         }
         if (SRC == SRC_X16) cp_async_wait_all();

@@ -21,7 +21,6 @@ namespace bqmoe {
 
 constexpr int kRouteThreads = 1024;
 constexpr int kRouteWarps = kRouteThreads / 32;
-constexpr int kMaxExperts = 512;
 
 // Extra CTAs of the first routing launch: BF16 token row `row` -> FP16 slot-order
 // row with a power-of-two factor (the tensor-core kernels' B operand), and a
@@ -163,16 +162,22 @@ struct RouteOut {
   int work_n;
 };
 
-// Both routing launches go out with programmatic dependent launch so that their
-// CTAs are resident before the previous kernel ends; each waits for its
-// predecessor before touching memory and never triggers early (later kernels
-// read its outputs freely).
+// The routing launches go out with programmatic dependent launch so that their
+// CTAs are resident before the previous kernel ends, and each waits for its
+// predecessor before touching memory.  The rank launch triggers its dependent
+// (the scatter, which waits before reading) on entry.  The launch whose
+// successor is GEMM1 (BF16 x, staged here) also triggers on entry, so GEMM1 is
+// resident and set up by the time routing ends; GEMM1 then waits before its
+// first read of a routing output and triggers only after that wait.  Otherwise
+// routing never triggers early: its outputs are complete when the next kernel
+// starts, and every later kernel may read them before waiting.
 
 // P <= kRouteThreads: CTA 0 does the whole sort; CTAs 1..nstage stage x rows.
 __global__ void __launch_bounds__(kRouteThreads)
 k_route_one(const int32_t *__restrict__ ids, int P, int E, int pad, int ntok, int large_min, int large_tile,
             RouteOut o, RouteStaging st) {
   extern __shared__ int32_t sm[];
+  if (st.x != nullptr) pdl_trigger();  // the successor is GEMM1, which waits first
   pdl_wait();
   if (blockIdx.x > 0) {
     stage_x_row(st.x, st.H, st.x16, st.xfac, st.zero, st.zero_n, blockIdx.x - 1, gridDim.x - 1);
@@ -214,6 +219,7 @@ __global__ void __launch_bounds__(kRouteThreads)
 k_route_rank(const int32_t *__restrict__ ids, int P, int E, int nchunk, int32_t *__restrict__ chunk_hist,
              int32_t *__restrict__ pair_pos, RouteStaging st) {
   extern __shared__ int32_t sm[];
+  pdl_trigger();
   pdl_wait();
   if ((int)blockIdx.x >= nchunk) {
     stage_x_row(st.x, st.H, st.x16, st.xfac, st.zero, st.zero_n, blockIdx.x - nchunk, gridDim.x - nchunk);
@@ -242,8 +248,9 @@ k_route_rank(const int32_t *__restrict__ ids, int P, int E, int nchunk, int32_t 
 // slots are filled by all CTAs (expert e by CTA e mod nchunk).
 __global__ void __launch_bounds__(kRouteThreads)
 k_route_scatter(const int32_t *__restrict__ ids, int P, int E, int pad, int ntok, int large_min, int large_tile,
-                int nchunk, const int32_t *__restrict__ chunk_hist, RouteOut o) {
+                int nchunk, const int32_t *__restrict__ chunk_hist, RouteOut o, int early) {
   extern __shared__ int32_t sm[];
+  if (early) pdl_trigger();  // the successor is GEMM1, which waits first
   pdl_wait();
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int c = blockIdx.x;
@@ -333,7 +340,7 @@ cudaError_t launch_route(const int32_t *ids, int P, int E, int pad, int ntok, in
       cudaSuccess)
     return err;
   return launch_pdl(k_route_scatter, dim3(nchunk), dim3(kRouteThreads), smem2, s, ids, P, E, pad, ntok, large_min,
-                    large_tile, nchunk, chunk_hist, o);
+                    large_tile, nchunk, chunk_hist, o, stg != nullptr ? 1 : 0);
 }
 
 }  // namespace bqmoe

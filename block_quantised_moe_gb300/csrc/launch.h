@@ -1,15 +1,20 @@
 // Kernel launch with programmatic dependent launch (PDL).
 //
-// Every kernel of a forward except the routing kernel is launched with
-// programmatic stream serialisation: it may start while its predecessor is
-// still running.  Protocol (all kernels of this library follow it):
-//   * the routing kernel waits for its predecessor before it touches memory and
-//     never triggers early, so its outputs (the expert lists, offsets, sorted
-//     pairs) are complete when any later kernel of the forward starts, and may
-//     be read before waiting;
+// Every kernel of a forward is launched with programmatic stream
+// serialisation: it may start while its predecessor is still running.
+// Protocol (all kernels of this library follow it):
 //   * a kernel calls pdl_trigger() on entry and pdl_wait() before it reads any
-//     other output of an earlier kernel; every thread that did not wait waits
-//     before it exits, so a kernel's completion implies its predecessor's.
+//     output of an earlier kernel; every thread that did not wait waits before
+//     it exits, so a kernel's completion implies its predecessor's;
+//   * routing triggers early only where its successor waits before reading:
+//     the rank launch (followed by the scatter), and, with BF16 x, the launch
+//     followed by the register-dequant GEMM1, which then waits before it
+//     triggers (so it has passed its wait, and routing has completed, before
+//     any later kernel starts);
+//   * routing outputs (the expert lists, offsets, sorted pairs, pair_pos) are
+//     therefore complete when any kernel after GEMM1 starts, and when any
+//     kernel after a routing launch that did not trigger early starts; those
+//     kernels may read them before waiting.
 #pragma once
 
 #include <cuda_runtime.h>

@@ -49,7 +49,6 @@ int &launch_counter() {
 
 namespace {
 
-constexpr int kMaxExperts = 512;
 constexpr int kMaxTopK = 16;
 constexpr int kPad = 16;        // expert groups are padded to this many pairs
 constexpr int kFp4Tile = 128;   // ... and to this many with the block-scaled FP4 kernel
@@ -380,6 +379,7 @@ static moe_status run_forward(moe_binding b, cudaStream_t stream, cudaEvent_t *e
   }
   a.work = at<int32_t>(sc, S.work);
   a.tiny = (int64_t)P.max_tokens * K * 8 <= E;
+  a.wait_first = staged ? 1 : 0;  // routing (which staged x) triggered GEMM1 early
   err = launch_grouped_mma(L.wfmt, SRC_X16, stage1, a, L.n13, E, ntok, stream);
   if (err == cudaSuccess && P.tc_on) {
     GroupedArgs t = a;
@@ -401,6 +401,7 @@ static moe_status run_forward(moe_binding b, cudaStream_t stream, cudaEvent_t *e
     }
   }
   a.out_amax = nullptr;
+  a.wait_first = 0;
   if (err != cudaSuccess) return MOE_ERR_CUDA;
 
   // re-quantise h for NVFP4 / MXFP8 activations (rows past offsets[E] are skipped)
