@@ -66,6 +66,7 @@ __device__ void rank_chunk(const int32_t *__restrict__ ids, int p0, int P, int E
   const unsigned drops = __ballot_sync(0xffffffffu, p < P && !valid);
   if (lane == 0 && drops) atomicAdd(dropped, __popc(drops));
   __syncthreads();
+#pragma unroll 4
   for (int e = warp; e < E; e += kRouteWarps) {  // exclusive prefix over the warps, per expert
     const int v = warp_hist[e * kRouteWarps + lane];
     int incl = v;
@@ -87,64 +88,66 @@ __device__ void rank_chunk(const int32_t *__restrict__ ids, int p0, int P, int E
 // experts (1..large_min-1 pairs) with the prefix of their passes of ntok tokens,
 // and "large" experts (>= large_min pairs) with the prefix of their tiles of
 // large_tile tokens.  The grouped kernels split (expert, pass | tile, row
-// block) items evenly.
+// block) items evenly.  Lane l owns the consecutive experts [l*per, l*per+per)
+// (per = ceil(E/32)): it sums its experts, one warp scan per quantity turns the
+// sums into the lane's starting offsets, and the lane then writes its experts
+// in order, so the lists stay ascending.
+__device__ __forceinline__ int round_up_div(int c, int d) { return (c + d - 1) / d; }
+
 __device__ void scan_experts(const int32_t *hist, int E, int pad, int ntok, int large_min, int large_tile,
                              int32_t *base, bool lists, int32_t *__restrict__ active, int32_t *__restrict__ passes,
                              int32_t *__restrict__ large, int32_t *__restrict__ large_tiles) {
   const int lane = threadIdx.x & 31;
-  int carry = 0;
-  for (int e0 = 0; e0 < E; e0 += 32) {
-    const int e = e0 + lane;
-    const int c = e < E ? hist[e] : 0;
-    const int v = (c + pad - 1) / pad * pad;
-    int incl = v;
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-      const int n = __shfl_up_sync(0xffffffffu, incl, o);
-      if (lane >= o) incl += n;
+  const int per = (E + 31) / 32;
+  const int e0 = min(E, lane * per), e1 = min(E, e0 + per);
+  // the lane's padded pairs, small experts and their passes, large experts and their tiles
+  int v[5] = {0, 0, 0, 0, 0};
+  for (int e = e0; e < e1; ++e) {
+    const int c = hist[e];
+    v[0] += round_up_div(c, pad) * pad;
+    if (c > 0 && c < large_min) {
+      v[1] += 1;
+      v[2] += round_up_div(c, ntok);
+    } else if (c >= large_min) {
+      v[3] += 1;
+      v[4] += round_up_div(c, large_tile);
     }
-    if (e < E) base[e] = carry + incl - v;
-    carry += __shfl_sync(0xffffffffu, incl, 31);
   }
-  if (lane == 0) base[E] = carry;
-  if (!lists) return;
-  int ns = 0, nl = 0, cs = 0, cl = 0;
-  for (int e0 = 0; e0 < E; e0 += 32) {
-    const int e = e0 + lane;
-    const int c = e < E ? hist[e] : 0;
-    const bool sm = c > 0 && c < large_min, lg = c >= large_min;
-    const unsigned msm = __ballot_sync(0xffffffffu, sm), mlg = __ballot_sync(0xffffffffu, lg);
-    const unsigned below = (1u << lane) - 1u;
-    const int vs = sm ? (c + ntok - 1) / ntok : 0, vl = lg ? (c + large_tile - 1) / large_tile : 0;
-    int is = vs, il = vl;
+  int incl[5];
 #pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-      const int ts = __shfl_up_sync(0xffffffffu, is, o), tl = __shfl_up_sync(0xffffffffu, il, o);
-      if (lane >= o) {
-        is += ts;
-        il += tl;
-      }
+  for (int q = 0; q < 5; ++q) incl[q] = v[q];
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+#pragma unroll
+    for (int q = 0; q < 5; ++q) {
+      const int n = __shfl_up_sync(0xffffffffu, incl[q], o);
+      if (lane >= o) incl[q] += n;
     }
-    if (sm) {
-      const int i = ns + __popc(msm & below);
-      active[1 + i] = e;
-      passes[i] = cs + is - vs;
-    }
-    if (lg) {
-      const int i = nl + __popc(mlg & below);
-      large[1 + i] = e;
-      large_tiles[i] = cl + il - vl;
-    }
-    ns += __popc(msm);
-    nl += __popc(mlg);
-    cs += __shfl_sync(0xffffffffu, is, 31);
-    cl += __shfl_sync(0xffffffffu, il, 31);
   }
-  if (lane == 0) {
-    active[0] = ns;
-    passes[ns] = cs;
-    large[0] = nl;
-    large_tiles[nl] = cl;
+  int b = incl[0] - v[0], ns = incl[1] - v[1], cs = incl[2] - v[2], nl = incl[3] - v[3], cl = incl[4] - v[4];
+  for (int e = e0; e < e1; ++e) {
+    const int c = hist[e];
+    base[e] = b;
+    b += round_up_div(c, pad) * pad;
+    if (!lists) continue;
+    if (c > 0 && c < large_min) {
+      active[1 + ns] = e;
+      passes[ns++] = cs;
+      cs += round_up_div(c, ntok);
+    } else if (c >= large_min) {
+      large[1 + nl] = e;
+      large_tiles[nl++] = cl;
+      cl += round_up_div(c, large_tile);
+    }
+  }
+  if (lane == 31) {  // the inclusive sums of the last lane are the totals
+    base[E] = incl[0];
+    if (lists) {
+      active[0] = incl[1];
+      passes[incl[1]] = incl[2];
+      large[0] = incl[3];
+      large_tiles[incl[3]] = incl[4];
+    }
   }
 }
 
@@ -173,7 +176,7 @@ struct RouteOut {
 // starts, and every later kernel may read them before waiting.
 
 // P <= kRouteThreads: CTA 0 does the whole sort; CTAs 1..nstage stage x rows.
-__global__ void __launch_bounds__(kRouteThreads)
+__global__ void __launch_bounds__(kRouteThreads, 1)
 k_route_one(const int32_t *__restrict__ ids, int P, int E, int pad, int ntok, int large_min, int large_tile,
             RouteOut o, RouteStaging st) {
   extern __shared__ int32_t sm[];
@@ -215,7 +218,7 @@ k_route_one(const int32_t *__restrict__ ids, int P, int E, int pad, int ntok, in
 // chunk_hist[c][0..E-1] = its expert counts, chunk_hist[c][E] = its invalid ids
 // and pair_pos[p] = the pair's rank among the chunk's pairs of its expert (-1
 // for an invalid id); CTAs past nchunk stage x rows.
-__global__ void __launch_bounds__(kRouteThreads)
+__global__ void __launch_bounds__(kRouteThreads, 1)
 k_route_rank(const int32_t *__restrict__ ids, int P, int E, int nchunk, int32_t *__restrict__ chunk_hist,
              int32_t *__restrict__ pair_pos, RouteStaging st) {
   extern __shared__ int32_t sm[];
@@ -246,7 +249,7 @@ k_route_rank(const int32_t *__restrict__ ids, int P, int E, int nchunk, int32_t 
 // padded totals, and places its chunk's pairs at base + pre + local rank.
 // CTA 0 writes the counts, offsets, expert lists and status; the padding
 // slots are filled by all CTAs (expert e by CTA e mod nchunk).
-__global__ void __launch_bounds__(kRouteThreads)
+__global__ void __launch_bounds__(kRouteThreads, 1)
 k_route_scatter(const int32_t *__restrict__ ids, int P, int E, int pad, int ntok, int large_min, int large_tile,
                 int nchunk, const int32_t *__restrict__ chunk_hist, RouteOut o, int early) {
   extern __shared__ int32_t sm[];
