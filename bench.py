@@ -79,12 +79,20 @@ def barrier(world):
 
 
 def max_over_ranks(v, world):
+    """The largest of the ranks' values (the slowest rank's time), on every rank."""
     if world == 1:
         return v
     import torch.distributed as dist
-    t = torch.tensor([v], dtype=torch.float64, device="cuda")
+    dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([v], dtype=torch.float64, device=dev)
     dist.all_reduce(t, op=dist.ReduceOp.MAX)
     return float(t.item())
+
+
+def job_throughput(units_per_rank, world, seconds_max):
+    """Whole-job units per second: every rank's units over the slowest rank's time
+    (independent replicas, so the work grows with the number of ranks)."""
+    return world * units_per_rank / seconds_max
 
 
 # ----------------------------------------------------------------- clocks
@@ -372,7 +380,7 @@ def main():
         torch.cuda.synchronize()
         barrier(world)
     ms = max_over_ranks(start.elapsed_time(end), world)
-    value = world * T * args.steps / (ms / 1e3)
+    value = job_throughput(T * args.steps, world, ms / 1e3)
 
     used = ev_sets[:max(1, min(NG, n_rep))]
     stage_ms = np.zeros(abi.MOE_NUM_STAGES)
@@ -426,7 +434,7 @@ def main():
     for i in range(n_e2e):
         abi.moe_run_host(binds[i % R].handle, xh, ih, wh, oh, stream)
     e2e_s = max_over_ranks(time.perf_counter() - t0, world)
-    e2e_value = world * T * n_e2e / e2e_s
+    e2e_value = job_throughput(T * n_e2e, world, e2e_s)
 
     line = {
         "metric": "moe_layer_tokens_per_s", "value": value, "unit": "tokens/s", "n_gpus": world,
