@@ -176,6 +176,9 @@ struct RouteOut {
 // starts, and every later kernel may read them before waiting.
 
 // P <= kRouteThreads: CTA 0 does the whole sort; CTAs 1..nstage stage x rows.
+// Up to 64 registers (one CTA per SM): the expert scan spills at 32.  Its x
+// staging CTAs number T + 1 <= 1025 here; the chunked launches below keep 32
+// registers so that two of their (many) staging CTAs fit on an SM.
 __global__ void __launch_bounds__(kRouteThreads, 1)
 k_route_one(const int32_t *__restrict__ ids, int P, int E, int pad, int ntok, int large_min, int large_tile,
             RouteOut o, RouteStaging st) {
@@ -218,7 +221,7 @@ k_route_one(const int32_t *__restrict__ ids, int P, int E, int pad, int ntok, in
 // chunk_hist[c][0..E-1] = its expert counts, chunk_hist[c][E] = its invalid ids
 // and pair_pos[p] = the pair's rank among the chunk's pairs of its expert (-1
 // for an invalid id); CTAs past nchunk stage x rows.
-__global__ void __launch_bounds__(kRouteThreads, 1)
+__global__ void __launch_bounds__(kRouteThreads)
 k_route_rank(const int32_t *__restrict__ ids, int P, int E, int nchunk, int32_t *__restrict__ chunk_hist,
              int32_t *__restrict__ pair_pos, RouteStaging st) {
   extern __shared__ int32_t sm[];
@@ -249,7 +252,7 @@ k_route_rank(const int32_t *__restrict__ ids, int P, int E, int nchunk, int32_t 
 // padded totals, and places its chunk's pairs at base + pre + local rank.
 // CTA 0 writes the counts, offsets, expert lists and status; the padding
 // slots are filled by all CTAs (expert e by CTA e mod nchunk).
-__global__ void __launch_bounds__(kRouteThreads, 1)
+__global__ void __launch_bounds__(kRouteThreads)
 k_route_scatter(const int32_t *__restrict__ ids, int P, int E, int pad, int ntok, int large_min, int large_tile,
                 int nchunk, const int32_t *__restrict__ chunk_hist, RouteOut o, int early) {
   extern __shared__ int32_t sm[];
