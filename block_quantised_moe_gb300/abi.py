@@ -44,7 +44,7 @@ EXPORTS = (
     "moe_status_str", "moe_plan_weights", "moe_prepare_weights", "moe_is_supported", "moe_plan",
     "moe_bind", "moe_run", "moe_run_timed", "moe_run_host", "moe_device_status", "moe_debug_routing", "moe_quantize",
     "moe_destroy_weight_plan", "moe_destroy_plan", "moe_destroy_binding", "moe_run_no_alloc", "moe_launch_count",
-    "moe_measure_mma_peak",
+    "moe_measure_mma_peak", "moe_selftest_wait_timeout",
 )
 
 
@@ -80,6 +80,7 @@ _sig = {
     "moe_destroy_plan": (None, [_vp]),
     "moe_destroy_binding": (None, [_vp]),
     "moe_run_no_alloc": (_i32, [_vp, _vp, _vp, _vp, _vp, _i32, _vp, _vp]),
+    "moe_selftest_wait_timeout": (_i32, [_vp, _vp, _P(_i32)]),
 }
 for _name, (_res, _args) in _sig.items():
     _f = getattr(_lib, _name)
@@ -204,6 +205,16 @@ def moe_device_status(binding, stream=None):
     rc = _lib.moe_device_status(binding, _stream(stream), st)
     if rc not in (MOE_OK, MOE_ERR_TIMEOUT):
         _check(rc, "moe_device_status")
+    return rc, list(st)
+
+
+def moe_selftest_wait_timeout(status_dev, stream=None):
+    """Let one bounded device wait run out: -> (status code, [flags, 0, 0, 0]).
+    MOE_ERR_TIMEOUT is the expected code and is returned, not raised."""
+    st = (_i32 * 4)()
+    rc = _lib.moe_selftest_wait_timeout(_stream(stream), _ptr(status_dev), st)
+    if rc not in (MOE_OK, MOE_ERR_TIMEOUT):
+        _check(rc, "moe_selftest_wait_timeout")
     return rc, list(st)
 
 

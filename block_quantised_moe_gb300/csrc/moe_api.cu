@@ -12,6 +12,7 @@
 #include "internal.h"
 #include "launch.h"
 #include "moe.h"
+#include "sync.cuh"
 
 using namespace bqmoe;
 
@@ -511,6 +512,32 @@ moe_status moe_device_status(moe_binding b, cudaStream_t stream, int32_t *status
       return MOE_ERR_CUDA;
     if (cudaStreamSynchronize(stream) != cudaSuccess) return MOE_ERR_CUDA;
   }
+  for (int i = 0; i < 4; ++i) status[i] = st[i];
+  return (st[ST_FLAGS] & ST_FLAG_TIMEOUT) ? MOE_ERR_TIMEOUT : MOE_OK;
+}
+
+namespace bqmoe {
+// One thread waits, bounded, on an mbarrier that nothing arrives on, and
+// records the timeout the way every kernel of the forward does.
+__global__ void k_wait_timeout_probe(int32_t *status) {
+  __shared__ __align__(8) uint64_t bar;
+  if (threadIdx.x != 0) return;
+  const uint32_t b = (uint32_t)__cvta_generic_to_shared(&bar);
+  mbar_init(b, 1);
+  asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  if (!mbar_wait(b, 0)) atomicOr(&status[ST_FLAGS], ST_FLAG_TIMEOUT);
+}
+}  // namespace bqmoe
+
+moe_status moe_selftest_wait_timeout(cudaStream_t stream, int32_t *status_dev, int32_t *status) {
+  if (!status_dev || !status) return MOE_ERR_INVALID_ARG;
+  if (cudaMemsetAsync(status_dev, 0, 4 * sizeof(int32_t), stream) != cudaSuccess) return MOE_ERR_CUDA;
+  bqmoe::k_wait_timeout_probe<<<1, 32, 0, stream>>>(status_dev);
+  if (cudaGetLastError() != cudaSuccess) return MOE_ERR_CUDA;
+  int32_t st[4] = {0, 0, 0, 0};
+  if (cudaMemcpyAsync(st, status_dev, sizeof st, cudaMemcpyDeviceToHost, stream) != cudaSuccess ||
+      cudaStreamSynchronize(stream) != cudaSuccess)
+    return MOE_ERR_CUDA;
   for (int i = 0; i < 4; ++i) status[i] = st[i];
   return (st[ST_FLAGS] & ST_FLAG_TIMEOUT) ? MOE_ERR_TIMEOUT : MOE_OK;
 }

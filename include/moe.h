@@ -238,6 +238,18 @@ MOE_API moe_status moe_debug_routing(moe_binding b, cudaStream_t stream, int32_t
                              int32_t *offsets, int32_t *pair_pos,
                              int32_t *sorted_pair, int32_t sorted_cap);
 
+/* Self-test of the failure detection (no counterpart on the pages).  Every
+ * device-side wait in this library is bounded: a wait that nothing completes
+ * gives up after about two seconds, sets bit 1 (timeout) of the status word
+ * and lets its kernel return, so the CUDA context stays usable.  This call
+ * clears the caller's device status word `status_dev` (int32_t[4]), launches
+ * one CTA on `stream` whose mbarrier wait nothing completes, copies the status
+ * word to host `status[4]` and synchronises `stream`.  Returns MOE_ERR_TIMEOUT
+ * when the wait gave up (the expected outcome), MOE_OK if it did not,
+ * MOE_ERR_INVALID_ARG for a null pointer, MOE_ERR_CUDA on a CUDA error.  Takes
+ * about two seconds; allocates nothing. */
+MOE_API moe_status moe_selftest_wait_timeout(cudaStream_t stream, int32_t *status_dev, int32_t *status);
+
 /* ------------------------------------------------------ no-allocation run -- */
 
 /* Size of the library-owned scratch array behind moe_run_no_alloc. */
