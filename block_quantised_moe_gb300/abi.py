@@ -44,7 +44,7 @@ EXPORTS = (
     "moe_status_str", "moe_plan_weights", "moe_prepare_weights", "moe_is_supported", "moe_plan",
     "moe_bind", "moe_run", "moe_run_timed", "moe_run_host", "moe_device_status", "moe_debug_routing", "moe_quantize",
     "moe_destroy_weight_plan", "moe_destroy_plan", "moe_destroy_binding", "moe_run_no_alloc", "moe_launch_count",
-    "moe_measure_mma_peak", "moe_selftest_wait_timeout",
+    "moe_measure_mma_peak", "moe_selftest_wait_timeout", "moe_debug_hidden",
 )
 
 
@@ -81,6 +81,7 @@ _sig = {
     "moe_destroy_binding": (None, [_vp]),
     "moe_run_no_alloc": (_i32, [_vp, _vp, _vp, _vp, _vp, _i32, _vp, _vp]),
     "moe_selftest_wait_timeout": (_i32, [_vp, _vp, _P(_i32)]),
+    "moe_debug_hidden": (_i32, [_vp, _vp, _P(ctypes.c_float), _i32, _P(_i32)]),
 }
 for _name, (_res, _args) in _sig.items():
     _f = getattr(_lib, _name)
@@ -206,6 +207,15 @@ def moe_device_status(binding, stream=None):
     if rc not in (MOE_OK, MOE_ERR_TIMEOUT):
         _check(rc, "moe_device_status")
     return rc, list(st)
+
+
+def moe_debug_hidden(binding, intermediate, rows_cap, stream=None):
+    """GEMM1's h of the last run, [rows, I] float32 in sorted-slot order."""
+    h = np.zeros((rows_cap, intermediate), np.float32)
+    n = _i32()
+    _check(_lib.moe_debug_hidden(binding, _stream(stream), h.ctypes.data_as(_P(ctypes.c_float)), rows_cap,
+                                 ctypes.byref(n)), "moe_debug_hidden")
+    return h[:n.value]
 
 
 def moe_selftest_wait_timeout(status_dev, stream=None):

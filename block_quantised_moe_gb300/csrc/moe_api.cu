@@ -516,6 +516,25 @@ moe_status moe_device_status(moe_binding b, cudaStream_t stream, int32_t *status
   return (st[ST_FLAGS] & ST_FLAG_TIMEOUT) ? MOE_ERR_TIMEOUT : MOE_OK;
 }
 
+moe_status moe_debug_hidden(moe_binding b, cudaStream_t stream, float *h, int32_t rows_cap, int32_t *rows) {
+  if (!b || !h || !rows || rows_cap < 0) return MOE_ERR_INVALID_ARG;
+  *rows = 0;
+  if (b->T == 0) return MOE_OK;
+  const ScratchLayout &S = b->P.S;
+  int32_t n = 0;
+  if (cudaMemcpyAsync(&n, b->scratch + S.offsets + sizeof(int32_t) * b->P.L.E, sizeof n, cudaMemcpyDeviceToHost,
+                      stream) != cudaSuccess ||
+      cudaStreamSynchronize(stream) != cudaSuccess)
+    return MOE_ERR_CUDA;
+  if (n > rows_cap) return MOE_ERR_CAPACITY;
+  if (cudaMemcpyAsync(h, b->scratch + S.h, sizeof(float) * (size_t)n * b->P.L.I, cudaMemcpyDeviceToHost, stream) !=
+          cudaSuccess ||
+      cudaStreamSynchronize(stream) != cudaSuccess)
+    return MOE_ERR_CUDA;
+  *rows = n;
+  return MOE_OK;
+}
+
 namespace bqmoe {
 // One thread waits, bounded, on an mbarrier that nothing arrives on, and
 // records the timeout the way every kernel of the forward does.

@@ -127,6 +127,10 @@ class Binding:
     def device_status(self, stream=None):
         return abi.moe_device_status(self.handle, stream)
 
+    def hidden(self):
+        L = self.plan.layer
+        return abi.moe_debug_hidden(self.handle, L.I, self.T * self.plan.top_k + L.E * self.plan.m_tile)
+
     def routing(self):
         L = self.plan.layer
         return abi.moe_debug_routing(self.handle, L.E, self.T * self.plan.top_k,

@@ -238,6 +238,15 @@ MOE_API moe_status moe_debug_routing(moe_binding b, cudaStream_t stream, int32_t
                              int32_t *offsets, int32_t *pair_pos,
                              int32_t *sorted_pair, int32_t sorted_cap);
 
+/* Copy GEMM1's output h of the last run to host memory and synchronise
+ * `stream` (for checks of the first contraction on its own): h [rows][I] FP32,
+ * one row per slot of the expert-sorted pair list (moe_debug_routing's
+ * sorted_pair gives each slot's pair; rows of padding slots are unspecified),
+ * before any re-quantisation.  *rows = offsets[E].  MOE_ERR_CAPACITY if
+ * rows_cap < offsets[E]; a run with no tokens gives *rows = 0. */
+MOE_API moe_status moe_debug_hidden(moe_binding b, cudaStream_t stream, float *h, int32_t rows_cap,
+                                    int32_t *rows);
+
 /* Self-test of the failure detection (no counterpart on the pages).  Every
  * device-side wait in this library is bounded: a wait that nothing completes
  * gives up after about two seconds, sets bit 1 (timeout) of the status word

@@ -115,17 +115,23 @@ def silu(a: np.ndarray) -> np.ndarray:
         return a * (np.float32(1.0) / (np.float32(1.0) + np.exp(-a)))
 
 
-def expert_ffn(layer: QuantLayer, e: int, xh: np.ndarray, afmt: str, dequant=None) -> np.ndarray:
-    """Steps 3-4 and W^2_e h^ for rows ``xh`` [n, H] routed to expert ``e``."""
-    mats, w2 = dequant if dequant is not None else layer.dequant_expert(e)
+def expert_hidden(layer: QuantLayer, e: int, xh: np.ndarray, dequant=None) -> np.ndarray:
+    """Step 3: h [n, I] float32 of expert ``e`` for activation rows ``xh`` [n, H]."""
+    mats = (dequant if dequant is not None else layer.dequant_expert(e))[0]
     if layer.gated:
         a = xh @ mats[0].T
         b = xh @ mats[1].T
-        h = silu(a) * b
-    else:
-        r = np.maximum(xh @ mats[0].T, np.float32(0.0))
-        h = r * r
-    hh = quant.qdq_rows(h.astype(np.float32), afmt)
+        return (silu(a) * b).astype(np.float32)
+    r = np.maximum(xh @ mats[0].T, np.float32(0.0))
+    return (r * r).astype(np.float32)
+
+
+def expert_ffn(layer: QuantLayer, e: int, xh: np.ndarray, afmt: str, dequant=None) -> np.ndarray:
+    """Steps 3-4 and W^2_e h^ for rows ``xh`` [n, H] routed to expert ``e``."""
+    dq = dequant if dequant is not None else layer.dequant_expert(e)
+    w2 = dq[1]
+    h = expert_hidden(layer, e, xh, dq)
+    hh = quant.qdq_rows(h, afmt)
     return (hh @ w2.T).astype(np.float32)
 
 
