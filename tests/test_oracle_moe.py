@@ -140,6 +140,38 @@ def test_forward_matches_float64_brute_force(wfmt, act, afmt):
     assert np.max(np.abs(y - yb)) <= 1e-5 * (np.abs(yb) + np.sqrt(np.mean(yb ** 2))).max()
 
 
+def bf_hidden(xh, L, e):
+    """Step 3 for one activation row by scalar loops in float64: h [I]."""
+    H, I = L.hidden, L.intermediate
+    c13, s13 = L.w13_codes[e], L.w13_scales[e]
+    g13 = L.w13_global[e] if L.w13_global is not None else [None, None]
+    h = []
+    for i in range(I):
+        if L.gated:
+            a = sum(bf_weight(c13, s13, g13[0], i, j, L.wfmt) * xh[j] for j in range(H))
+            u = sum(bf_weight(c13, s13, g13[1], I + i, j, L.wfmt) * xh[j] for j in range(H))
+            h.append(a / (1.0 + math.exp(-a)) * u)
+        else:
+            r = sum(bf_weight(c13, s13, g13[0], i, j, L.wfmt) * xh[j] for j in range(H))
+            h.append(max(r, 0.0) ** 2)
+    return np.array(h)
+
+
+@pytest.mark.parametrize("wfmt,act,afmt", MODES)
+def test_expert_hidden_matches_float64_brute_force(wfmt, act, afmt):
+    # step 3 on its own (the GPU's GEMM1 output is compared with this function)
+    E, H, I, T = 3, 64, 32, 3
+    L = make_layer(E, H, I, wfmt, act, seed=4)
+    x, _, _ = make_inputs(T, H, E, 1, seed=4)
+    xh = quant.qdq_rows(x, afmt)
+    for e in range(E):
+        h = moe.expert_hidden(L, e, xh)
+        hb = np.stack([bf_hidden(bf_qdq(x[t], afmt), L, e) for t in range(T)])
+        assert h.shape == (T, I) and h.dtype == np.float32
+        assert np.linalg.norm(h - hb) / np.linalg.norm(hb) < 2e-6
+        assert np.max(np.abs(h - hb)) <= 1e-5 * (np.abs(hb) + np.sqrt(np.mean(hb ** 2))).max()
+
+
 # ------------------------------------------------------------- invariants
 
 @pytest.fixture(scope="module", params=MODES[:3], ids=lambda m: "-".join(m))
