@@ -1,22 +1,25 @@
 #!/usr/bin/env python
 """MoE-layer throughput of libmoe on GB300, one JSON line on rank 0.
 
-Workload: the decode layer E=128 experts, hidden 2048, intermediate 768, top-8,
-NVFP4 weights with BF16 activations and gated SiLU, at T tokens per step
-(default 64; 1, 4 and 16 are the other decode batch sizes of this layer).  A
-step is one full forward of the layer (routing, GEMM1 + SiLU, GEMM2 x topk
-weight, combine) through the C ABI over one batch of seeded synthetic input.
-Steps rotate over R independent layer replicas and routing draws whose packed
-weights together exceed L2, so every step streams its experts from HBM.
+Headline workload: the prefill layer E=256 experts, hidden 7168, intermediate
+2048, top-8, T=8192 tokens, NVFP4 weights with BF16 activations (W4A16) and
+gated SiLU -- the largest single-GPU configuration of this op.  A step is one
+full forward of the layer (routing, GEMM1 + SiLU, GEMM2 x topk weight,
+combine) through the C ABI over one batch of seeded synthetic input.
 
 ``value`` is tokens/s with inputs resident in HBM, timed with CUDA events on
-the launching stream; ``e2e`` is the same through ``moe_run_host`` with pinned
-host buffers (H2D of x / ids / weights and D2H of the output inside the timed
-loop).  ``roofline`` is for the dominant kernel, from per-stage CUDA events
-recorded by ``moe_run_timed`` inside the timed region.  ``cpu_baseline`` times
-the CPU oracle on a bounded sample.  ``--impl reference`` times only the oracle
-(the reference arm).  Multi-GPU runs (torchrun) are independent replicas: one
-layer per rank, no collective on the data path, weak scaling.
+the launching stream over replays of CUDA graphs of the forward; ``e2e`` is the
+same through ``moe_run_host`` with pinned host buffers (H2D of x / ids /
+weights and D2H of the output inside the timed loop).  ``roofline`` is for the
+dominant kernel, from per-stage CUDA events recorded by ``moe_run_timed``
+inside the timed region.  ``cpu_baseline`` times the CPU oracle on a bounded
+sample.  ``rows`` carries the other workloads (W4A4 prefill, the decode
+layers, MXFP4 x MXFP8), each with its own step time and roofline.  Steps rotate
+over R layer replicas and routing draws whose touched bytes together exceed L2
+several times over, so every step streams its experts from HBM.
+``--impl reference`` times only the oracle (the reference arm).  Multi-GPU
+runs (torchrun) are independent replicas: one layer per rank, no collective on
+the data path, weak scaling.
 """
 
 from __future__ import annotations
@@ -25,6 +28,7 @@ import argparse
 import ctypes
 import hashlib
 import json
+import math
 import os
 import statistics
 import sys
@@ -37,19 +41,34 @@ import torch
 ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
-DEFAULT_CONFIG = "decode_e128_h2048_i768_k8"
+HEADLINE = ("prefill_w4a16_e256_h7168_i2048_k8", 8192)
+# the other workloads of the op, reported under "rows"
+ROWS = [("prefill_w4a4_e256_h7168_i2048_k8", 8192)] + \
+    [("decode_e128_h2048_i768_k8", t) for t in (1, 4, 16, 64)] + \
+    [("decode_zipf_e256_h7168_i2048_k8", t) for t in (1, 8, 32, 128)] + \
+    [("mxfp4_mxfp8_relu2_e128_h4096_i1024_k4", t) for t in (1, 64, 4096)]
+L2_BYTES = 126.5e6
+# committed ncu summaries per workload (profiles/)
+PROFILES = {
+    "prefill_w4a16_e256_h7168_i2048_k8": "profiles/k_grouped_tc_prefill_e32_h7168_t2048.md",
+    "prefill_w4a4_e256_h7168_i2048_k8": "profiles/k_grouped_fp4_prefill_e32_h7168_t2048.md",
+    "decode_e128_h2048_i768_k8": "profiles/k_grouped_mma_decode_e128_h2048_t64.md",
+}
 
 
 def parse():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=2000)
-    ap.add_argument("--warmup", type=int, default=50)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--config", default=DEFAULT_CONFIG)
-    ap.add_argument("--tokens", type=int, default=64)
-    ap.add_argument("--replicas", type=int, default=4)
-    ap.add_argument("--e2e-steps", type=int, default=300)
+    ap.add_argument("--config", default=None, help="run this workload alone as the headline")
+    ap.add_argument("--tokens", type=int, default=None)
+    ap.add_argument("--rows", default=None,
+                    help="'all' (default with the headline), 'none', or workload:T pairs, comma separated")
+    ap.add_argument("--row-steps", type=int, default=None, help="timed steps per extra row (default: --steps)")
+    ap.add_argument("--max-replicas", type=int, default=16)
+    ap.add_argument("--e2e-steps", type=int, default=20)
     ap.add_argument("--cpu-budget-s", type=float, default=12.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--experts", type=int, default=None,
@@ -233,8 +252,9 @@ def oracle_prepare(cfg, x, ids, w, n_pairs, seed=0):
     ids_c = np.where(ids_s >= 0, remap[np.clip(ids_s, 0, E - 1)], -1)[toks]
     gated = cfg["act"] == "silu"
     w13s, w2s = [], []
+    dev = "cuda" if torch.cuda.is_available() else "cpu"
     for e in used:
-        a, b = synth.make_expert_weights(int(e), H, I, gated, seed, device="cuda")
+        a, b = synth.make_expert_weights(int(e), H, I, gated, seed, device=dev)
         w13s.append([m.cpu().numpy() for m in a]), w2s.append(b.cpu().numpy())
     L = moe.quantize_layer(w13s, w2s, cfg["wfmt"], cfg["act"])
     xs, ws = x[toks], w[toks]
@@ -258,11 +278,17 @@ def time_repeated(fn, min_seconds):
             return el / n, n
 
 
+def workload_name(name, T, E_override=None):
+    return f"{name} T={T}" + (f" E={E_override}" if E_override else "")
+
+
 def run_reference(args, cfg, world, rank):
     if rank != 0:
         return
     from block_quantised_moe_gb300 import synth
-    T, K = args.tokens, cfg["K"]
+    name = args.config or HEADLINE[0]
+    T = args.tokens or (HEADLINE[1] if name == HEADLINE[0] else synth.CONFIGS[name]["tokens"][-1])
+    K = cfg["K"]
     x = synth.make_x(T, cfg["H"], 0).float().numpy()
     ids, w = synth.make_routing(T, cfg["E"], K, 0, zipf=cfg["zipf"])
     ids, w = ids.numpy(), w.numpy()
@@ -281,7 +307,7 @@ def run_reference(args, cfg, world, rank):
         "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": 1e3 * total / args.steps, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f32", "data": "synthetic",
-        "config": {"workload": f"{args.config} T={T}", "sample_per_step": desc},
+        "config": {"workload": workload_name(name, T), "sample_per_step": desc},
         "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": cores, "kind": "oracle",
                          "sample": f"per step: {desc}; oracle forward only (weights quantised untimed)"},
         "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
@@ -291,58 +317,127 @@ def run_reference(args, cfg, world, rank):
 
 # ------------------------------------------------------------------ our arm
 
-def main():
-    args = parse()
-    from block_quantised_moe_gb300 import synth
-    cfg = dict(synth.CONFIGS[args.config])
+def replicas_for(touched_bytes, packed_bytes, max_replicas):
+    """Layer replicas (each with its own routing draw) so that a replica's
+    touched experts come back only after several L2 capacities of other bytes;
+    at most 64 GB of copies."""
+    if touched_bytes >= 3 * L2_BYTES:
+        return 1
+    want = math.ceil(3 * L2_BYTES / max(touched_bytes, 1.0)) + 1
+    cap = max(1, int(64e9 // max(packed_bytes, 1)))
+    return int(max(1, min(want, max_replicas, cap)))
+
+
+class Layers:
+    """Packed layers shared by the workloads (a layer does not depend on T)."""
+
+    def __init__(self):
+        self.cache = {}
+
+    def get(self, cfg, need_fp4_tiles):
+        from block_quantised_moe_gb300 import layer
+        key = (cfg["E"], cfg["H"], cfg["I"], cfg["wfmt"], cfg["act"])
+        ent = self.cache.get(key)
+        if ent is None or (need_fp4_tiles and not ent.fp4_tiles):
+            # NVFP4 layers of the big shape carry the FP4 tiles too, so that the
+            # W4A16, W4A4 and decode workloads share one packed buffer
+            tiles = cfg["wfmt"] == "nvfp4" and (need_fp4_tiles or cfg["H"] % 256 == 0 and cfg["I"] % 256 == 0
+                                               and cfg["E"] >= 256)
+            self.cache.pop(key, None)
+            torch.cuda.empty_cache()
+            ck = layer.make_experts_gpu(cfg["E"], cfg["H"], cfg["I"], cfg["wfmt"], cfg["act"], seed=0)
+            ent = layer.PackedLayer(ck, cfg["H"], cfg["I"], fp4_tiles=tiles)
+            ent.fp4_tiles = tiles
+            del ck
+            self.cache[key] = ent
+        return ent
+
+
+def algorithmic(cfg, T, touched):
+    """Algorithmic HBM bytes of the layer and of each kernel, and FLOPs, per step."""
+    E, H, I, K = cfg["E"], cfg["H"], cfg["I"], cfg["K"]
+    b13, b2 = expert_bytes(cfg)
+    x_bytes, out_bytes, route_bytes = T * H * 2, T * H * 2, T * K * 8
+    layer_bytes = touched * (b13 + b2) + x_bytes + out_bytes + route_bytes
+    kernel_bytes = {"gemm1": touched * b13 + x_bytes, "gemm2": touched * b2 + T * K * 4,
+                    "combine": out_bytes, "route": T * K * 4}
+    n13 = 2 * I if cfg["act"] == "silu" else I
+    kernel_flops = {"gemm1": 2.0 * T * K * n13 * H, "gemm2": 2.0 * T * K * H * I}
+    flops = kernel_flops["gemm1"] + kernel_flops["gemm2"]
+    return layer_bytes, kernel_bytes, kernel_flops, flops
+
+
+def roofline_of(stage_ms, kernel_bytes, kernel_flops, cfg, afmt, pairs):
+    """Dominant stage, its bound and achieved / peak (see the roofline conventions)."""
+    from block_quantised_moe_gb300 import abi
+    names = abi.STAGES
+    dom = int(np.argmax(stage_ms))
+    dom_name = names[dom]
+    hbm, peak_kind = peaks()
+    tc_peak, tc_kind = tensor_peak(cfg, afmt, pairs)
+    dom_bytes = kernel_bytes.get(dom_name, 0.0)
+    dom_flops = kernel_flops.get(dom_name, 0.0)
+    dom_s = stage_ms[dom] * 1e-3
+    if dom_flops / (tc_peak * 1e12) > dom_bytes / (hbm * 1e9):
+        roof = {"kernel": dom_name, "bound": "tensor", "achieved": dom_flops / dom_s / 1e12 if dom_s > 0 else 0.0,
+                "peak": tc_peak, "peak_kind": tc_kind, "unit": "TFLOP/s"}
+        roof["frac"] = roof["achieved"] / tc_peak
+        # the same kernel against the byte floor, for context
+        roof["hbm_frac"] = dom_bytes / dom_s / 1e9 / hbm if dom_s > 0 else 0.0
+    else:
+        roof = {"kernel": dom_name, "bound": "hbm", "achieved": dom_bytes / dom_s / 1e9 if dom_s > 0 else 0.0,
+                "peak": hbm, "peak_kind": peak_kind, "unit": "GB/s"}
+        roof["frac"] = roof["achieved"] / hbm
+    roof.update(algorithmic_bytes=dom_bytes, algorithmic_flops=dom_flops)
+    return roof
+
+
+def measure(name, T, args, world, rank, layers, steps, headline=False):
+    """Time `steps` forwards of workload `name` at T tokens; returns the row."""
+    from block_quantised_moe_gb300 import abi, layer, synth
+    cfg = dict(synth.CONFIGS[name])
     if args.experts:
         cfg["E"] = args.experts
-    world, rank, local = dist_setup(args)
-    if args.impl == "reference":
-        run_reference(args, cfg, world, rank)
-        return
-
-    from block_quantised_moe_gb300 import build
-    if local == 0:
-        build.build()
-    barrier(world)
-    from block_quantised_moe_gb300 import abi, layer
-
-    E, H, I, K, T = cfg["E"], cfg["H"], cfg["I"], cfg["K"], args.tokens
+    E, H, I, K = cfg["E"], cfg["H"], cfg["I"], cfg["K"]
     afmt = cfg["afmt"]
-    R = max(1, args.replicas)
-    seed_base = 1000 * rank
-    ck = layer.make_experts_gpu(E, H, I, cfg["wfmt"], cfg["act"], seed=0)
-    # W4A4 layers also carry the FP4 tiles of the block-scaled tensor-core kernel
-    packed0 = layer.PackedLayer(ck, H, I, fp4_tiles=cfg["wfmt"] == "nvfp4" and afmt == "nvfp4")
-    del ck
-    packed = [packed0.packed] + [packed0.packed.clone() for _ in range(R - 1)]
+    fp4 = cfg["wfmt"] == "nvfp4" and afmt == "nvfp4"
+    packed0 = layers.get(cfg, fp4)
     plan = layer.Plan(packed0, K, T, afmt)
+    seed_base = 1000 * rank
+    # routing draws first: the replica count depends on the touched bytes
+    b13, b2 = expert_bytes(cfg)
+    draws = []
+    for r in range(args.max_replicas):
+        ids, w = synth.make_routing(T, E, K, seed_base + r, zipf=cfg["zipf"])
+        draws.append((ids, w, len(np.unique(ids.numpy()))))
+    R = replicas_for(np.mean([d[2] for d in draws]) * (b13 + b2), packed0.packed.numel(), args.max_replicas)
+    R = max(1, min(R, steps))
+    packed = [packed0.packed] + [packed0.packed.clone() for _ in range(R - 1)]
     xs, idss, ws, outs, binds, touched = [], [], [], [], [], []
     for r in range(R):
         x = synth.make_x(T, H, seed_base + r).cuda()
-        ids, w = synth.make_routing(T, E, K, seed_base + r, zipf=cfg["zipf"])
-        touched.append(len(np.unique(ids.numpy())))
+        ids, w, tch = draws[r]
         ids, w = ids.cuda(), w.cuda()
         out = torch.empty(T, H, dtype=torch.bfloat16, device="cuda")
-        xs.append(x), idss.append(ids), ws.append(w), outs.append(out)
+        xs.append(x), idss.append(ids), ws.append(w), outs.append(out), touched.append(tch)
         binds.append(plan.bind(x, ids, w, out, packed=packed[r]))
     stream = torch.cuda.current_stream()
     torch.cuda.synchronize()
 
-    # The timed steps replay CUDA graphs of L = 4R forwards (replicas in
-    # rotation, so every step streams a different layer copy).  The first
-    # forward of each of the NG graphs records per-stage events (external event
-    # nodes), so after the timed loop each event set holds the stage times of
-    # its graph's last replay inside the timed region.
+    # The timed steps replay CUDA graphs of R forwards (one per replica, in
+    # rotation).  Up to 4 forwards of each of the NG graphs record per-stage
+    # events (external event nodes), so after the timed loop each event set
+    # holds the stage times of its forward in its graph's last replay.
     n_ev = abi.MOE_NUM_STAGES + 1
-    L, NG = 4 * R, 8
-    ev_sets = []
-    for _ in range(NG):
-        evs = [torch.cuda.Event(enable_timing=True) for _ in range(n_ev)]
-        for e in evs:
-            e.record(stream)  # creates the handles
-        ev_sets.append(evs)
+    NG = 8
+    ev_fwd = sorted(set(int(i * R / min(R, 4)) for i in range(min(R, 4))))
+    ev_sets = {}
+    for j in range(NG):
+        for i in ev_fwd:
+            evs = [torch.cuda.Event(enable_timing=True) for _ in range(n_ev)]
+            for e in evs:
+                e.record(stream)  # creates the handles
+            ev_sets[(j, i)] = evs
     for i in range(args.warmup):
         binds[i % R].run(stream)
     torch.cuda.synchronize()
@@ -353,11 +448,11 @@ def main():
         for j in range(NG):
             g = torch.cuda.CUDAGraph()
             g.capture_begin()
-            for i in range(L):
-                if i == 0:
-                    abi.moe_run_timed(binds[0].handle, [e.cuda_event for e in ev_sets[j]], cap)
+            for i in range(R):
+                if i in ev_fwd:
+                    abi.moe_run_timed(binds[i].handle, [e.cuda_event for e in ev_sets[(j, i)]], cap)
                 else:
-                    binds[i % R].run(cap)
+                    binds[i].run(cap)
             g.capture_end()
             graphs.append(g)
     torch.cuda.synchronize()
@@ -366,7 +461,7 @@ def main():
     torch.cuda.synchronize()
     barrier(world)
 
-    n_rep, rem = divmod(args.steps, L)
+    n_rep, rem = divmod(steps, R)
     start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     with ClockSampler() as clk:
         torch.cuda.synchronize()
@@ -380,94 +475,143 @@ def main():
         torch.cuda.synchronize()
         barrier(world)
     ms = max_over_ranks(start.elapsed_time(end), world)
-    value = job_throughput(T * args.steps, world, ms / 1e3)
+    value = job_throughput(T * steps, world, ms / 1e3)
 
-    used = ev_sets[:max(1, min(NG, n_rep))]
+    used = [(j, i) for j in range(min(NG, n_rep)) for i in ev_fwd]
     stage_ms = np.zeros(abi.MOE_NUM_STAGES)
-    for evs in used:
+    for key in used:
+        evs = ev_sets[key]
         for s_ in range(abi.MOE_NUM_STAGES):
             stage_ms[s_] += evs[s_].elapsed_time(evs[s_ + 1])
-    stage_ms /= len(used)
-
-    # algorithmic bytes (HBM) of the whole layer and of each kernel, per step
-    b13, b2 = expert_bytes(cfg)
-    tch = float(np.mean(touched))
-    x_bytes, out_bytes, route_bytes = T * H * 2, T * H * 2, T * K * 8
-    layer_bytes = tch * (b13 + b2) + x_bytes + out_bytes + route_bytes
-    kernel_bytes = {"gemm1": tch * b13 + x_bytes, "gemm2": tch * b2 + T * K * 4,
-                    "combine": out_bytes, "route": T * K * 4}
-    flops = 2 * T * K * (3 if cfg["act"] == "silu" else 2) * H * I
-    n13 = 2 * I if cfg["act"] == "silu" else I
-    kernel_flops = {"gemm1": 2.0 * T * K * n13 * H, "gemm2": 2.0 * T * K * H * I}
-    names = abi.STAGES
-    dom = int(np.argmax(stage_ms))
-    dom_name = names[dom]
-    hbm, peak_kind = peaks()
-    tc_peak, tc_kind = tensor_peak(cfg, afmt, T * K)
-    dom_bytes = kernel_bytes.get(dom_name, 0.0)
-    dom_flops = kernel_flops.get(dom_name, 0.0)
-    dom_s = stage_ms[dom] * 1e-3
-    # the kernel's bound is the larger of its two floors: bytes at the HBM peak, FLOPs at the tensor peak
-    if dom_flops / (tc_peak * 1e12) > dom_bytes / (hbm * 1e9):
-        roof = {"kernel": dom_name, "bound": "tensor", "achieved": dom_flops / dom_s / 1e12 if dom_s > 0 else 0.0,
-                "peak": tc_peak, "peak_kind": tc_kind, "unit": "TFLOP/s"}
-        roof["frac"] = roof["achieved"] / tc_peak
-    else:
-        roof = {"kernel": dom_name, "bound": "hbm", "achieved": dom_bytes / dom_s / 1e9 if dom_s > 0 else 0.0,
-                "peak": hbm, "peak_kind": peak_kind, "unit": "GB/s"}
-        roof["frac"] = roof["achieved"] / hbm
-    rec, src_hash = traffic_record("k_grouped_mma.cu")
-    traffic = None
-    if rec and rec.get("src_sha256_16") == src_hash and rec.get("workload") == f"{args.config} T={T}":
-        traffic = rec.get("per_launch", {}).get(dom_name)
-
-    # end to end through moe_run_host: pinned host buffers, copies inside the loop
-    xh = xs[0].cpu().pin_memory()
-    ih = idss[0].cpu().pin_memory()
-    wh = ws[0].cpu().pin_memory()
-    oh = torch.empty(T, H, dtype=torch.bfloat16).pin_memory()
-    n_e2e = max(1, min(args.e2e_steps, args.steps))
-    for _ in range(3):
-        abi.moe_run_host(binds[0].handle, xh, ih, wh, oh, stream)
-    barrier(world)
-    t0 = time.perf_counter()
-    for i in range(n_e2e):
-        abi.moe_run_host(binds[i % R].handle, xh, ih, wh, oh, stream)
-    e2e_s = max_over_ranks(time.perf_counter() - t0, world)
-    e2e_value = job_throughput(T * n_e2e, world, e2e_s)
-
-    line = {
-        "metric": "moe_layer_tokens_per_s", "value": value, "unit": "tokens/s", "n_gpus": world,
-        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms / args.steps,
-        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
-        "data": "synthetic",
-        "config": {"workload": f"{args.config} T={T}" + (f" E={E}" if args.experts else ""), "experts": E, "hidden": H, "intermediate": I,
-                   "top_k": K, "weights": cfg["wfmt"], "activations": afmt, "act": cfg["act"],
-                   "tokens": T, "parallelism": f"replicas x{world}",
-                   "l2": f"{R} layer replicas x {packed0.packed.numel() / 1e6:.0f} MB rotated per step (> L2)",
-                   "touched_experts_mean": tch},
-        "hbm_gbs_layer": layer_bytes / (ms / args.steps * 1e-3) / 1e9,
-        "tflops": flops / (ms / args.steps * 1e-3) / 1e12,
-        "stage_us": {n: round(1e3 * v, 3) for n, v in zip(names, stage_ms)},
-        "roofline": dict(roof, traffic=traffic, algorithmic_bytes=dom_bytes, algorithmic_flops=dom_flops),
-        "layer_roofline_frac": layer_bytes / (ms / args.steps * 1e-3) / 1e9 / hbm,
-        "gpu_launches": args.steps * launches_per_fwd,
-        "timing": f"CUDA graphs of {L} forwards replayed; stage events from the last replay of each of "
-                  f"{len(used)} graphs",
-        "e2e": {"value": e2e_value, "unit": "tokens/s", "h2d_bytes_per_step": T * H * 2 + T * K * 8,
-                "d2h_bytes_per_step": T * H * 2, "steps": n_e2e},
+    stage_ms /= max(1, len(used))
+    # touched experts of the forwards whose events are used
+    tch_ev = float(np.mean([touched[i] for (_, i) in used])) if used else float(np.mean(touched))
+    layer_bytes, kernel_bytes, kernel_flops, flops = algorithmic(cfg, T, tch_ev)
+    layer_bytes_all, _, _, _ = algorithmic(cfg, T, float(np.mean(touched)))
+    roof = roofline_of(stage_ms, kernel_bytes, kernel_flops, cfg, afmt, T * K)
+    step_s = ms / steps * 1e-3
+    hbm, _ = peaks()
+    row = {
+        "workload": workload_name(name, T, args.experts), "value": value, "unit": "tokens/s",
+        "ms_per_step": ms / steps, "steps": steps,
+        "config": {"experts": E, "hidden": H, "intermediate": I, "top_k": K, "weights": cfg["wfmt"],
+                   "activations": afmt, "act": cfg["act"], "tokens": T,
+                   "l2": f"{R} layer replica(s) x {packed0.packed.numel() / 1e6:.0f} MB, each with its own "
+                         f"routing draw, rotated per step; {tch_ev:.1f} touched experts x "
+                         f"{(b13 + b2) / 1e6:.1f} MB per step"
+                         + ("; inputs larger than L2" if tch_ev * (b13 + b2) > L2_BYTES else ""),
+                   "touched_experts_mean": float(np.mean(touched))},
+        "hbm_gbs_layer": layer_bytes_all / step_s / 1e9,
+        "layer_roofline_frac": layer_bytes_all / step_s / 1e9 / hbm,
+        "tflops": flops / step_s / 1e12,
+        "stage_us": {n: round(1e3 * v, 3) for n, v in zip(abi.STAGES, stage_ms)},
+        "roofline": roof,
+        "gpu_launches": steps * launches_per_fwd,
+        "timing": f"CUDA graphs of {R} forwards replayed; stage events from {len(used)} forwards inside the "
+                  "timed region (the last replay of each graph)",
         "clocks": clk.summary(),
     }
+    prof = PROFILES.get(name)
+    if prof and os.path.exists(os.path.join(ROOT, prof)):
+        row["roofline"]["profile"] = prof
+    rec, src_hash = traffic_record("k_grouped_mma.cu")
+    traffic = None
+    if rec and rec.get("src_sha256_16") == src_hash and rec.get("workload") == workload_name(name, T):
+        traffic = rec.get("per_launch", {}).get(roof["kernel"])
+    row["roofline"]["traffic"] = traffic
 
+    if headline:
+        # end to end through moe_run_host: pinned host buffers, copies inside the loop
+        xh = xs[0].cpu().pin_memory()
+        ih = idss[0].cpu().pin_memory()
+        wh = ws[0].cpu().pin_memory()
+        oh = torch.empty(T, H, dtype=torch.bfloat16).pin_memory()
+        n_e2e = max(1, min(args.e2e_steps, steps))
+        for _ in range(3):
+            abi.moe_run_host(binds[0].handle, xh, ih, wh, oh, stream)
+        barrier(world)
+        t0 = time.perf_counter()
+        for i in range(n_e2e):
+            abi.moe_run_host(binds[i % R].handle, xh, ih, wh, oh, stream)
+        e2e_s = max_over_ranks(time.perf_counter() - t0, world)
+        row["e2e"] = {"value": job_throughput(T * n_e2e, world, e2e_s), "unit": "tokens/s",
+                      "h2d_bytes_per_step": T * H * 2 + T * K * 8, "d2h_bytes_per_step": T * H * 2,
+                      "steps": n_e2e}
+        row["_sample"] = (cfg, xs[0], idss[0], ws[0])
+    del graphs, binds, packed, plan
+    torch.cuda.synchronize()
+    torch.cuda.empty_cache()
+    return row
+
+
+def parse_rows(args):
+    from block_quantised_moe_gb300 import synth
+    spec = args.rows if args.rows is not None else ("none" if args.config else "all")
+    if spec == "none":
+        return []
+    if spec == "all":
+        return list(ROWS)
+    out = []
+    for item in spec.split(","):
+        n, t = item.split(":")
+        assert n in synth.CONFIGS, n
+        out.append((n, int(t)))
+    return out
+
+
+def main():
+    args = parse()
+    from block_quantised_moe_gb300 import synth
+    name = args.config or HEADLINE[0]
+    cfg = dict(synth.CONFIGS[name])
+    if args.experts:
+        cfg["E"] = args.experts
+    T = args.tokens or (HEADLINE[1] if name == HEADLINE[0] else cfg["tokens"][-1])
+    world, rank, local = dist_setup(args)
+    if args.impl == "reference":
+        run_reference(args, cfg, world, rank)
+        return
+
+    from block_quantised_moe_gb300 import build
+    if local == 0:
+        build.build()
+    barrier(world)
+
+    layers = Layers()
+    head = measure(name, T, args, world, rank, layers, args.steps, headline=True)
+    cfg_s, x_s, ids_s, w_s = head.pop("_sample")
+    rows = {}
+    # the extra workloads run at N=1 only (multi-GPU runs time the headline)
+    if world == 1:
+        for (n, t) in parse_rows(args):
+            if (n, t) == (name, T):
+                continue
+            r = measure(n, t, args, world, rank, layers, args.row_steps or args.steps)
+            rows[r.pop("workload")] = r
+    line = {
+        "metric": "moe_layer_tokens_per_s", "value": head["value"], "unit": "tokens/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": head["ms_per_step"],
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+        "data": "synthetic",
+        "config": dict({"workload": head["workload"], "parallelism": f"replicas x{world}",
+                        "mma_operands": "fp16 (fp4 weights dequantised in shared memory) x fp16 activations, "
+                                        "f32 accumulate" if cfg["afmt"] == "bf16" else cfg["afmt"]},
+                       **head["config"]),
+        "hbm_gbs_layer": head["hbm_gbs_layer"], "layer_roofline_frac": head["layer_roofline_frac"],
+        "tflops": head["tflops"], "stage_us": head["stage_us"], "roofline": head["roofline"],
+        "gpu_launches": head["gpu_launches"], "timing": head["timing"], "e2e": head["e2e"],
+        "clocks": head["clocks"], "rows": rows,
+    }
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        x_np = xs[0].float().cpu().numpy()
-        ids_np, w_np = idss[0].cpu().numpy(), ws[0].cpu().numpy()
-        # two tokens' pairs, forward repeated for about cpu_budget_s
-        fwd, tok, desc = oracle_prepare(cfg, x_np, ids_np, w_np, min(T * K, 2 * K))
+        x_np = x_s.float().cpu().numpy()
+        ids_np, w_np = ids_s.cpu().numpy(), w_s.cpu().numpy()
+        # a couple of (token, slot) pairs, forward repeated for about cpu_budget_s
+        n_pairs = 2 if cfg_s["H"] * cfg_s["I"] > 4e6 else min(T * cfg_s["K"], 2 * cfg_s["K"])
+        fwd, tok, desc = oracle_prepare(cfg_s, x_np, ids_np, w_np, n_pairs)
         dt, n = time_repeated(fwd, args.cpu_budget_s)
         line["cpu_baseline"] = {"value": tok / dt, "unit": "tokens/s", "cores": len(os.sched_getaffinity(0)),
                                 "kind": "oracle",
-                                "sample": f"{desc} of {args.config} T={T}; forward only, mean of {n} calls"}
+                                "sample": f"{desc} of {head['workload']}; forward only, mean of {n} calls"}
     if rank == 0:
         print(json.dumps(line), flush=True)
     if world > 1:

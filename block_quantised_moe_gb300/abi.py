@@ -44,7 +44,7 @@ EXPORTS = (
     "moe_status_str", "moe_plan_weights", "moe_prepare_weights", "moe_is_supported", "moe_plan",
     "moe_bind", "moe_run", "moe_run_timed", "moe_run_host", "moe_device_status", "moe_debug_routing", "moe_quantize",
     "moe_destroy_weight_plan", "moe_destroy_plan", "moe_destroy_binding", "moe_run_no_alloc", "moe_launch_count",
-    "moe_measure_mma_peak", "moe_selftest_wait_timeout", "moe_debug_hidden",
+    "moe_measure_mma_peak", "moe_selftest_wait_timeout", "moe_debug_hidden", "moe_no_alloc_device_status",
 )
 
 
@@ -80,6 +80,7 @@ _sig = {
     "moe_destroy_plan": (None, [_vp]),
     "moe_destroy_binding": (None, [_vp]),
     "moe_run_no_alloc": (_i32, [_vp, _vp, _vp, _vp, _vp, _i32, _vp, _vp]),
+    "moe_no_alloc_device_status": (_i32, [_vp, _vp, _P(_i32)]),
     "moe_selftest_wait_timeout": (_i32, [_vp, _vp, _P(_i32)]),
     "moe_debug_hidden": (_i32, [_vp, _vp, _P(ctypes.c_float), _i32, _P(_i32)]),
 }
@@ -263,3 +264,13 @@ def moe_run_no_alloc(plan, packed, x, topk_ids, topk_weights, num_tokens, out, s
     """Forward with the library's own static scratch, for callers that cannot allocate."""
     _check(_lib.moe_run_no_alloc(plan, _ptr(packed), _ptr(x), _ptr(topk_ids), _ptr(topk_weights),
                                  num_tokens, _ptr(out), _stream(stream)), "moe_run_no_alloc")
+
+
+def moe_no_alloc_device_status(plan, stream=None):
+    """Status word of the last moe_run_no_alloc: -> (status code, [flags, dropped, 0, 0]);
+    MOE_ERR_TIMEOUT is returned, not raised."""
+    st = (_i32 * 4)()
+    rc = _lib.moe_no_alloc_device_status(plan, _stream(stream), st)
+    if rc not in (MOE_OK, MOE_ERR_TIMEOUT):
+        _check(rc, "moe_no_alloc_device_status")
+    return rc, list(st)

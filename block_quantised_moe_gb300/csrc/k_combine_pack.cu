@@ -1,5 +1,6 @@
 // Per-token combine of the expert outputs, and the one-time weight packer.
 #include <algorithm>
+#include <mutex>
 
 #include "common.cuh"
 #include "internal.h"
@@ -117,15 +118,31 @@ cudaError_t launch_combine(const void *part, bool part_bf16, int H, const int32_
                            cudaStream_t s) {
   if (T <= 0) return cudaSuccess;
   if (K > kMaxK || H % 8) return cudaErrorInvalidValue;
-  // one resident wave of blocks, each looping over its tokens
-  static int sms = 0, occ[2] = {0, 0};
-  if (!sms) {
-    int dev = 0, n = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
-        cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ[0], k_combine<false>, kCombThreads, 0) != cudaSuccess ||
-        cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ[1], k_combine<true>, kCombThreads, 0) != cudaSuccess)
-      return cudaErrorUnknown;
-    sms = n;
+  // one resident wave of blocks, each looping over its tokens; the SM count and
+  // occupancy are looked up once per device (under a lock: several host threads
+  // may launch forwards on different devices)
+  constexpr int kMaxDev = 64;
+  static std::mutex mu;
+  static int dev_sms[kMaxDev], dev_occ[kMaxDev][2];
+  int dev = 0, sms = 0, occ[2] = {0, 0};
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0) return cudaErrorInvalidDevice;
+  {
+    std::lock_guard<std::mutex> lock(mu);
+    if (dev >= kMaxDev || dev_sms[dev] == 0) {
+      if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
+          cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ[0], k_combine<false>, kCombThreads, 0) != cudaSuccess ||
+          cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ[1], k_combine<true>, kCombThreads, 0) != cudaSuccess)
+        return cudaErrorUnknown;
+      if (dev < kMaxDev) {
+        dev_sms[dev] = sms;
+        dev_occ[dev][0] = occ[0];
+        dev_occ[dev][1] = occ[1];
+      }
+    } else {
+      sms = dev_sms[dev];
+      occ[0] = dev_occ[dev][0];
+      occ[1] = dev_occ[dev][1];
+    }
   }
   const int gx = (H + kCombThreads * 8 - 1) / (kCombThreads * 8);
   const int gy = std::max(1, std::min(T, sms * std::max(1, occ[part_bf16 ? 1 : 0]) / gx));
@@ -139,7 +156,7 @@ cudaError_t launch_combine(const void *part, bool part_bf16, int H, const int32_
 // ------------------------------------------------------------------- packer
 //
 // One-time preparation of the experts (b12x project page, section "Using it":
-// "weights prepped once per model", fused_moe.prepare_weights).  The packed
+// fused_moe.prepare_weights, run once per model).  The packed
 // buffer holds W13 and W2 re-tiled for the tensor-core kernels (below) in
 // 256-byte aligned segments, and the global scales gathered into an [E][4]
 // FP32 table (gate|w1, up, down, 1); MXFP4 has no globals and gets 1.0.

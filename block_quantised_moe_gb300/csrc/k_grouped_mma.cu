@@ -1,8 +1,9 @@
 // Grouped expert contractions on the tensor cores with register-resident
 // dequantisation, for NVFP4 weights (any activation format).
 //
-// moe.fused_moe's "W4A16 (BF16 activations, inline FP4 weight dequant)" and its
-// decode path (b12x project page, section "What's in here").  At decode sizes an
+// moe.fused_moe's W4A16 mode (BF16 activations against FP4 weights dequantised
+// in the kernel) and its small-batch decode path (b12x project page, section
+// "What's in here").  At decode sizes an
 // expert sees a handful of tokens, so the layer is bound by streaming the
 // touched experts' packed bytes from HBM; the tensor cores only have to keep the
 // multiply-adds off the FP32 pipe.  Design:

@@ -643,22 +643,57 @@ __device__ __align__(256) uint8_t g_no_alloc_scratch[kNoAllocScratchBytes];
 
 constexpr int kNoAllocMaxDevices = 64;
 std::mutex g_no_alloc_mu;
-void *g_no_alloc_addr[kNoAllocMaxDevices];  // device address of the array, per device
+struct NoAllocSlot {
+  void *addr = nullptr;         // device address of the array in context `ctx`
+  unsigned long long ctx = 0;   // unique id of that context (0: unknown)
+};
+NoAllocSlot g_no_alloc[kNoAllocMaxDevices];
 
-// Device address of the array on the current device.  The first call on a
-// device looks it up with cudaGetSymbolAddress (with that device current); the
-// host-side symbol itself is only a stand-in and must never reach a kernel.
+// Unique id of the current CUDA context, through the driver entry points (the
+// library does not link the driver API); 0 if it cannot be had.  A device
+// reset or a torn-down primary context gives the next context a new id, so a
+// stale device address is never reused.
+unsigned long long current_ctx_id() {
+  using GetCurrent = int (*)(void **);
+  using GetId = int (*)(void *, unsigned long long *);
+  static GetCurrent get_current = nullptr;
+  static GetId get_id = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void *f = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &f, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      get_current = reinterpret_cast<GetCurrent>(f);
+    f = nullptr;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetId", &f, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      get_id = reinterpret_cast<GetId>(f);
+  });
+  void *ctx = nullptr;
+  unsigned long long id = 0;
+  if (!get_current || !get_id || get_current(&ctx) != 0 || ctx == nullptr || get_id(ctx, &id) != 0) return 0;
+  return id;
+}
+
+// Device address of the array in the current device's context.  The first
+// call in a context looks it up with cudaGetSymbolAddress (with that device
+// current); the host-side symbol itself is only a stand-in and must never
+// reach a kernel.
 moe_status no_alloc_scratch(void **out) {
   int dev = -1;
   if (cudaGetDevice(&dev) != cudaSuccess) return MOE_ERR_CUDA;
   if (dev < 0 || dev >= kNoAllocMaxDevices) return MOE_ERR_UNSUPPORTED;
   std::lock_guard<std::mutex> lock(g_no_alloc_mu);
-  if (g_no_alloc_addr[dev] == nullptr) {
+  NoAllocSlot &slot = g_no_alloc[dev];
+  const unsigned long long ctx = current_ctx_id();
+  if (slot.addr == nullptr || ctx == 0 || ctx != slot.ctx) {
     void *p = nullptr;
     if (cudaGetSymbolAddress(&p, g_no_alloc_scratch) != cudaSuccess || p == nullptr) return MOE_ERR_CUDA;
-    g_no_alloc_addr[dev] = p;
+    slot.addr = p;
+    slot.ctx = current_ctx_id();  // the lookup may have created the context
   }
-  *out = g_no_alloc_addr[dev];
+  *out = slot.addr;
   return MOE_OK;
 }
 
@@ -689,4 +724,18 @@ extern "C" moe_status moe_run_no_alloc(moe_plan_t plan, const void *packed, cons
   b.T = num_tokens;
   b.out = out;
   return run_impl(&b, stream, nullptr);
+}
+
+extern "C" moe_status moe_no_alloc_device_status(moe_plan_t plan, cudaStream_t stream, int32_t *status) {
+  if (!plan || !status) return MOE_ERR_INVALID_ARG;
+  void *scratch = nullptr;
+  moe_status st = no_alloc_scratch(&scratch);
+  if (st != MOE_OK) return st;
+  int32_t w[4] = {0, 0, 0, 0};
+  if (cudaMemcpyAsync(w, static_cast<uint8_t *>(scratch) + plan->S.status, sizeof w, cudaMemcpyDeviceToHost,
+                      stream) != cudaSuccess ||
+      cudaStreamSynchronize(stream) != cudaSuccess)
+    return MOE_ERR_CUDA;
+  for (int i = 0; i < 4; ++i) status[i] = w[i];
+  return (w[ST_FLAGS] & ST_FLAG_TIMEOUT) ? MOE_ERR_TIMEOUT : MOE_OK;
 }

@@ -2,36 +2,39 @@
  * moe.h -- C ABI of the GB300 (sm_103a) block-quantised fused MoE library.
  *
  * The operation is the fused routed-expert FFN over FP4 block-quantised expert
- * weights ("moe.fused_moe: fused FP4 MoE across a micro-kernel decode path, a
- * unified dynamic path ..., and W4A16 (BF16 activations, inline FP4 weight
- * dequant)", b12x project page (shadowgraph.io), section "What's in here"):
+ * weights: the pages' moe.fused_moe, which runs a small-batch decode path, a
+ * persistent-grid path and a W4A16 mode where BF16 activations meet FP4
+ * weights dequantised inside the kernel (b12x project page (shadowgraph.io),
+ * section "What's in here"):
  *
  *     y_t = sum_k  w_tk * W2_e( act( W13_e x^_t ) ),   e = topk_ids[t, k]
  *
  * with act = SiLU(gate) * up (gated) or max(., 0)^2 (non-gated ReLU^2; vLLM
- * docs "b12x Linear and MoE Backends", section "ModelOpt block codecs": routed
- * experts use bias-free SiLU or non-gated ReLU^2).  Supported formats follow
- * the same docs, section "Supported Configurations": NVFP4 weights with BF16,
- * NVFP4 or MXFP8 activations; MXFP4 weights with BF16 or MXFP8 activations.
+ * docs "b12x Linear and MoE Backends", section "ModelOpt block codecs": the
+ * routed experts carry no bias and use SiLU or a non-gated ReLU^2).  Supported
+ * formats follow the same docs, section "Supported Configurations": NVFP4
+ * weights with BF16, NVFP4 or MXFP8 activations; MXFP4 weights with BF16 or
+ * MXFP8 activations.
  *
  * The calls mirror the pages' plan -> scratch -> bind -> run contract (b12x
  * project page, section "Using it"):
  *
  *   moe_plan_weights    host only; decides the packed layout of the experts.
  *   moe_prepare_weights one-time repack of the checkpoint tensors into that
- *                       layout on the GPU ("weights prepped once per model").
+ *                       layout on the GPU (the pages prepare the weights once
+ *                       per model).
  *   moe_plan            host only; fixes every launch decision for a capacity
  *                       (max_tokens) and reports the scratch size.  Live token
  *                       counts are not part of a plan (b12x has moved to
  *                       FlashInfer, section "Technical layout and contracts":
- *                       keep live request counts out of compile keys, fixed
- *                       workspace capacity).
- *   moe_bind            host only; records pointers ("bind only narrows/views,
- *                       never allocates").
+ *                       the workspace has a fixed capacity and live request
+ *                       counts never enter a compile key).
+ *   moe_bind            host only; records pointers (on the pages, bind only
+ *                       makes views of caller tensors and never allocates).
  *   moe_run             launches the kernels on the caller's stream; it never
  *                       allocates, synchronises or compiles, so it can be
- *                       captured in a CUDA graph ("run* executes and is
- *                       CUDA-graph-capture safe").
+ *                       captured in a CUDA graph (the pages' run is safe under
+ *                       CUDA-graph capture).
  *
  * Ownership.  The caller owns all device memory: source weights, the packed
  * buffer, scratch, activations, ids, weights and the output.  The library owns
@@ -131,7 +134,7 @@ MOE_API moe_status moe_plan_weights(const moe_weight_desc *desc, moe_weight_plan
                             size_t *packed_bytes);
 
 /* Repack checkpoint tensors into `packed` (b12x project page, "Using it":
- * fused_moe.prepare_weights, weights prepped once per model).  All pointers
+ * fused_moe.prepare_weights, run once per model).  All pointers
  * are device pointers, read-only except `packed`.  Source layout (the
  * modelopt_nvfp4 reading: row-major, K contiguous, two E2M1 codes per byte,
  * element 2j in the low nibble):
@@ -279,15 +282,27 @@ MOE_API moe_status moe_selftest_wait_timeout(cudaStream_t stream, int32_t *statu
  *   - Plans whose scratch (moe_plan's scratch_bytes) exceeds
  *     MOE_NO_ALLOC_SCRATCH_BYTES are rejected with MOE_ERR_CAPACITY, as is
  *     num_tokens > max_tokens; bad pointers give MOE_ERR_INVALID_ARG.
- *   - The first call on a device looks up the array's device address (with
- *     that device current); make that first call before any stream capture.
+ *   - The first call in a CUDA context looks up the array's device address
+ *     (with that device current); make that first call before any stream
+ *     capture.  A device reset gives the device a new context, and the next
+ *     call looks the address up again.
  *   - All calls share the one array, which keeps the last call's contents; each
  *     call clears what must start at zero.  Calls that overlap on the GPU (other
  *     streams, other host threads) race on it: serialise them.
+ *   - Dropped ids and timed-out device waits are recorded in a status word
+ *     inside the array; read it with moe_no_alloc_device_status.
  * Asynchronous on `stream` like moe_run. */
 MOE_API moe_status moe_run_no_alloc(moe_plan_t plan, const void *packed, const void *x,
                                     const int32_t *topk_ids, const float *topk_weights,
                                     int32_t num_tokens, void *out, cudaStream_t stream);
+
+/* Status word of the last moe_run_no_alloc with tokens on the current device
+ * (no counterpart on the pages): copies it from the library's array to host
+ * `status[4]` and synchronises `stream`.  Same layout and return codes as
+ * moe_device_status: MOE_ERR_TIMEOUT when a bounded device wait gave up,
+ * otherwise MOE_OK (status[0] bit 0 and status[1] report dropped ids).
+ * `plan` is the plan of that call.  Allocates nothing. */
+MOE_API moe_status moe_no_alloc_device_status(moe_plan_t plan, cudaStream_t stream, int32_t *status);
 
 /* ------------------------------------------------------------ quantiser -- */
 

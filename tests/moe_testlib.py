@@ -36,22 +36,46 @@ def check_close(y: np.ndarray, y_ref: np.ndarray, what: str = "") -> dict:
 
 
 _ORACLE_EXPERT_CACHE: dict = {}
+# experts with at least this many weight elements are quantised in the oracle pool
+_POOL_MIN_ELEMS = 4 << 20
 
 
 def oracle_expert(E, H, I, wfmt, act, e, seed=0):
     """Oracle-quantised expert e: (codes13, scales13, g13, codes2, scales2, g2) as numpy."""
-    from oracle import quant
     key = (E, H, I, wfmt, act, e, seed)
     if key not in _ORACLE_EXPERT_CACHE:
-        gated = act == "silu"
-        w13, w2 = synth.make_expert_weights(e, H, I, gated, seed, device="cuda")
-        cs, ss, gs = [], [], []
-        for m in w13:
-            c, s, g = quant.quantize_weight_matrix(m.cpu().numpy(), wfmt)
-            cs.append(c), ss.append(s), gs.append(g)
-        c2, s2, g2 = quant.quantize_weight_matrix(w2.cpu().numpy(), wfmt)
-        _ORACLE_EXPERT_CACHE[key] = (np.concatenate(cs), np.concatenate(ss), gs, c2, s2, g2)
+        prefetch_oracle_experts(E, H, I, wfmt, act, [e], seed)
     return _ORACLE_EXPERT_CACHE[key]
+
+
+def prefetch_oracle_experts(E, H, I, wfmt, act, experts, seed=0):
+    """Quantise the listed experts with the oracle quantiser (in the worker pool
+    for large experts), from the same seeded FP32 draws as the GPU layer."""
+    import oracle_pool
+    gated = act == "silu"
+    missing = [int(e) for e in experts if (E, H, I, wfmt, act, int(e), seed) not in _ORACLE_EXPERT_CACHE]
+    if not missing:
+        return
+    if (3 if gated else 2) * H * I < _POOL_MIN_ELEMS or len(missing) == 1:
+        for e in missing:
+            w13, w2 = synth.make_expert_weights(e, H, I, gated, seed, device="cuda")
+            _ORACLE_EXPERT_CACHE[(E, H, I, wfmt, act, e, seed)] = oracle_pool.quantize_expert(
+                [m.cpu().numpy() for m in w13], w2.cpu().numpy(), wfmt)
+        return
+    ex = oracle_pool.pool()
+    inflight = {}
+    todo = list(missing)
+    while todo or inflight:
+        while todo and len(inflight) < 2 * oracle_pool.workers():
+            e = todo.pop(0)
+            w13, w2 = synth.make_expert_weights(e, H, I, gated, seed, device="cuda")
+            fut = ex.submit(oracle_pool.quantize_expert, [m.cpu().numpy() for m in w13], w2.cpu().numpy(), wfmt)
+            inflight[fut] = e
+        import concurrent.futures as cf
+        done, _ = cf.wait(list(inflight), return_when=cf.FIRST_COMPLETED)
+        for fut in done:
+            e = inflight.pop(fut)
+            _ORACLE_EXPERT_CACHE[(E, H, I, wfmt, act, e, seed)] = fut.result()
 
 
 def oracle_layer_for(ck, H, I, experts, seed=0, check_codes=True):
@@ -60,6 +84,7 @@ def oracle_layer_for(ck, H, I, experts, seed=0, check_codes=True):
     from oracle import moe
     E = ck.num_experts
     wfmt, act = ck.wfmt, ck.act
+    prefetch_oracle_experts(E, H, I, wfmt, act, experts, seed)
     parts = [oracle_expert(E, H, I, wfmt, act, int(e), seed) for e in experts]
     if check_codes:
         for e, (c13, s13, g13, c2, s2, g2) in zip(experts, parts):
@@ -81,20 +106,44 @@ def oracle_layer_for(ck, H, I, experts, seed=0, check_codes=True):
 
 
 def oracle_forward(ck, H, I, x, ids, w, afmt, tokens=None, seed=0):
-    """Oracle y for the given token rows (all by default), in FP32."""
+    """Oracle y for the given token rows (all by default), in FP32.  Large
+    layers run in the worker pool, a chunk of tokens per job (tokens are
+    independent in the oracle's definition)."""
     from oracle import moe
+    import oracle_pool
     x = x.float().cpu().numpy()
     ids = ids.cpu().numpy()
     w = w.cpu().numpy()
     if tokens is not None:
         x, ids, w = x[tokens], ids[tokens], w[tokens]
     E = ck.num_experts
-    used = np.unique(ids[(ids >= 0) & (ids < E)])
+    valid = (ids >= 0) & (ids < E)
+    used = np.unique(ids[valid])
+    prefetch_oracle_experts(E, H, I, ck.wfmt, ck.act, used, seed)
+    L = oracle_layer_for(ck, H, I, used, seed)
     remap = np.full(E, -1, np.int64)
     remap[used] = np.arange(len(used))
-    ids_c = np.where((ids >= 0) & (ids < E), remap[np.clip(ids, 0, E - 1)], -1)
-    L = oracle_layer_for(ck, H, I, used, seed)
-    return moe.moe_forward(x, ids_c, w, L, afmt)
+    ids_c = np.where(valid, remap[np.clip(ids, 0, E - 1)], -1)
+    T = x.shape[0]
+    big = H * I >= _POOL_MIN_ELEMS // 2 and T > 1
+    if not big:
+        return moe.moe_forward(x, ids_c, w, L, afmt)
+    n = min(T, oracle_pool.workers())
+    chunks = np.array_split(np.arange(T), n)
+    futs = []
+    for ch in chunks:
+        sub = ids_c[ch]
+        u = np.unique(sub[sub >= 0])
+        rm = np.full(len(used), -1, np.int64)
+        rm[u] = np.arange(len(u))
+        sub_c = np.where(sub >= 0, rm[np.clip(sub, 0, None)], -1)
+        Lc = moe.QuantLayer(
+            wfmt=L.wfmt, act=L.act, w13_codes=L.w13_codes[u], w13_scales=L.w13_scales[u],
+            w13_global=None if L.w13_global is None else L.w13_global[u],
+            w2_codes=L.w2_codes[u], w2_scales=L.w2_scales[u],
+            w2_global=None if L.w2_global is None else L.w2_global[u])
+        futs.append(oracle_pool.pool().submit(oracle_pool.forward_tokens, x[ch], sub_c, w[ch], Lc, afmt))
+    return np.concatenate([f.result() for f in futs], axis=0)
 
 
 def make_inputs(cfg, T, seed=0, device="cuda"):

@@ -108,7 +108,7 @@ def test_decode_zipf_e256_h7168(lib, T):
     ck, packed = gpu_layer(lib, cfg["E"], cfg["H"], cfg["I"], cfg["wfmt"], cfg["act"])
     x, ids, w = tl.make_inputs(cfg, T)
     out, _, _ = run(lib, packed, x, ids, w, cfg["K"], cfg["afmt"])
-    toks = tl.sample_tokens(T, 2)
+    toks = tl.sample_tokens(T, 16)
     y_ref = tl.oracle_forward(ck, cfg["H"], cfg["I"], x, ids, w, cfg["afmt"], tokens=toks)
     tl.check_close(out.float().cpu().numpy()[toks], y_ref, f"zipf T={T}")
 
@@ -122,11 +122,40 @@ def test_prefill_e256_h7168(lib, name, fp4_tiles):
     T = cfg["tokens"][0]
     x, ids, w = tl.make_inputs(cfg, T)
     out, _, _ = run(lib, packed, x, ids, w, cfg["K"], cfg["afmt"])
-    toks = tl.sample_tokens(T, 2, seed=1)
+    toks = tl.sample_tokens(T, 8, seed=1)
     y_ref = tl.oracle_forward(ck, cfg["H"], cfg["I"], x, ids, w, cfg["afmt"], tokens=toks)
     tl.check_close(out.float().cpu().numpy()[toks], y_ref, name)
     # every output row is finite and no row was left unwritten
     assert torch.isfinite(out.float()).all()
+
+
+# --------------------------------------- full-length K, every token compared
+
+FULL_K_MODES = [  # E, H, I, K, weights, activation, activations, FP4 tiles
+    (8, 7168, 2048, 4, "nvfp4", "silu", "bf16", False),
+    (8, 7168, 2048, 4, "nvfp4", "silu", "nvfp4", False),
+    (8, 7168, 2048, 4, "nvfp4", "silu", "mxfp8", False),
+    (8, 7168, 2048, 4, "nvfp4", "silu", "nvfp4", True),
+    (8, 4096, 1024, 4, "mxfp4", "relu2", "mxfp8", False),
+]
+
+
+@pytest.mark.parametrize("E,H,I,K,wfmt,act,afmt,fp4_tiles", FULL_K_MODES)
+def test_full_length_k_every_token(lib, E, H, I, K, wfmt, act, afmt, fp4_tiles):
+    # The large-layer shapes (112 or 64 k-blocks of 64 per GEMM1 tile, 32 or 16
+    # per GEMM2 tile) on 8 experts: 256 tokens x top-4 = 1024 pairs, about 128
+    # per expert, so every expert runs on the tcgen05 kernels and ragged
+    # 128-token tiles occur; every output element is compared with the oracle.
+    T = 256
+    ck, packed = gpu_layer(lib, E, H, I, wfmt, act, fp4_tiles=fp4_tiles)
+    cfg = dict(E=E, H=H, I=I, K=K, zipf=None)
+    x, ids, w = tl.make_inputs(cfg, T, seed=7)
+    counts = np.bincount(ids.cpu().numpy().reshape(-1), minlength=E)
+    assert counts.min() >= 32 and (counts % 128 != 0).any()
+    out, b, _ = run(lib, packed, x, ids, w, K, afmt)
+    assert b.device_status()[0] == 0
+    y_ref = tl.oracle_forward(ck, H, I, x, ids, w, afmt)
+    tl.check_close(out.float().cpu().numpy(), y_ref, f"full K {wfmt}/{act}/{afmt} tiles={fp4_tiles}")
 
 
 # ------------------------------------------- tcgen05 path (experts with many pairs)

@@ -19,6 +19,8 @@ CASES = [  # E, H, I, K, weights, activation, activations, T
     (16, 512, 256, 4, "nvfp4", "relu2", "nvfp4", 16),
     (8, 256, 512, 2, "nvfp4", "silu", "bf16", 600),
     (8, 256, 512, 2, "mxfp4", "relu2", "mxfp8", 600),
+    (8, 7168, 2048, 4, "nvfp4", "silu", "bf16", 256),   # full-length K on the tcgen05 kernel
+    (8, 4096, 1024, 4, "mxfp4", "relu2", "mxfp8", 256),
 ]
 
 

@@ -20,7 +20,12 @@ def setup():
     cfg = synth.CONFIGS["decode_e128_h2048_i768_k8"]
     ck = layer.make_experts_gpu(cfg["E"], cfg["H"], cfg["I"], cfg["wfmt"], cfg["act"])
     packed = layer.PackedLayer(ck, cfg["H"], cfg["I"])
+    packed.ck = ck
     return abi, layer, cfg, packed
+
+
+def packed_ck(setup):
+    return setup[3].ck
 
 
 def test_no_alloc_matches_moe_run_on_two_calls_in_a_row(setup):
@@ -30,13 +35,24 @@ def test_no_alloc_matches_moe_run_on_two_calls_in_a_row(setup):
     assert plan.scratch_bytes <= abi.MOE_NO_ALLOC_SCRATCH_BYTES
     for call, seed in enumerate((11, 12)):  # different inputs: stale scratch must not leak into call 2
         x, ids, w = tl.make_inputs(cfg, T, seed=seed)
+        if call == 1:
+            ids[0, 0] = cfg["E"] + 3  # one out-of-range id: dropped and counted in the status word
         ref = torch.empty(T, cfg["H"], dtype=torch.bfloat16, device="cuda")
         b = plan.bind(x, ids, w, ref)
         b.run()
+        rc_ref, st_ref = b.device_status()
         got = torch.full((T, cfg["H"]), float("nan"), dtype=torch.bfloat16, device="cuda")
         abi.moe_run_no_alloc(plan.handle, packed.packed, x, ids, w, T, got)
+        rc, st = abi.moe_no_alloc_device_status(plan.handle)
         torch.cuda.synchronize()
-        tl.check_close(got.float().cpu().numpy(), ref.float().cpu().numpy(), f"no-alloc call {call + 1}")
+        # same plan, kernels, launch order and inputs: the outputs are bit-identical
+        assert torch.equal(got, ref), f"no-alloc call {call + 1} differs from moe_run"
+        assert rc == abi.MOE_OK and rc_ref == abi.MOE_OK
+        assert st == st_ref == ([0, 0, 0, 0] if call == 0 else [1, 1, 0, 0])
+        # and both agree with the oracle
+        tl.check_close(got.float().cpu().numpy(),
+                       tl.oracle_forward(packed_ck(setup), cfg["H"], cfg["I"], x, ids, w, cfg["afmt"]),
+                       f"no-alloc call {call + 1}")
 
 
 def test_no_alloc_rejects_plans_beyond_its_scratch(setup):
