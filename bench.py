@@ -424,68 +424,78 @@ def measure(name, T, args, world, rank, layers, steps, headline=False):
     stream = torch.cuda.current_stream()
     torch.cuda.synchronize()
 
-    # The timed steps replay CUDA graphs of R forwards (one per replica, in
-    # rotation).  Up to 4 forwards of each of the NG graphs record per-stage
-    # events (external event nodes), so after the timed loop each event set
-    # holds the stage times of its forward in its graph's last replay.
+    # The timed steps replay CUDA graphs of forwards in replica rotation: one
+    # graph of L = min(steps, 64) forwards, replayed steps // L times, and one
+    # of the remaining steps % L, so exactly `steps` forwards run, with no
+    # instrumentation.  Per-stage times come from a second loop of the same
+    # forwards in which every forward records stage events (moe_run_timed,
+    # external event nodes); events split the programmatic overlap between the
+    # stages, so stage times slightly overstate kernel times.
     n_ev = abi.MOE_NUM_STAGES + 1
-    NG = 8
-    ev_fwd = sorted(set(int(i * R / min(R, 4)) for i in range(min(R, 4))))
-    ev_sets = {}
-    for j in range(NG):
-        for i in ev_fwd:
-            evs = [torch.cuda.Event(enable_timing=True) for _ in range(n_ev)]
-            for e in evs:
-                e.record(stream)  # creates the handles
-            ev_sets[(j, i)] = evs
+    L = max(1, min(steps, 64))
+    n_rep, rem = divmod(steps, L)
     for i in range(args.warmup):
         binds[i % R].run(stream)
     torch.cuda.synchronize()
     launches_per_fwd = abi.moe_launch_count(binds[0].handle)
     cap = torch.cuda.Stream()
-    graphs = []
-    with torch.cuda.stream(cap):
-        for j in range(NG):
-            g = torch.cuda.CUDAGraph()
+
+    def capture(n, first, ev_sets=None):
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.stream(cap):
             g.capture_begin()
-            for i in range(R):
-                if i in ev_fwd:
-                    abi.moe_run_timed(binds[i].handle, [e.cuda_event for e in ev_sets[(j, i)]], cap)
+            for i in range(n):
+                b = binds[(first + i) % R]
+                if ev_sets is not None:
+                    abi.moe_run_timed(b.handle, [e.cuda_event for e in ev_sets[i]], cap)
                 else:
-                    binds[i].run(cap)
+                    b.run(cap)
             g.capture_end()
-            graphs.append(g)
+        return g
+
+    g_main = capture(L, 0)
+    g_rem = capture(rem, (n_rep * L) % R) if rem else None
+    ev_sets = []
+    for _ in range(L):
+        evs = [torch.cuda.Event(enable_timing=True) for _ in range(n_ev)]
+        for e in evs:
+            e.record(stream)  # creates the handles
+        ev_sets.append(evs)
+    g_ev = capture(L, 0, ev_sets)
     torch.cuda.synchronize()
-    for g in graphs:  # upload and warm every graph
-        g.replay()
+    for g in (g_main, g_rem, g_ev):  # upload and warm every graph
+        if g is not None:
+            g.replay()
     torch.cuda.synchronize()
     barrier(world)
 
-    n_rep, rem = divmod(steps, R)
     start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     with ClockSampler() as clk:
         torch.cuda.synchronize()
         barrier(world)
         start.record(stream)
         for c in range(n_rep):
-            graphs[c % NG].replay()
-        for i in range(rem):
-            binds[i % R].run(stream)
+            g_main.replay()
+        if g_rem is not None:
+            g_rem.replay()
         end.record(stream)
         torch.cuda.synchronize()
         barrier(world)
+        # stage-timing loop: the same L forwards, each with its stage events
+        g_ev.replay()
+        torch.cuda.synchronize()
     ms = max_over_ranks(start.elapsed_time(end), world)
     value = job_throughput(T * steps, world, ms / 1e3)
 
-    used = [(j, i) for j in range(min(NG, n_rep)) for i in ev_fwd]
+    used = list(range(L))
     stage_ms = np.zeros(abi.MOE_NUM_STAGES)
-    for key in used:
-        evs = ev_sets[key]
+    for i in used:
+        evs = ev_sets[i]
         for s_ in range(abi.MOE_NUM_STAGES):
             stage_ms[s_] += evs[s_].elapsed_time(evs[s_ + 1])
-    stage_ms /= max(1, len(used))
+    stage_ms /= len(used)
     # touched experts of the forwards whose events are used
-    tch_ev = float(np.mean([touched[i] for (_, i) in used])) if used else float(np.mean(touched))
+    tch_ev = float(np.mean([touched[i % R] for i in used]))
     layer_bytes, kernel_bytes, kernel_flops, flops = algorithmic(cfg, T, tch_ev)
     layer_bytes_all, _, _, _ = algorithmic(cfg, T, float(np.mean(touched)))
     roof = roofline_of(stage_ms, kernel_bytes, kernel_flops, cfg, afmt, T * K)
@@ -507,8 +517,8 @@ def measure(name, T, args, world, rank, layers, steps, headline=False):
         "stage_us": {n: round(1e3 * v, 3) for n, v in zip(abi.STAGES, stage_ms)},
         "roofline": roof,
         "gpu_launches": steps * launches_per_fwd,
-        "timing": f"CUDA graphs of {R} forwards replayed; stage events from {len(used)} forwards inside the "
-                  "timed region (the last replay of each graph)",
+        "timing": f"CUDA graph replays of {steps} forwards over {R} layer replica(s), uninstrumented; "
+                  f"stage events from a second replay of {len(used)} instrumented forwards right after",
         "clocks": clk.summary(),
     }
     prof = PROFILES.get(name)
@@ -538,7 +548,7 @@ def measure(name, T, args, world, rank, layers, steps, headline=False):
                       "h2d_bytes_per_step": T * H * 2 + T * K * 8, "d2h_bytes_per_step": T * H * 2,
                       "steps": n_e2e}
         row["_sample"] = (cfg, xs[0], idss[0], ws[0])
-    del graphs, binds, packed, plan
+    del g_main, g_rem, g_ev, binds, packed, plan
     torch.cuda.synchronize()
     torch.cuda.empty_cache()
     return row

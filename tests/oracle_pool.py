@@ -55,6 +55,6 @@ def quantize_expert(mats13, w2, wfmt):
 
 
 def forward_tokens(x, ids_c, w, layer, afmt):
-    """Oracle forward of a chunk of token rows."""
-    from oracle import moe
-    return moe.moe_forward(x, ids_c, w, layer, afmt)
+    """Oracle forward of a chunk of token rows, with its re-quantisation envelope."""
+    import requant_envelope
+    return requant_envelope.forward_with_envelope(x, ids_c, w, layer, afmt)
