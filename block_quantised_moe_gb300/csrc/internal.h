@@ -139,6 +139,11 @@ cudaError_t launch_stage_x16(int src, const void *act, const uint8_t *act_scales
 // or MXFP4 weights (BF16 operands), both from the packed fragment layout.
 bool tc_supported(int rows_total, int K);
 cudaError_t launch_grouped_tc(int stage, int wfmt, const GroupedArgs &a, int rows_total, int E, cudaStream_t s);
+// The same contractions on CTA pairs (tcgen05.mma.cta_group::2, M = 256, token
+// tiles of up to 256 from routing's large_tile = 256 prefix): rows_total a
+// multiple of 256.
+bool tc2_supported(int rows_total, int K);
+cudaError_t launch_grouped_tc2(int stage, int wfmt, const GroupedArgs &a, int rows_total, cudaStream_t s);
 // Block-scaled FP4 tcgen05 kernel for NVFP4 weights with NVFP4 activations (the
 // weights' FP4 tiles; a.act / act_scales / act_g = the quantised activations).
 bool fp4_tc_supported(int rows_total, int K);

@@ -25,6 +25,7 @@ struct moe_plan_s {
   int K = 0, max_tokens = 0, afmt = 0, pad = 16;
   bool tc_on = false;  // experts with >= large_min pairs run on the tcgen05 kernel
   bool fp4_on = false; // ... on the block-scaled FP4 kernel (W4A4 with the weights' FP4 tiles)
+  bool tc2_on = false; // ... otherwise on the CTA-pair kernel (token tiles of up to 256)
   int large_min = 0x7FFFFFFF;
   ScratchLayout S;
 };
@@ -170,6 +171,7 @@ moe_status moe_plan(const moe_caps *c, moe_plan_t *out, size_t *scratch_bytes, i
   P.fp4_on = P.tc_on && P.afmt == MOE_A_NVFP4 && L.fp4_tiles && fp4_tc_supported(L.n13, L.H) &&
              fp4_tc_supported(L.H, L.I);
   if (P.fp4_on) P.pad = kFp4Tile;
+  P.tc2_on = P.tc_on && !P.fp4_on && tc2_supported(L.n13, L.H) && tc2_supported(L.H, L.I);
   S.cap_sorted = round_up(Pmax + (int64_t)L.E * (P.pad - 1), P.pad);
   size_t o = 0;
   auto take = [&](size_t bytes) {
@@ -309,7 +311,8 @@ static moe_status run_forward(moe_binding b, cudaStream_t stream, cudaEvent_t *e
   RouteStaging stg{static_cast<const __nv_bfloat16 *>(b->x), T, H, at<__half>(sc, S.x16), at<float>(sc, S.xfac),
                    at<float>(sc, S.hamax), S.cap_sorted};
   const bool staged = P.afmt == MOE_A_BF16;
-  if ((err = launch_route(b->ids, T * K, E, P.pad, ntok, P.large_min, 128, counts, offsets, sorted, pair_pos, active,
+  if ((err = launch_route(b->ids, T * K, E, P.pad, ntok, P.large_min, P.tc2_on ? 256 : 128, counts, offsets, sorted,
+                          pair_pos, active,
                           passes, large, large_tiles, status, at<int32_t>(sc, S.route_hist), at<int32_t>(sc, S.work),
                           2 * kWorkSlots, staged ? &stg : nullptr,
                           stream)) != cudaSuccess)
@@ -398,7 +401,8 @@ static moe_status run_forward(moe_binding b, cudaStream_t stream, cudaEvent_t *e
         t.act = at<__half>(sc, S.xb16);
         t.act_g = nullptr;
       }
-      err = launch_grouped_tc(stage1, L.wfmt, t, L.n13, E, stream);
+      err = P.tc2_on ? launch_grouped_tc2(stage1, L.wfmt, t, L.n13, stream)
+                     : launch_grouped_tc(stage1, L.wfmt, t, L.n13, E, stream);
     }
   }
   a.out_amax = nullptr;
@@ -458,7 +462,8 @@ static moe_status run_forward(moe_binding b, cudaStream_t stream, cudaEvent_t *e
     t.act_scales = nullptr;
     t.act_g = nv ? at<float>(sc, S.h16fac) : nullptr;
     t.act_by_token = 0;
-    err = launch_grouped_tc(STAGE_DOWN, L.wfmt, t, H, E, stream);
+    err = P.tc2_on ? launch_grouped_tc2(STAGE_DOWN, L.wfmt, t, H, stream)
+                   : launch_grouped_tc(STAGE_DOWN, L.wfmt, t, H, E, stream);
   }
   if (err != cudaSuccess) return MOE_ERR_CUDA;
   if (mark(MOE_STAGE_COMBINE) != cudaSuccess) return MOE_ERR_CUDA;
