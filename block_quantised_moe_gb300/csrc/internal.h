@@ -56,6 +56,7 @@ struct ScratchLayout {
   size_t h16 = 0, h16fac = 0;           // tcgen05 path: 16-bit h rows (and their FP16 factors)
   size_t xb16 = 0;                      // tcgen05 path, MXFP4: BF16 slot-order x rows
   size_t xt = 0, ht = 0;                // FP4 path: x^ / h^ as slot-major 128-row tiles (codes + scales)
+  size_t xs16 = 0;                      // CTA-pair path: GEMM1's 16-bit x rows gathered into slot order
   size_t part = 0, total = 0;
 };
 
@@ -135,15 +136,20 @@ cudaError_t launch_grouped_mma(int wfmt, int src, int stage, const GroupedArgs &
 cudaError_t launch_stage_x16(int src, const void *act, const uint8_t *act_scales, const float *act_g, int T, int K,
                              __half *x16, float *fac, float *zero, int64_t zero_n, cudaStream_t s);
 
-// tcgen05 kernels for experts with many pairs: NVFP4 weights (FP16 operands)
-// or MXFP4 weights (BF16 operands), both from the packed fragment layout.
-bool tc_supported(int rows_total, int K);
-cudaError_t launch_grouped_tc(int stage, int wfmt, const GroupedArgs &a, int rows_total, int E, cudaStream_t s);
-// The same contractions on CTA pairs (tcgen05.mma.cta_group::2, M = 256, token
-// tiles of up to 256 from routing's large_tile = 256 prefix): rows_total a
-// multiple of 256.
+// tcgen05 kernels for experts with many pairs, on CTA pairs
+// (tcgen05.mma.cta_group::2, M = 256, token tiles of up to 256 from routing's
+// large_tile = 256 prefix): NVFP4 weights (FP16 operands) or MXFP4 weights
+// (BF16 operands), both from the packed fragment layout; rows_total a multiple
+// of 256.
 bool tc2_supported(int rows_total, int K);
-cudaError_t launch_grouped_tc2(int stage, int wfmt, const GroupedArgs &a, int rows_total, cudaStream_t s);
+// a.act: the activation rows in slot order, b_rows of a.K 16-bit values (GEMM1:
+// x gathered with launch_gather_slot_rows; GEMM2: h16).
+cudaError_t launch_grouped_tc2(int stage, int wfmt, const GroupedArgs &a, int rows_total, int64_t b_rows,
+                               cudaStream_t s);
+// dst[s] = src[sorted[s] / top_k] (rows of cols16 16-bit values) for the live
+// slots s < *n_live; padding slots are skipped.
+cudaError_t launch_gather_slot_rows(const void *src, const int32_t *sorted, const int32_t *n_live, int top_k,
+                                    int cols16, int64_t cap_rows, void *dst, cudaStream_t s);
 // Block-scaled FP4 tcgen05 kernel for NVFP4 weights with NVFP4 activations (the
 // weights' FP4 tiles; a.act / act_scales / act_g = the quantised activations).
 bool fp4_tc_supported(int rows_total, int K);

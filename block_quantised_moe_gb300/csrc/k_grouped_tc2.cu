@@ -6,38 +6,45 @@
 // here").  The contraction of an expert is a dense GEMM once it sees more than
 // a few dozen tokens.  On one SM an M=128 N=128 K=16 MMA reads 8 KB of
 // operands from shared memory while the producers write the dequantised
-// weight tile and the gathered activation tile through the same port, so a
-// single-CTA kernel is held by shared-memory bandwidth well below the tensor
-// pipe's rate.  Here two CTAs of a cluster form one MMA: each holds 128 weight
-// rows (its A half) and half of the token tile (its B half), and the leader
-// CTA issues M=256 N<=256 K=16 MMAs that read both CTAs' shared memory, so
-// every byte written to shared memory feeds twice the FLOPs:
+// weight tile and the activation tile through the same port, so a single-CTA
+// kernel is held by shared-memory bandwidth well below the tensor pipe's rate.
+// Here two CTAs of a cluster form one MMA: each holds 128 weight rows (its A
+// half) and half of the token tile (its B half), and the leader CTA issues
+// M=256 N<=256 K=16 MMAs that read both CTAs' shared memory, so every byte
+// written to shared memory feeds twice the FLOPs:
 //
 //   D[256 weight rows x N tokens] += A[256 x 64] * B[N x 64]^T per 64-K block
 //
 // * A: each CTA's 128-row block of the packed experts (the same fragment-order
-//   bytes the decode kernel streams), loaded four k-blocks ahead into
-//   registers by eight producer warps, dequantised to FP16 (NVFP4: E2M1 x E4M3
-//   is exact) or BF16 (MXFP4: E2M1 x 2^X is exact) and written in the UMMA
-//   K-major 128-byte-swizzled layout.
-// * B: N/2 activation rows per CTA (FP16 slot-order rows with a power-of-two
-//   factor, or BF16), gathered by two producer warps with cp.async and
-//   zero-filled past the tile's last token.
+//   bytes the decode kernel streams), loaded into registers four of its
+//   k-blocks ahead by eight producer warps in two groups that produce
+//   alternate k-blocks (one warp's chain of conversions, stores and proxy
+//   fence per k-block is latency bound), dequantised to FP16 (NVFP4: E2M1 x
+//   E4M3 is exact) or BF16 (MXFP4: E2M1 x 2^X is exact) and written in the
+//   UMMA K-major 128-byte-swizzled layout; a 6-stage ring.
+// * B: the tile's activation rows are consecutive slots of the expert-sorted
+//   list (GEMM1's x rows are gathered into slot order beforehand, GEMM2's h
+//   rows already are), so a CTA's B half of a k-block is one 2-D tensor copy
+//   (TMA, 128 rows x 64 columns, 128-byte swizzle); a 6-stage ring.
 // * Token tiles: an expert with c pairs is cut into ceil(c / 256) tiles of
 //   equal size (rounded up to 16), so no tile is a nearly empty remainder;
 //   the MMA's N is the tile's size rounded up to 16.
-// * The leader's MMA thread waits for both CTAs' producers (they arrive on the
-//   leader's mbarriers across the cluster), issues 4 MMAs per k-block into one
-//   of two TMEM accumulators (2 x 256 columns) and releases the stages of both
-//   CTAs with a multicast tcgen05.commit; each CTA's four epilogue warps read
-//   their 128 rows of the accumulator (SiLU(gate)*up, ReLU^2, or the
-//   topk_weight scaling of the down projection) while the next tile's MMAs run.
+// * A relay thread in each CTA turns "this CTA's operands of a k-block are in
+//   shared memory" into one arrival on the leader's ready barrier; the
+//   leader's MMA thread waits on that one barrier, issues 4 MMAs into one of
+//   two TMEM accumulators (2 x 256 columns) and releases both CTAs' stages
+//   with multicast tcgen05.commits.  Each CTA's four epilogue warps read their
+//   128 rows of the accumulator (SiLU(gate)*up, ReLU^2, or the topk_weight
+//   scaling of the down projection) while the next tile's MMAs run.
 // * Work items are (large expert, token tile, pair of 128-row blocks), dealt
 //   round-robin over persistent clusters (one CTA per SM).
 // * Every wait is a bounded mbarrier wait; on a timeout the kernel sets the
 //   status flag, every CTA still reaches the final cluster barrier, and the
 //   leader drains its MMAs before the pair's tensor memory is released.
 #include <algorithm>
+#include <mutex>
+#include <cstdio>
+#include <cstdlib>
 
 #include "common.cuh"
 #include "dequant.cuh"
@@ -45,26 +52,32 @@
 #include "launch.h"
 #include "sync.cuh"
 #include "tcgen05.cuh"
+#include "tmap.h"
 
 namespace bqmoe {
 
-constexpr int k2EpiWarps = 4, k2AWarps = 8, k2BWarps = 2;
-constexpr int k2MmaWarp = k2EpiWarps + k2AWarps + k2BWarps;  // warp 14
-constexpr int k2Threads = (k2MmaWarp + 1) * 32;
+constexpr int k2EpiWarps = 4, k2AWarps = 8, k2BWarps = 1;
+constexpr int k2MmaWarp = k2EpiWarps + k2AWarps + k2BWarps;  // warp 13
+constexpr int k2RelayWarp = k2MmaWarp + 1;                     // warp 14
+constexpr int k2Threads = (k2RelayWarp + 1) * 32;
 constexpr int k2MaxN = 256;                 // tokens per pair tile
 constexpr int k2HalfRows = k2MaxN / 2;      // B rows per CTA
 constexpr int k2ABytes = 128 * 64 * 2;      // one 128 x 64 16-bit block
 constexpr int k2BBytes = k2HalfRows * 64 * 2;
-constexpr int k2AStages = 4;
+// Separate rings for the two operands: the weight tiles are produced from
+// registers a few k-blocks ahead, while the activation tiles come from global
+// memory by tensor copies whose latency needs a deeper ring.
+constexpr int k2AStages = 6;
 constexpr int k2BStages = 6;
-constexpr int k2BLag = 4;                   // cp.async stages a B thread keeps in flight
-constexpr int k2APrefetch = 4;              // k-blocks of packed A bytes an A thread keeps in flight
+constexpr int k2RStages = 8;                // ready barriers (both CTAs' operands of a k-block), by k-block
+constexpr int k2APrefetch = 4;              // k-blocks of its group's packed A bytes an A thread keeps in flight
+constexpr int k2AGroups = 2;                // A warp groups producing alternate k-blocks
+constexpr int k2AThreadsPerGroup = k2AWarps * 32 / k2AGroups;
 constexpr int k2RingBytes = k2AStages * k2ABytes + k2BStages * k2BBytes;
 constexpr int k2AccCols = k2MaxN;           // TMEM columns per accumulator buffer
 constexpr int k2TmemCols = 2 * k2AccCols;   // double buffered
-constexpr int k2BRows = k2HalfRows * 8 / (k2BWarps * 32);  // 16-byte chunks per B thread per k-block
-constexpr int k2Bars = 2 * k2AStages + 2 * k2BStages + 4 + 1;
-static_assert(k2AWarps * 32 == 8 * 32, "one fragment chunk per A thread per k-block");
+constexpr int k2Bars = 2 * k2AStages + 2 * k2BStages + k2RStages + 4 + 1;
+static_assert(k2AWarps * 32 == 256 && 256 % (k2AGroups * 32) == 0, "8 fragment chunks per k-block over the A groups");
 
 // ------------------------------------------------------------ cluster helpers
 
@@ -112,6 +125,19 @@ __device__ __forceinline__ bool mbar_wait_c(uint32_t bar, uint32_t parity) {
     if ((it & 255u) == 0 && globaltimer_ns() - t0 > kWaitNs) return false;
   }
 }
+// 2-D tiled tensor copy global -> shared with completion (bytes) on `bar`.
+__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap *map, int x, int y, uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];" ::"r"(
+          dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(bar)
+      : "memory");
+}
+// Arrive on `bar` once all of this thread's earlier cp.async copies have landed
+// (the arrival is not counted in advance: the barrier's count includes it).
+__device__ __forceinline__ void cp_async_arrive_noinc(uint32_t bar) {
+  asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(bar) : "memory");
+}
 __device__ __forceinline__ void cluster_sync_all() {
   asm volatile("barrier.cluster.arrive.release;\n\tbarrier.cluster.wait.acquire;" ::: "memory");
 }
@@ -130,6 +156,57 @@ __device__ __forceinline__ void tc2_commit_both(uint32_t bar) {
       "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;" ::"r"(bar),
       "h"((uint16_t)3)
       : "memory");
+}
+
+// One fragment chunk of a packed 64-K step (16 code bytes of lane `ln` of
+// 16-row tile `tile`, and the lane group's block scales), dequantised to
+// 16-bit values (NVFP4: E2M1 x E4M3 in FP16, exact; MXFP4: E2M1 x 2^X in BF16,
+// exact) and stored at its slot positions in the 128-byte-swizzled K-major tile.
+template <int WF>
+__device__ __forceinline__ void dequant_chunk_store(uint8_t *tileA, uint4 cch, uint2 sch, int tile, int ln) {
+  const int g = ln >> 2, c4 = ln & 3;
+  const int r0 = 16 * tile + g, r1 = r0 + 8;
+  const uint32_t cw[4] = {cch.x, cch.y, cch.z, cch.w};
+  uint32_t o[4][4];  // 16-bit pairs of mma j: (r0, k), (r1, k), (r0, k + 8), (r1, k + 8)
+  if (WF == W_NVFP4) {
+    uint32_t sp[4];
+    e4m3x4_to_f16x2x2(sch.x, sp[0], sp[1]);
+    e4m3x4_to_f16x2x2(sch.y, sp[2], sp[3]);
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const uint32_t s_lo = sp[2 * (j >> 1)], s_hi = sp[2 * (j >> 1) + 1];
+      uint32_t af[4];
+      e2m1x8_to_f16x2x4(cw[j], af);
+      o[j][0] = hmul2(af[0], s_lo);
+      o[j][1] = hmul2(af[1], s_hi);
+      o[j][2] = hmul2(af[2], s_lo);
+      o[j][3] = hmul2(af[3], s_hi);
+    }
+  } else {
+    const uint32_t sw = sch.x;  // (r0 block 0, r0 block 1, r1 block 0, r1 block 1)
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const float s_lo = e8m0_to_f32((sw >> (8 * (j >> 1))) & 0xFFu);
+      const float s_hi = e8m0_to_f32((sw >> (16 + 8 * (j >> 1))) & 0xFFu);
+      uint32_t af[4];
+      e2m1x8_to_f16x2x4(cw[j], af);
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        const float2 v = __half22float2(*reinterpret_cast<const __half2 *>(&af[q]));
+        const float sc = (q & 1) ? s_hi : s_lo;
+        __nv_bfloat162 b2 = __floats2bfloat162_rn(v.x * sc, v.y * sc);
+        o[j][q] = *reinterpret_cast<uint32_t *>(&b2);
+      }
+    }
+  }
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    const int k = 16 * j + 2 * c4;
+    *reinterpret_cast<uint32_t *>(tileA + sw128_elem(r0, k)) = o[j][0];
+    *reinterpret_cast<uint32_t *>(tileA + sw128_elem(r1, k)) = o[j][1];
+    *reinterpret_cast<uint32_t *>(tileA + sw128_elem(r0, k + 8)) = o[j][2];
+    *reinterpret_cast<uint32_t *>(tileA + sw128_elem(r1, k + 8)) = o[j][3];
+  }
 }
 
 // ------------------------------------------------------------------ work items
@@ -172,7 +249,8 @@ struct Tc2Cursor {
 // ------------------------------------------------------------------ kernel
 
 template <int STAGE, int WF>
-__global__ void __launch_bounds__(k2Threads, 1) k_grouped_tc2(const GroupedArgs a) {
+__global__ void __launch_bounds__(k2Threads, 1) k_grouped_tc2(const GroupedArgs a,
+                                                              const __grid_constant__ CUtensorMap bmap) {
   extern __shared__ uint8_t smem_raw[];
   // 1024-byte aligned base for the swizzled tiles (the same offset in both CTAs)
   const uint32_t raw_s = (uint32_t)__cvta_generic_to_shared(smem_raw);
@@ -181,26 +259,28 @@ __global__ void __launch_bounds__(k2Threads, 1) k_grouped_tc2(const GroupedArgs 
   const uint32_t ringA = base_s, ringB = base_s + k2AStages * k2ABytes;
   uint64_t *bars = reinterpret_cast<uint64_t *>(base + k2RingBytes);
   uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + k2Bars);
-  const uint32_t afull0 = (uint32_t)__cvta_generic_to_shared(bars);
-  const uint32_t aempty0 = afull0 + 8u * k2AStages;
-  const uint32_t bfull0 = aempty0 + 8u * k2AStages;
-  const uint32_t bempty0 = bfull0 + 8u * k2BStages;
-  const uint32_t tfull0 = bempty0 + 8u * k2BStages;  // 2
-  const uint32_t tempty0 = tfull0 + 16u;             // 2
-  const uint32_t drain = tempty0 + 16u;              // 1
+  const uint32_t afull0 = (uint32_t)__cvta_generic_to_shared(bars);  // this CTA's A tile is written
+  const uint32_t aempty0 = afull0 + 8u * k2AStages;                  // the pair's MMAs have read the A stage
+  const uint32_t bfull0 = aempty0 + 8u * k2AStages;                  // this CTA's B tile has landed
+  const uint32_t bempty0 = bfull0 + 8u * k2BStages;                  // the pair's MMAs have read the B stage
+  const uint32_t ready0 = bempty0 + 8u * k2BStages;                  // leader: both CTAs' operands are ready
+  const uint32_t tfull0 = ready0 + 8u * k2RStages;                   // 2
+  const uint32_t tempty0 = tfull0 + 16u;                             // 2
+  const uint32_t drain = tempty0 + 16u;                              // 1
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const uint32_t rank = cluster_rank();  // 0: leader (issues the MMAs), 1: peer
   pdl_trigger();
   if (threadIdx.x == 0) {
     for (int i = 0; i < k2AStages; ++i) {
-      mbar_init(afull0 + 8u * i, 2 * k2AWarps);
+      mbar_init(afull0 + 8u * i, k2AWarps / k2AGroups);
       mbar_init(aempty0 + 8u * i, 1);
     }
     for (int i = 0; i < k2BStages; ++i) {
-      mbar_init(bfull0 + 8u * i, 2 * k2BWarps);
+      mbar_init(bfull0 + 8u * i, 1);
       mbar_init(bempty0 + 8u * i, 1);
     }
+    for (int i = 0; i < k2RStages; ++i) mbar_init(ready0 + 8u * i, 2);
     for (int b = 0; b < 2; ++b) {
       mbar_init(tfull0 + 8u * b, 1);
       mbar_init(tempty0 + 8u * b, 2 * k2EpiWarps);
@@ -235,32 +315,43 @@ __global__ void __launch_bounds__(k2Threads, 1) k_grouped_tc2(const GroupedArgs 
 
   if (warp >= k2EpiWarps && warp < k2EpiWarps + k2AWarps) {
     // ------------------------------------------------------ A producers
-    // Lane t holds fragment chunk t of the k-block (16-row tile t / 32, lane
-    // t % 32): 16 code bytes and its lane group's block scales, dequantised to
-    // 16-bit values written at their slot positions in the swizzled tile.
+    // The A warps form k2AGroups groups; group q produces the k-blocks n with
+    // n % k2AGroups == q, so several stages are dequantised at once (one
+    // warp's chain of conversions, stores and fence per k-block is latency
+    // bound).  Thread tg of a group holds fragment chunks tg + 128 i of its
+    // k-blocks (16-row tile chunk / 32, lane chunk % 32): 16 code bytes and the
+    // lane group's block scales, dequantised to 16-bit values written at their
+    // slot positions in the swizzled tile.
     constexpr int SB = WF == W_NVFP4 ? 4608 : 4352;  // bytes of one 64-K step of a block
+    constexpr int CPT = k2AGroups;                   // chunks per thread per k-block
     const int t = threadIdx.x - k2EpiWarps * 32;    // 0..255
-    const int tile = t >> 5, ln = t & 31;
-    const int g = ln >> 2, c4 = ln & 3;
-    const int r0 = 16 * tile + g, r1 = r0 + 8;
-    const uint32_t afull_leader = mapa(afull0, 0);
-    int slot = 0;
-    uint32_t phase = 0;
-    uint4 pch[k2APrefetch];
-    uint2 psc[k2APrefetch];
-    auto load = [&](const Tc2Item &it, int kb, uint4 &c, uint2 &s) {
+    const int grp = t / (k2AThreadsPerGroup), tg = t % k2AThreadsPerGroup;
+    const int ln = tg & 31;
+    // Software pipeline over the group's k-blocks of this cluster's flat
+    // (item, k-block) sequence: register slot d holds the packed bytes of the
+    // group's step i with i % k2APrefetch = d, loaded k2APrefetch steps ahead
+    // (possibly from a later item).  The slots are indexed statically (the
+    // loop is unrolled by the depth), so no register move ever waits on a
+    // younger load than the one being consumed.
+    uint4 pch[k2APrefetch][CPT];
+    uint2 psc[k2APrefetch][CPT];
+    auto load = [&](const Tc2Item &it, int kb, uint4 (&c)[CPT], uint2 (&sc)[CPT]) {
       const int blk = 2 * it.bp + (int)rank;
       const uint8_t *step = a.codes + (size_t)it.e * a.codes_expert + ((size_t)blk * nk + kb) * SB;
-      c = __ldg(reinterpret_cast<const uint4 *>(step + tile * 512 + ln * 16));
-      if (WF == W_NVFP4) s = __ldg(reinterpret_cast<const uint2 *>(step + 4096 + tile * 64 + (ln >> 2) * 8));
-      else s = make_uint2(__ldg(reinterpret_cast<const uint32_t *>(step + 4096 + tile * 32 + (ln >> 2) * 4)), 0u);
+#pragma unroll
+      for (int i = 0; i < CPT; ++i) {
+        const int tile = (tg >> 5) + (k2AThreadsPerGroup / 32) * i;
+        c[i] = __ldg(reinterpret_cast<const uint4 *>(step + tile * 512 + ln * 16));
+        if (WF == W_NVFP4) sc[i] = __ldg(reinterpret_cast<const uint2 *>(step + 4096 + tile * 64 + (ln >> 2) * 8));
+        else sc[i] = make_uint2(__ldg(reinterpret_cast<const uint32_t *>(step + 4096 + tile * 32 + (ln >> 2) * 4)), 0u);
+      }
     };
-    Tc2Cursor pcur = cur;  // cursor of the prefetch (k2APrefetch k-blocks ahead)
+    Tc2Cursor pcur = cur;  // cursor of the prefetch
     int pw = w0, pkb = 0;
     bool pv = pw < W;
     Tc2Item pit;
     if (pv) pit = pcur.at(a, pw, nbp);
-    auto advance = [&]() {
+    auto advance1 = [&]() {
       if (++pkb == nk) {
         pkb = 0;
         pw += wstep;
@@ -268,141 +359,91 @@ __global__ void __launch_bounds__(k2Threads, 1) k_grouped_tc2(const GroupedArgs 
         if (pv) pit = pcur.at(a, pw, nbp);
       }
     };
+    auto advance = [&]() {  // to the group's next k-block
+#pragma unroll
+      for (int q = 0; q < k2AGroups; ++q)
+        if (pv) advance1();
+    };
+    for (int q = 0; q < grp && pv; ++q) advance1();  // the group's first k-block
 #pragma unroll
     for (int d = 0; d < k2APrefetch; ++d) {
       if (pv) load(pit, pkb, pch[d], psc[d]);
       advance();
     }
-    for (int w = w0; w < W && ok; w += wstep) {
-      for (int kb = 0; kb < nk; ++kb) {
-        const uint4 cch = pch[0];
-        const uint2 sch = psc[0];
+    const int n_items = w0 < W ? (W - w0 + wstep - 1) / wstep : 0;
+    const int total = n_items * nk;
+    for (int n0 = grp; n0 < total && ok; n0 += k2APrefetch * k2AGroups) {
 #pragma unroll
-        for (int d = 0; d + 1 < k2APrefetch; ++d) {
-          pch[d] = pch[d + 1];
-          psc[d] = psc[d + 1];
+      for (int d = 0; d < k2APrefetch; ++d) {
+        const int n = n0 + d * k2AGroups;  // k-block of this step
+        if (n >= total) break;
+        uint4 cch[CPT];
+        uint2 sch[CPT];
+#pragma unroll
+        for (int i = 0; i < CPT; ++i) {
+          cch[i] = pch[d][i];
+          sch[i] = psc[d][i];
         }
-        if (pv) load(pit, pkb, pch[k2APrefetch - 1], psc[k2APrefetch - 1]);
+        if (pv) load(pit, pkb, pch[d], psc[d]);
         advance();
-        if (!mbar_wait_c(aempty0 + 8u * slot, phase ^ 1u)) {
+        const int slot = n % k2AStages;
+        const uint32_t phase = (uint32_t)(n / k2AStages) & 1u;
+        if (!mbar_wait(aempty0 + 8u * slot, phase ^ 1u)) {
           ok = false;
           break;
         }
         uint8_t *tileA = base + (size_t)slot * k2ABytes;
-        const uint32_t cw[4] = {cch.x, cch.y, cch.z, cch.w};
-        uint32_t o[4][4];  // 16-bit pairs of mma j: (r0, k), (r1, k), (r0, k + 8), (r1, k + 8)
-        if (WF == W_NVFP4) {
-          uint32_t sp[4];
-          e4m3x4_to_f16x2x2(sch.x, sp[0], sp[1]);
-          e4m3x4_to_f16x2x2(sch.y, sp[2], sp[3]);
 #pragma unroll
-          for (int j = 0; j < 4; ++j) {
-            const uint32_t s_lo = sp[2 * (j >> 1)], s_hi = sp[2 * (j >> 1) + 1];
-            uint32_t af[4];
-            e2m1x8_to_f16x2x4(cw[j], af);
-            o[j][0] = hmul2(af[0], s_lo);
-            o[j][1] = hmul2(af[1], s_hi);
-            o[j][2] = hmul2(af[2], s_lo);
-            o[j][3] = hmul2(af[3], s_hi);
-          }
-        } else {
-          const uint32_t sw = sch.x;  // (r0 block 0, r0 block 1, r1 block 0, r1 block 1)
-#pragma unroll
-          for (int j = 0; j < 4; ++j) {
-            const float s_lo = e8m0_to_f32((sw >> (8 * (j >> 1))) & 0xFFu);
-            const float s_hi = e8m0_to_f32((sw >> (16 + 8 * (j >> 1))) & 0xFFu);
-            uint32_t af[4];
-            e2m1x8_to_f16x2x4(cw[j], af);
-#pragma unroll
-            for (int q = 0; q < 4; ++q) {
-              const float2 v = __half22float2(*reinterpret_cast<const __half2 *>(&af[q]));
-              const float sc = (q & 1) ? s_hi : s_lo;
-              __nv_bfloat162 b2 = __floats2bfloat162_rn(v.x * sc, v.y * sc);
-              o[j][q] = *reinterpret_cast<uint32_t *>(&b2);
-            }
-          }
-        }
-#pragma unroll
-        for (int j = 0; j < 4; ++j) {
-          const int k = 16 * j + 2 * c4;
-          *reinterpret_cast<uint32_t *>(tileA + sw128_elem(r0, k)) = o[j][0];
-          *reinterpret_cast<uint32_t *>(tileA + sw128_elem(r1, k)) = o[j][1];
-          *reinterpret_cast<uint32_t *>(tileA + sw128_elem(r0, k + 8)) = o[j][2];
-          *reinterpret_cast<uint32_t *>(tileA + sw128_elem(r1, k + 8)) = o[j][3];
-        }
+        for (int i = 0; i < CPT; ++i)
+          dequant_chunk_store<WF>(tileA, cch[i], sch[i], (tg >> 5) + (k2AThreadsPerGroup / 32) * i, ln);
         fence_async_smem();
         __syncwarp();
-        if (lane == 0) mbar_arrive_remote(afull_leader + 8u * slot);
-        if (++slot == k2AStages) {
-          slot = 0;
-          phase ^= 1u;
-        }
+        if (lane == 0) mbar_arrive(afull0 + 8u * slot);
       }
     }
   } else if (warp >= k2EpiWarps + k2AWarps && warp < k2MmaWarp) {
-    // ------------------------------------------------------ B producers
-    const int t = threadIdx.x - (k2EpiWarps + k2AWarps) * 32;  // 0..63
-    const int cc = t & 7;                                      // 16-byte chunk of the row
-    constexpr int kRowStep = k2BWarps * 32 / 8;                // rows between a thread's chunks
-    const bool by_token = a.act_by_token != 0;
-    const uint32_t bfull_leader = mapa(bfull0, 0);
-    int slot = 0, issued = 0;
-    uint32_t phase = 0;
-    const __half *act = reinterpret_cast<const __half *>(a.act);
-    pdl_wait();  // activation rows come from the preceding kernels
-    for (int w = w0; w < W && ok; w += wstep) {
-      const Tc2Item it = cur.at(a, w, nbp);
-      const int half = it.n >> 1;  // rows of this CTA's B half
-      int rid[k2BRows];
-#pragma unroll
-      for (int i = 0; i < k2BRows; ++i) {
-        const int r = (t >> 3) + kRowStep * i;
-        const int n = (int)rank * half + r;  // token of the tile
-        rid[i] = (r < half && n < it.ntok) ? (by_token ? a.sorted_pair[it.s0 + n] / a.top_k : it.s0 + n)
-                                           : (r < half ? -1 : -2);
-      }
-      for (int kb = 0; kb < nk; ++kb) {
-        if (!mbar_wait_c(bempty0 + 8u * slot, phase ^ 1u)) {
-          ok = false;
-          break;
-        }
-        const uint32_t stB = ringB + (uint32_t)slot * k2BBytes;
-#pragma unroll
-        for (int i = 0; i < k2BRows; ++i) {
-          if (rid[i] == -2) continue;  // beyond the rows the MMA reads
-          const int r = (t >> 3) + kRowStep * i;
-          const uint32_t dst = stB + (uint32_t)((r >> 3) * 1024 + (r & 7) * 128 + (((cc ^ r) & 7) << 4));
-          const __half *src = act + (int64_t)(rid[i] < 0 ? 0 : rid[i]) * K + kb * 64 + cc * 8;
-          cp_async16(dst, src, rid[i] >= 0);
-        }
-        cp_async_commit();
-        ++issued;
-        if (issued > k2BLag) {  // the stage issued k2BLag steps ago has landed: hand it to the MMA
-          cp_async_wait_group<k2BLag>();
-          fence_async_smem();
-          __syncwarp();
-          if (lane == 0) mbar_arrive_remote(bfull_leader + 8u * ((slot + k2BStages - k2BLag) % k2BStages));
-        }
-        if (++slot == k2BStages) {
-          slot = 0;
-          phase ^= 1u;
+    // ------------------------------------------------------ B producer
+    // The tile's activation rows are consecutive slots of the expert-sorted
+    // list (GEMM1: x rows gathered into slot order beforehand; GEMM2: h rows),
+    // so a stage's B half is one 2-D tensor copy: rows [s0 + rank * N/2, +128)
+    // x columns [64 kb, +64).  Rows past the tile's live tokens feed only MMA
+    // columns that the epilogue discards; rows past the tensor read as zeros.
+    if (lane == 0) {
+      int slot = 0;
+      uint32_t phase = 0;
+      uint32_t issued = 0, issued_parity = 0;  // per slot: has a copy, parity of its last phase
+      pdl_wait();  // activation rows come from the preceding kernels
+      for (int w = w0; w < W && ok; w += wstep) {
+        const Tc2Item it = cur.at(a, w, nbp);
+        const int y = it.s0 + (int)rank * (it.n >> 1);
+        for (int kb = 0; kb < nk; ++kb) {
+          if (!mbar_wait(bempty0 + 8u * slot, phase ^ 1u)) {
+            ok = false;
+            break;
+          }
+          const uint32_t bar = bfull0 + 8u * slot;
+          mbar_expect_tx(bar, k2BBytes);
+          tma_load_2d(ringB + (uint32_t)slot * k2BBytes, &bmap, kb * 64, y, bar);
+          issued |= 1u << slot;
+          issued_parity = (issued_parity & ~(1u << slot)) | (phase << slot);
+          if (++slot == k2BStages) {
+            slot = 0;
+            phase ^= 1u;
+          }
         }
       }
+      // Never leave with a tensor copy in flight into this CTA's shared memory.
+      for (int i = 0; i < k2BStages; ++i)
+        if (issued & (1u << i)) mbar_wait(bfull0 + 8u * i, (issued_parity >> i) & 1u);
     }
-    cp_async_wait_group<0>();
-    fence_async_smem();
     __syncwarp();
-    if (ok && lane == 0) {  // the last k2BLag stages
-      for (int back = issued < k2BLag ? issued : k2BLag; back >= 1; --back)
-        mbar_arrive_remote(bfull_leader + 8u * ((slot + k2BStages - back) % k2BStages));
-    }
   } else if (warp == k2MmaWarp) {
     // ------------------------------------------------------ MMA issuer (leader CTA)
     if (rank == 0 && lane == 0) {
       constexpr uint32_t fmt = WF == W_MXFP4 ? 1u : 0u;  // operand type: 0 = F16, 1 = BF16
       const uint32_t idesc0 = (1u << 4) | (fmt << 7) | (fmt << 10) | ((uint32_t)(256 >> 4) << 24);
-      int sa = 0, sb = 0, li = 0;
-      uint32_t pa = 0, pb = 0;
+      int sa = 0, sb = 0, sr = 0, li = 0;
+      uint32_t pr = 0;
       for (int w = w0; w < W && ok; w += wstep, ++li) {
         const Tc2Item it = cur.at(a, w, nbp);
         const uint32_t idesc = idesc0 | ((uint32_t)(it.n >> 3) << 17);
@@ -414,7 +455,7 @@ __global__ void __launch_bounds__(k2Threads, 1) k_grouped_tc2(const GroupedArgs 
         tc_fence_after();
         const uint32_t d0 = tmem + (uint32_t)(b * k2AccCols);
         for (int kb = 0; kb < nk; ++kb) {
-          if (!mbar_wait_c(afull0 + 8u * sa, pa) || !mbar_wait_c(bfull0 + 8u * sb, pb)) {
+          if (!mbar_wait(ready0 + 8u * sr, pr)) {
             ok = false;
             break;
           }
@@ -427,13 +468,11 @@ __global__ void __launch_bounds__(k2Threads, 1) k_grouped_tc2(const GroupedArgs 
           tc2_commit_both(aempty0 + 8u * sa);  // frees both CTAs' stages once these MMAs have read them
           tc2_commit_both(bempty0 + 8u * sb);
           any_mma = true;
-          if (++sa == k2AStages) {
-            sa = 0;
-            pa ^= 1u;
-          }
-          if (++sb == k2BStages) {
-            sb = 0;
-            pb ^= 1u;
+          if (++sa == k2AStages) sa = 0;
+          if (++sb == k2BStages) sb = 0;
+          if (++sr == k2RStages) {
+            sr = 0;
+            pr ^= 1u;
           }
         }
         if (!ok) break;
@@ -449,6 +488,45 @@ __global__ void __launch_bounds__(k2Threads, 1) k_grouped_tc2(const GroupedArgs 
       }
     }
     __syncwarp();
+  } else if (warp == k2RelayWarp) {
+    // ------------------------------------------------------ relay (both CTAs)
+    // One thread per CTA turns "this CTA's stage is full" (its A warps'
+    // arrivals and its B tensor copy) into one arrival on the leader's ready
+    // barrier, so the MMA thread waits on a single barrier per k-block.  The
+    // relay has observed the stage's writes (acquire) before it arrives; the
+    // peer's arrival is relaxed, because a release at cluster scope here
+    // would wait for every memory access the SM has in flight (the tensor
+    // copies and weight loads of the next stages) and stall the pipeline by
+    // about half a microsecond per k-block.  The leader's MMAs read the peer's
+    // stage only after that arrival, when its writes have completed.
+    if (lane == 0) {
+      const uint32_t ready_leader = mapa(ready0, 0);
+      int sa = 0, sb = 0, sr = 0;
+      uint32_t pa = 0, pb = 0;
+      for (int w = w0; w < W && ok; w += wstep) {
+        for (int kb = 0; kb < nk; ++kb) {
+          if (!mbar_wait(afull0 + 8u * sa, pa) || !mbar_wait(bfull0 + 8u * sb, pb)) {
+            ok = false;
+            break;
+          }
+          if (rank == 0)
+            mbar_arrive(ready0 + 8u * sr);
+          else
+            asm volatile("mbarrier.arrive.relaxed.cluster.shared::cluster.b64 _, [%0];" ::"r"(ready_leader + 8u * sr)
+                         : "memory");
+          if (++sa == k2AStages) {
+            sa = 0;
+            pa ^= 1u;
+          }
+          if (++sb == k2BStages) {
+            sb = 0;
+            pb ^= 1u;
+          }
+          if (++sr == k2RStages) sr = 0;
+        }
+      }
+    }
+    __syncwarp();
   } else {
     // ------------------------------------------------------ epilogue (both CTAs)
     const int m = warp * 32 + lane;  // accumulator row = TMEM lane
@@ -459,7 +537,7 @@ __global__ void __launch_bounds__(k2Threads, 1) k_grouped_tc2(const GroupedArgs 
     for (int w = w0; w < W && ok; w += wstep, ++li) {
       const Tc2Item it = cur.at(a, w, nbp);
       const int b = li & 1;
-      if (!mbar_wait_c(tfull0 + 8u * b, (li >> 1) & 1)) {
+      if (!mbar_wait(tfull0 + 8u * b, (li >> 1) & 1)) {
         ok = false;
         break;
       }
@@ -546,7 +624,7 @@ static_assert(k2RingBytes + 1024 + 8 * k2Bars + 16 <= 227 * 1024, "shared memory
 bool tc2_supported(int rows_total, int K) { return rows_total % 256 == 0 && K % 64 == 0; }
 
 template <int STAGE, int WF>
-static cudaError_t launch_tc2_one(const GroupedArgs &a, int rows_total, cudaStream_t s) {
+static cudaError_t launch_tc2_one(const GroupedArgs &a, int rows_total, int64_t b_rows, cudaStream_t s) {
   auto kern = k_grouped_tc2<STAGE, WF>;
   const size_t smem = tc2_smem_bytes();
   cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
@@ -575,24 +653,90 @@ static cudaError_t launch_tc2_one(const GroupedArgs &a, int rows_total, cudaStre
   if (clusters <= 0) return cudaErrorInvalidConfiguration;
   GroupedArgs g = a;
   g.n_blocks = rows_total / 128;
-  return launch_pdl_cluster(kern, dim3(2 * clusters), dim3(k2Threads), smem, 2, s, g);
+  CUtensorMap bmap;
+  if ((err = encode_rows16_sw128(&bmap, a.act, (uint64_t)b_rows, (uint64_t)a.K, k2HalfRows)) != cudaSuccess)
+    return err;
+  return launch_pdl_cluster(kern, dim3(2 * clusters), dim3(k2Threads), smem, 2, s, g, bmap);
 }
 
 template <int WF>
-static cudaError_t launch_tc2_wf(int stage, const GroupedArgs &a, int rows_total, cudaStream_t s) {
+static cudaError_t launch_tc2_wf(int stage, const GroupedArgs &a, int rows_total, int64_t b_rows, cudaStream_t s) {
   switch (stage) {
-    case STAGE_GATED: return launch_tc2_one<STAGE_GATED, WF>(a, rows_total, s);
-    case STAGE_RELU2: return launch_tc2_one<STAGE_RELU2, WF>(a, rows_total, s);
-    case STAGE_DOWN: return launch_tc2_one<STAGE_DOWN, WF>(a, rows_total, s);
+    case STAGE_GATED: return launch_tc2_one<STAGE_GATED, WF>(a, rows_total, b_rows, s);
+    case STAGE_RELU2: return launch_tc2_one<STAGE_RELU2, WF>(a, rows_total, b_rows, s);
+    case STAGE_DOWN: return launch_tc2_one<STAGE_DOWN, WF>(a, rows_total, b_rows, s);
   }
   return cudaErrorInvalidValue;
 }
 
-cudaError_t launch_grouped_tc2(int stage, int wfmt, const GroupedArgs &a, int rows_total, cudaStream_t s) {
+cudaError_t launch_grouped_tc2(int stage, int wfmt, const GroupedArgs &a, int rows_total, int64_t b_rows,
+                               cudaStream_t s) {
   if (!tc2_supported(rows_total, a.K)) return cudaErrorInvalidValue;
-  if (wfmt == W_NVFP4) return launch_tc2_wf<W_NVFP4>(stage, a, rows_total, s);
-  if (wfmt == W_MXFP4) return launch_tc2_wf<W_MXFP4>(stage, a, rows_total, s);
+  if (wfmt == W_NVFP4) return launch_tc2_wf<W_NVFP4>(stage, a, rows_total, b_rows, s);
+  if (wfmt == W_MXFP4) return launch_tc2_wf<W_MXFP4>(stage, a, rows_total, b_rows, s);
   return cudaErrorInvalidValue;
+}
+
+// ------------------------------------------------------------ tensor maps
+
+cudaError_t encode_rows16_sw128(CUtensorMap *map, const void *base, uint64_t rows, uint64_t cols, uint32_t box_rows) {
+  using Encode = CUresult (*)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *, const cuuint64_t *,
+                              const cuuint64_t *, const cuuint32_t *, const cuuint32_t *, CUtensorMapInterleave,
+                              CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+  static Encode encode = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void *f = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      encode = reinterpret_cast<Encode>(f);
+  });
+  if (!encode) return cudaErrorNotSupported;
+  if (rows == 0) rows = 1;
+  const cuuint64_t dim[2] = {cols, rows};
+  const cuuint64_t stride[1] = {cols * 2};
+  const cuuint32_t box[2] = {64, box_rows};
+  const cuuint32_t estr[2] = {1, 1};
+  const CUresult r = encode(map, CU_TENSOR_MAP_DATA_TYPE_UINT16, 2, const_cast<void *>(base), dim, stride, box, estr,
+                            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
+}
+
+// ------------------------------------------- token rows -> expert-sorted slot rows
+//
+// dst[s] = src[sorted_pair[s] / top_k] for every live slot s < offsets[E] (one
+// warp per row, 16-byte copies), so that the pair kernel's activation tiles
+// are contiguous rows; padding slots are left as they are (they feed only
+// discarded MMA columns).
+__global__ void __launch_bounds__(256) k_gather_slot_rows(const uint4 *__restrict__ src, const int32_t *__restrict__ sorted,
+                                                          const int32_t *__restrict__ n_live, int top_k, int row_chunks,
+                                                          uint4 *__restrict__ dst) {
+  pdl_trigger();
+  pdl_wait();
+  const int lane = threadIdx.x & 31;
+  const int64_t live = *n_live;
+  for (int64_t s = (int64_t)blockIdx.x * 8 + (threadIdx.x >> 5); s < live; s += (int64_t)gridDim.x * 8) {
+    const int p = sorted[s];
+    if (p < 0) continue;
+    const uint4 *a = src + (int64_t)(p / top_k) * row_chunks;
+    uint4 *b = dst + s * row_chunks;
+    for (int c = lane; c < row_chunks; c += 32) b[c] = a[c];
+  }
+}
+
+cudaError_t launch_gather_slot_rows(const void *src, const int32_t *sorted, const int32_t *n_live, int top_k,
+                                    int cols16, int64_t cap_rows, void *dst, cudaStream_t s) {
+  if (cap_rows <= 0) return cudaSuccess;
+  if (cols16 % 8) return cudaErrorInvalidValue;
+  int dev = 0, sms = 0;
+  cudaError_t err;
+  if ((err = cudaGetDevice(&dev)) != cudaSuccess) return err;
+  if ((err = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) return err;
+  const int grid = (int)std::min<int64_t>((cap_rows + 7) / 8, (int64_t)sms * 8);
+  return launch_pdl(k_gather_slot_rows, dim3(grid), dim3(256), 0, s, reinterpret_cast<const uint4 *>(src), sorted,
+                    n_live, top_k, cols16 / 8, reinterpret_cast<uint4 *>(dst));
 }
 
 }  // namespace bqmoe

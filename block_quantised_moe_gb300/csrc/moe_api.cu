@@ -167,11 +167,11 @@ moe_status moe_plan(const moe_caps *c, moe_plan_t *out, size_t *scratch_bytes, i
   // FP4 tiles, both operands as E2M1 codes on the block-scaled FP4 MMA.  The FP4
   // kernel reads its activation rows as slot-major 128-row tiles, so its plans
   // pad every expert's group to 128 slots.
-  P.tc_on = Pmax >= 1024 && tc_supported(L.n13, L.H) && tc_supported(L.H, L.I);
+  P.tc_on = Pmax >= 1024 && tc2_supported(L.n13, L.H) && tc2_supported(L.H, L.I);
   P.fp4_on = P.tc_on && P.afmt == MOE_A_NVFP4 && L.fp4_tiles && fp4_tc_supported(L.n13, L.H) &&
              fp4_tc_supported(L.H, L.I);
   if (P.fp4_on) P.pad = kFp4Tile;
-  P.tc2_on = P.tc_on && !P.fp4_on && tc2_supported(L.n13, L.H) && tc2_supported(L.H, L.I);
+  P.tc2_on = P.tc_on && !P.fp4_on;
   S.cap_sorted = round_up(Pmax + (int64_t)L.E * (P.pad - 1), P.pad);
   size_t o = 0;
   auto take = [&](size_t bytes) {
@@ -218,6 +218,7 @@ moe_status moe_plan(const moe_caps *c, moe_plan_t *out, size_t *scratch_bytes, i
       S.ht = take((size_t)(S.cap_sorted / kFp4Tile) * (L.I / 256) * WeightLayout::kFp4TileBytes);
     } else {
       if (L.wfmt == MOE_W_MXFP4) S.xb16 = take(2 * (size_t)T * L.H);
+      if (P.tc2_on) S.xs16 = take(2 * (size_t)S.cap_sorted * L.H);
       S.h16 = take(2 * (size_t)S.cap_sorted * L.I);
       if (L.wfmt == MOE_W_NVFP4) S.h16fac = take(4 * (size_t)S.cap_sorted);
     }
@@ -368,8 +369,8 @@ static moe_status run_forward(moe_binding b, cudaStream_t stream, cudaEvent_t *e
   a.act_g = at<float>(sc, S.xfac);
   a.out_amax = P.afmt == MOE_A_BF16 ? at<float>(sc, S.hamax) : nullptr;
 
-  // GEMM1 + activation -> h
-  if (mark(MOE_STAGE_GEMM1) != cudaSuccess) return MOE_ERR_CUDA;
+  // GEMM1 + activation -> h (its activation staging for the tensor-core kernels
+  // is timed with the activation quantiser's stage)
   a.codes = b->packed + L.off_c13;
   a.codes_expert = L.blk13_expert();
   a.K = H;
@@ -381,6 +382,13 @@ static moe_status run_forward(moe_binding b, cudaStream_t stream, cudaEvent_t *e
                            nullptr, at<__half>(sc, S.xb16), nullptr, true, stream);
     if (err != cudaSuccess) return MOE_ERR_CUDA;
   }
+  if (P.tc2_on) {  // the pair kernel reads GEMM1's activation rows in slot order, one tensor copy per stage
+    err = launch_gather_slot_rows(nv ? static_cast<const void *>(at<__half>(sc, S.x16))
+                                     : static_cast<const void *>(at<__half>(sc, S.xb16)),
+                                  sorted, offsets + E, K, H, S.cap_sorted, at<__half>(sc, S.xs16), stream);
+    if (err != cudaSuccess) return MOE_ERR_CUDA;
+  }
+  if (mark(MOE_STAGE_GEMM1) != cudaSuccess) return MOE_ERR_CUDA;
   a.work = at<int32_t>(sc, S.work);
   a.tiny = (int64_t)P.max_tokens * K * 8 <= E;
   a.wait_first = staged ? 1 : 0;  // routing (which staged x) triggered GEMM1 early
@@ -401,8 +409,8 @@ static moe_status run_forward(moe_binding b, cudaStream_t stream, cudaEvent_t *e
         t.act = at<__half>(sc, S.xb16);
         t.act_g = nullptr;
       }
-      err = P.tc2_on ? launch_grouped_tc2(stage1, L.wfmt, t, L.n13, stream)
-                     : launch_grouped_tc(stage1, L.wfmt, t, L.n13, E, stream);
+      t.act = at<__half>(sc, S.xs16);
+      err = launch_grouped_tc2(stage1, L.wfmt, t, L.n13, S.cap_sorted, stream);
     }
   }
   a.out_amax = nullptr;
@@ -462,8 +470,7 @@ static moe_status run_forward(moe_binding b, cudaStream_t stream, cudaEvent_t *e
     t.act_scales = nullptr;
     t.act_g = nv ? at<float>(sc, S.h16fac) : nullptr;
     t.act_by_token = 0;
-    err = P.tc2_on ? launch_grouped_tc2(STAGE_DOWN, L.wfmt, t, H, stream)
-                   : launch_grouped_tc(STAGE_DOWN, L.wfmt, t, H, E, stream);
+    err = launch_grouped_tc2(STAGE_DOWN, L.wfmt, t, H, S.cap_sorted, stream);
   }
   if (err != cudaSuccess) return MOE_ERR_CUDA;
   if (mark(MOE_STAGE_COMBINE) != cudaSuccess) return MOE_ERR_CUDA;
