@@ -50,7 +50,7 @@ ROWS = [("prefill_w4a4_e256_h7168_i2048_k8", 8192)] + \
 L2_BYTES = 126.5e6
 # committed ncu summaries per workload (profiles/)
 PROFILES = {
-    "prefill_w4a16_e256_h7168_i2048_k8": "profiles/k_grouped_tc_prefill_e32_h7168_t2048.md",
+    "prefill_w4a16_e256_h7168_i2048_k8": "profiles/k_grouped_tc2_prefill_e32_h7168_t2048.md",
     "prefill_w4a4_e256_h7168_i2048_k8": "profiles/k_grouped_fp4_prefill_e32_h7168_t2048.md",
     "decode_e128_h2048_i768_k8": "profiles/k_grouped_mma_decode_e128_h2048_t64.md",
 }
