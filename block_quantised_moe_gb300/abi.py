@@ -34,6 +34,7 @@ MOE_G_NONE, MOE_G_PER_TENSOR, MOE_G_PER_ROW = 0, 1, 2
 MOE_NUM_STAGES = 6
 STAGES = ("route", "quant_x", "gemm1", "quant_h", "gemm2", "combine")
 MOE_NO_ALLOC_SCRATCH_BYTES = 32 << 20
+MOE_OPT_SINGLE_LAUNCH = 1
 
 WFMT = {"nvfp4": MOE_W_NVFP4, "mxfp4": MOE_W_MXFP4}
 AFMT = {"bf16": MOE_A_BF16, "nvfp4": MOE_A_NVFP4, "mxfp8": MOE_A_MXFP8}
@@ -45,6 +46,7 @@ EXPORTS = (
     "moe_bind", "moe_run", "moe_run_timed", "moe_run_host", "moe_device_status", "moe_debug_routing", "moe_quantize",
     "moe_destroy_weight_plan", "moe_destroy_plan", "moe_destroy_binding", "moe_run_no_alloc", "moe_launch_count",
     "moe_measure_mma_peak", "moe_selftest_wait_timeout", "moe_debug_hidden", "moe_no_alloc_device_status",
+    "moe_plan_set_option", "moe_selftest_grid_barrier_timeout",
 )
 
 
@@ -81,6 +83,8 @@ _sig = {
     "moe_destroy_binding": (None, [_vp]),
     "moe_run_no_alloc": (_i32, [_vp, _vp, _vp, _vp, _vp, _i32, _vp, _vp]),
     "moe_no_alloc_device_status": (_i32, [_vp, _vp, _P(_i32)]),
+    "moe_plan_set_option": (_i32, [_vp, _i32, _i32]),
+    "moe_selftest_grid_barrier_timeout": (_i32, [_vp, _vp, _P(_i32)]),
     "moe_selftest_wait_timeout": (_i32, [_vp, _vp, _P(_i32)]),
     "moe_debug_hidden": (_i32, [_vp, _vp, _P(ctypes.c_float), _i32, _P(_i32)]),
 }
@@ -273,4 +277,18 @@ def moe_no_alloc_device_status(plan, stream=None):
     rc = _lib.moe_no_alloc_device_status(plan, _stream(stream), st)
     if rc not in (MOE_OK, MOE_ERR_TIMEOUT):
         _check(rc, "moe_no_alloc_device_status")
+    return rc, list(st)
+
+
+def moe_plan_set_option(plan, option, value):
+    _check(_lib.moe_plan_set_option(plan, option, value), "moe_plan_set_option")
+
+
+def moe_selftest_grid_barrier_timeout(binding, stream=None):
+    """One single-launch forward with a grid-barrier arrival withheld: -> (status code,
+    [flags, dropped, 0, 0]); MOE_ERR_TIMEOUT is the expected code and is returned, not raised."""
+    st = (_i32 * 4)()
+    rc = _lib.moe_selftest_grid_barrier_timeout(binding, _stream(stream), st)
+    if rc not in (MOE_OK, MOE_ERR_TIMEOUT):
+        _check(rc, "moe_selftest_grid_barrier_timeout")
     return rc, list(st)

@@ -57,6 +57,7 @@ struct ScratchLayout {
   size_t xb16 = 0;                      // tcgen05 path, MXFP4: BF16 slot-order x rows
   size_t xt = 0, ht = 0;                // FP4 path: x^ / h^ as slot-major 128-row tiles (codes + scales)
   size_t xs16 = 0;                      // CTA-pair path: GEMM1's 16-bit x rows gathered into slot order
+  size_t gbar = 0;                      // single-launch path: grid barrier words
   size_t part = 0, total = 0;
 };
 
@@ -160,6 +161,12 @@ cudaError_t launch_grouped_fp4(int stage, const GroupedArgs &a, int rows_total, 
 cudaError_t launch_stage_h16(int src, const void *act, const uint8_t *act_scales, const float *act_g, int K,
                              int64_t rows, const int32_t *rows_dev, __half *h16, float *fac, bool out_bf16,
                              cudaStream_t s);
+
+// Single-launch decode forward (unified.cuh): supported formats and sizes,
+// and the launch (args filled by the caller; nst / ngroups set here).
+struct UnifiedArgs;
+bool unified_supported(int wfmt, int afmt, int P, int E, int K);
+cudaError_t launch_unified(int wfmt, int afmt, int stage1, int ntok, bool tiny, UnifiedArgs u, cudaStream_t s);
 
 // Ordered per-token sum of the partials (FP32, or BF16 when part_bf16).
 cudaError_t launch_combine(const void *part, bool part_bf16, int H, const int32_t *pair_pos, int T, int K,

@@ -1,0 +1,7 @@
+// Instantiations of the single-launch decode forward (unified.cuh) for one
+// weight format and activation format.
+#include "unified.cuh"
+
+namespace bqmoe {
+BQMOE_UNIFIED_LAUNCHER(launch_unified_mx_bf16, W_MXFP4, A_BF16)
+}  // namespace bqmoe

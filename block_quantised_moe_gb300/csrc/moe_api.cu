@@ -13,6 +13,7 @@
 #include "launch.h"
 #include "moe.h"
 #include "sync.cuh"
+#include "unified.cuh"
 
 using namespace bqmoe;
 
@@ -26,6 +27,8 @@ struct moe_plan_s {
   bool tc_on = false;  // experts with >= large_min pairs run on the tcgen05 kernel
   bool fp4_on = false; // ... on the block-scaled FP4 kernel (W4A4 with the weights' FP4 tiles)
   bool tc2_on = false; // ... otherwise on the CTA-pair kernel (token tiles of up to 256)
+  bool unified_ok = false;  // decode plan the single-launch forward supports
+  bool unified_on = false;  // ... and moe_run uses it (MOE_OPT_SINGLE_LAUNCH)
   int large_min = 0x7FFFFFFF;
   ScratchLayout S;
 };
@@ -172,6 +175,8 @@ moe_status moe_plan(const moe_caps *c, moe_plan_t *out, size_t *scratch_bytes, i
              fp4_tc_supported(L.H, L.I);
   if (P.fp4_on) P.pad = kFp4Tile;
   P.tc2_on = P.tc_on && !P.fp4_on;
+  P.unified_ok = !P.tc_on && unified_supported(L.wfmt, P.afmt, (int)Pmax, L.E, P.K);
+  P.unified_on = P.unified_ok;
   S.cap_sorted = round_up(Pmax + (int64_t)L.E * (P.pad - 1), P.pad);
   size_t o = 0;
   auto take = [&](size_t bytes) {
@@ -190,6 +195,7 @@ moe_status moe_plan(const moe_caps *c, moe_plan_t *out, size_t *scratch_bytes, i
   S.large_tiles = take(4 * (size_t)(L.E + 1));
   S.route_hist = take(4 * (size_t)route_chunks((int)Pmax) * (L.E + 1));
   S.work = take(4 * 2 * (size_t)kWorkSlots);
+  S.gbar = take(16);
   if (P.afmt == MOE_A_NVFP4) {
     S.xq_codes = take((size_t)T * L.H / 2);
     S.xq_scales = take((size_t)T * L.H / 16);
@@ -235,6 +241,17 @@ moe_status moe_plan(const moe_caps *c, moe_plan_t *out, size_t *scratch_bytes, i
   return MOE_OK;
 }
 
+moe_status moe_plan_set_option(moe_plan_t plan, int32_t option, int32_t value) {
+  if (!plan) return MOE_ERR_INVALID_ARG;
+  if (option == MOE_OPT_SINGLE_LAUNCH) {
+    if (value != 0 && value != 1) return MOE_ERR_INVALID_ARG;
+    if (value == 1 && !plan->unified_ok) return MOE_ERR_UNSUPPORTED;
+    plan->unified_on = value == 1;
+    return MOE_OK;
+  }
+  return MOE_ERR_INVALID_ARG;
+}
+
 moe_status moe_bind(moe_plan_t plan, void *scratch, size_t scratch_bytes, const void *packed, const void *x,
                     const int32_t *topk_ids, const float *topk_weights, int32_t num_tokens, void *out,
                     moe_binding *out_binding) {
@@ -265,6 +282,91 @@ moe_status moe_bind(moe_plan_t plan, void *scratch, size_t scratch_bytes, const 
 }
 
 static moe_status run_forward(moe_binding b, cudaStream_t stream, cudaEvent_t *ev);
+
+// The single-launch decode forward (unified.cuh) on the binding's buffers;
+// `withhold` >= 0 is the failure-detection self-test (CTA 0 withholds its
+// arrival at that grid barrier).
+static moe_status run_unified(moe_binding b, cudaStream_t stream, int withhold) {
+  const moe_plan_s &P = b->P;
+  const WeightLayout &L = P.L;
+  const ScratchLayout &S = P.S;
+  uint8_t *sc = b->scratch;
+  const int T = b->T, K = P.K, E = L.E, H = L.H, I = L.I;
+  const bool wide = (int64_t)P.max_tokens * K > (int64_t)8 * E;
+  const int ntok = mma_tokens_per_pass(H, I, wide);
+  UnifiedArgs u{};
+  u.x = static_cast<const __nv_bfloat16 *>(b->x);
+  u.ids = b->ids;
+  u.T = T;
+  u.K = K;
+  u.E = E;
+  u.H = H;
+  u.I = I;
+  u.pad = P.pad;
+  u.ntok = ntok;
+  u.ro = RouteOut{at<int32_t>(sc, S.counts), at<int32_t>(sc, S.offsets), at<int32_t>(sc, S.sorted),
+                  at<int32_t>(sc, S.pair_pos), at<int32_t>(sc, S.active), at<int32_t>(sc, S.passes),
+                  at<int32_t>(sc, S.large), at<int32_t>(sc, S.large_tiles), at<int32_t>(sc, S.status),
+                  at<int32_t>(sc, S.work), 2 * kWorkSlots};
+  u.x16 = at<__half>(sc, S.x16);
+  u.xfac = at<float>(sc, S.xfac);
+  u.hamax = at<float>(sc, S.hamax);
+  u.cap_sorted = S.cap_sorted;
+  const bool a16 = P.afmt == MOE_A_BF16;
+  if (!a16) {
+    u.xq_codes = at<uint8_t>(sc, S.xq_codes);
+    u.xq_scales = at<uint8_t>(sc, S.xq_scales);
+    u.xq_g = P.afmt == MOE_A_NVFP4 ? at<float>(sc, S.xq_g) : nullptr;
+    u.hq_codes = at<uint8_t>(sc, S.hq_codes);
+    u.hq_scales = at<uint8_t>(sc, S.hq_scales);
+    u.hq_g = P.afmt == MOE_A_NVFP4 ? at<float>(sc, S.hq_g) : nullptr;
+  }
+  GroupedArgs a{};
+  a.counts = u.ro.counts;
+  a.offsets = u.ro.offsets;
+  a.sorted_pair = u.ro.sorted_pair;
+  a.active = u.ro.active;
+  a.passes = u.ro.passes;
+  a.large = u.ro.large;
+  a.large_tiles = u.ro.large_tiles;
+  a.status = u.ro.status;
+  a.top_k = K;
+  a.topk_weights = b->w;
+  a.globals = reinterpret_cast<const float *>(b->packed + L.off_g);
+  a.I = I;
+  a.tiny = (int64_t)P.max_tokens * K * 8 <= E;
+  GroupedArgs g1 = a;  // GEMM1: staged x rows -> h (+ the per-pair |h| maxima for BF16 activations)
+  g1.codes = b->packed + L.off_c13;
+  g1.codes_expert = L.blk13_expert();
+  g1.K = H;
+  g1.n_rows = I;
+  g1.n_blocks = L.n13 / 128;
+  g1.act = u.x16;
+  g1.act_g = u.xfac;
+  g1.out_amax = a16 ? u.hamax : nullptr;
+  g1.out = at<float>(sc, S.h);
+  g1.work = u.ro.work;
+  GroupedArgs g2 = a;  // GEMM2: h (or its re-quantised codes) -> FP32 partials x topk weight
+  g2.codes = b->packed + L.off_c2;
+  g2.codes_expert = L.blk2_expert();
+  g2.K = I;
+  g2.n_rows = H;
+  g2.n_blocks = H / 128;
+  g2.act = a16 ? static_cast<const void *>(g1.out) : static_cast<const void *>(u.hq_codes);
+  g2.act_scales = a16 ? nullptr : u.hq_scales;
+  g2.act_g = a16 ? u.hamax : u.hq_g;
+  g2.out = at<float>(sc, S.part);
+  g2.out_bf16 = 0;
+  g2.work = u.ro.work + kWorkSlots;
+  u.g1 = g1;
+  u.g2 = g2;
+  u.part = g2.out;
+  u.out = static_cast<__nv_bfloat16 *>(b->out);
+  u.gbar = at<int32_t>(sc, S.gbar);
+  u.withhold = withhold;
+  const int stage1 = L.act == MOE_ACT_SILU_GATED ? STAGE_GATED : STAGE_RELU2;
+  return cuda_status(launch_unified(L.wfmt, P.afmt, stage1, ntok, a.tiny, u, stream));
+}
 
 static moe_status run_impl(moe_binding b, cudaStream_t stream, cudaEvent_t *ev) {
   launch_counter() = 0;
@@ -298,6 +400,7 @@ static moe_status run_forward(moe_binding b, cudaStream_t stream, cudaEvent_t *e
   float *h = at<float>(sc, S.h);
   float *part = at<float>(sc, S.part);
   cudaError_t err;
+  if (P.unified_on && ev == nullptr) return run_unified(b, stream, -1);
 
   if ((err = mark(MOE_STAGE_ROUTE)) != cudaSuccess) return MOE_ERR_CUDA;
   int32_t *active = at<int32_t>(sc, S.active);
@@ -571,6 +674,16 @@ moe_status moe_selftest_wait_timeout(cudaStream_t stream, int32_t *status_dev, i
     return MOE_ERR_CUDA;
   for (int i = 0; i < 4; ++i) status[i] = st[i];
   return (st[ST_FLAGS] & ST_FLAG_TIMEOUT) ? MOE_ERR_TIMEOUT : MOE_OK;
+}
+
+moe_status moe_selftest_grid_barrier_timeout(moe_binding b, cudaStream_t stream, int32_t *status) {
+  if (!b || !status) return MOE_ERR_INVALID_ARG;
+  if (!b->P.unified_on || b->T == 0) return MOE_ERR_UNSUPPORTED;
+  launch_counter() = 0;
+  const moe_status st = run_unified(b, stream, 1);  // barrier 1: after GEMM1
+  b->launches = launch_counter();
+  if (st != MOE_OK) return st;
+  return moe_device_status(b, stream, status);
 }
 
 moe_status moe_debug_routing(moe_binding b, cudaStream_t stream, int32_t *counts, int32_t *offsets,

@@ -167,6 +167,24 @@ MOE_API moe_status moe_is_supported(const moe_caps *caps);
 MOE_API moe_status moe_plan(const moe_caps *caps, moe_plan_t *out, size_t *scratch_bytes,
                     int32_t *m_tile);
 
+/* Plan options (moe_plan_set_option).
+ * MOE_OPT_SINGLE_LAUNCH: 1 (the default where supported) runs a decode plan's
+ *   whole forward as one persistent launch, the pages' unified dynamic path
+ *   (b12x project page, "What's in here": a persistent-grid path for NVFP4 and
+ *   MXFP8 activations): routing, the activation quantiser, GEMM1, the h
+ *   re-quantiser, GEMM2 and the combine run as phases of one cooperative grid,
+ *   separated by grid barriers whose waits are bounded.  Supported for plans of
+ *   at most 1024 (token, slot) pairs (max_tokens x top_k) with NVFP4 weights
+ *   and BF16, NVFP4 or MXFP8 activations, or MXFP4 weights and BF16 or MXFP8
+ *   activations.  0 runs one launch per stage.  Both give bit-identical
+ *   outputs; moe_run_timed always runs one launch per stage. */
+enum { MOE_OPT_SINGLE_LAUNCH = 1 };
+
+/* Set a plan option; applies to bindings made afterwards.  Host only.
+ * MOE_ERR_UNSUPPORTED if the plan cannot take the value, MOE_ERR_INVALID_ARG
+ * for an unknown option. */
+MOE_API moe_status moe_plan_set_option(moe_plan_t plan, int32_t option, int32_t value);
+
 /* Record the pointers of one forward (b12x project page, "Using it":
  * fused_moe.bind(plan, scratch=..., a=x, experts=..., topk_weights=tw,
  * topk_ids=ti)).  Host only; nothing is read or written on the device.
@@ -261,6 +279,18 @@ MOE_API moe_status moe_debug_hidden(moe_binding b, cudaStream_t stream, float *h
  * MOE_ERR_INVALID_ARG for a null pointer, MOE_ERR_CUDA on a CUDA error.  Takes
  * about two seconds; allocates nothing. */
 MOE_API moe_status moe_selftest_wait_timeout(cudaStream_t stream, int32_t *status_dev, int32_t *status);
+
+/* Self-test of the single-launch forward's grid barriers (no counterpart on
+ * the pages).  Runs the binding's single-launch forward once with CTA 0
+ * withholding its arrival at the grid barrier after GEMM1: the other CTAs'
+ * bounded waits give up after about two seconds, set bit 1 (timeout) of the
+ * status word and carry on, and the kernel returns (the output of this run is
+ * void).  Copies the status word to host `status[4]` and synchronises
+ * `stream`.  Returns MOE_ERR_TIMEOUT when the waits gave up (the expected
+ * outcome), MOE_OK if they did not, MOE_ERR_UNSUPPORTED if the binding's plan
+ * does not run as a single launch.  A following moe_run on the binding is a
+ * normal forward. */
+MOE_API moe_status moe_selftest_grid_barrier_timeout(moe_binding b, cudaStream_t stream, int32_t *status);
 
 /* ------------------------------------------------------ no-allocation run -- */
 

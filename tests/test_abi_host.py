@@ -153,3 +153,29 @@ def test_prepare_weights_argument_checks(abi):
     wm, _ = abi.moe_plan_weights(8, 256, 512, "mxfp4", "relu2")
     assert call(wm, fake, fake, fake, fake, fake, None, fake, None) == 1  # MXFP4 takes no globals
     abi.moe_destroy_weight_plan(w), abi.moe_destroy_weight_plan(wm)
+
+
+def test_single_launch_option_follows_the_plan(abi):
+    # decode plans (at most 1024 pairs) of the supported formats may run as one
+    # launch; a plan with tensor-core experts (1024+ pairs) may not
+    wp, _ = abi.moe_plan_weights(128, 2048, 768, "nvfp4", "silu")
+    small, _, _ = abi.moe_plan(wp, 8, 64, "bf16")
+    big, _, _ = abi.moe_plan(wp, 8, 4096, "bf16")
+    abi.moe_plan_set_option(small, abi.MOE_OPT_SINGLE_LAUNCH, 0)
+    abi.moe_plan_set_option(small, abi.MOE_OPT_SINGLE_LAUNCH, 1)
+    with pytest.raises(abi.MoeError) as ei:
+        abi.moe_plan_set_option(big, abi.MOE_OPT_SINGLE_LAUNCH, 1)
+    assert ei.value.status == abi.MOE_ERR_UNSUPPORTED
+    abi.moe_plan_set_option(big, abi.MOE_OPT_SINGLE_LAUNCH, 0)
+    for bad in ((99, 1), (abi.MOE_OPT_SINGLE_LAUNCH, 2)):
+        with pytest.raises(abi.MoeError) as ei:
+            abi.moe_plan_set_option(small, *bad)
+        assert ei.value.status == abi.MOE_ERR_INVALID_ARG
+    # MXFP4 weights with NVFP4 activations are not a supported pair at all
+    wmx, _ = abi.moe_plan_weights(128, 4096, 1024, "mxfp4", "relu2")
+    mx, _, _ = abi.moe_plan(wmx, 4, 64, "mxfp8")
+    abi.moe_plan_set_option(mx, abi.MOE_OPT_SINGLE_LAUNCH, 1)
+    for p in (small, big, mx):
+        abi.moe_destroy_plan(p)
+    abi.moe_destroy_weight_plan(wp)
+    abi.moe_destroy_weight_plan(wmx)

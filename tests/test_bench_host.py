@@ -51,12 +51,26 @@ def test_tensor_peak_follows_the_mma_kind():
     assert small == pytest.approx(f16)
 
 
-def test_traffic_is_reported_only_for_the_measured_source():
-    rec, src_hash = bench.traffic_record("k_grouped_mma.cu")
-    path = os.path.join(ROOT, "block_quantised_moe_gb300", "csrc", "k_grouped_mma.cu")
-    assert src_hash == hashlib.sha256(open(path, "rb").read()).hexdigest()[:16]
-    assert rec is not None and set(rec["per_launch"]) == {"gemm1", "gemm2"}
-    # bench.py reports rec["per_launch"] only while rec["src_sha256_16"] equals
-    # src_hash (and the workload matches); a changed kernel reports null
+def test_traffic_is_reported_only_for_the_measured_source(tmp_path, monkeypatch):
+    # a record counts only while its kernel source hashes to what it was measured on
+    src = "k_grouped_mma.cu"
+    good = bench.src_hash(src)
+    prof = tmp_path / "profiles"
+    prof.mkdir()
+    rec = {"workload": "w T=1", "kernel_source": "block_quantised_moe_gb300/csrc/" + src,
+           "per_launch": {"gemm1": 123.0}, "command": "ncu --metrics dram__bytes_read.sum"}
+    for sha, want in ((good, 123.0), ("0" * 16, None)):
+        (prof / "traffic.json").write_text(json.dumps({"records": [dict(rec, src_sha256_16=sha)]}))
+        monkeypatch.setattr(bench, "ROOT", str(tmp_path))
+        # src_hash reads the real source tree
+        monkeypatch.setattr(bench, "src_hash", lambda s, _h=good: _h)
+        assert bench.traffic_for("w T=1", "gemm1") == want
+        assert bench.traffic_for("other T=1", "gemm1") is None
+        assert bench.traffic_for("w T=1", "gemm2") is None
+
+
+def test_committed_traffic_records_name_their_command():
     stored = json.load(open(os.path.join(ROOT, "profiles", "traffic.json")))
-    assert stored["command"].startswith("ncu ")
+    for rec in stored["records"]:
+        assert rec["command"].startswith("ncu ")
+        assert set(rec["per_launch"]) <= {"gemm1", "gemm2", "combine", "route", "quant_x", "quant_h"}
