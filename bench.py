@@ -45,8 +45,10 @@ HEADLINE = ("prefill_w4a16_e256_h7168_i2048_k8", 8192)
 # the other workloads of the op, reported under "rows"
 ROWS = [("prefill_w4a4_e256_h7168_i2048_k8", 8192)] + \
     [("decode_e128_h2048_i768_k8", t) for t in (1, 4, 16, 64)] + \
+    [("decode_e128_h2048_i768_k8", t, "single-launch") for t in (1, 64)] + \
     [("decode_zipf_e256_h7168_i2048_k8", t) for t in (1, 8, 32, 128)] + \
-    [("mxfp4_mxfp8_relu2_e128_h4096_i1024_k4", t) for t in (1, 64, 4096)]
+    [("mxfp4_mxfp8_relu2_e128_h4096_i1024_k4", t) for t in (1, 64, 4096)] + \
+    [("mxfp4_mxfp8_relu2_e128_h4096_i1024_k4", 1, "single-launch")]
 L2_BYTES = 126.5e6
 # committed ncu summaries per workload (profiles/)
 PROFILES = {
@@ -404,7 +406,7 @@ def roofline_of(stage_ms, kernel_bytes, kernel_flops, cfg, afmt, pairs):
     return roof
 
 
-def measure(name, T, args, world, rank, layers, steps, headline=False):
+def measure(name, T, args, world, rank, layers, steps, headline=False, variant=None):
     """Time `steps` forwards of workload `name` at T tokens; returns the row."""
     from block_quantised_moe_gb300 import abi, layer, synth
     cfg = dict(synth.CONFIGS[name])
@@ -415,6 +417,8 @@ def measure(name, T, args, world, rank, layers, steps, headline=False):
     fp4 = cfg["wfmt"] == "nvfp4" and afmt == "nvfp4"
     packed0 = layers.get(cfg, fp4)
     plan = layer.Plan(packed0, K, T, afmt)
+    if variant == "single-launch":
+        abi.moe_plan_set_option(plan.handle, abi.MOE_OPT_SINGLE_LAUNCH, 1)
     seed_base = 1000 * rank
     # routing draws first: the replica count depends on the touched bytes
     b13, b2 = expert_bytes(cfg)
@@ -521,7 +525,8 @@ def measure(name, T, args, world, rank, layers, steps, headline=False):
                 "algorithmic_bytes": layer_bytes, "algorithmic_flops": flops,
                 "duration": "step time of the uninstrumented graph replays (an upper bound on the kernel's)"}
     row = {
-        "workload": workload_name(name, T, args.experts), "value": value, "unit": "tokens/s",
+        "workload": workload_name(name, T, args.experts) + (f" {variant}" if variant else ""), "value": value,
+        "unit": "tokens/s",
         "ms_per_step": ms / steps, "steps": steps,
         "config": {"experts": E, "hidden": H, "intermediate": I, "top_k": K, "weights": cfg["wfmt"],
                    "activations": afmt, "act": cfg["act"], "tokens": T,
@@ -579,9 +584,9 @@ def parse_rows(args):
         return list(ROWS)
     out = []
     for item in spec.split(","):
-        n, t = item.split(":")
-        assert n in synth.CONFIGS, n
-        out.append((n, int(t)))
+        parts = item.split(":")
+        assert parts[0] in synth.CONFIGS, parts[0]
+        out.append((parts[0], int(parts[1])) + tuple(parts[2:]))
     return out
 
 
@@ -609,10 +614,12 @@ def main():
     rows = {}
     # the extra workloads run at N=1 only (multi-GPU runs time the headline)
     if world == 1:
-        for (n, t) in parse_rows(args):
-            if (n, t) == (name, T):
+        for row_spec in parse_rows(args):
+            n, t = row_spec[0], row_spec[1]
+            variant = row_spec[2] if len(row_spec) > 2 else None
+            if (n, t) == (name, T) and variant is None:
                 continue
-            r = measure(n, t, args, world, rank, layers, args.row_steps or args.steps)
+            r = measure(n, t, args, world, rank, layers, args.row_steps or args.steps, variant=variant)
             rows[r.pop("workload")] = r
     line = {
         "metric": "moe_layer_tokens_per_s", "value": head["value"], "unit": "tokens/s", "n_gpus": world,

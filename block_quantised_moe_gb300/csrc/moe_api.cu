@@ -176,7 +176,7 @@ moe_status moe_plan(const moe_caps *c, moe_plan_t *out, size_t *scratch_bytes, i
   if (P.fp4_on) P.pad = kFp4Tile;
   P.tc2_on = P.tc_on && !P.fp4_on;
   P.unified_ok = !P.tc_on && unified_supported(L.wfmt, P.afmt, (int)Pmax, L.E, P.K);
-  P.unified_on = P.unified_ok;
+  P.unified_on = false;  // opt-in: measured slower than the PDL-overlapped launches (see moe.h)
   S.cap_sorted = round_up(Pmax + (int64_t)L.E * (P.pad - 1), P.pad);
   size_t o = 0;
   auto take = [&](size_t bytes) {

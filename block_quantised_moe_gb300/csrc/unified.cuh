@@ -17,12 +17,11 @@
 //
 // Every phase performs the same arithmetic, in the same order, as the
 // multi-launch forward (the same device code), so the two paths give
-// bit-identical outputs.  A grid barrier is an arrival counter and a
-// generation word in scratch, cleared before the launch; the last CTA to
-// arrive resets the counter and advances the generation, the others spin on
-// the generation with a two-second bound, after which they record a timeout
-// in the status word and go on (the results are then void, the context stays
-// usable).
+// bit-identical outputs.  The grid barriers share one arrival counter in
+// scratch, cleared before the launch; a CTA waits, with a two-second bound,
+// until every CTA's arrival at the barrier is counted, after which it records
+// a timeout in the status word and goes on (the results are then void, the
+// context stays usable).
 #pragma once
 
 #include "common.cuh"
@@ -56,37 +55,39 @@ struct UnifiedArgs {
   int nst1, nst2, ngroups;
   const float *part;       // [cap][H] FP32 partials (GEMM2's output)
   __nv_bfloat16 *out;      // [T][H]
-  int32_t *gbar;           // grid barrier: [0] arrivals, [1] generation (both 0 before the launch)
-  int withhold;            // self-test: CTA 0 does not arrive at this barrier (-1: never)
+  int32_t *gbar;           // grid barrier: arrivals over the launch (0 before it)
+  int withhold;            // self-test: CTA 0 does not arrive at the barrier with this tag (-1: never);
+                           // tags: 0 after routing, 1 after GEMM1, 2 after the h quantiser, 3 after GEMM2
 };
 
 // ------------------------------------------------------------ grid barrier
 
-// All CTAs of the (cooperative, fully resident) grid meet here.  Bounded:
-// false after kWaitNs without the last arrival.
-__device__ __forceinline__ bool grid_sync(const UnifiedArgs &u, int index, int *flag_smem) {
+// All CTAs of the (cooperative, fully resident) grid meet here.  The
+// barrier word counts arrivals over the whole launch (cleared before it):
+// the launch's barrier number `seq` (0, 1, 2, ...) is complete when seq + 1
+// arrivals per CTA have been counted.  Arrivals are fire-and-forget reductions with release semantics
+// (no CTA waits for its own atomic's round trip through L2), waiters poll with
+// acquire loads.  Bounded: false after kWaitNs without the last arrival.
+__device__ __forceinline__ bool grid_sync(const UnifiedArgs &u, int seq, int tag, int *flag_smem) {
   __syncthreads();
   if (threadIdx.x == 0) {
     bool ok = true;
-    if (!(u.withhold == index && blockIdx.x == 0)) {
-      volatile int32_t *gen = u.gbar + 1;
-      const int32_t g0 = *gen;
-      __threadfence();  // this CTA's writes before its arrival
-      const int32_t old = atomicAdd(u.gbar, 1);
-      if (old == (int32_t)gridDim.x - 1) {
-        atomicExch(u.gbar, 0);
-        __threadfence();
-        atomicAdd(u.gbar + 1, 1);
-      } else {
+    if (!(u.withhold == tag && blockIdx.x == 0)) {
+      asm volatile("red.release.gpu.global.add.u32 [%0], 1;" ::"l"(u.gbar) : "memory");
+      const uint32_t target = (uint32_t)(seq + 1) * gridDim.x;
+      uint32_t seen;
+      asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(seen) : "l"(u.gbar) : "memory");
+      if (seen < target) {
         const unsigned long long t0 = globaltimer_ns();
-        for (uint32_t it = 1; *gen == g0; ++it) {
+        for (uint32_t it = 1;; ++it) {
+          asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(seen) : "l"(u.gbar) : "memory");
+          if (seen >= target) break;
           if ((it & 63u) == 0 && globaltimer_ns() - t0 > kWaitNs) {
             ok = false;
             break;
           }
         }
       }
-      __threadfence();  // the other CTAs' writes after the barrier
     }
     *flag_smem = ok ? 1 : 0;
     if (!ok) atomicOr(&u.ro.status[ST_FLAGS], ST_FLAG_TIMEOUT);
@@ -335,11 +336,12 @@ __global__ void __maxnreg__(kMmaMaxRegs) k_unified(const UnifiedArgs u) {
         for (int64_t i = (int64_t)gw * 32 + lane; i < u.cap_sorted; i += (int64_t)nw * 32) u.hamax[i] = 0.f;
     }
   }
-  grid_sync(u, 0, &sync_flag);
+  int seq = 0;
+  grid_sync(u, seq++, 0, &sync_flag);
 
   // phase 1: GEMM1
   grouped_mma_run<WF, SRC_X16, STAGE1, NT, false>(u.g1, u.nst1, u.ngroups, smem, cta, ncta);
-  grid_sync(u, 1, &sync_flag);
+  grid_sync(u, seq++, 1, &sync_flag);
 
   // phase 2: h re-quantisation
   constexpr int SRC2 = AF == A_BF16 ? SRC_H_F32 : (AF == A_NVFP4 ? SRC_H_NVFP4 : SRC_H_MXFP8);
@@ -347,12 +349,12 @@ __global__ void __maxnreg__(kMmaMaxRegs) k_unified(const UnifiedArgs u) {
     const int64_t live = u.ro.offsets[u.E];
     for (int64_t row = (int64_t)cta * nwarps + warp; row < live; row += (int64_t)ncta * nwarps)
       if (u.ro.sorted_pair[row] >= 0) quant_h_row<AF>(u, row, lane);
-    grid_sync(u, 2, &sync_flag);
+    grid_sync(u, seq++, 2, &sync_flag);
   }
 
   // phase 3: GEMM2
   grouped_mma_run<WF, SRC2, STAGE_DOWN, NT, false>(u.g2, u.nst2, u.ngroups, smem, cta, ncta);
-  grid_sync(u, 3, &sync_flag);
+  grid_sync(u, seq++, 3, &sync_flag);
 
   // phase 4: combine
   for (int t = cta; t < u.T; t += ncta) combine_token(u, t);

@@ -88,6 +88,7 @@ def test_withheld_grid_barrier_arrival_times_out_and_the_next_forward_is_correct
     T = 16
     x, ids, w = tl.make_inputs(cfg, T, seed=9)
     plan = layer.Plan(packed, cfg["K"], T, cfg["afmt"])
+    abi.moe_plan_set_option(plan.handle, abi.MOE_OPT_SINGLE_LAUNCH, 1)
     out = torch.empty(T, cfg["H"], dtype=torch.bfloat16, device="cuda")
     b = plan.bind(x, ids, w, out)
     rc, st = abi.moe_selftest_grid_barrier_timeout(b.handle)
