@@ -220,8 +220,12 @@ def expert_bytes(cfg):
 
 
 def src_hash(kernel_src):
-    path = os.path.join(ROOT, "block_quantised_moe_gb300", "csrc", kernel_src)
-    return hashlib.sha256(open(path, "rb").read()).hexdigest()[:16]
+    """First 16 hex digits of the SHA-256 of a kernel's source file(s), concatenated."""
+    files = [kernel_src] if isinstance(kernel_src, str) else list(kernel_src)
+    d = hashlib.sha256()
+    for f in files:
+        d.update(open(os.path.join(ROOT, "block_quantised_moe_gb300", "csrc", os.path.basename(f)), "rb").read())
+    return d.hexdigest()[:16]
 
 
 def traffic_for(workload, stage):
@@ -236,7 +240,7 @@ def traffic_for(workload, stage):
     for rec in recs:
         if rec.get("workload") != workload or stage not in rec.get("per_launch", {}):
             continue
-        src = os.path.basename(rec.get("kernel_source", ""))
+        src = rec.get("kernel_source")
         if src and rec.get("src_sha256_16") == src_hash(src):
             return rec["per_launch"][stage]
     return None

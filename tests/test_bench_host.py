@@ -57,7 +57,7 @@ def test_traffic_is_reported_only_for_the_measured_source(tmp_path, monkeypatch)
     good = bench.src_hash(src)
     prof = tmp_path / "profiles"
     prof.mkdir()
-    rec = {"workload": "w T=1", "kernel_source": "block_quantised_moe_gb300/csrc/" + src,
+    rec = {"workload": "w T=1", "kernel_source": [src],
            "per_launch": {"gemm1": 123.0}, "command": "ncu --metrics dram__bytes_read.sum"}
     for sha, want in ((good, 123.0), ("0" * 16, None)):
         (prof / "traffic.json").write_text(json.dumps({"records": [dict(rec, src_sha256_16=sha)]}))
