@@ -29,11 +29,11 @@
 // * Token tiles: an expert with c pairs is cut into ceil(c / 256) tiles of
 //   equal size (rounded up to 16), so no tile is a nearly empty remainder;
 //   the MMA's N is the tile's size rounded up to 16.
-// * A relay thread in each CTA turns "this CTA's operands of a k-block are in
-//   shared memory" into one arrival on the leader's ready barrier; the
-//   leader's MMA thread waits on that one barrier, issues 4 MMAs into one of
-//   two TMEM accumulators (2 x 256 columns) and releases both CTAs' stages
-//   with multicast tcgen05.commits.  Each CTA's four epilogue warps read their
+// * A relay thread in each CTA turns "this CTA's operands of two k-blocks are
+//   in shared memory" into one arrival on the leader's ready barrier; the
+//   leader's MMA thread waits on that one barrier, issues 8 MMAs into one of
+//   two TMEM accumulators (2 x 256 columns) and releases both CTAs' two
+//   stages with one multicast tcgen05.commit.  K is a multiple of 128.  Each CTA's four epilogue warps read their
 //   128 rows of the accumulator (SiLU(gate)*up, ReLU^2, or the topk_weight
 //   scaling of the down projection) while the next tile's MMAs run.
 // * Work items are (large expert, token tile, pair of 128-row blocks), dealt
@@ -59,27 +59,49 @@ namespace bqmoe {
 constexpr int k2EpiWarps = 4, k2AWarps = 8, k2BWarps = 1;
 constexpr int k2MmaWarp = k2EpiWarps + k2AWarps + k2BWarps;  // warp 13
 constexpr int k2RelayWarp = k2MmaWarp + 1;                     // warp 14
-constexpr int k2Threads = (k2RelayWarp + 1) * 32;
+constexpr int k2LoadWarp = k2RelayWarp + 1;                     // warp 15
+constexpr int k2Threads = (k2LoadWarp + 1) * 32;
 constexpr int k2MaxN = 256;                 // tokens per pair tile
 constexpr int k2HalfRows = k2MaxN / 2;      // B rows per CTA
 constexpr int k2ABytes = 128 * 64 * 2;      // one 128 x 64 16-bit block
 constexpr int k2BBytes = k2HalfRows * 64 * 2;
-// Separate rings for the two operands: the weight tiles are produced from
-// registers a few k-blocks ahead, while the activation tiles come from global
-// memory by tensor copies whose latency needs a deeper ring.
+// Rings: the packed weight bytes of a k-block (one contiguous run per 128-row
+// block) arrive by bulk copies into a raw ring that runs up to k2RawStages
+// k-blocks ahead of the A warps, which dequantise from it into the A ring; the
+// activation tiles arrive by tensor copies into the B ring.
 constexpr int k2AStages = 6;
 constexpr int k2BStages = 6;
-constexpr int k2RStages = 8;                // ready barriers (both CTAs' operands of a k-block), by k-block
-constexpr int k2APrefetch = 4;              // k-blocks of its group's packed A bytes an A thread keeps in flight
+// The MMA thread consumes the stages two k-blocks at a time: one wait on the
+// leader's ready barrier and one commit per pair of stages (A and B stages 2q
+// and 2q + 1 share the empty barrier of pair q), which halves the per-k-block
+// synchronisation on the issuing thread.
+constexpr int k2Pairs = k2AStages / 2;
+constexpr int k2RStages = 4;                // ready barriers, by pair of k-blocks
+static_assert(k2AStages == k2BStages && k2AStages % 2 == 0 && k2RStages > k2Pairs, "paired stages");
+constexpr int k2RawStages = 6;             // packed weight bytes of a k-block, by k-block
+constexpr int k2RawBytes = 4608;            // bytes of one 64-K step of a 128-row block (NVFP4; MXFP4: 4352)
 constexpr int k2AGroups = 2;                // A warp groups producing alternate k-blocks
 constexpr int k2AThreadsPerGroup = k2AWarps * 32 / k2AGroups;
-constexpr int k2RingBytes = k2AStages * k2ABytes + k2BStages * k2BBytes;
+constexpr int k2RingBytes = k2AStages * k2ABytes + k2BStages * k2BBytes + k2RawStages * k2RawBytes;
 constexpr int k2AccCols = k2MaxN;           // TMEM columns per accumulator buffer
 constexpr int k2TmemCols = 2 * k2AccCols;   // double buffered
-constexpr int k2Bars = 2 * k2AStages + 2 * k2BStages + k2RStages + 4 + 1;
+constexpr int k2Bars = k2AStages + k2BStages + k2Pairs + k2RStages + 4 + 1 + 2 * k2RawStages;
 static_assert(k2AWarps * 32 == 256 && 256 % (k2AGroups * 32) == 0, "8 fragment chunks per k-block over the A groups");
 
 // ------------------------------------------------------------ cluster helpers
+
+// Named barrier 1 over the four epilogue warps (threads 0..127).
+__device__ __forceinline__ void epi_bar_sync() { asm volatile("bar.sync 1, 128;" ::: "memory"); }
+// The same barrier, returning whether every epilogue thread passed `v`.
+__device__ __forceinline__ bool epi_bar_and(bool v) {
+  uint32_t r;
+  asm volatile(
+      "{\n\t.reg .pred p, q;\n\tsetp.ne.u32 p, %1, 0;\n\tbar.red.and.pred q, 1, 128, p;\n\tselp.u32 %0, 1, 0, q;\n\t}"
+      : "=r"(r)
+      : "r"((uint32_t)v)
+      : "memory");
+  return r != 0;
+}
 
 __device__ __forceinline__ uint32_t cluster_rank() {
   uint32_t r;
@@ -257,16 +279,22 @@ __global__ void __launch_bounds__(k2Threads, 1) k_grouped_tc2(const GroupedArgs 
   const uint32_t base_s = (raw_s + 1023u) & ~1023u;
   uint8_t *base = smem_raw + (base_s - raw_s);
   const uint32_t ringA = base_s, ringB = base_s + k2AStages * k2ABytes;
+  const uint32_t ringR = ringB + k2BStages * k2BBytes;
+  const uint8_t *rawR = base + (ringR - base_s);
   uint64_t *bars = reinterpret_cast<uint64_t *>(base + k2RingBytes);
   uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + k2Bars);
+  // per-column factors of the epilogue, two items deep: [2][k2MaxN] activation
+  // factor, then [2][k2MaxN] topk weight
+  float *colinfo = reinterpret_cast<float *>(base + k2RingBytes + 8 * k2Bars + 16);
   const uint32_t afull0 = (uint32_t)__cvta_generic_to_shared(bars);  // this CTA's A tile is written
-  const uint32_t aempty0 = afull0 + 8u * k2AStages;                  // the pair's MMAs have read the A stage
-  const uint32_t bfull0 = aempty0 + 8u * k2AStages;                  // this CTA's B tile has landed
-  const uint32_t bempty0 = bfull0 + 8u * k2BStages;                  // the pair's MMAs have read the B stage
-  const uint32_t ready0 = bempty0 + 8u * k2BStages;                  // leader: both CTAs' operands are ready
+  const uint32_t bfull0 = afull0 + 8u * k2AStages;                   // this CTA's B tile has landed
+  const uint32_t empty0 = bfull0 + 8u * k2BStages;                   // the pair's MMAs have read a pair of stages
+  const uint32_t ready0 = empty0 + 8u * k2Pairs;                     // leader: both CTAs' operands of a pair
   const uint32_t tfull0 = ready0 + 8u * k2RStages;                   // 2
   const uint32_t tempty0 = tfull0 + 16u;                             // 2
   const uint32_t drain = tempty0 + 16u;                              // 1
+  const uint32_t rfull0 = drain + 8u;                                // raw weight bytes have landed
+  const uint32_t rempty0 = rfull0 + 8u * k2RawStages;                // the A group has read them
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const uint32_t rank = cluster_rank();  // 0: leader (issues the MMAs), 1: peer
@@ -274,18 +302,19 @@ __global__ void __launch_bounds__(k2Threads, 1) k_grouped_tc2(const GroupedArgs 
   if (threadIdx.x == 0) {
     for (int i = 0; i < k2AStages; ++i) {
       mbar_init(afull0 + 8u * i, k2AWarps / k2AGroups);
-      mbar_init(aempty0 + 8u * i, 1);
-    }
-    for (int i = 0; i < k2BStages; ++i) {
       mbar_init(bfull0 + 8u * i, 1);
-      mbar_init(bempty0 + 8u * i, 1);
     }
+    for (int i = 0; i < k2Pairs; ++i) mbar_init(empty0 + 8u * i, 1);
     for (int i = 0; i < k2RStages; ++i) mbar_init(ready0 + 8u * i, 2);
     for (int b = 0; b < 2; ++b) {
       mbar_init(tfull0 + 8u * b, 1);
       mbar_init(tempty0 + 8u * b, 2 * k2EpiWarps);
     }
     mbar_init(drain, 1);
+    for (int i = 0; i < k2RawStages; ++i) {
+      mbar_init(rfull0 + 8u * i, 1);
+      mbar_init(rempty0 + 8u * i, k2AWarps / k2AGroups);
+    }
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
   if (warp == k2MmaWarp) {  // one warp of each CTA of the pair allocates, together
@@ -317,89 +346,48 @@ __global__ void __launch_bounds__(k2Threads, 1) k_grouped_tc2(const GroupedArgs 
     // ------------------------------------------------------ A producers
     // The A warps form k2AGroups groups; group q produces the k-blocks n with
     // n % k2AGroups == q, so several stages are dequantised at once (one
-    // warp's chain of conversions, stores and fence per k-block is latency
-    // bound).  Thread tg of a group holds fragment chunks tg + 128 i of its
-    // k-blocks (16-row tile chunk / 32, lane chunk % 32): 16 code bytes and the
-    // lane group's block scales, dequantised to 16-bit values written at their
-    // slot positions in the swizzled tile.
-    constexpr int SB = WF == W_NVFP4 ? 4608 : 4352;  // bytes of one 64-K step of a block
+    // warp's chain of loads, conversions, stores and fence per k-block is
+    // latency bound).  Thread tg of a group takes fragment chunks tg + 128 i of
+    // its k-blocks (16-row tile chunk / 32, lane chunk % 32) from the raw ring:
+    // 16 code bytes and the lane group's block scales, dequantised to 16-bit
+    // values written at their slot positions in the swizzled tile.
     constexpr int CPT = k2AGroups;                   // chunks per thread per k-block
     const int t = threadIdx.x - k2EpiWarps * 32;    // 0..255
     const int grp = t / (k2AThreadsPerGroup), tg = t % k2AThreadsPerGroup;
     const int ln = tg & 31;
-    // Software pipeline over the group's k-blocks of this cluster's flat
-    // (item, k-block) sequence: register slot d holds the packed bytes of the
-    // group's step i with i % k2APrefetch = d, loaded k2APrefetch steps ahead
-    // (possibly from a later item).  The slots are indexed statically (the
-    // loop is unrolled by the depth), so no register move ever waits on a
-    // younger load than the one being consumed.
-    uint4 pch[k2APrefetch][CPT];
-    uint2 psc[k2APrefetch][CPT];
-    auto load = [&](const Tc2Item &it, int kb, uint4 (&c)[CPT], uint2 (&sc)[CPT]) {
-      const int blk = 2 * it.bp + (int)rank;
-      const uint8_t *step = a.codes + (size_t)it.e * a.codes_expert + ((size_t)blk * nk + kb) * SB;
+    const int n_items = w0 < W ? (W - w0 + wstep - 1) / wstep : 0;
+    const int total = n_items * nk;
+    for (int n = grp; n < total && ok; n += k2AGroups) {
+      const int r = n % k2RawStages;
+      if (!mbar_wait(rfull0 + 8u * r, (uint32_t)(n / k2RawStages) & 1u)) {
+        ok = false;
+        break;
+      }
+      const uint8_t *step = rawR + (size_t)r * k2RawBytes;
+      uint4 cch[CPT];
+      uint2 sch[CPT];
 #pragma unroll
       for (int i = 0; i < CPT; ++i) {
         const int tile = (tg >> 5) + (k2AThreadsPerGroup / 32) * i;
-        c[i] = __ldg(reinterpret_cast<const uint4 *>(step + tile * 512 + ln * 16));
-        if (WF == W_NVFP4) sc[i] = __ldg(reinterpret_cast<const uint2 *>(step + 4096 + tile * 64 + (ln >> 2) * 8));
-        else sc[i] = make_uint2(__ldg(reinterpret_cast<const uint32_t *>(step + 4096 + tile * 32 + (ln >> 2) * 4)), 0u);
+        cch[i] = *reinterpret_cast<const uint4 *>(step + tile * 512 + ln * 16);
+        if (WF == W_NVFP4) sch[i] = *reinterpret_cast<const uint2 *>(step + 4096 + tile * 64 + (ln >> 2) * 8);
+        else sch[i] = make_uint2(*reinterpret_cast<const uint32_t *>(step + 4096 + tile * 32 + (ln >> 2) * 4), 0u);
       }
-    };
-    Tc2Cursor pcur = cur;  // cursor of the prefetch
-    int pw = w0, pkb = 0;
-    bool pv = pw < W;
-    Tc2Item pit;
-    if (pv) pit = pcur.at(a, pw, nbp);
-    auto advance1 = [&]() {
-      if (++pkb == nk) {
-        pkb = 0;
-        pw += wstep;
-        pv = pw < W;
-        if (pv) pit = pcur.at(a, pw, nbp);
+      const int slot = n % k2AStages;
+      const bool got = mbar_wait(empty0 + 8u * (slot >> 1), ((uint32_t)(n / k2AStages) & 1u) ^ 1u);
+      __syncwarp();  // every lane's reads of the raw stage are done
+      if (lane == 0) mbar_arrive(rempty0 + 8u * r);
+      if (!got) {
+        ok = false;
+        break;
       }
-    };
-    auto advance = [&]() {  // to the group's next k-block
+      uint8_t *tileA = base + (size_t)slot * k2ABytes;
 #pragma unroll
-      for (int q = 0; q < k2AGroups; ++q)
-        if (pv) advance1();
-    };
-    for (int q = 0; q < grp && pv; ++q) advance1();  // the group's first k-block
-#pragma unroll
-    for (int d = 0; d < k2APrefetch; ++d) {
-      if (pv) load(pit, pkb, pch[d], psc[d]);
-      advance();
-    }
-    const int n_items = w0 < W ? (W - w0 + wstep - 1) / wstep : 0;
-    const int total = n_items * nk;
-    for (int n0 = grp; n0 < total && ok; n0 += k2APrefetch * k2AGroups) {
-#pragma unroll
-      for (int d = 0; d < k2APrefetch; ++d) {
-        const int n = n0 + d * k2AGroups;  // k-block of this step
-        if (n >= total) break;
-        uint4 cch[CPT];
-        uint2 sch[CPT];
-#pragma unroll
-        for (int i = 0; i < CPT; ++i) {
-          cch[i] = pch[d][i];
-          sch[i] = psc[d][i];
-        }
-        if (pv) load(pit, pkb, pch[d], psc[d]);
-        advance();
-        const int slot = n % k2AStages;
-        const uint32_t phase = (uint32_t)(n / k2AStages) & 1u;
-        if (!mbar_wait(aempty0 + 8u * slot, phase ^ 1u)) {
-          ok = false;
-          break;
-        }
-        uint8_t *tileA = base + (size_t)slot * k2ABytes;
-#pragma unroll
-        for (int i = 0; i < CPT; ++i)
-          dequant_chunk_store<WF>(tileA, cch[i], sch[i], (tg >> 5) + (k2AThreadsPerGroup / 32) * i, ln);
-        fence_async_smem();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(afull0 + 8u * slot);
-      }
+      for (int i = 0; i < CPT; ++i)
+        dequant_chunk_store<WF>(tileA, cch[i], sch[i], (tg >> 5) + (k2AThreadsPerGroup / 32) * i, ln);
+      fence_async_smem();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(afull0 + 8u * slot);
     }
   } else if (warp >= k2EpiWarps + k2AWarps && warp < k2MmaWarp) {
     // ------------------------------------------------------ B producer
@@ -417,7 +405,7 @@ __global__ void __launch_bounds__(k2Threads, 1) k_grouped_tc2(const GroupedArgs 
         const Tc2Item it = cur.at(a, w, nbp);
         const int y = it.s0 + (int)rank * (it.n >> 1);
         for (int kb = 0; kb < nk; ++kb) {
-          if (!mbar_wait(bempty0 + 8u * slot, phase ^ 1u)) {
+          if (!mbar_wait(empty0 + 8u * (slot >> 1), phase ^ 1u)) {
             ok = false;
             break;
           }
@@ -442,8 +430,7 @@ __global__ void __launch_bounds__(k2Threads, 1) k_grouped_tc2(const GroupedArgs 
     if (rank == 0 && lane == 0) {
       constexpr uint32_t fmt = WF == W_MXFP4 ? 1u : 0u;  // operand type: 0 = F16, 1 = BF16
       const uint32_t idesc0 = (1u << 4) | (fmt << 7) | (fmt << 10) | ((uint32_t)(256 >> 4) << 24);
-      int sa = 0, sb = 0, sr = 0, li = 0;
-      uint32_t pr = 0;
+      int q = 0, li = 0;  // pairs of k-blocks consumed over the launch
       for (int w = w0; w < W && ok; w += wstep, ++li) {
         const Tc2Item it = cur.at(a, w, nbp);
         const uint32_t idesc = idesc0 | ((uint32_t)(it.n >> 3) << 17);
@@ -454,26 +441,23 @@ __global__ void __launch_bounds__(k2Threads, 1) k_grouped_tc2(const GroupedArgs 
         }
         tc_fence_after();
         const uint32_t d0 = tmem + (uint32_t)(b * k2AccCols);
-        for (int kb = 0; kb < nk; ++kb) {
-          if (!mbar_wait(ready0 + 8u * sr, pr)) {
+        for (int kp = 0; kp < nk; kp += 2, ++q) {
+          if (!mbar_wait(ready0 + 8u * (q % k2RStages), (uint32_t)(q / k2RStages) & 1u)) {
             ok = false;
             break;
           }
           tc_fence_after();
-          const uint64_t da = umma_desc_sw128(ringA + (uint32_t)sa * k2ABytes);
-          const uint64_t db = umma_desc_sw128(ringB + (uint32_t)sb * k2BBytes);
 #pragma unroll
-          for (int j = 0; j < 4; ++j)  // K = 16 per MMA: advance the start address by 32 bytes
-            tc2_mma_f16(d0, da + 2u * j, db + 2u * j, idesc, (kb > 0 || j > 0) ? 1u : 0u);
-          tc2_commit_both(aempty0 + 8u * sa);  // frees both CTAs' stages once these MMAs have read them
-          tc2_commit_both(bempty0 + 8u * sb);
-          any_mma = true;
-          if (++sa == k2AStages) sa = 0;
-          if (++sb == k2BStages) sb = 0;
-          if (++sr == k2RStages) {
-            sr = 0;
-            pr ^= 1u;
+          for (int h = 0; h < 2; ++h) {
+            const int slot = (2 * q + h) % k2AStages;
+            const uint64_t da = umma_desc_sw128(ringA + (uint32_t)slot * k2ABytes);
+            const uint64_t db = umma_desc_sw128(ringB + (uint32_t)slot * k2BBytes);
+#pragma unroll
+            for (int j = 0; j < 4; ++j)  // K = 16 per MMA: advance the start address by 32 bytes
+              tc2_mma_f16(d0, da + 2u * j, db + 2u * j, idesc, (kp > 0 || h > 0 || j > 0) ? 1u : 0u);
           }
+          tc2_commit_both(empty0 + 8u * (q % k2Pairs));  // frees both CTAs' stages once these MMAs have read them
+          any_mma = true;
         }
         if (!ok) break;
         tc2_commit_both(tfull0 + 8u * b);
@@ -492,116 +476,189 @@ __global__ void __launch_bounds__(k2Threads, 1) k_grouped_tc2(const GroupedArgs 
     // ------------------------------------------------------ relay (both CTAs)
     // One thread per CTA turns "this CTA's stage is full" (its A warps'
     // arrivals and its B tensor copy) into one arrival on the leader's ready
-    // barrier, so the MMA thread waits on a single barrier per k-block.  The
+    // barrier, so the MMA thread waits on a single barrier per pair.  The
     // relay has observed the stage's writes (acquire) before it arrives; the
     // peer's arrival is relaxed, because a release at cluster scope here
     // would wait for every memory access the SM has in flight (the tensor
     // copies and weight loads of the next stages) and stall the pipeline by
-    // about half a microsecond per k-block.  The leader's MMAs read the peer's
+    // about half a microsecond per pair.  The leader's MMAs read the peer's
     // stage only after that arrival, when its writes have completed.
     if (lane == 0) {
       const uint32_t ready_leader = mapa(ready0, 0);
-      int sa = 0, sb = 0, sr = 0;
-      uint32_t pa = 0, pb = 0;
+      int q = 0;
       for (int w = w0; w < W && ok; w += wstep) {
-        for (int kb = 0; kb < nk; ++kb) {
-          if (!mbar_wait(afull0 + 8u * sa, pa) || !mbar_wait(bfull0 + 8u * sb, pb)) {
-            ok = false;
-            break;
+        for (int kp = 0; kp < nk && ok; kp += 2, ++q) {
+#pragma unroll
+          for (int h = 0; h < 2; ++h) {
+            const int n = 2 * q + h, slot = n % k2AStages;
+            const uint32_t ph = (uint32_t)(n / k2AStages) & 1u;
+            if (!mbar_wait(afull0 + 8u * slot, ph) || !mbar_wait(bfull0 + 8u * slot, ph)) {
+              ok = false;
+              break;
+            }
           }
+          if (!ok) break;
           if (rank == 0)
-            mbar_arrive(ready0 + 8u * sr);
+            mbar_arrive(ready0 + 8u * (q % k2RStages));
           else
-            asm volatile("mbarrier.arrive.relaxed.cluster.shared::cluster.b64 _, [%0];" ::"r"(ready_leader + 8u * sr)
+            asm volatile("mbarrier.arrive.relaxed.cluster.shared::cluster.b64 _, [%0];" ::"r"(
+                             ready_leader + 8u * (q % k2RStages))
                          : "memory");
-          if (++sa == k2AStages) {
-            sa = 0;
-            pa ^= 1u;
-          }
-          if (++sb == k2BStages) {
-            sb = 0;
-            pb ^= 1u;
-          }
-          if (++sr == k2RStages) sr = 0;
         }
       }
     }
     __syncwarp();
+  } else if (warp == k2LoadWarp) {
+    // ------------------------------------------------------ raw weight loader
+    // One bulk copy per k-block of this CTA's 128-row block of the item's
+    // expert: the packed codes and scales of a 64-K step are contiguous.
+    if (lane == 0) {
+      constexpr uint32_t SB = WF == W_NVFP4 ? 4608u : 4352u;
+      int r = 0;
+      uint32_t phase = 0;
+      uint32_t issued = 0, issued_parity = 0;  // per slot: has a copy, parity of its last phase
+      for (int w = w0; w < W && ok; w += wstep) {
+        const Tc2Item it = cur.at(a, w, nbp);
+        const int blk = 2 * it.bp + (int)rank;
+        const uint8_t *src = a.codes + (size_t)it.e * a.codes_expert + (size_t)blk * nk * SB;
+        for (int kb = 0; kb < nk; ++kb) {
+          if (!mbar_wait(rempty0 + 8u * r, phase ^ 1u)) {
+            ok = false;
+            break;
+          }
+          const uint32_t bar = rfull0 + 8u * r;
+          mbar_expect_tx(bar, SB);
+          bulk_g2s(ringR + (uint32_t)r * k2RawBytes, src + (size_t)kb * SB, SB, bar);
+          issued |= 1u << r;
+          issued_parity = (issued_parity & ~(1u << r)) | (phase << r);
+          if (++r == k2RawStages) {
+            r = 0;
+            phase ^= 1u;
+          }
+        }
+      }
+      // Never leave with a bulk copy in flight into this CTA's shared memory.
+      for (int i = 0; i < k2RawStages; ++i)
+        if (issued & (1u << i)) mbar_wait(rfull0 + 8u * i, (issued_parity >> i) & 1u);
+    }
+    __syncwarp();
   } else {
     // ------------------------------------------------------ epilogue (both CTAs)
+    // The column factors of an item (slot -> pair -> activation factor and
+    // topk weight: two dependent global loads) are fetched one item ahead into
+    // shared memory by the 128 epilogue threads, so their latency overlaps the
+    // previous item's epilogue instead of stalling every 32-column chunk.  The
+    // four warps decide together (barrier with an AND vote) whether to go on,
+    // so none waits at the barrier for a warp that has stopped.
     const int m = warp * 32 + lane;  // accumulator row = TMEM lane
     const float *gl_all = a.globals;
     const uint32_t tempty_leader = mapa(tempty0, 0);
+    float *colf = colinfo, *colw = colinfo + 2 * k2MaxN;
+    int pn[2];
+    auto fetch_pairs = [&](const Tc2Item &it) {
+#pragma unroll
+      for (int q = 0; q < 2; ++q) {
+        const int nl = m + 128 * q;
+        pn[q] = nl < it.ntok ? a.sorted_pair[it.s0 + nl] : -1;
+      }
+    };
+    float fn[2], wn[2];
+    auto fetch_factors = [&](const Tc2Item &it) {
+#pragma unroll
+      for (int q = 0; q < 2; ++q) {
+        fn[q] = 0.f;
+        wn[q] = 0.f;
+        if (pn[q] >= 0) {
+          const int sl = it.s0 + m + 128 * q;
+          fn[q] = a.act_g ? a.act_g[a.act_by_token ? (int64_t)(pn[q] / a.top_k) : (int64_t)sl] : 1.f;
+          if (STAGE == STAGE_DOWN) wn[q] = a.topk_weights[pn[q]];
+        }
+      }
+    };
+    auto put_factors = [&](int buf) {
+#pragma unroll
+      for (int q = 0; q < 2; ++q) {
+        colf[buf * k2MaxN + m + 128 * q] = fn[q];
+        colw[buf * k2MaxN + m + 128 * q] = wn[q];
+      }
+    };
     pdl_wait();  // row factors come from the preceding kernels
+    Tc2Item it_next{};
+    if (w0 < W) {
+      it_next = cur.at(a, w0, nbp);
+      fetch_pairs(it_next);
+      fetch_factors(it_next);
+      put_factors(0);
+    }
+    epi_bar_sync();
     int li = 0;
     for (int w = w0; w < W && ok; w += wstep, ++li) {
-      const Tc2Item it = cur.at(a, w, nbp);
+      const Tc2Item it = it_next;
+      const bool more = w + wstep < W;
+      if (more) {
+        it_next = cur.at(a, w + wstep, nbp);
+        fetch_pairs(it_next);
+      }
       const int b = li & 1;
-      if (!mbar_wait(tfull0 + 8u * b, (li >> 1) & 1)) {
-        ok = false;
-        break;
-      }
-      tc_fence_after();
-      const float *gl = gl_all + 4 * it.e;
-      const int blk = 2 * it.bp + (int)rank;
-      const int tile = 8 * blk + (m >> 4), rr = m & 15;
-      for (int c0 = 0; c0 < it.n; c0 += 32) {
-        // Column info (slot, activation factor, topk weight) is fetched once per
-        // 32-column chunk, one column per lane, and broadcast with shuffles.
-        const int nl = c0 + lane;
-        const int sl = it.s0 + nl;
-        float f_l = 0.f, w_l = 0.f;
-        if (nl < it.ntok) {
-          const int p = a.sorted_pair[sl];
-          f_l = a.act_g ? a.act_g[a.act_by_token ? (int64_t)(p / a.top_k) : (int64_t)sl] : 1.f;
-          if (STAGE == STAGE_DOWN) w_l = a.topk_weights[p] * gl[2];
-        }
-        uint32_t raw[32];
-        tc_ld32(tmem + ((uint32_t)(warp * 32) << 16) + (uint32_t)(b * k2AccCols + c0), raw);
-        float hv[32];
+      const bool got = mbar_wait(tfull0 + 8u * b, (li >> 1) & 1);
+      if (more) fetch_factors(it_next);
+      if (got) {
+        tc_fence_after();
+        const float *gl = gl_all + 4 * it.e;
+        const int blk = 2 * it.bp + (int)rank;
+        const int tile = 8 * blk + (m >> 4), rr = m & 15;
+        for (int c0 = 0; c0 < it.n; c0 += 32) {
+          const float f_l = colf[b * k2MaxN + c0 + lane];
+          const float w_l = STAGE == STAGE_DOWN ? colw[b * k2MaxN + c0 + lane] * gl[2] : 0.f;
+          uint32_t raw[32];
+          tc_ld32(tmem + ((uint32_t)(warp * 32) << 16) + (uint32_t)(b * k2AccCols + c0), raw);
+          float hv[32];
 #pragma unroll
-        for (int j = 0; j < 32; ++j) {
-          const int n = c0 + j;
-          const bool live = n < it.ntok;
-          const int s = it.s0 + n;
-          const float f = __shfl_sync(0xffffffffu, f_l, j);
-          const float v = __uint_as_float(raw[j]) * f;
-          hv[j] = 0.f;
-          if (STAGE == STAGE_GATED) {
-            const float up = __shfl_down_sync(0xffffffffu, v, 8);
-            if (rr < 8) {
-              const float h = silu_f32(v * gl[0]) * (up * gl[1]);
-              if (live) a.out[(size_t)s * a.n_rows + tile * 8 + rr] = h;
-              hv[j] = live ? fabsf(h) : 0.f;
-            }
-          } else if (STAGE == STAGE_RELU2) {
-            const float r = fmaxf(v * gl[0], 0.f);
-            if (live) a.out[(size_t)s * a.n_rows + tile * 16 + rr] = r * r;
-            hv[j] = live ? r * r : 0.f;
-          } else {
-            const float wt = __shfl_sync(0xffffffffu, w_l, j);
-            if (live) store_partial(a, (size_t)s * a.n_rows + blk * 128 + m, wt * v);
-          }
-        }
-        if (STAGE != STAGE_DOWN && a.out_amax != nullptr) {
-          // reduce-scatter max over the 32 lanes: lane l ends with column c0 + l
-#pragma unroll
-          for (int step = 16; step >= 1; step >>= 1) {
-            const bool upper = (lane & step) != 0;
-#pragma unroll
-            for (int j = 0; j < step; ++j) {
-              const float send = upper ? hv[j] : hv[j + step];
-              const float keep = upper ? hv[j + step] : hv[j];
-              hv[j] = fmaxf(keep, __shfl_xor_sync(0xffffffffu, send, step));
+          for (int j = 0; j < 32; ++j) {
+            const int n = c0 + j;
+            const bool live = n < it.ntok;
+            const int s = it.s0 + n;
+            const float f = __shfl_sync(0xffffffffu, f_l, j);
+            const float v = __uint_as_float(raw[j]) * f;
+            hv[j] = 0.f;
+            if (STAGE == STAGE_GATED) {
+              const float up = __shfl_down_sync(0xffffffffu, v, 8);
+              if (rr < 8) {
+                const float h = silu_f32(v * gl[0]) * (up * gl[1]);
+                if (live) a.out[(size_t)s * a.n_rows + tile * 8 + rr] = h;
+                hv[j] = live ? fabsf(h) : 0.f;
+              }
+            } else if (STAGE == STAGE_RELU2) {
+              const float r = fmaxf(v * gl[0], 0.f);
+              if (live) a.out[(size_t)s * a.n_rows + tile * 16 + rr] = r * r;
+              hv[j] = live ? r * r : 0.f;
+            } else {
+              const float wt = __shfl_sync(0xffffffffu, w_l, j);
+              if (live) store_partial(a, (size_t)s * a.n_rows + blk * 128 + m, wt * v);
             }
           }
-          const int n = c0 + lane;
-          if (n < it.ntok) atomicMax(reinterpret_cast<unsigned *>(a.out_amax) + it.s0 + n, __float_as_uint(hv[0]));
+          if (STAGE != STAGE_DOWN && a.out_amax != nullptr) {
+            // reduce-scatter max over the 32 lanes: lane l ends with column c0 + l
+#pragma unroll
+            for (int step = 16; step >= 1; step >>= 1) {
+              const bool upper = (lane & step) != 0;
+#pragma unroll
+              for (int j = 0; j < step; ++j) {
+                const float send = upper ? hv[j] : hv[j + step];
+                const float keep = upper ? hv[j + step] : hv[j];
+                hv[j] = fmaxf(keep, __shfl_xor_sync(0xffffffffu, send, step));
+              }
+            }
+            const int n = c0 + lane;
+            if (n < it.ntok) atomicMax(reinterpret_cast<unsigned *>(a.out_amax) + it.s0 + n, __float_as_uint(hv[0]));
+          }
         }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive_remote(tempty_leader + 8u * b);
       }
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive_remote(tempty_leader + 8u * b);
+      if (more) put_factors((li + 1) & 1);
+      ok = epi_bar_and(got);  // buffer li + 1 is complete; buffer li is no longer read
     }
   }
 
@@ -618,10 +675,12 @@ __global__ void __launch_bounds__(k2Threads, 1) k_grouped_tc2(const GroupedArgs 
     asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(tmem), "n"(k2TmemCols));
 }
 
-static size_t tc2_smem_bytes() { return (size_t)k2RingBytes + 1024 + 8 * k2Bars + 16; }
-static_assert(k2RingBytes + 1024 + 8 * k2Bars + 16 <= 227 * 1024, "shared memory budget");
+constexpr int k2ColBytes = 4 * k2MaxN * 4;
+static size_t tc2_smem_bytes() { return (size_t)k2RingBytes + 1024 + 8 * k2Bars + 16 + k2ColBytes; }
+static_assert(k2RingBytes + 1024 + 8 * k2Bars + 16 + k2ColBytes <= 227 * 1024, "shared memory budget");
+static_assert((8 * k2Bars + 16) % 16 == 0, "column factors are 16-byte aligned");
 
-bool tc2_supported(int rows_total, int K) { return rows_total % 256 == 0 && K % 64 == 0; }
+bool tc2_supported(int rows_total, int K) { return rows_total % 256 == 0 && K % 128 == 0; }
 
 template <int STAGE, int WF>
 static cudaError_t launch_tc2_one(const GroupedArgs &a, int rows_total, int64_t b_rows, cudaStream_t s) {
