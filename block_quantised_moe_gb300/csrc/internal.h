@@ -48,6 +48,7 @@ struct WeightLayout {
 struct ScratchLayout {
   int64_t cap_sorted = 0;  // rows of the padded, expert-sorted pair list
   size_t status = 0, counts = 0, offsets = 0, sorted = 0, pair_pos = 0, active = 0, passes = 0, large = 0, large_tiles = 0;
+  size_t tiles = 0;       // token-tile records of the large experts (int4 each)
   size_t route_hist = 0;  // per-chunk expert counts of the chunked routing sort
   size_t work = 0;        // 2 x kWorkSlots work counters of the register-dequant kernel (GEMM1, GEMM2)
   size_t xq_codes = 0, xq_scales = 0, xq_g = 0;
@@ -86,7 +87,8 @@ struct GroupedArgs {
   const int32_t *active;  // [0] = number of experts with pairs, [1..] their ids (ascending)
   const int32_t *passes;  // [i] = passes of active experts before i (prefix, n_active + 1 entries)
   const int32_t *large;        // experts for the tcgen05 kernel: [0] = n, [1..] ids
-  const int32_t *large_tiles;  // [i] = 128-token tiles of large experts before i (prefix)
+  const int32_t *large_tiles;  // [i] = token tiles of large experts before i (prefix)
+  const int4 *tiles;           // per token tile of the large experts: (expert, first slot, live tokens, 0)
   int act_by_token;            // tcgen05 kernel: B rows indexed by token (GEMM1) or by slot (GEMM2)
   int32_t *status;        // device status word (timeout flag)
   int32_t *work;          // register-dequant kernel: kWorkSlots zeroed item counters
@@ -122,8 +124,8 @@ struct RouteStaging {
 int route_chunks(int P);
 cudaError_t launch_route(const int32_t *ids, int P, int E, int pad, int ntok, int large_min, int large_tile,
                          int32_t *counts, int32_t *offsets, int32_t *sorted_pair, int32_t *pair_pos, int32_t *active,
-                         int32_t *passes, int32_t *large, int32_t *large_tiles, int32_t *status, int32_t *chunk_hist,
-                         int32_t *work, int work_n, const RouteStaging *stg, cudaStream_t s);
+                         int32_t *passes, int32_t *large, int32_t *large_tiles, int4 *tiles, int32_t *status,
+                         int32_t *chunk_hist, int32_t *work, int work_n, const RouteStaging *stg, cudaStream_t s);
 
 // Register-dequant tensor-core grouped kernel (experts with few pairs), NVFP4 or
 // MXFP4 weights (wfmt); rows_total = rows of the stage's weight matrix (2I gated,

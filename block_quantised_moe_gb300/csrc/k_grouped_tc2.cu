@@ -90,6 +90,15 @@ static_assert(k2AWarps * 32 == 256 && 256 % (k2AGroups * 32) == 0, "8 fragment c
 
 // ------------------------------------------------------------ cluster helpers
 
+// True in exactly one lane of the (converged) warp, the same lane every time.
+__device__ __forceinline__ bool elect_one() {
+  uint32_t pred = 0;
+  asm volatile(
+      "{\n\t.reg .b32 r;\n\t.reg .pred p;\n\telect.sync r|p, 0xffffffff;\n\tselp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(pred));
+  return pred != 0;
+}
+
 // Named barrier 1 over the four epilogue warps (threads 0..127).
 __device__ __forceinline__ void epi_bar_sync() { asm volatile("bar.sync 1, 128;" ::: "memory"); }
 // The same barrier, returning whether every epilogue thread passed `v`.
@@ -237,36 +246,21 @@ struct Tc2Item {
   int e, s0, ntok, n, bp;  // expert, first slot, live tokens, MMA N, row-block pair
 };
 
-// Items (large expert i, token tile, row-block pair), in that order;
-// tiles[i] is the per-expert prefix of ceil(count / 256).  An expert's tiles
-// have equal sizes (a multiple of 16), the last one possibly shorter.
-struct Tc2Cursor {
-  int i = 0;
-  __device__ __forceinline__ void seek(const GroupedArgs &a, int w, int nbp) {
-    int lo = 0, hi = a.large[0] - 1;
-    while (lo < hi) {
-      const int mid = (lo + hi) >> 1;
-      if (a.large_tiles[mid + 1] * nbp > w) hi = mid;
-      else lo = mid + 1;
-    }
-    i = lo;
-  }
-  __device__ __forceinline__ Tc2Item at(const GroupedArgs &a, int w, int nbp) {
-    while (a.large_tiles[i + 1] * nbp <= w) ++i;
-    Tc2Item it;
-    it.e = a.large[1 + i];
-    const int nt = a.large_tiles[i + 1] - a.large_tiles[i];
-    const int local = w - a.large_tiles[i] * nbp;
-    const int tile = local / nbp;
-    it.bp = local % nbp;
-    const int cnt = a.counts[it.e];
-    const int tsz = (((cnt + nt - 1) / nt) + 15) & ~15;
-    it.s0 = a.offsets[it.e] + tile * tsz;
-    it.ntok = max(0, min(tsz, cnt - tile * tsz));
-    it.n = max(16, (it.ntok + 15) & ~15);
-    return it;
-  }
-};
+// Items (token tile of a large expert, row-block pair), in that order: item w
+// is row-block pair w % nbp of tile w / nbp, whose record the routing wrote
+// (expert, first slot, live tokens).  The MMA's N is the live tokens rounded
+// up to 16.  Every role loads the next item's record while it works on the
+// current one, so no dependent global load sits between two items.
+__device__ __forceinline__ int4 tc2_record(const GroupedArgs &a, int w, int nbp) { return a.tiles[w / nbp]; }
+__device__ __forceinline__ Tc2Item tc2_item(const int4 r, int w, int nbp) {
+  Tc2Item it;
+  it.e = r.x;
+  it.s0 = r.y;
+  it.ntok = r.z;
+  it.n = max(16, (r.z + 15) & ~15);
+  it.bp = w % nbp;
+  return it;
+}
 
 // ------------------------------------------------------------------ kernel
 
@@ -283,8 +277,7 @@ __global__ void __launch_bounds__(k2Threads, 1) k_grouped_tc2(const GroupedArgs 
   const uint8_t *rawR = base + (ringR - base_s);
   uint64_t *bars = reinterpret_cast<uint64_t *>(base + k2RingBytes);
   uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + k2Bars);
-  // per-column factors of the epilogue, two items deep: [2][k2MaxN] activation
-  // factor, then [2][k2MaxN] topk weight
+  // per-column factor of the epilogue, two items deep: [2][k2MaxN]
   float *colinfo = reinterpret_cast<float *>(base + k2RingBytes + 8 * k2Bars + 16);
   const uint32_t afull0 = (uint32_t)__cvta_generic_to_shared(bars);  // this CTA's A tile is written
   const uint32_t bfull0 = afull0 + 8u * k2AStages;                   // this CTA's B tile has landed
@@ -337,8 +330,7 @@ __global__ void __launch_bounds__(k2Threads, 1) k_grouped_tc2(const GroupedArgs 
   // Items are dealt round-robin over clusters: at any moment the pairs work on
   // neighbouring items, which share token tiles and weight blocks in L2.
   const int w0 = (int)cluster_id_x(), wstep = (int)cluster_count_x();
-  Tc2Cursor cur;
-  if (w0 < W) cur.seek(a, w0, nbp);
+  const int4 rec0 = w0 < W ? tc2_record(a, w0, nbp) : make_int4(0, 0, 0, 0);
   bool ok = true;
   bool any_mma = false;
 
@@ -396,22 +388,28 @@ __global__ void __launch_bounds__(k2Threads, 1) k_grouped_tc2(const GroupedArgs 
     // so a stage's B half is one 2-D tensor copy: rows [s0 + rank * N/2, +128)
     // x columns [64 kb, +64).  Rows past the tile's live tokens feed only MMA
     // columns that the epilogue discards; rows past the tensor read as zeros.
-    if (lane == 0) {
+    // The whole warp runs the loop; one elected lane issues the copies.
+    {
       int slot = 0;
       uint32_t phase = 0;
       uint32_t issued = 0, issued_parity = 0;  // per slot: has a copy, parity of its last phase
       pdl_wait();  // activation rows come from the preceding kernels
+      int4 rec = rec0;
       for (int w = w0; w < W && ok; w += wstep) {
-        const Tc2Item it = cur.at(a, w, nbp);
+        const Tc2Item it = tc2_item(rec, w, nbp);
+        if (w + wstep < W) rec = tc2_record(a, w + wstep, nbp);
         const int y = it.s0 + (int)rank * (it.n >> 1);
         for (int kb = 0; kb < nk; ++kb) {
-          if (!mbar_wait(empty0 + 8u * (slot >> 1), phase ^ 1u)) {
+          if (!__all_sync(0xffffffffu, mbar_wait(empty0 + 8u * (slot >> 1), phase ^ 1u))) {
             ok = false;
             break;
           }
           const uint32_t bar = bfull0 + 8u * slot;
-          mbar_expect_tx(bar, k2BBytes);
-          tma_load_2d(ringB + (uint32_t)slot * k2BBytes, &bmap, kb * 64, y, bar);
+          if (elect_one()) {
+            mbar_expect_tx(bar, k2BBytes);
+            tma_load_2d(ringB + (uint32_t)slot * k2BBytes, &bmap, kb * 64, y, bar);
+          }
+          __syncwarp();
           issued |= 1u << slot;
           issued_parity = (issued_parity & ~(1u << slot)) | (phase << slot);
           if (++slot == k2BStages) {
@@ -427,46 +425,57 @@ __global__ void __launch_bounds__(k2Threads, 1) k_grouped_tc2(const GroupedArgs 
     __syncwarp();
   } else if (warp == k2MmaWarp) {
     // ------------------------------------------------------ MMA issuer (leader CTA)
-    if (rank == 0 && lane == 0) {
+    // The whole warp runs the loop (waits, counters, descriptors), so every
+    // operand of the MMAs is warp-uniform, and one elected lane issues the
+    // MMAs and commits.  Issued from a single-thread branch instead, each
+    // cta_group::2 MMA cost about 130 cycles of issue whatever its N, which
+    // capped the tensor pipe at half its rate for N near 128.
+    if (rank == 0) {
       constexpr uint32_t fmt = WF == W_MXFP4 ? 1u : 0u;  // operand type: 0 = F16, 1 = BF16
       const uint32_t idesc0 = (1u << 4) | (fmt << 7) | (fmt << 10) | ((uint32_t)(256 >> 4) << 24);
       int q = 0, li = 0;  // pairs of k-blocks consumed over the launch
+      int4 rec = rec0;
       for (int w = w0; w < W && ok; w += wstep, ++li) {
-        const Tc2Item it = cur.at(a, w, nbp);
+        const Tc2Item it = tc2_item(rec, w, nbp);
+        if (w + wstep < W) rec = tc2_record(a, w + wstep, nbp);
         const uint32_t idesc = idesc0 | ((uint32_t)(it.n >> 3) << 17);
         const int b = li & 1;
-        if (!mbar_wait_c(tempty0 + 8u * b, ((li >> 1) & 1) ^ 1u)) {
+        if (!__all_sync(0xffffffffu, mbar_wait_c(tempty0 + 8u * b, ((li >> 1) & 1) ^ 1u))) {
           ok = false;
           break;
         }
         tc_fence_after();
         const uint32_t d0 = tmem + (uint32_t)(b * k2AccCols);
         for (int kp = 0; kp < nk; kp += 2, ++q) {
-          if (!mbar_wait(ready0 + 8u * (q % k2RStages), (uint32_t)(q / k2RStages) & 1u)) {
+          if (!__all_sync(0xffffffffu, mbar_wait(ready0 + 8u * (q % k2RStages), (uint32_t)(q / k2RStages) & 1u))) {
             ok = false;
             break;
           }
           tc_fence_after();
+          if (elect_one()) {
 #pragma unroll
-          for (int h = 0; h < 2; ++h) {
-            const int slot = (2 * q + h) % k2AStages;
-            const uint64_t da = umma_desc_sw128(ringA + (uint32_t)slot * k2ABytes);
-            const uint64_t db = umma_desc_sw128(ringB + (uint32_t)slot * k2BBytes);
+            for (int h = 0; h < 2; ++h) {
+              const int slot = (2 * q + h) % k2AStages;
+              const uint64_t da = umma_desc_sw128(ringA + (uint32_t)slot * k2ABytes);
+              const uint64_t db = umma_desc_sw128(ringB + (uint32_t)slot * k2BBytes);
 #pragma unroll
-            for (int j = 0; j < 4; ++j)  // K = 16 per MMA: advance the start address by 32 bytes
-              tc2_mma_f16(d0, da + 2u * j, db + 2u * j, idesc, (kp > 0 || h > 0 || j > 0) ? 1u : 0u);
+              for (int j = 0; j < 4; ++j)  // K = 16 per MMA: advance the start address by 32 bytes
+                tc2_mma_f16(d0, da + 2u * j, db + 2u * j, idesc, (kp > 0 || h > 0 || j > 0) ? 1u : 0u);
+            }
+            tc2_commit_both(empty0 + 8u * (q % k2Pairs));  // frees both CTAs' stages once these MMAs have read them
           }
-          tc2_commit_both(empty0 + 8u * (q % k2Pairs));  // frees both CTAs' stages once these MMAs have read them
+          __syncwarp();
           any_mma = true;
         }
         if (!ok) break;
-        tc2_commit_both(tfull0 + 8u * b);
+        if (elect_one()) tc2_commit_both(tfull0 + 8u * b);
+        __syncwarp();
       }
       // Every MMA of the pair completes before either CTA releases its shared
       // memory or the pair's tensor memory.
       if (any_mma) {
-        tc2_commit_both(drain);
-      } else {
+        if (elect_one()) tc2_commit_both(drain);
+      } else if (lane == 0) {
         mbar_arrive(drain);
         mbar_arrive_remote(mapa(drain, 1));
       }
@@ -512,23 +521,29 @@ __global__ void __launch_bounds__(k2Threads, 1) k_grouped_tc2(const GroupedArgs 
     // ------------------------------------------------------ raw weight loader
     // One bulk copy per k-block of this CTA's 128-row block of the item's
     // expert: the packed codes and scales of a 64-K step are contiguous.
-    if (lane == 0) {
+    // The whole warp runs the loop; one elected lane issues the copies.
+    {
       constexpr uint32_t SB = WF == W_NVFP4 ? 4608u : 4352u;
       int r = 0;
       uint32_t phase = 0;
       uint32_t issued = 0, issued_parity = 0;  // per slot: has a copy, parity of its last phase
+      int4 rec = rec0;
       for (int w = w0; w < W && ok; w += wstep) {
-        const Tc2Item it = cur.at(a, w, nbp);
+        const Tc2Item it = tc2_item(rec, w, nbp);
+        if (w + wstep < W) rec = tc2_record(a, w + wstep, nbp);
         const int blk = 2 * it.bp + (int)rank;
         const uint8_t *src = a.codes + (size_t)it.e * a.codes_expert + (size_t)blk * nk * SB;
         for (int kb = 0; kb < nk; ++kb) {
-          if (!mbar_wait(rempty0 + 8u * r, phase ^ 1u)) {
+          if (!__all_sync(0xffffffffu, mbar_wait(rempty0 + 8u * r, phase ^ 1u))) {
             ok = false;
             break;
           }
           const uint32_t bar = rfull0 + 8u * r;
-          mbar_expect_tx(bar, SB);
-          bulk_g2s(ringR + (uint32_t)r * k2RawBytes, src + (size_t)kb * SB, SB, bar);
+          if (elect_one()) {
+            mbar_expect_tx(bar, SB);
+            bulk_g2s(ringR + (uint32_t)r * k2RawBytes, src + (size_t)kb * SB, SB, bar);
+          }
+          __syncwarp();
           issued |= 1u << r;
           issued_parity = (issued_parity & ~(1u << r)) | (phase << r);
           if (++r == k2RawStages) {
@@ -544,16 +559,16 @@ __global__ void __launch_bounds__(k2Threads, 1) k_grouped_tc2(const GroupedArgs 
     __syncwarp();
   } else {
     // ------------------------------------------------------ epilogue (both CTAs)
-    // The column factors of an item (slot -> pair -> activation factor and
-    // topk weight: two dependent global loads) are fetched one item ahead into
-    // shared memory by the 128 epilogue threads, so their latency overlaps the
-    // previous item's epilogue instead of stalling every 32-column chunk.  The
-    // four warps decide together (barrier with an AND vote) whether to go on,
-    // so none waits at the barrier for a warp that has stopped.
+    // Each column's factor (activation factor; for the down projection times
+    // the topk weight and the expert's global scale) is fetched one item ahead
+    // into shared memory by the 128 epilogue threads (slot -> pair -> factors:
+    // dependent global loads whose latency then overlaps the previous item's
+    // epilogue) and read back as broadcast vector loads.  The four warps decide
+    // together (barrier with an AND vote) whether to go on, so none waits at
+    // the barrier for a warp that has stopped.
     const int m = warp * 32 + lane;  // accumulator row = TMEM lane
-    const float *gl_all = a.globals;
     const uint32_t tempty_leader = mapa(tempty0, 0);
-    float *colf = colinfo, *colw = colinfo + 2 * k2MaxN;
+    float *__restrict__ outp = a.out;
     int pn[2];
     auto fetch_pairs = [&](const Tc2Item &it) {
 #pragma unroll
@@ -562,41 +577,48 @@ __global__ void __launch_bounds__(k2Threads, 1) k_grouped_tc2(const GroupedArgs 
         pn[q] = nl < it.ntok ? a.sorted_pair[it.s0 + nl] : -1;
       }
     };
-    float fn[2], wn[2];
+    float cn[2], gn = 1.f;
     auto fetch_factors = [&](const Tc2Item &it) {
+      // the expert's global scale of this thread's rows (gate / up / single
+      // matrix), applied in the epilogue; the down projection's goes into the
+      // column factor
+      gn = a.globals[4 * it.e + ((STAGE == STAGE_GATED && (m & 15) >= 8) ? 1 : 0)];
+      const float g2 = STAGE == STAGE_DOWN ? a.globals[4 * it.e + 2] : 1.f;
 #pragma unroll
       for (int q = 0; q < 2; ++q) {
-        fn[q] = 0.f;
-        wn[q] = 0.f;
+        cn[q] = 0.f;
         if (pn[q] >= 0) {
           const int sl = it.s0 + m + 128 * q;
-          fn[q] = a.act_g ? a.act_g[a.act_by_token ? (int64_t)(pn[q] / a.top_k) : (int64_t)sl] : 1.f;
-          if (STAGE == STAGE_DOWN) wn[q] = a.topk_weights[pn[q]];
+          const float f = a.act_g ? a.act_g[a.act_by_token ? (int64_t)(pn[q] / a.top_k) : (int64_t)sl] : 1.f;
+          cn[q] = STAGE == STAGE_DOWN ? f * (a.topk_weights[pn[q]] * g2) : f;
         }
       }
     };
     auto put_factors = [&](int buf) {
 #pragma unroll
-      for (int q = 0; q < 2; ++q) {
-        colf[buf * k2MaxN + m + 128 * q] = fn[q];
-        colw[buf * k2MaxN + m + 128 * q] = wn[q];
-      }
+      for (int q = 0; q < 2; ++q) colinfo[buf * k2MaxN + m + 128 * q] = cn[q];
     };
     pdl_wait();  // row factors come from the preceding kernels
     Tc2Item it_next{};
+    float gsel_next = 1.f;
+    int4 rec = make_int4(0, 0, 0, 0);  // record of the item after next
     if (w0 < W) {
-      it_next = cur.at(a, w0, nbp);
+      it_next = tc2_item(rec0, w0, nbp);
+      if (w0 + wstep < W) rec = tc2_record(a, w0 + wstep, nbp);
       fetch_pairs(it_next);
       fetch_factors(it_next);
       put_factors(0);
+      gsel_next = gn;
     }
     epi_bar_sync();
     int li = 0;
     for (int w = w0; w < W && ok; w += wstep, ++li) {
       const Tc2Item it = it_next;
+      const float gsel = gsel_next;
       const bool more = w + wstep < W;
       if (more) {
-        it_next = cur.at(a, w + wstep, nbp);
+        it_next = tc2_item(rec, w + wstep, nbp);
+        if (w + 2 * wstep < W) rec = tc2_record(a, w + 2 * wstep, nbp);
         fetch_pairs(it_next);
       }
       const int b = li & 1;
@@ -604,60 +626,101 @@ __global__ void __launch_bounds__(k2Threads, 1) k_grouped_tc2(const GroupedArgs 
       if (more) fetch_factors(it_next);
       if (got) {
         tc_fence_after();
-        const float *gl = gl_all + 4 * it.e;
         const int blk = 2 * it.bp + (int)rank;
         const int tile = 8 * blk + (m >> 4), rr = m & 15;
+        const float *colc = colinfo + b * k2MaxN;
         for (int c0 = 0; c0 < it.n; c0 += 32) {
-          const float f_l = colf[b * k2MaxN + c0 + lane];
-          const float w_l = STAGE == STAGE_DOWN ? colw[b * k2MaxN + c0 + lane] * gl[2] : 0.f;
           uint32_t raw[32];
           tc_ld32(tmem + ((uint32_t)(warp * 32) << 16) + (uint32_t)(b * k2AccCols + c0), raw);
-          float hv[32];
+          float v[32];
 #pragma unroll
-          for (int j = 0; j < 32; ++j) {
-            const int n = c0 + j;
-            const bool live = n < it.ntok;
-            const int s = it.s0 + n;
-            const float f = __shfl_sync(0xffffffffu, f_l, j);
-            const float v = __uint_as_float(raw[j]) * f;
-            hv[j] = 0.f;
-            if (STAGE == STAGE_GATED) {
-              const float up = __shfl_down_sync(0xffffffffu, v, 8);
-              if (rr < 8) {
-                const float h = silu_f32(v * gl[0]) * (up * gl[1]);
-                if (live) a.out[(size_t)s * a.n_rows + tile * 8 + rr] = h;
-                hv[j] = live ? fabsf(h) : 0.f;
-              }
-            } else if (STAGE == STAGE_RELU2) {
-              const float r = fmaxf(v * gl[0], 0.f);
-              if (live) a.out[(size_t)s * a.n_rows + tile * 16 + rr] = r * r;
-              hv[j] = live ? r * r : 0.f;
-            } else {
-              const float wt = __shfl_sync(0xffffffffu, w_l, j);
-              if (live) store_partial(a, (size_t)s * a.n_rows + blk * 128 + m, wt * v);
-            }
+          for (int q = 0; q < 8; ++q) {
+            const float4 c4 = *reinterpret_cast<const float4 *>(colc + c0 + 4 * q);
+            v[4 * q + 0] = __uint_as_float(raw[4 * q + 0]) * c4.x;
+            v[4 * q + 1] = __uint_as_float(raw[4 * q + 1]) * c4.y;
+            v[4 * q + 2] = __uint_as_float(raw[4 * q + 2]) * c4.z;
+            v[4 * q + 3] = __uint_as_float(raw[4 * q + 3]) * c4.w;
           }
-          if (STAGE != STAGE_DOWN && a.out_amax != nullptr) {
-            // reduce-scatter max over the 32 lanes: lane l ends with column c0 + l
+          if (STAGE == STAGE_GATED) {
+            // Rows 0-7 of each 16-row group are gate rows, 8-15 the matching up
+            // rows.  Columns go in pairs: a gate lane finishes the even column
+            // (its up value from lane + 8), an up lane the odd one (its gate
+            // value from lane - 8), so every lane evaluates one SiLU per pair.
+            const bool up_lane = rr >= 8;
+            const int hrow = tile * 8 + (rr & 7);
+            float hv[16];
 #pragma unroll
-            for (int step = 16; step >= 1; step >>= 1) {
-              const bool upper = (lane & step) != 0;
-#pragma unroll
-              for (int j = 0; j < step; ++j) {
-                const float send = upper ? hv[j] : hv[j + step];
-                const float keep = upper ? hv[j + step] : hv[j];
-                hv[j] = fmaxf(keep, __shfl_xor_sync(0xffffffffu, send, step));
-              }
+            for (int p = 0; p < 16; ++p) {
+              const float x0 = v[2 * p] * gsel, x1 = v[2 * p + 1] * gsel;
+              const float other = __shfl_xor_sync(0xffffffffu, up_lane ? x0 : x1, 8);
+              const float gate = up_lane ? other : x0, up = up_lane ? x1 : other;
+              const float h = silu_f32(gate) * up;
+              const int n = c0 + 2 * p + (up_lane ? 1 : 0);
+              const bool live = n < it.ntok;
+              if (live) outp[(size_t)(it.s0 + n) * a.n_rows + hrow] = h;
+              hv[p] = live ? fabsf(h) : 0.f;
             }
-            const int n = c0 + lane;
-            if (n < it.ntok) atomicMax(reinterpret_cast<unsigned *>(a.out_amax) + it.s0 + n, __float_as_uint(hv[0]));
+            if (a.out_amax != nullptr) {
+              // reduce-scatter max over the 16 lanes holding the same column
+              // parity (lane bits 4, 2, 1, 0): lane l ends with pair
+              // (bit 4 of l) * 8 + (l & 7), column parity bit 3 of l
+#pragma unroll
+              for (int hs = 8, k = 0; hs >= 1; hs >>= 1, ++k) {
+                const int step = k == 0 ? 16 : hs;
+                const bool upper = (lane & step) != 0;
+#pragma unroll
+                for (int j = 0; j < hs; ++j) {
+                  const float send = upper ? hv[j] : hv[j + hs];
+                  const float keep = upper ? hv[j + hs] : hv[j];
+                  hv[j] = fmaxf(keep, __shfl_xor_sync(0xffffffffu, send, step));
+                }
+              }
+              const int n = c0 + 2 * (((lane >> 4) & 1) * 8 + (lane & 7)) + ((lane >> 3) & 1);
+              if (n < it.ntok)
+                atomicMax(reinterpret_cast<unsigned *>(a.out_amax) + it.s0 + n, __float_as_uint(hv[0]));
+            }
+          } else if (STAGE == STAGE_RELU2) {
+            float hv[32];
+#pragma unroll
+            for (int j = 0; j < 32; ++j) {
+              const int n = c0 + j;
+              const bool live = n < it.ntok;
+              const float r = fmaxf(v[j] * gsel, 0.f);
+              if (live) outp[(size_t)(it.s0 + n) * a.n_rows + tile * 16 + rr] = r * r;
+              hv[j] = live ? r * r : 0.f;
+            }
+            if (a.out_amax != nullptr) {
+              // reduce-scatter max over the 32 lanes: lane l ends with column c0 + l
+#pragma unroll
+              for (int step = 16; step >= 1; step >>= 1) {
+                const bool upper = (lane & step) != 0;
+#pragma unroll
+                for (int j = 0; j < step; ++j) {
+                  const float send = upper ? hv[j] : hv[j + step];
+                  const float keep = upper ? hv[j + step] : hv[j];
+                  hv[j] = fmaxf(keep, __shfl_xor_sync(0xffffffffu, send, step));
+                }
+              }
+              const int n = c0 + lane;
+              if (n < it.ntok)
+                atomicMax(reinterpret_cast<unsigned *>(a.out_amax) + it.s0 + n, __float_as_uint(hv[0]));
+            }
+          } else {
+#pragma unroll
+            for (int j = 0; j < 32; ++j) {
+              const int n = c0 + j;
+              if (n < it.ntok) store_partial(a, (size_t)(it.s0 + n) * a.n_rows + blk * 128 + m, v[j]);
+            }
           }
         }
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive_remote(tempty_leader + 8u * b);
       }
-      if (more) put_factors((li + 1) & 1);
+      if (more) {
+        put_factors((li + 1) & 1);
+        gsel_next = gn;
+      }
       ok = epi_bar_and(got);  // buffer li + 1 is complete; buffer li is no longer read
     }
   }
@@ -675,7 +738,7 @@ __global__ void __launch_bounds__(k2Threads, 1) k_grouped_tc2(const GroupedArgs 
     asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(tmem), "n"(k2TmemCols));
 }
 
-constexpr int k2ColBytes = 4 * k2MaxN * 4;
+constexpr int k2ColBytes = 2 * k2MaxN * 4;
 static size_t tc2_smem_bytes() { return (size_t)k2RingBytes + 1024 + 8 * k2Bars + 16 + k2ColBytes; }
 static_assert(k2RingBytes + 1024 + 8 * k2Bars + 16 + k2ColBytes <= 227 * 1024, "shared memory budget");
 static_assert((8 * k2Bars + 16) % 16 == 0, "column factors are 16-byte aligned");

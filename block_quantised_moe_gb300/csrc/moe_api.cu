@@ -193,6 +193,8 @@ moe_status moe_plan(const moe_caps *c, moe_plan_t *out, size_t *scratch_bytes, i
   S.passes = take(4 * (size_t)(L.E + 1));
   S.large = take(4 * (size_t)(L.E + 1));
   S.large_tiles = take(4 * (size_t)(L.E + 1));
+  // tiles of at least 128 tokens: at most one more per large expert than P / 128
+  S.tiles = take(16 * ((size_t)Pmax / 128 + (size_t)L.E + 1));
   S.route_hist = take(4 * (size_t)route_chunks((int)Pmax) * (L.E + 1));
   S.work = take(4 * 2 * (size_t)kWorkSlots);
   S.gbar = take(16);
@@ -306,7 +308,7 @@ static moe_status run_unified(moe_binding b, cudaStream_t stream, int withhold) 
   u.ntok = ntok;
   u.ro = RouteOut{at<int32_t>(sc, S.counts), at<int32_t>(sc, S.offsets), at<int32_t>(sc, S.sorted),
                   at<int32_t>(sc, S.pair_pos), at<int32_t>(sc, S.active), at<int32_t>(sc, S.passes),
-                  at<int32_t>(sc, S.large), at<int32_t>(sc, S.large_tiles), at<int32_t>(sc, S.status),
+                  at<int32_t>(sc, S.large), at<int32_t>(sc, S.large_tiles), at<int32_t>(sc, S.status), nullptr,
                   at<int32_t>(sc, S.work), 2 * kWorkSlots};
   u.x16 = at<__half>(sc, S.x16);
   u.xfac = at<float>(sc, S.xfac);
@@ -417,7 +419,8 @@ static moe_status run_forward(moe_binding b, cudaStream_t stream, cudaEvent_t *e
   const bool staged = P.afmt == MOE_A_BF16;
   if ((err = launch_route(b->ids, T * K, E, P.pad, ntok, P.large_min, P.tc2_on ? 256 : 128, counts, offsets, sorted,
                           pair_pos, active,
-                          passes, large, large_tiles, status, at<int32_t>(sc, S.route_hist), at<int32_t>(sc, S.work),
+                          passes, large, large_tiles, at<int4>(sc, S.tiles), status, at<int32_t>(sc, S.route_hist),
+                          at<int32_t>(sc, S.work),
                           2 * kWorkSlots, staged ? &stg : nullptr,
                           stream)) != cudaSuccess)
     return MOE_ERR_CUDA;
@@ -430,6 +433,7 @@ static moe_status run_forward(moe_binding b, cudaStream_t stream, cudaEvent_t *e
   a.passes = passes;
   a.large = large;
   a.large_tiles = large_tiles;
+  a.tiles = at<int4>(sc, S.tiles);
   a.status = status;
   a.top_k = K;
   a.topk_weights = b->w;
