@@ -89,6 +89,7 @@ struct GroupedArgs {
   const int32_t *large;        // experts for the tcgen05 kernel: [0] = n, [1..] ids
   const int32_t *large_tiles;  // [i] = token tiles of large experts before i (prefix)
   const int4 *tiles;           // per token tile of the large experts: (expert, first slot, live tokens, 0)
+                               // (balanced tiles of up to 256 for the CTA-pair kernel, 128 for the FP4 one)
   int act_by_token;            // tcgen05 kernel: B rows indexed by token (GEMM1) or by slot (GEMM2)
   int32_t *status;        // device status word (timeout flag)
   int32_t *work;          // register-dequant kernel: kWorkSlots zeroed item counters
@@ -124,8 +125,9 @@ struct RouteStaging {
 int route_chunks(int P);
 cudaError_t launch_route(const int32_t *ids, int P, int E, int pad, int ntok, int large_min, int large_tile,
                          int32_t *counts, int32_t *offsets, int32_t *sorted_pair, int32_t *pair_pos, int32_t *active,
-                         int32_t *passes, int32_t *large, int32_t *large_tiles, int4 *tiles, int32_t *status,
-                         int32_t *chunk_hist, int32_t *work, int work_n, const RouteStaging *stg, cudaStream_t s);
+                         int32_t *passes, int32_t *large, int32_t *large_tiles, int4 *tiles, int balanced,
+                         int32_t *status, int32_t *chunk_hist, int32_t *work, int work_n, const RouteStaging *stg,
+                         cudaStream_t s);
 
 // Register-dequant tensor-core grouped kernel (experts with few pairs), NVFP4 or
 // MXFP4 weights (wfmt); rows_total = rows of the stage's weight matrix (2I gated,

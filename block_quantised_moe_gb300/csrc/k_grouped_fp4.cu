@@ -28,6 +28,12 @@
 //   in-order pipe, between the MMAs, and measured slower.)
 // * Epilogue: D x the weights' FP32 global x the row's FP32 activation global,
 //   then SiLU(g)*u or ReLU^2 (GEMM1) or the topk_weight (GEMM2).
+// * Items (128-token tile, 128-row block) come from the per-tile records the
+//   routing writes (expert, first slot, live tokens); each role loads the next
+//   item's record while it works on the current one.  The copy and MMA roles
+//   run their loops on the whole warp and issue from one elected lane, so the
+//   operands of the issued instructions are warp-uniform (issued from a
+//   single-thread branch, each MMA cost about 130 cycles of issue).
 // Every wait is a bounded mbarrier wait; a timeout sets the status flag, and
 // the MMA warp drains its MMAs before TMEM is released.
 #include <algorithm>
@@ -62,6 +68,28 @@ static_assert(kF4SfCol0 + kF4Stages * kF4SfCols <= kF4TmemCols, "TMEM budget");
 // Instruction descriptor of kind::mxf4nvf4: A and B E2M1 (format 1), K-major,
 // N >> 3 at bit 17, UE4M3 scales (bit 23 = 0), M >> 4 at bit 24, K = 64.
 constexpr uint32_t kF4Idesc = (1u << 7) | (1u << 10) | ((uint32_t)(kF4N >> 3) << 17) | ((uint32_t)(128 >> 4) << 24);
+
+// True in exactly one lane of the (converged) warp, the same lane every time.
+__device__ __forceinline__ bool fp4_elect_one() {
+  uint32_t pred = 0;
+  asm volatile(
+      "{\n\t.reg .b32 r;\n\t.reg .pred p;\n\telect.sync r|p, 0xffffffff;\n\tselp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(pred));
+  return pred != 0;
+}
+
+struct F4Item {
+  int e, bp, s0, ntok;
+};
+__device__ __forceinline__ int4 fp4_record(const GroupedArgs &a, int w, int nblk) { return a.tiles[w / nblk]; }
+__device__ __forceinline__ F4Item fp4_item(const int4 r, int w, int nblk) {
+  F4Item it;
+  it.e = r.x;
+  it.s0 = r.y;
+  it.ntok = r.z;
+  it.bp = w % nblk;
+  return it;
+}
 
 __device__ __forceinline__ void tc_mma_fp4(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t sfa,
                                            uint32_t sfb, uint32_t accumulate) {
@@ -129,29 +157,33 @@ __global__ void __launch_bounds__(kF4Threads, 1) k_grouped_fp4(const GroupedArgs
   // Items (large expert, 128-token tile, 128-row block) dealt round-robin, so
   // that neighbouring CTAs share token tiles and weight blocks in L2.
   const int w0 = blockIdx.x, wstep = gridDim.x;
-  TcCursor cur;
-  if (w0 < W) cur.seek(a, w0, nblk);
+  const int4 rec0 = w0 < W ? fp4_record(a, w0, nblk) : make_int4(0, 0, 0, 0);
   bool ok = true;
   const bool by_token = a.act_by_token != 0;
 
   if (warp == kF4AWarp) {
     // ------------------------------------------------------ weight tiles
-    if (lane == 0) {
+    {
       int slot = 0;
       uint32_t phase = 0;
       uint32_t issued = 0, issued_parity = 0;
+      int4 rec = rec0;
       for (int w = w0; w < W && ok; w += wstep) {
-        const TcItem it = cur.at(a, w, nblk);
+        const F4Item it = fp4_item(rec, w, nblk);
+        if (w + wstep < W) rec = fp4_record(a, w + wstep, nblk);
         const uint8_t *tiles = a.codes + (size_t)it.e * a.codes_expert + (size_t)it.bp * nkb * (kF4TileBytes + kF4SfBytes);
         for (int kb = 0; kb < nkb; ++kb) {
-          if (!mbar_wait(aempty0 + 8u * slot, phase ^ 1u)) {
+          if (!__all_sync(0xffffffffu, mbar_wait(aempty0 + 8u * slot, phase ^ 1u))) {
             ok = false;
             break;
           }
           // the tile's codes and, right after them, its scale words in TMEM order
-          mbar_expect_tx(afull0 + 8u * slot, kF4StageBytes);
-          bulk_g2s(ringA + (uint32_t)slot * kF4StageBytes, tiles + (size_t)kb * kF4StageBytes, kF4StageBytes,
-                   afull0 + 8u * slot);
+          if (fp4_elect_one()) {
+            mbar_expect_tx(afull0 + 8u * slot, kF4StageBytes);
+            bulk_g2s(ringA + (uint32_t)slot * kF4StageBytes, tiles + (size_t)kb * kF4StageBytes, kF4StageBytes,
+                     afull0 + 8u * slot);
+          }
+          __syncwarp();
           issued |= 1u << slot;
           issued_parity = (issued_parity & ~(1u << slot)) | (phase << slot);
           if (++slot == kF4Stages) {
@@ -170,23 +202,28 @@ __global__ void __launch_bounds__(kF4Threads, 1) k_grouped_fp4(const GroupedArgs
     // The activation rows of an item's 128 slots are one slot-major tile per
     // 256-K block (written by the row quantiser; expert groups are padded to
     // 128 slots, so a tile never straddles two experts): one bulk copy each.
-    if (lane == 0) {
+    {
       int slot = 0;
       uint32_t phase = 0;
       uint32_t issued = 0, issued_parity = 0;
       const uint8_t *act = reinterpret_cast<const uint8_t *>(a.act);
       pdl_wait();  // the activation tiles come from the preceding kernel
+      int4 rec = rec0;
       for (int w = w0; w < W && ok; w += wstep) {
-        const TcItem it = cur.at(a, w, nblk);
+        const F4Item it = fp4_item(rec, w, nblk);
+        if (w + wstep < W) rec = fp4_record(a, w + wstep, nblk);
         const uint8_t *tiles = act + (size_t)(it.s0 / kF4N) * nkb * kF4StageBytes;
         for (int kb = 0; kb < nkb; ++kb) {
-          if (!mbar_wait(bempty0 + 8u * slot, phase ^ 1u)) {
+          if (!__all_sync(0xffffffffu, mbar_wait(bempty0 + 8u * slot, phase ^ 1u))) {
             ok = false;
             break;
           }
-          mbar_expect_tx(bfull0 + 8u * slot, kF4StageBytes);
-          bulk_g2s(ringB + (uint32_t)slot * kF4StageBytes, tiles + (size_t)kb * kF4StageBytes, kF4StageBytes,
-                   bfull0 + 8u * slot);
+          if (fp4_elect_one()) {
+            mbar_expect_tx(bfull0 + 8u * slot, kF4StageBytes);
+            bulk_g2s(ringB + (uint32_t)slot * kF4StageBytes, tiles + (size_t)kb * kF4StageBytes, kF4StageBytes,
+                     bfull0 + 8u * slot);
+          }
+          __syncwarp();
           issued |= 1u << slot;
           issued_parity = (issued_parity & ~(1u << slot)) | (phase << slot);
           if (++slot == kF4Stages) {
@@ -241,13 +278,13 @@ __global__ void __launch_bounds__(kF4Threads, 1) k_grouped_fp4(const GroupedArgs
     }
   } else if (warp == kF4MmaWarp) {
     // ------------------------------------------------------ MMA issuer
-    if (lane == 0) {
+    {
       int sa = 0, li = 0;
       uint32_t pa = 0;
       bool any = false;
       for (int w = w0; w < W && ok; w += wstep, ++li) {
         const int b = li & 1;
-        if (!mbar_wait(tempty0 + 8u * b, ((li >> 1) & 1) ^ 1u)) {
+        if (!__all_sync(0xffffffffu, mbar_wait(tempty0 + 8u * b, ((li >> 1) & 1) ^ 1u))) {
           ok = false;
           break;
         }
@@ -255,20 +292,25 @@ __global__ void __launch_bounds__(kF4Threads, 1) k_grouped_fp4(const GroupedArgs
         const uint32_t d = tmem + (uint32_t)(b * kF4AccCols);
         for (int kb = 0; kb < nkb; ++kb) {
           // A, B and scale-factor rings advance together
-          if (!mbar_wait(afull0 + 8u * sa, pa) || !mbar_wait(bfull0 + 8u * sa, pa) || !mbar_wait(sfull0 + 8u * sa, pa)) {
+          const bool got = mbar_wait(afull0 + 8u * sa, pa) && mbar_wait(bfull0 + 8u * sa, pa) &&
+                           mbar_wait(sfull0 + 8u * sa, pa);
+          if (!__all_sync(0xffffffffu, got)) {
             ok = false;
             break;
           }
           tc_fence_after();
-          const uint64_t da = umma_desc_sw128(ringA + (uint32_t)sa * kF4StageBytes);
-          const uint64_t db = umma_desc_sw128(ringB + (uint32_t)sa * kF4StageBytes);
-          const uint32_t sf = tmem + (uint32_t)(kF4SfCol0 + sa * kF4SfCols);
+          if (fp4_elect_one()) {
+            const uint64_t da = umma_desc_sw128(ringA + (uint32_t)sa * kF4StageBytes);
+            const uint64_t db = umma_desc_sw128(ringB + (uint32_t)sa * kF4StageBytes);
+            const uint32_t sf = tmem + (uint32_t)(kF4SfCol0 + sa * kF4SfCols);
 #pragma unroll
-          for (int j = 0; j < 4; ++j)  // K = 64 per MMA: 32 bytes of each operand row
-            tc_mma_fp4(d, da + 2u * j, db + 2u * j, sf + 4u * j, sf + 16u + 4u * j, (kb > 0 || j > 0) ? 1u : 0u);
-          tc_commit(aempty0 + 8u * sa);
-          tc_commit(bempty0 + 8u * sa);
-          tc_commit(sempty0 + 8u * sa);
+            for (int j = 0; j < 4; ++j)  // K = 64 per MMA: 32 bytes of each operand row
+              tc_mma_fp4(d, da + 2u * j, db + 2u * j, sf + 4u * j, sf + 16u + 4u * j, (kb > 0 || j > 0) ? 1u : 0u);
+            tc_commit(aempty0 + 8u * sa);
+            tc_commit(bempty0 + 8u * sa);
+            tc_commit(sempty0 + 8u * sa);
+          }
+          __syncwarp();
           any = true;
           if (++sa == kF4Stages) {
             sa = 0;
@@ -276,10 +318,12 @@ __global__ void __launch_bounds__(kF4Threads, 1) k_grouped_fp4(const GroupedArgs
           }
         }
         if (!ok) break;
-        tc_commit(tfull0 + 8u * b);
+        if (fp4_elect_one()) tc_commit(tfull0 + 8u * b);
+        __syncwarp();
       }
       if (any) {  // all issued MMAs complete before TMEM can be released
-        tc_commit(drain);
+        if (fp4_elect_one()) tc_commit(drain);
+        __syncwarp();
         mbar_wait(drain, 0);
       }
     }
@@ -291,14 +335,19 @@ __global__ void __launch_bounds__(kF4Threads, 1) k_grouped_fp4(const GroupedArgs
     constexpr int kCh = kF4N / 2 / 32;
     pdl_wait();                      // activation globals come from the preceding kernel
     int li = 0;
+    int4 rec = rec0;
     for (int w = w0; w < W && ok; w += wstep, ++li) {
-      const TcItem it = cur.at(a, w, nblk);
+      const F4Item it = fp4_item(rec, w, nblk);
+      if (w + wstep < W) rec = fp4_record(a, w + wstep, nblk);
       const int b = li & 1;
-      const float *gl = a.globals + 4 * it.e;
+      // the expert's global scale of this thread's rows (gate / up / single
+      // matrix), applied here; the down projection's goes into the column factor
+      const float gsel = a.globals[4 * it.e + ((STAGE == STAGE_GATED && (m & 15) >= 8) ? 1 : 0)];
+      const float g2 = STAGE == STAGE_DOWN ? a.globals[4 * it.e + 2] : 1.f;
       // Per column (one per lane and 32-column chunk, broadcast with shuffles):
-      // the activation row's FP32 global and, for the down projection, the
-      // topk weight -- loaded before the accumulator is ready.
-      float f_l[kCh], w_l[kCh];
+      // the activation row's FP32 global, times the topk weight and the global
+      // scale for the down projection -- loaded before the accumulator is ready.
+      float c_l[kCh];
       {
         int p_l[kCh];
 #pragma unroll
@@ -309,11 +358,10 @@ __global__ void __launch_bounds__(kF4Threads, 1) k_grouped_fp4(const GroupedArgs
 #pragma unroll
         for (int ch = 0; ch < kCh; ++ch) {
           const int nl = cbase + 32 * ch + lane;
-          f_l[ch] = 0.f;
-          w_l[ch] = 0.f;
+          c_l[ch] = 0.f;
           if (p_l[ch] >= 0) {
-            f_l[ch] = a.act_g[by_token ? (int64_t)(p_l[ch] / a.top_k) : (int64_t)(it.s0 + nl)];
-            if (STAGE == STAGE_DOWN) w_l[ch] = a.topk_weights[p_l[ch]] * gl[2];
+            const float f = a.act_g[by_token ? (int64_t)(p_l[ch] / a.top_k) : (int64_t)(it.s0 + nl)];
+            c_l[ch] = STAGE == STAGE_DOWN ? f * (a.topk_weights[p_l[ch]] * g2) : f;
           }
         }
       }
@@ -324,26 +372,41 @@ __global__ void __launch_bounds__(kF4Threads, 1) k_grouped_fp4(const GroupedArgs
       tc_fence_after();
       const int blk = it.bp;
       const int tile = 8 * blk + (m >> 4), rr = m & 15;
+      float *__restrict__ outp = a.out;
 #pragma unroll
       for (int ch = 0; ch < kCh; ++ch) {
         const int c0 = cbase + 32 * ch;
         uint32_t raw[32];
         tc_ld32(tmem + ((uint32_t)((warp & 3) * 32) << 16) + (uint32_t)(b * kF4AccCols + c0), raw);
+        float v[32];
 #pragma unroll
-        for (int j = 0; j < 32; ++j) {
-          const int n = c0 + j;
-          const bool live = n < it.ntok;
-          const int s = it.s0 + n;
-          const float v = __uint_as_float(raw[j]) * __shfl_sync(0xffffffffu, f_l[ch], j);
-          if (STAGE == STAGE_GATED) {
-            const float up = __shfl_down_sync(0xffffffffu, v, 8);
-            if (rr < 8 && live) a.out[(size_t)s * a.n_rows + tile * 8 + rr] = silu_f32(v * gl[0]) * (up * gl[1]);
-          } else if (STAGE == STAGE_RELU2) {
-            const float r = fmaxf(v * gl[0], 0.f);
-            if (live) a.out[(size_t)s * a.n_rows + tile * 16 + rr] = r * r;
-          } else {
-            const float wt = __shfl_sync(0xffffffffu, w_l[ch], j);
-            if (live) store_partial(a, (size_t)s * a.n_rows + blk * 128 + m, wt * v);
+        for (int j = 0; j < 32; ++j) v[j] = __uint_as_float(raw[j]) * __shfl_sync(0xffffffffu, c_l[ch], j);
+        if (STAGE == STAGE_GATED) {
+          // Rows 0-7 of each 16-row group are gate rows, 8-15 the matching up
+          // rows; columns go in pairs, each lane evaluating one SiLU per pair
+          // (a gate lane the even column, an up lane the odd one).
+          const bool up_lane = rr >= 8;
+          const int hrow = tile * 8 + (rr & 7);
+#pragma unroll
+          for (int p = 0; p < 16; ++p) {
+            const float x0 = v[2 * p] * gsel, x1 = v[2 * p + 1] * gsel;
+            const float other = __shfl_xor_sync(0xffffffffu, up_lane ? x0 : x1, 8);
+            const float gate = up_lane ? other : x0, up = up_lane ? x1 : other;
+            const int n = c0 + 2 * p + (up_lane ? 1 : 0);
+            if (n < it.ntok) outp[(size_t)(it.s0 + n) * a.n_rows + hrow] = silu_f32(gate) * up;
+          }
+        } else if (STAGE == STAGE_RELU2) {
+#pragma unroll
+          for (int j = 0; j < 32; ++j) {
+            const int n = c0 + j;
+            const float r = fmaxf(v[j] * gsel, 0.f);
+            if (n < it.ntok) outp[(size_t)(it.s0 + n) * a.n_rows + tile * 16 + rr] = r * r;
+          }
+        } else {
+#pragma unroll
+          for (int j = 0; j < 32; ++j) {
+            const int n = c0 + j;
+            if (n < it.ntok) store_partial(a, (size_t)(it.s0 + n) * a.n_rows + blk * 128 + m, v[j]);
           }
         }
       }

@@ -120,7 +120,7 @@ k_route_one(const int32_t *__restrict__ ids, int P, int E, int pad, int ntok, in
   rank_chunk(ids, 0, P, E, warp_hist, hist, &dropped, my_id, my_local);
   if (warp == 0)
     scan_experts(hist, E, pad, ntok, large_min, large_tile, base, true, o.active, o.passes, o.large, o.large_tiles,
-                 o.tiles);
+                 o.tiles, o.balanced != 0);
   __syncthreads();
   for (int e = tid; e <= E; e += kRouteThreads) o.offsets[e] = base[e];
   for (int e = tid; e < E; e += kRouteThreads) o.counts[e] = hist[e];
@@ -211,7 +211,7 @@ k_route_scatter(const int32_t *__restrict__ ids, int P, int E, int pad, int ntok
   __syncthreads();
   if (warp == 0)
     scan_experts(tot, E, pad, ntok, large_min, large_tile, base, c == 0, o.active, o.passes, o.large, o.large_tiles,
-                 o.tiles);
+                 o.tiles, o.balanced != 0);
   __syncthreads();
   if (c == 0) {
     for (int e = tid; e <= E; e += kRouteThreads) o.offsets[e] = base[e];
@@ -236,10 +236,12 @@ int route_chunks(int P) { return P <= kRouteThreads ? 0 : (P + kRouteThreads - 1
 
 cudaError_t launch_route(const int32_t *ids, int P, int E, int pad, int ntok, int large_min, int large_tile,
                          int32_t *counts, int32_t *offsets, int32_t *sorted_pair, int32_t *pair_pos, int32_t *active,
-                         int32_t *passes, int32_t *large, int32_t *large_tiles, int4 *tiles, int32_t *status,
-                         int32_t *chunk_hist, int32_t *work, int work_n, const RouteStaging *stg, cudaStream_t s) {
+                         int32_t *passes, int32_t *large, int32_t *large_tiles, int4 *tiles, int balanced,
+                         int32_t *status, int32_t *chunk_hist, int32_t *work, int work_n, const RouteStaging *stg,
+                         cudaStream_t s) {
   if (E > kMaxExperts || E < 1) return cudaErrorInvalidValue;
-  const RouteOut o{counts, offsets, sorted_pair, pair_pos, active, passes, large, large_tiles, status, tiles, work, work_n};
+  const RouteOut o{counts, offsets, sorted_pair, pair_pos, active,   passes, large,
+                   large_tiles, status, tiles, balanced, work, work_n};
   const RouteStaging st = stg ? *stg : RouteStaging{nullptr, 0, 0, nullptr, nullptr, nullptr, 0};
   const int T = stg ? stg->T : 0;
   const int nchunk = route_chunks(P);

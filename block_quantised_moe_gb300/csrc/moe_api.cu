@@ -308,7 +308,7 @@ static moe_status run_unified(moe_binding b, cudaStream_t stream, int withhold) 
   u.ntok = ntok;
   u.ro = RouteOut{at<int32_t>(sc, S.counts), at<int32_t>(sc, S.offsets), at<int32_t>(sc, S.sorted),
                   at<int32_t>(sc, S.pair_pos), at<int32_t>(sc, S.active), at<int32_t>(sc, S.passes),
-                  at<int32_t>(sc, S.large), at<int32_t>(sc, S.large_tiles), at<int32_t>(sc, S.status), nullptr,
+                  at<int32_t>(sc, S.large), at<int32_t>(sc, S.large_tiles), at<int32_t>(sc, S.status), nullptr, 0,
                   at<int32_t>(sc, S.work), 2 * kWorkSlots};
   u.x16 = at<__half>(sc, S.x16);
   u.xfac = at<float>(sc, S.xfac);
@@ -419,7 +419,8 @@ static moe_status run_forward(moe_binding b, cudaStream_t stream, cudaEvent_t *e
   const bool staged = P.afmt == MOE_A_BF16;
   if ((err = launch_route(b->ids, T * K, E, P.pad, ntok, P.large_min, P.tc2_on ? 256 : 128, counts, offsets, sorted,
                           pair_pos, active,
-                          passes, large, large_tiles, at<int4>(sc, S.tiles), status, at<int32_t>(sc, S.route_hist),
+                          passes, large, large_tiles, at<int4>(sc, S.tiles), P.tc2_on ? 1 : 0, status,
+                          at<int32_t>(sc, S.route_hist),
                           at<int32_t>(sc, S.work),
                           2 * kWorkSlots, staged ? &stg : nullptr,
                           stream)) != cudaSuccess)

@@ -19,14 +19,15 @@ namespace bqmoe {
 // in order, so the lists stay ascending.  With `tiles`, the lists pass also
 // writes one record per token tile of the large experts, in item order:
 // (expert, first slot, live tokens, 0).  An expert with c pairs has
-// nt = ceil(c / large_tile) tiles of equal size rounded up to 16 (the last one
-// possibly shorter), so that no tile is a nearly empty remainder.
+// nt = ceil(c / large_tile) tiles: with `balanced`, of equal size rounded up
+// to 16 (the last one possibly shorter), so that no tile is a nearly empty
+// remainder; otherwise of large_tile pairs each but the last.
 __device__ __forceinline__ int round_up_div(int c, int d) { return (c + d - 1) / d; }
 
 static __device__ void scan_experts(const int32_t *hist, int E, int pad, int ntok, int large_min, int large_tile,
                              int32_t *base, bool lists, int32_t *__restrict__ active, int32_t *__restrict__ passes,
                              int32_t *__restrict__ large, int32_t *__restrict__ large_tiles,
-                             int4 *__restrict__ tiles) {
+                             int4 *__restrict__ tiles, bool balanced) {
   const int lane = threadIdx.x & 31;
   const int per = (E + 31) / 32;
   const int e0 = min(E, lane * per), e1 = min(E, e0 + per);
@@ -69,7 +70,7 @@ static __device__ void scan_experts(const int32_t *hist, int E, int pad, int nto
       large_tiles[nl++] = cl;
       const int nt = round_up_div(c, large_tile);
       if (tiles != nullptr) {
-        const int tsz = (round_up_div(c, nt) + 15) & ~15;
+        const int tsz = balanced ? (round_up_div(c, nt) + 15) & ~15 : large_tile;
         for (int t = 0; t < nt; ++t) tiles[cl + t] = make_int4(e, base[e] + t * tsz, max(0, min(tsz, c - t * tsz)), 0);
       }
       cl += nt;
@@ -97,6 +98,7 @@ __device__ __forceinline__ void write_status(int32_t *status, int dropped) {
 struct RouteOut {
   int32_t *counts, *offsets, *sorted_pair, *pair_pos, *active, *passes, *large, *large_tiles, *status;
   int4 *tiles;    // token tiles of the large experts (may be null)
+  int balanced;   // tiles of equal size (else of large_tile pairs but the last)
   int32_t *work;  // work_n counters of the grouped kernels, zeroed here
   int work_n;
 };

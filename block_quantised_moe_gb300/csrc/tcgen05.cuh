@@ -60,40 +60,6 @@ __device__ __forceinline__ void cp_async_wait_group() {
 }
 __device__ __forceinline__ void fence_async_smem() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
 
-// ------------------------------------------------------------------ work items
-
-struct TcItem {
-  int e, tile, bp, s0, ntok;
-};
-
-// Items (large expert i, 128-token tile, row-block pair), in that order;
-// tiles[i] is the per-expert prefix of ceil(count / 128).
-struct TcCursor {
-  static constexpr int kTile = 128;  // tokens per tile
-  int i = 0;
-  __device__ __forceinline__ void seek(const GroupedArgs &a, int w, int nbp) {
-    int lo = 0, hi = a.large[0] - 1;
-    while (lo < hi) {
-      const int mid = (lo + hi) >> 1;
-      if (a.large_tiles[mid + 1] * nbp > w) hi = mid;
-      else lo = mid + 1;
-    }
-    i = lo;
-  }
-  __device__ __forceinline__ TcItem at(const GroupedArgs &a, int w, int nbp) {
-    while (a.large_tiles[i + 1] * nbp <= w) ++i;
-    TcItem it;
-    it.e = a.large[1 + i];
-    const int local = w - a.large_tiles[i] * nbp;
-    it.tile = local / nbp;
-    it.bp = local % nbp;
-    const int cnt = a.counts[it.e];
-    it.s0 = a.offsets[it.e] + it.tile * kTile;
-    it.ntok = min(kTile, cnt - it.tile * kTile);
-    return it;
-  }
-};
-
 // TMEM store of 16 consecutive 32-bit columns of this warp's 32 lanes.
 __device__ __forceinline__ void tc_st16(uint32_t taddr, const uint32_t (&r)[16]) {
   asm volatile(

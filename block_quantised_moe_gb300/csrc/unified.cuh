@@ -138,7 +138,7 @@ static __device__ void route_in_cta(const UnifiedArgs &u, int32_t *sm) {
   // no expert goes to the tensor-core kernels on this path
   if (warp == 0)
     scan_experts(hist, E, u.pad, u.ntok, 0x7FFFFFFF, 256, base, true, u.ro.active, u.ro.passes, u.ro.large,
-                 u.ro.large_tiles, nullptr);
+                 u.ro.large_tiles, nullptr, false);
   __syncthreads();
   for (int e = tid; e <= E; e += blockDim.x) u.ro.offsets[e] = base[e];
   for (int e = tid; e < E; e += blockDim.x) u.ro.counts[e] = hist[e];
