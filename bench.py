@@ -50,11 +50,17 @@ ROWS = [("prefill_w4a4_e256_h7168_i2048_k8", 8192)] + \
     [("mxfp4_mxfp8_relu2_e128_h4096_i1024_k4", t) for t in (1, 64, 4096)] + \
     [("mxfp4_mxfp8_relu2_e128_h4096_i1024_k4", 1, "single-launch")]
 L2_BYTES = 126.5e6
-# committed ncu summaries per workload (profiles/)
+# committed ncu summaries (profiles/) per (workload, T), else per workload
 PROFILES = {
     "prefill_w4a16_e256_h7168_i2048_k8": "profiles/k_grouped_tc2_prefill_e32_h7168_t2048.md",
     "prefill_w4a4_e256_h7168_i2048_k8": "profiles/k_grouped_fp4_prefill_e32_h7168_t2048.md",
     "decode_e128_h2048_i768_k8": "profiles/k_grouped_mma_decode_e128_h2048_t64.md",
+    ("decode_e128_h2048_i768_k8", 1): "profiles/k_grouped_mma_decode_e128_h2048_t1.md",
+    ("decode_zipf_e256_h7168_i2048_k8", 1): "profiles/k_grouped_mma_zipf_e256_h7168_t1.md",
+    ("decode_zipf_e256_h7168_i2048_k8", 128): "profiles/k_grouped_mma_zipf_e256_h7168_t128.md",
+    ("mxfp4_mxfp8_relu2_e128_h4096_i1024_k4", 1): "profiles/k_grouped_mma_mxfp4_mxfp8_e128_h4096_t1.md",
+    ("mxfp4_mxfp8_relu2_e128_h4096_i1024_k4", 64): "profiles/k_grouped_mma_mxfp4_mxfp8_e128_h4096_t64.md",
+    ("mxfp4_mxfp8_relu2_e128_h4096_i1024_k4", 4096): "profiles/k_grouped_tc2_mxfp4_mxfp8_e128_h4096_t4096.md",
 }
 
 
@@ -550,7 +556,7 @@ def measure(name, T, args, world, rank, layers, steps, headline=False, variant=N
                   f"stage events from a second replay of {len(used)} instrumented forwards right after",
         "clocks": clk.summary(),
     }
-    prof = PROFILES.get(name)
+    prof = PROFILES.get((name, T), PROFILES.get(name))
     if prof and os.path.exists(os.path.join(ROOT, prof)):
         row["roofline"]["profile"] = prof
     row["roofline"]["traffic"] = traffic_for(workload_name(name, T, args.experts), roof["kernel"])

@@ -183,11 +183,11 @@ def moe_run_timed(binding, events, stream=None):
     _check(_lib.moe_run_timed(binding, _stream(stream), arr), "moe_run_timed")
 
 
-MOE_PEAK_F16, MOE_PEAK_FP4 = 0, 1
+MOE_PEAK_F16, MOE_PEAK_FP4, MOE_PEAK_MXFP8 = 0, 1, 2
 
 
 def moe_measure_mma_peak(kind, n, iters=20000):
-    """Back-to-back tcgen05.mma issue rate (TFLOP/s) for kind MOE_PEAK_F16 / MOE_PEAK_FP4."""
+    """Back-to-back tcgen05.mma issue rate (TFLOP/s) for kind MOE_PEAK_F16 / MOE_PEAK_FP4 / MOE_PEAK_MXFP8."""
     t = ctypes.c_float(0)
     _check(_lib.moe_measure_mma_peak(kind, n, iters, ctypes.byref(t)), "moe_measure_mma_peak")
     return t.value

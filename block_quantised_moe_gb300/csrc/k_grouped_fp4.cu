@@ -69,14 +69,6 @@ static_assert(kF4SfCol0 + kF4Stages * kF4SfCols <= kF4TmemCols, "TMEM budget");
 // N >> 3 at bit 17, UE4M3 scales (bit 23 = 0), M >> 4 at bit 24, K = 64.
 constexpr uint32_t kF4Idesc = (1u << 7) | (1u << 10) | ((uint32_t)(kF4N >> 3) << 17) | ((uint32_t)(128 >> 4) << 24);
 
-// True in exactly one lane of the (converged) warp, the same lane every time.
-__device__ __forceinline__ bool fp4_elect_one() {
-  uint32_t pred = 0;
-  asm volatile(
-      "{\n\t.reg .b32 r;\n\t.reg .pred p;\n\telect.sync r|p, 0xffffffff;\n\tselp.u32 %0, 1, 0, p;\n\t}"
-      : "=r"(pred));
-  return pred != 0;
-}
 
 struct F4Item {
   int e, bp, s0, ntok;
@@ -178,7 +170,7 @@ __global__ void __launch_bounds__(kF4Threads, 1) k_grouped_fp4(const GroupedArgs
             break;
           }
           // the tile's codes and, right after them, its scale words in TMEM order
-          if (fp4_elect_one()) {
+          if (elect_one()) {
             mbar_expect_tx(afull0 + 8u * slot, kF4StageBytes);
             bulk_g2s(ringA + (uint32_t)slot * kF4StageBytes, tiles + (size_t)kb * kF4StageBytes, kF4StageBytes,
                      afull0 + 8u * slot);
@@ -218,7 +210,7 @@ __global__ void __launch_bounds__(kF4Threads, 1) k_grouped_fp4(const GroupedArgs
             ok = false;
             break;
           }
-          if (fp4_elect_one()) {
+          if (elect_one()) {
             mbar_expect_tx(bfull0 + 8u * slot, kF4StageBytes);
             bulk_g2s(ringB + (uint32_t)slot * kF4StageBytes, tiles + (size_t)kb * kF4StageBytes, kF4StageBytes,
                      bfull0 + 8u * slot);
@@ -299,7 +291,7 @@ __global__ void __launch_bounds__(kF4Threads, 1) k_grouped_fp4(const GroupedArgs
             break;
           }
           tc_fence_after();
-          if (fp4_elect_one()) {
+          if (elect_one()) {
             const uint64_t da = umma_desc_sw128(ringA + (uint32_t)sa * kF4StageBytes);
             const uint64_t db = umma_desc_sw128(ringB + (uint32_t)sa * kF4StageBytes);
             const uint32_t sf = tmem + (uint32_t)(kF4SfCol0 + sa * kF4SfCols);
@@ -318,11 +310,11 @@ __global__ void __launch_bounds__(kF4Threads, 1) k_grouped_fp4(const GroupedArgs
           }
         }
         if (!ok) break;
-        if (fp4_elect_one()) tc_commit(tfull0 + 8u * b);
+        if (elect_one()) tc_commit(tfull0 + 8u * b);
         __syncwarp();
       }
       if (any) {  // all issued MMAs complete before TMEM can be released
-        if (fp4_elect_one()) tc_commit(drain);
+        if (elect_one()) tc_commit(drain);
         __syncwarp();
         mbar_wait(drain, 0);
       }

@@ -90,14 +90,6 @@ static_assert(k2AWarps * 32 == 256 && 256 % (k2AGroups * 32) == 0, "8 fragment c
 
 // ------------------------------------------------------------ cluster helpers
 
-// True in exactly one lane of the (converged) warp, the same lane every time.
-__device__ __forceinline__ bool elect_one() {
-  uint32_t pred = 0;
-  asm volatile(
-      "{\n\t.reg .b32 r;\n\t.reg .pred p;\n\telect.sync r|p, 0xffffffff;\n\tselp.u32 %0, 1, 0, p;\n\t}"
-      : "=r"(pred));
-  return pred != 0;
-}
 
 // Named barrier 1 over the four epilogue warps (threads 0..127).
 __device__ __forceinline__ void epi_bar_sync() { asm volatile("bar.sync 1, 128;" ::: "memory"); }

@@ -1,8 +1,10 @@
 // Measurement helper: back-to-back tcgen05.mma issue rate, the roofline
-// denominator of the prefill kernels for their MMA kinds (the FP4 kind has no
-// cuBLAS counterpart to time against).  One CTA per SM, one thread issuing
-// MMAs from fixed 128-byte-swizzled shared-memory operands into TMEM; the
-// block-scaled kind reads UE4M3 1.0 scale factors from TMEM.
+// denominator of the prefill kernels for their MMA kinds (the block-scaled
+// kinds have no cuBLAS counterpart to time against).  One CTA per SM; one warp
+// runs the loop and an elected lane issues MMAs from fixed 128-byte-swizzled
+// shared-memory operands into TMEM.  The block-scaled kinds read 1.0 scale
+// factors from TMEM: UE4M3 for the NVFP4 kind (E2M1 x E2M1, K = 64 per MMA),
+// UE8M0 for the MX FP8 kind (E4M3 x E4M3, K = 32 per MMA, one scale per 32).
 #include "common.cuh"
 #include "internal.h"
 #include "moe.h"
@@ -38,10 +40,10 @@ __global__ void __launch_bounds__(128, 1) k_mma_peak(int iters, int32_t *status)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
-  if (KIND == 1) {  // scale factors 1.0 (E4M3 0x38) for A and B, every quadrant
+  if (KIND != 0) {  // scale factors 1.0 (UE4M3 0x38, UE8M0 0x7F) for A and B, every quadrant
     uint32_t r[16];
 #pragma unroll
-    for (int j = 0; j < 16; ++j) r[j] = 0x38383838u;
+    for (int j = 0; j < 16; ++j) r[j] = KIND == 1 ? 0x38383838u : 0x7F7F7F7Fu;
     tc_st16(tmem + ((uint32_t)(warp * 32) << 16) + 256, r);
     tc_wait_st();
   }
@@ -49,28 +51,41 @@ __global__ void __launch_bounds__(128, 1) k_mma_peak(int iters, int32_t *status)
   __syncthreads();
   tc_fence_after();
   bool ok = true;
-  if (tid == 0) {
+  if (warp == 0) {
     const uint64_t ad = umma_desc_sw128(base_s), bd = umma_desc_sw128(base_s + 32768);
     for (int it = 0; it < iters; ++it) {
+      if (elect_one()) {
 #pragma unroll
-      for (int j = 0; j < 4; ++j) {
-        if (KIND == 0) {
-          tc_mma_f16(tmem, ad + 2u * j, bd + 2u * j,
-                     (1u << 4) | ((uint32_t)(N >> 3) << 17) | ((uint32_t)(128 >> 4) << 24), 1u);
-        } else {
-          asm volatile(
-              "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %6, 0;\n\t"
-              "tcgen05.mma.cta_group::1.kind::mxf4nvf4.block_scale.scale_vec::4X [%0], %1, %2, %3, [%4], [%5], p;\n\t}" ::"r"(
-                  tmem),
-              "l"(ad + 2u * j), "l"(bd + 2u * j),
-              "r"((1u << 7) | (1u << 10) | ((uint32_t)(N >> 3) << 17) | ((uint32_t)(128 >> 4) << 24)),
-              "r"(tmem + 256), "r"(tmem + 260), "r"(1u));
+        for (int j = 0; j < 4; ++j) {  // 32 bytes of each operand row per MMA
+          if (KIND == 0) {
+            tc_mma_f16(tmem, ad + 2u * j, bd + 2u * j,
+                       (1u << 4) | ((uint32_t)(N >> 3) << 17) | ((uint32_t)(128 >> 4) << 24), 1u);
+          } else if (KIND == 1) {
+            asm volatile(
+                "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %6, 0;\n\t"
+                "tcgen05.mma.cta_group::1.kind::mxf4nvf4.block_scale.scale_vec::4X [%0], %1, %2, %3, [%4], [%5], "
+                "p;\n\t}" ::"r"(tmem),
+                "l"(ad + 2u * j), "l"(bd + 2u * j),
+                "r"((1u << 7) | (1u << 10) | ((uint32_t)(N >> 3) << 17) | ((uint32_t)(128 >> 4) << 24)),
+                "r"(tmem + 256), "r"(tmem + 260), "r"(1u));
+          } else {
+            // E4M3 x E4M3 (type 0), UE8M0 scales (bit 23), scale-factor data ID 0
+            asm volatile(
+                "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %6, 0;\n\t"
+                "tcgen05.mma.cta_group::1.kind::mxf8f6f4.block_scale.scale_vec::1X [%0], %1, %2, %3, [%4], [%5], "
+                "p;\n\t}" ::"r"(tmem),
+                "l"(ad + 2u * j), "l"(bd + 2u * j),
+                "r"(((uint32_t)(N >> 3) << 17) | (1u << 23) | ((uint32_t)(128 >> 4) << 24)), "r"(tmem + 256),
+                "r"(tmem + 260), "r"(1u));
+          }
         }
       }
+      __syncwarp();
     }
-    tc_commit(mb);
+    if (elect_one()) tc_commit(mb);
+    __syncwarp();
     ok = mbar_wait(mb, 0);
-    if (!ok) atomicOr(&status[0], ST_FLAG_TIMEOUT);
+    if (!ok && tid == 0) atomicOr(&status[0], ST_FLAG_TIMEOUT);
   }
   tc_fence_before();
   __syncthreads();
@@ -83,11 +98,13 @@ __global__ void __launch_bounds__(128, 1) k_mma_peak(int iters, int32_t *status)
 using namespace bqmoe;
 
 moe_status moe_measure_mma_peak(int32_t kind, int32_t n, int32_t iters, float *tflops) {
-  if (!tflops || iters < 1 || (kind != MOE_PEAK_F16 && kind != MOE_PEAK_FP4) || (n != 128 && n != 256))
+  if (!tflops || iters < 1 || (kind != MOE_PEAK_F16 && kind != MOE_PEAK_FP4 && kind != MOE_PEAK_MXFP8) ||
+      (n != 128 && n != 256))
     return MOE_ERR_INVALID_ARG;
   void (*k)(int, int32_t *) = nullptr;
   if (kind == MOE_PEAK_F16) k = n == 128 ? k_mma_peak<0, 128> : k_mma_peak<0, 256>;
-  else k = n == 128 ? k_mma_peak<1, 128> : k_mma_peak<1, 256>;
+  else if (kind == MOE_PEAK_FP4) k = n == 128 ? k_mma_peak<1, 128> : k_mma_peak<1, 256>;
+  else k = n == 128 ? k_mma_peak<2, 128> : k_mma_peak<2, 256>;
   int dev = 0, sms = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
     return MOE_ERR_CUDA;
@@ -112,7 +129,7 @@ moe_status moe_measure_mma_peak(int32_t kind, int32_t n, int32_t iters, float *t
     } else if (h & ST_FLAG_TIMEOUT) {
       st = MOE_ERR_TIMEOUT;
     } else {
-      const double k_per = kind == MOE_PEAK_F16 ? 16.0 : 64.0;
+      const double k_per = kind == MOE_PEAK_F16 ? 16.0 : kind == MOE_PEAK_FP4 ? 64.0 : 32.0;
       *tflops = (float)(2.0 * 128 * n * k_per * 4 * (double)iters * sms / (ms * 1e-3) / 1e12);
     }
   }

@@ -26,6 +26,19 @@ __device__ __forceinline__ uint32_t sw128_elem(int r, int k) {
   return (uint32_t)((r >> 3) * 1024 + (r & 7) * 128 + ((((k >> 3) ^ r) & 7) << 4) + (k & 7) * 2);
 }
 
+// True in exactly one lane of the (converged) warp, the same lane every time.
+// The tensor-core and bulk-copy instructions are issued from such a lane of a
+// warp that runs the surrounding loop as a whole: their operands are then
+// warp-uniform.  (From a single-thread branch, a cta_group::2 MMA was measured
+// at about 130 cycles of issue whatever its N.)
+__device__ __forceinline__ bool elect_one() {
+  uint32_t pred = 0;
+  asm volatile(
+      "{\n\t.reg .b32 r;\n\t.reg .pred p;\n\telect.sync r|p, 0xffffffff;\n\tselp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(pred));
+  return pred != 0;
+}
+
 __device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
 __device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
 

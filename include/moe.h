@@ -371,11 +371,13 @@ MOE_API void moe_destroy_binding(moe_binding b);
 
 /* Issue rate of back-to-back tensor-core MMAs on this device, in TFLOP/s: one
  * CTA per SM issuing `iters` x 4 tcgen05.mma (M=128, N = n in {128, 256}) from
- * fixed shared-memory operands.  kind: MOE_PEAK_F16 (kind::f16, K=16) or
- * MOE_PEAK_FP4 (kind::mxf4nvf4 block_scale scale_vec::4X, K=64).  The roofline
+ * fixed shared-memory operands.  kind: MOE_PEAK_F16 (kind::f16, K=16),
+ * MOE_PEAK_FP4 (kind::mxf4nvf4 block_scale scale_vec::4X, E2M1 x E2M1 with
+ * UE4M3 scales, K=64) or MOE_PEAK_MXFP8 (kind::mxf8f6f4 block_scale
+ * scale_vec::1X, E4M3 x E4M3 with UE8M0 scales, K=32).  The roofline
  * denominator of the prefill kernels (no counterpart on the pages).  Allocates
  * 16 bytes of device memory and two events, synchronises the device. */
-enum { MOE_PEAK_F16 = 0, MOE_PEAK_FP4 = 1 };
+enum { MOE_PEAK_F16 = 0, MOE_PEAK_FP4 = 1, MOE_PEAK_MXFP8 = 2 };
 MOE_API moe_status moe_measure_mma_peak(int32_t kind, int32_t n, int32_t iters, float *tflops);
 
 #ifdef __cplusplus
