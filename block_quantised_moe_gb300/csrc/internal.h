@@ -44,6 +44,10 @@ struct WeightLayout {
   int step_bytes() const { return 4096 + 128 * 64 / bs; }
 };
 
+// One slot-major MX FP8 activation tile (128 slots x 128 K) of the block-scaled
+// FP8 kernel: 16 KB of E4M3 codes + 512 bytes of UE8M0 scales in TMEM order.
+constexpr int kMx8TileBytes = 16384 + 512;
+
 // Scratch owned by the caller and carved by the plan (offsets in bytes).
 struct ScratchLayout {
   int64_t cap_sorted = 0;  // rows of the padded, expert-sorted pair list
@@ -159,6 +163,12 @@ cudaError_t launch_gather_slot_rows(const void *src, const int32_t *sorted, cons
 // weights' FP4 tiles; a.act / act_scales / act_g = the quantised activations).
 bool fp4_tc_supported(int rows_total, int K);
 cudaError_t launch_grouped_fp4(int stage, const GroupedArgs &a, int rows_total, cudaStream_t s);
+// Block-scaled FP8 kernel (kind::mxf8f6f4) for MXFP4 weights x MXFP8
+// activations, experts with many pairs: the weights' packed fragments widened
+// to E4M3 in shared memory, the activations as slot-major MX FP8 tiles
+// (launch_quant_blocks with tiles), 128-token tiles from a.tiles.
+bool mx8_tc_supported(int rows_total, int K);
+cudaError_t launch_grouped_mx8(int stage, const GroupedArgs &a, int rows_total, cudaStream_t s);
 // h (or its re-quantised codes) as 16-bit rows for the tcgen05 GEMM2: FP16 with a
 // per-row factor, or BF16 with factor 1 (out_bf16; also MXFP8 x^ -> BF16 rows).
 // rows_dev (device, nullable) caps the rows actually converted.
@@ -186,9 +196,13 @@ cudaError_t launch_quant_rows_nvfp4(const void *src, bool src_bf16, int64_t rows
                                     uint8_t *codes, uint8_t *scales, float *g, const int32_t *rows_dev,
                                     const int32_t *row_live, cudaStream_t s, uint8_t *tiles = nullptr,
                                     const int32_t *tile_slots = nullptr, int top_k = 0);
+// With `tiles` (MXFP8 only, cols a multiple of 128): also the slot-major MX FP8
+// tiles of the block-scaled FP8 kernel, token row r to the slots
+// tile_slots[r * top_k + k] (top_k > 0), or row r to slot r (top_k == 0).
 cudaError_t launch_quant_blocks(int qfmt, const void *src, bool src_bf16, int64_t rows, int64_t cols,
                                 int64_t rows_per_global, const float *g, uint8_t *codes, uint8_t *scales,
-                                const int32_t *rows_dev, const int32_t *row_live, cudaStream_t s);
+                                const int32_t *rows_dev, const int32_t *row_live, cudaStream_t s,
+                                uint8_t *tiles = nullptr, const int32_t *tile_slots = nullptr, int top_k = 0);
 cudaError_t launch_amax_tensor(const void *src, bool src_bf16, int64_t batch, int64_t elems, float *amax,
                                cudaStream_t s);
 cudaError_t launch_amax_to_global(float *g, int64_t n, cudaStream_t s);

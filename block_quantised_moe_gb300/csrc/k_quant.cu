@@ -171,12 +171,49 @@ k_quant_rows_nvfp4_cta(const void *__restrict__ src, int64_t cols, uint8_t *__re
   }
 }
 
+// Slot-major MX FP8 tiles of the block-scaled FP8 kernel: per 128 slots and
+// 128-K block, 16 KB of E4M3 codes in the 128-byte-swizzled K-major layout
+// with the K order of each 32-element block transposed as a 8 x 4 matrix
+// (logical element 4i + c at physical 8c + i, the order in which that kernel
+// writes its widened weights), then 512 bytes of UE8M0 scales in TMEM order
+// (lane i, column c = slot i + 32c; byte = the 32-K block within the 128).
+// Block b of slot `slot`: codes c (element 4w + i in byte i of c[w]), scale s.
+__device__ __forceinline__ void mx8_tile_put(uint8_t *tiles, int64_t slot, int64_t b, int64_t nkb,
+                                             const uint32_t (&c)[8], uint32_t s) {
+  const int64_t kb = b >> 2;
+  const int qb = (int)(b & 3);
+  const int r = (int)(slot & 127);
+  uint8_t *tile = tiles + ((slot >> 7) * nkb + kb) * kMx8TileBytes;
+  // physical word w = byte (w >> 1) of logical words 4 (w & 1) .. 4 (w & 1) + 3:
+  // a 4 x 4 byte transpose of c[0..3] (even w) and of c[4..7] (odd w)
+  uint32_t o[2][4];
+#pragma unroll
+  for (int gq = 0; gq < 2; ++gq) {
+    const uint32_t t0 = __byte_perm(c[4 * gq], c[4 * gq + 1], 0x5140), t1 = __byte_perm(c[4 * gq], c[4 * gq + 1], 0x7362);
+    const uint32_t t2 = __byte_perm(c[4 * gq + 2], c[4 * gq + 3], 0x5140),
+                   t3 = __byte_perm(c[4 * gq + 2], c[4 * gq + 3], 0x7362);
+    o[gq][0] = __byte_perm(t0, t2, 0x5410);
+    o[gq][1] = __byte_perm(t0, t2, 0x7632);
+    o[gq][2] = __byte_perm(t1, t3, 0x5410);
+    o[gq][3] = __byte_perm(t1, t3, 0x7632);
+  }
+  uint8_t *row = tile + (r >> 3) * 1024 + (r & 7) * 128;
+  const int ch = 2 * qb;  // 16-byte chunk of the row's 128 bytes
+  *reinterpret_cast<uint4 *>(row + (((ch ^ r) & 7) << 4)) = make_uint4(o[0][0], o[1][0], o[0][1], o[1][1]);
+  *reinterpret_cast<uint4 *>(row + ((((ch + 1) ^ r) & 7) << 4)) = make_uint4(o[0][2], o[1][2], o[0][3], o[1][3]);
+  tile[16384 + (r & 31) * 16 + (r >> 5) * 4 + qb] = (uint8_t)s;
+}
+
 // One thread per block; NVFP4 reads its global from g[row / rows_per_global].
+// With `tiles` (MXFP8, cols a multiple of 128) the block also goes to the
+// slot-major MX FP8 tiles: a token row (tile_slots = pair_pos, top_k > 0) to
+// each of its valid slots, a slot row (top_k == 0) to its own slot.
 template <int QF, bool BF16>
 __global__ void __launch_bounds__(kQThreads)
 k_quant_blocks(const void *__restrict__ src, int64_t rows, int64_t cols, int64_t rows_per_global,
                const float *__restrict__ g, uint8_t *__restrict__ codes, uint8_t *__restrict__ scales,
-               const int32_t *__restrict__ rows_dev, const int32_t *__restrict__ row_live) {
+               const int32_t *__restrict__ rows_dev, const int32_t *__restrict__ row_live,
+               uint8_t *__restrict__ tiles, const int32_t *__restrict__ tile_slots, int top_k) {
   constexpr int bs = QF == Q_NVFP4 ? 16 : 32;
   pdl_trigger();
   pdl_wait();
@@ -203,6 +240,12 @@ k_quant_blocks(const void *__restrict__ src, int64_t rows, int64_t cols, int64_t
         uint4 *dst = reinterpret_cast<uint4 *>(codes + e0);
         dst[0] = make_uint4(c[0], c[1], c[2], c[3]);
         dst[1] = make_uint4(c[4], c[5], c[6], c[7]);
+        if (tiles != nullptr) {
+          for (int k = 0; k < (top_k > 0 ? top_k : 1); ++k) {
+            const int64_t slot = top_k > 0 ? (int64_t)tile_slots[row * top_k + k] : row;
+            if (slot >= 0) mx8_tile_put(tiles, slot, b, cols / 128, c, s);
+          }
+        }
       } else {
         *reinterpret_cast<uint4 *>(codes + e0 / 2) = make_uint4(c[0], c[1], c[2], c[3]);
       }
@@ -270,13 +313,15 @@ cudaError_t launch_quant_rows_nvfp4(const void *src, bool src_bf16, int64_t rows
 
 cudaError_t launch_quant_blocks(int qfmt, const void *src, bool src_bf16, int64_t rows, int64_t cols,
                                 int64_t rows_per_global, const float *g, uint8_t *codes, uint8_t *scales,
-                                const int32_t *rows_dev, const int32_t *row_live, cudaStream_t s) {
+                                const int32_t *rows_dev, const int32_t *row_live, cudaStream_t s, uint8_t *tiles,
+                                const int32_t *tile_slots, int top_k) {
   if (rows <= 0) return cudaSuccess;
+  if (tiles != nullptr && (qfmt != Q_MXFP8 || cols % 128 != 0)) return cudaErrorInvalidValue;
   const int bs = qfmt == Q_NVFP4 ? 16 : 32;
   const int grid = grid_for(rows * (cols / bs), kQThreads);
 #define QB(QF, B) \
   return launch_pdl(k_quant_blocks<QF, B>, dim3(grid), dim3(kQThreads), 0, s, src, rows, cols, rows_per_global, g, \
-                    codes, scales, rows_dev, row_live)
+                    codes, scales, rows_dev, row_live, tiles, tile_slots, top_k)
   if (qfmt == Q_NVFP4) { if (src_bf16) QB(Q_NVFP4, true); else QB(Q_NVFP4, false); }
   else if (qfmt == Q_MXFP4) { if (src_bf16) QB(Q_MXFP4, true); else QB(Q_MXFP4, false); }
   else if (qfmt == Q_MXFP8) { if (src_bf16) QB(Q_MXFP8, true); else QB(Q_MXFP8, false); }

@@ -26,6 +26,7 @@ struct moe_plan_s {
   int K = 0, max_tokens = 0, afmt = 0, pad = 16;
   bool tc_on = false;  // experts with >= large_min pairs run on the tcgen05 kernel
   bool fp4_on = false; // ... on the block-scaled FP4 kernel (W4A4 with the weights' FP4 tiles)
+  bool mx8_on = false; // ... on the block-scaled FP8 kernel (MXFP4 weights x MXFP8 activations)
   bool tc2_on = false; // ... otherwise on the CTA-pair kernel (token tiles of up to 256)
   bool unified_ok = false;  // decode plan the single-launch forward supports
   bool unified_on = false;  // ... and moe_run uses it (MOE_OPT_SINGLE_LAUNCH)
@@ -167,14 +168,18 @@ moe_status moe_plan(const moe_caps *c, moe_plan_t *out, size_t *scratch_bytes, i
   // kLargeMin pairs to the tcgen05 kernels (dense tiles of 128 tokens): FP16
   // operands with row factors for NVFP4, BF16 operands for MXFP4 (E2M1 * 2^X and
   // E4M3 * 2^X are exact in BF16, not in FP16), and, for W4A4 with the weights'
-  // FP4 tiles, both operands as E2M1 codes on the block-scaled FP4 MMA.  The FP4
-  // kernel reads its activation rows as slot-major 128-row tiles, so its plans
-  // pad every expert's group to 128 slots.
+  // FP4 tiles, both operands as E2M1 codes on the block-scaled FP4 MMA; MXFP4
+  // weights with MXFP8 activations run on the block-scaled FP8 MMA (weights
+  // widened to E4M3, both operands' E8M0 scales as they are).  The block-scaled
+  // kernels read their activation rows as slot-major 128-row tiles, so their
+  // plans pad every expert's group to 128 slots.
   P.tc_on = Pmax >= 1024 && tc2_supported(L.n13, L.H) && tc2_supported(L.H, L.I);
   P.fp4_on = P.tc_on && P.afmt == MOE_A_NVFP4 && L.fp4_tiles && fp4_tc_supported(L.n13, L.H) &&
              fp4_tc_supported(L.H, L.I);
-  if (P.fp4_on) P.pad = kFp4Tile;
-  P.tc2_on = P.tc_on && !P.fp4_on;
+  P.mx8_on = P.tc_on && L.wfmt == MOE_W_MXFP4 && P.afmt == MOE_A_MXFP8 && mx8_tc_supported(L.n13, L.H) &&
+             mx8_tc_supported(L.H, L.I);
+  if (P.fp4_on || P.mx8_on) P.pad = kFp4Tile;
+  P.tc2_on = P.tc_on && !P.fp4_on && !P.mx8_on;
   P.unified_ok = !P.tc_on && unified_supported(L.wfmt, P.afmt, (int)Pmax, L.E, P.K);
   P.unified_on = false;  // opt-in: measured slower than the PDL-overlapped launches (see moe.h)
   S.cap_sorted = round_up(Pmax + (int64_t)L.E * (P.pad - 1), P.pad);
@@ -224,6 +229,10 @@ moe_status moe_plan(const moe_caps *c, moe_plan_t *out, size_t *scratch_bytes, i
       // activation tiles: per 128 slots and 256-K block, 16 KB of codes + 2 KB of scales
       S.xt = take((size_t)(S.cap_sorted / kFp4Tile) * (L.H / 256) * WeightLayout::kFp4TileBytes);
       S.ht = take((size_t)(S.cap_sorted / kFp4Tile) * (L.I / 256) * WeightLayout::kFp4TileBytes);
+    } else if (P.mx8_on) {
+      // activation tiles: per 128 slots and 128-K block, 16 KB of codes + 512 bytes of scales
+      S.xt = take((size_t)(S.cap_sorted / kFp4Tile) * (L.H / 128) * kMx8TileBytes);
+      S.ht = take((size_t)(S.cap_sorted / kFp4Tile) * (L.I / 128) * kMx8TileBytes);
     } else {
       if (L.wfmt == MOE_W_MXFP4) S.xb16 = take(2 * (size_t)T * L.H);
       if (P.tc2_on) S.xs16 = take(2 * (size_t)S.cap_sorted * L.H);
@@ -455,7 +464,8 @@ static moe_status run_forward(moe_binding b, cudaStream_t stream, cudaEvent_t *e
     a.act_g = at<float>(sc, S.xq_g);
   } else if (P.afmt == MOE_A_MXFP8) {
     err = launch_quant_blocks(Q_MXFP8, b->x, true, T, H, 1, nullptr, at<uint8_t>(sc, S.xq_codes),
-                              at<uint8_t>(sc, S.xq_scales), nullptr, nullptr, stream);
+                              at<uint8_t>(sc, S.xq_scales), nullptr, nullptr, stream,
+                              P.mx8_on ? at<uint8_t>(sc, S.xt) : nullptr, pair_pos, K);
     src1 = SRC_X_MXFP8;
     a.act = at<uint8_t>(sc, S.xq_codes);
     a.act_scales = at<uint8_t>(sc, S.xq_scales);
@@ -485,7 +495,7 @@ static moe_status run_forward(moe_binding b, cudaStream_t stream, cudaEvent_t *e
   a.n_rows = I;
   a.out = h;
   const int stage1 = L.act == MOE_ACT_SILU_GATED ? STAGE_GATED : STAGE_RELU2;
-  if (!nv && P.tc_on) {  // MXFP4 tcgen05 operands: x or x^ as BF16 slot-order rows, factor 1
+  if (!nv && P.tc2_on) {  // MXFP4 tcgen05 operands: x or x^ as BF16 slot-order rows, factor 1
     err = launch_stage_h16(P.afmt == MOE_A_MXFP8 ? SRC_H_MXFP8 : SRC_X_BF16, x_src, x_src_scales, nullptr, H, T,
                            nullptr, at<__half>(sc, S.xb16), nullptr, true, stream);
     if (err != cudaSuccess) return MOE_ERR_CUDA;
@@ -504,7 +514,13 @@ static moe_status run_forward(moe_binding b, cudaStream_t stream, cudaEvent_t *e
   if (err == cudaSuccess && P.tc_on) {
     GroupedArgs t = a;
     t.act_by_token = 1;
-    if (P.fp4_on) {
+    if (P.mx8_on) {
+      t.act = at<uint8_t>(sc, S.xt);  // x^ as slot-major MX FP8 tiles
+      t.act_scales = nullptr;
+      t.act_g = nullptr;
+      t.out_amax = nullptr;
+      err = launch_grouped_mx8(stage1, t, L.n13, stream);
+    } else if (P.fp4_on) {
       t.codes = b->packed + L.off_t13;
       t.codes_expert = L.t13_expert();
       t.act = at<uint8_t>(sc, S.xt);  // x^ as slot-major FP4 tiles; per-token globals
@@ -541,7 +557,8 @@ static moe_status run_forward(moe_binding b, cudaStream_t stream, cudaEvent_t *e
     a.act_g = at<float>(sc, S.hq_g);
   } else if (P.afmt == MOE_A_MXFP8) {
     err = launch_quant_blocks(Q_MXFP8, h, false, S.cap_sorted, I, 1, nullptr, at<uint8_t>(sc, S.hq_codes),
-                              at<uint8_t>(sc, S.hq_scales), offsets + E, sorted, stream);
+                              at<uint8_t>(sc, S.hq_scales), offsets + E, sorted, stream,
+                              P.mx8_on ? at<uint8_t>(sc, S.ht) : nullptr, nullptr, 0);
     src2 = SRC_H_MXFP8;
     a.act = at<uint8_t>(sc, S.hq_codes);
     a.act_scales = at<uint8_t>(sc, S.hq_scales);
@@ -550,7 +567,7 @@ static moe_status run_forward(moe_binding b, cudaStream_t stream, cudaEvent_t *e
   if (err != cudaSuccess) return MOE_ERR_CUDA;
 
   // GEMM2 * topk_weight -> partials, then the ordered combine
-  if (P.tc_on && !P.fp4_on) {  // 16-bit slot-order rows of h (or of its re-quantised codes) for the tcgen05 GEMM2
+  if (P.tc2_on) {  // 16-bit slot-order rows of h (or of its re-quantised codes) for the CTA-pair GEMM2
     err = launch_stage_h16(src2, a.act, a.act_scales, a.act_g, I, S.cap_sorted, offsets + E, at<__half>(sc, S.h16),
                            nv ? at<float>(sc, S.h16fac) : nullptr, !nv, stream);
     if (err != cudaSuccess) return MOE_ERR_CUDA;
@@ -564,7 +581,14 @@ static moe_status run_forward(moe_binding b, cudaStream_t stream, cudaEvent_t *e
   if (mark(MOE_STAGE_GEMM2) != cudaSuccess) return MOE_ERR_CUDA;
   a.work = at<int32_t>(sc, S.work) + kWorkSlots;
   err = launch_grouped_mma(L.wfmt, src2, STAGE_DOWN, a, H, E, ntok, stream);
-  if (err == cudaSuccess && P.tc_on && P.fp4_on) {
+  if (err == cudaSuccess && P.tc_on && P.mx8_on) {
+    GroupedArgs t = a;  // h^ as slot-major MX FP8 tiles
+    t.act = at<uint8_t>(sc, S.ht);
+    t.act_scales = nullptr;
+    t.act_g = nullptr;
+    t.act_by_token = 0;
+    err = launch_grouped_mx8(STAGE_DOWN, t, H, stream);
+  } else if (err == cudaSuccess && P.tc_on && P.fp4_on) {
     GroupedArgs t = a;  // h^ as slot-major FP4 tiles; per-slot globals
     t.codes = b->packed + L.off_t2;
     t.codes_expert = L.t2_expert();
