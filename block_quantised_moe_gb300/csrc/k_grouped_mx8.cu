@@ -16,7 +16,7 @@
 //
 // * A: the packed MXFP4 weights (the fragment-order bytes the decode kernel
 //   streams; two 64-K steps per 128-K block, one bulk copy into a raw ring).
-//   Two groups of four converter warps take alternate 128-K blocks; each
+//   Three groups of four converter warps take every third 128-K block; each
 //   widens its rows' codes to E4M3 (cvt to f16x2, then to e4m3x2) and writes
 //   the 128-byte-swizzled K-major A tile.  In the packed fragments, lane c of
 //   a quad holds, per 32-element block, the elements 16e + 8j + 4h + c of two
@@ -53,12 +53,12 @@
 
 namespace bqmoe {
 
-constexpr int k8EpiWarps = 4;                      // warps 0-3: epilogue (lane quadrant = warp)
-constexpr int k8CvtWarp0 = 4;                      // warps 4-11: two groups of four converter warps
-constexpr int k8CvtGroups = 2;
-constexpr int k8LoadWarp = 12;                     // raw weight bulk copies
-constexpr int k8BWarp = 13;                        // activation tile bulk copies
-constexpr int k8MmaWarp = 14;                      // MMA issue
+constexpr int k8EpiWarps = 8;                      // warps 0-7: epilogue (lane quadrant w % 4, column half w / 4)
+constexpr int k8CvtWarp0 = 8;                      // warps 8-19: three groups of four converter warps
+constexpr int k8CvtGroups = 3;
+constexpr int k8LoadWarp = k8CvtWarp0 + 4 * k8CvtGroups;  // raw weight bulk copies
+constexpr int k8BWarp = k8LoadWarp + 1;                   // activation tile bulk copies
+constexpr int k8MmaWarp = k8BWarp + 1;                    // MMA issue
 constexpr int k8Threads = (k8MmaWarp + 1) * 32;
 constexpr int k8N = 128;                           // tokens per tile
 constexpr int k8StepBytes = 4352;                  // one 64-K step of a 128-row MXFP4 block (codes + scales)
@@ -181,8 +181,8 @@ __global__ void __launch_bounds__(k8Threads, 1) k_grouped_mx8(const GroupedArgs 
 
   if (warp >= k8CvtWarp0 && warp < k8CvtWarp0 + 4 * k8CvtGroups) {
     // ------------------------------------------------------ converters
-    // Group g (warps 4 + 4g .. 7 + 4g) takes the 128-K blocks n with
-    // n % 2 == g.  Warp quadrant q handles rows 32q .. 32q + 31 (16-row tiles
+    // Group g (warps 8 + 4g .. 11 + 4g) takes the 128-K blocks n with
+    // n % 3 == g.  Warp quadrant q handles rows 32q .. 32q + 31 (16-row tiles
     // 2q and 2q + 1): from each 64-K step, lane (r, c) of a tile's fragment
     // chunk holds rows r and r + 8 at K pairs 16j + 2c and 16j + 8 + 2c.
     const int grp = (warp - k8CvtWarp0) >> 2, q = warp & 3;
@@ -383,7 +383,8 @@ __global__ void __launch_bounds__(k8Threads, 1) k_grouped_mx8(const GroupedArgs 
     __syncwarp();
   } else {
     // ------------------------------------------------------ epilogue
-    const int m = warp * 32 + lane;  // accumulator row = TMEM lane
+    const int m = (warp & 3) * 32 + lane;  // accumulator row = TMEM lane
+    const int cbase = (warp >> 2) * (k8N / 2);  // this warp's half of the 128 token columns
     pdl_wait();                      // row factors come from the preceding kernels
     int li = 0;
     int4 rec = rec0;
@@ -395,10 +396,10 @@ __global__ void __launch_bounds__(k8Threads, 1) k_grouped_mx8(const GroupedArgs 
       const float g2 = STAGE == STAGE_DOWN ? a.globals[4 * it.e + 2] : 1.f;
       // per column (one per lane and 32-column chunk, broadcast with shuffles):
       // for the down projection the topk weight times the global scale
-      float c_l[4];
+      float c_l[2];
 #pragma unroll
-      for (int ch = 0; ch < 4; ++ch) {
-        const int nl = 32 * ch + lane;
+      for (int ch = 0; ch < 2; ++ch) {
+        const int nl = cbase + 32 * ch + lane;
         c_l[ch] = 1.f;
         if (STAGE == STAGE_DOWN) c_l[ch] = nl < it.ntok ? a.topk_weights[a.sorted_pair[it.s0 + nl]] * g2 : 0.f;
       }
@@ -411,11 +412,11 @@ __global__ void __launch_bounds__(k8Threads, 1) k_grouped_mx8(const GroupedArgs 
       const int tile = 8 * blk + (m >> 4), rr = m & 15;
       float *__restrict__ outp = a.out;
 #pragma unroll
-      for (int ch = 0; ch < 4; ++ch) {
-        const int c0 = 32 * ch;
+      for (int ch = 0; ch < 2; ++ch) {
+        const int c0 = cbase + 32 * ch;
         if (c0 >= it.ntok) break;
         uint32_t raw[32];
-        tc_ld32(tmem + ((uint32_t)(warp * 32) << 16) + (uint32_t)(b * k8AccCols + c0), raw);
+        tc_ld32(tmem + ((uint32_t)((warp & 3) * 32) << 16) + (uint32_t)(b * k8AccCols + c0), raw);
         if (STAGE == STAGE_GATED) {
           // rows 0-7 of each 16-row group are gate rows, 8-15 the matching up
           // rows; columns in pairs, one SiLU per lane per pair
