@@ -35,6 +35,7 @@ MOE_NUM_STAGES = 6
 STAGES = ("route", "quant_x", "gemm1", "quant_h", "gemm2", "combine")
 MOE_NO_ALLOC_SCRATCH_BYTES = 32 << 20
 MOE_OPT_SINGLE_LAUNCH = 1
+MOE_OPT_OUT_F32 = 2
 
 WFMT = {"nvfp4": MOE_W_NVFP4, "mxfp4": MOE_W_MXFP4}
 AFMT = {"bf16": MOE_A_BF16, "nvfp4": MOE_A_NVFP4, "mxfp8": MOE_A_MXFP8}

@@ -183,8 +183,9 @@ bool unified_supported(int wfmt, int afmt, int P, int E, int K);
 cudaError_t launch_unified(int wfmt, int afmt, int stage1, int ntok, bool tiny, UnifiedArgs u, cudaStream_t s);
 
 // Ordered per-token sum of the partials (FP32, or BF16 when part_bf16).
+// out: BF16 [T][H], or FP32 with out_f32 (a rank's partial of a tensor-parallel layer).
 cudaError_t launch_combine(const void *part, bool part_bf16, int H, const int32_t *pair_pos, int T, int K,
-                           void *out_bf16, cudaStream_t s);
+                           void *out, bool out_f32, cudaStream_t s);
 
 // Quantisers.  `rows_dev`, when non-null, is a device int with the number of
 // rows that are live; rows at or beyond it are skipped, and so are rows r with

@@ -45,7 +45,7 @@ __device__ __forceinline__ void load_part8(const void *part, size_t idx, float (
 template <bool BF16>
 __global__ void __launch_bounds__(kCombThreads)
 k_combine(const void *__restrict__ part, int H, const int32_t *__restrict__ pair_pos, int T, int K,
-          __nv_bfloat16 *__restrict__ out) {
+          void *__restrict__ out, int out_f32) {
   pdl_trigger();
   const int c = (blockIdx.x * kCombThreads + threadIdx.x) * 8;
   if (c >= H) {
@@ -107,15 +107,22 @@ k_combine(const void *__restrict__ part, int H, const int32_t *__restrict__ pair
           }
       }
     }
-    __align__(16) __nv_bfloat162 o[4];
+    if (out_f32) {  // a rank's partial of a tensor-parallel layer, summed across ranks before rounding
+      float4 *o4 = reinterpret_cast<float4 *>(reinterpret_cast<float *>(out) + (size_t)t * H + c);
+      o4[0] = make_float4(acc[0], acc[1], acc[2], acc[3]);
+      o4[1] = make_float4(acc[4], acc[5], acc[6], acc[7]);
+    } else {
+      __align__(16) __nv_bfloat162 o[4];
 #pragma unroll
-    for (int e = 0; e < 4; ++e) o[e] = __floats2bfloat162_rn(acc[2 * e], acc[2 * e + 1]);
-    *reinterpret_cast<uint4 *>(out + (size_t)t * H + c) = *reinterpret_cast<const uint4 *>(o);
+      for (int e = 0; e < 4; ++e) o[e] = __floats2bfloat162_rn(acc[2 * e], acc[2 * e + 1]);
+      *reinterpret_cast<uint4 *>(reinterpret_cast<__nv_bfloat16 *>(out) + (size_t)t * H + c) =
+          *reinterpret_cast<const uint4 *>(o);
+    }
   }
 }
 
 cudaError_t launch_combine(const void *part, bool part_bf16, int H, const int32_t *pair_pos, int T, int K, void *out,
-                           cudaStream_t s) {
+                           bool out_f32, cudaStream_t s) {
   if (T <= 0) return cudaSuccess;
   if (K > kMaxK || H % 8) return cudaErrorInvalidValue;
   // one resident wave of blocks, each looping over its tokens; the SM count and
@@ -147,10 +154,10 @@ cudaError_t launch_combine(const void *part, bool part_bf16, int H, const int32_
   const int gx = (H + kCombThreads * 8 - 1) / (kCombThreads * 8);
   const int gy = std::max(1, std::min(T, sms * std::max(1, occ[part_bf16 ? 1 : 0]) / gx));
   if (part_bf16)
-    return launch_pdl(k_combine<true>, dim3(gx, gy), dim3(kCombThreads), 0, s, part, H, pair_pos, T, K,
-                      reinterpret_cast<__nv_bfloat16 *>(out));
-  return launch_pdl(k_combine<false>, dim3(gx, gy), dim3(kCombThreads), 0, s, part, H, pair_pos, T, K,
-                    reinterpret_cast<__nv_bfloat16 *>(out));
+    return launch_pdl(k_combine<true>, dim3(gx, gy), dim3(kCombThreads), 0, s, part, H, pair_pos, T, K, out,
+                      out_f32 ? 1 : 0);
+  return launch_pdl(k_combine<false>, dim3(gx, gy), dim3(kCombThreads), 0, s, part, H, pair_pos, T, K, out,
+                    out_f32 ? 1 : 0);
 }
 
 // ------------------------------------------------------------------- packer

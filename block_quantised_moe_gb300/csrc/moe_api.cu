@@ -30,6 +30,7 @@ struct moe_plan_s {
   bool tc2_on = false; // ... otherwise on the CTA-pair kernel (token tiles of up to 256)
   bool unified_ok = false;  // decode plan the single-launch forward supports
   bool unified_on = false;  // ... and moe_run uses it (MOE_OPT_SINGLE_LAUNCH)
+  bool out_f32 = false;     // FP32 output (MOE_OPT_OUT_F32)
   int large_min = 0x7FFFFFFF;
   ScratchLayout S;
 };
@@ -256,8 +257,14 @@ moe_status moe_plan_set_option(moe_plan_t plan, int32_t option, int32_t value) {
   if (!plan) return MOE_ERR_INVALID_ARG;
   if (option == MOE_OPT_SINGLE_LAUNCH) {
     if (value != 0 && value != 1) return MOE_ERR_INVALID_ARG;
-    if (value == 1 && !plan->unified_ok) return MOE_ERR_UNSUPPORTED;
+    if (value == 1 && (!plan->unified_ok || plan->out_f32)) return MOE_ERR_UNSUPPORTED;
     plan->unified_on = value == 1;
+    return MOE_OK;
+  }
+  if (option == MOE_OPT_OUT_F32) {
+    if (value != 0 && value != 1) return MOE_ERR_INVALID_ARG;
+    if (value == 1 && plan->unified_on) return MOE_ERR_UNSUPPORTED;
+    plan->out_f32 = value == 1;
     return MOE_OK;
   }
   return MOE_ERR_INVALID_ARG;
@@ -606,7 +613,8 @@ static moe_status run_forward(moe_binding b, cudaStream_t stream, cudaEvent_t *e
   }
   if (err != cudaSuccess) return MOE_ERR_CUDA;
   if (mark(MOE_STAGE_COMBINE) != cudaSuccess) return MOE_ERR_CUDA;
-  if ((err = launch_combine(part, P.tc_on, H, pair_pos, T, K, b->out, stream)) != cudaSuccess) return MOE_ERR_CUDA;
+  if ((err = launch_combine(part, P.tc_on, H, pair_pos, T, K, b->out, P.out_f32, stream)) != cudaSuccess)
+    return MOE_ERR_CUDA;
   if (mark(MOE_NUM_STAGES) != cudaSuccess) return MOE_ERR_CUDA;
   return MOE_OK;
 }
@@ -643,7 +651,8 @@ moe_status moe_run_host(moe_binding b, const void *x_host, const int32_t *ids_ho
     return MOE_ERR_CUDA;
   moe_status st = moe_run(b, stream);
   if (st != MOE_OK) return st;
-  if (cudaMemcpyAsync(out_host, b->out, T * H * 2, cudaMemcpyDeviceToHost, stream) != cudaSuccess)
+  if (cudaMemcpyAsync(out_host, b->out, T * H * (b->P.out_f32 ? 4 : 2), cudaMemcpyDeviceToHost, stream) !=
+      cudaSuccess)
     return MOE_ERR_CUDA;
   return cuda_status(cudaStreamSynchronize(stream));
 }

@@ -182,7 +182,14 @@ MOE_API moe_status moe_plan(const moe_caps *caps, moe_plan_t *out, size_t *scrat
  *   per-stage launches faster on decode batches than the grid barriers of the
  *   single launch.  Both give bit-identical outputs; moe_run_timed always runs
  *   one launch per stage. */
-enum { MOE_OPT_SINGLE_LAUNCH = 1 };
+/* MOE_OPT_OUT_F32: 1 makes `out` FP32 [num_tokens, H] instead of BF16: the
+ *   forward's per-token sums before their rounding to BF16, for a layer split
+ *   over ranks along the intermediate dimension (tensor parallelism: b12x
+ *   project page, "What's in here", the fused FP4 TP MoE), where each rank's
+ *   result is a partial sum that the ranks add in a fixed order before
+ *   rounding.  Not combinable with MOE_OPT_SINGLE_LAUNCH (MOE_ERR_UNSUPPORTED).
+ *   moe_run_host copies 4-byte elements back. */
+enum { MOE_OPT_SINGLE_LAUNCH = 1, MOE_OPT_OUT_F32 = 2 };
 
 /* Set a plan option; applies to bindings made afterwards.  Host only.
  * MOE_ERR_UNSUPPORTED if the plan cannot take the value, MOE_ERR_INVALID_ARG
@@ -198,7 +205,7 @@ MOE_API moe_status moe_plan_set_option(moe_plan_t plan, int32_t option, int32_t 
  *   topk_ids      device, int32 [num_tokens, K]; ids outside [0, E) are dropped
  *   topk_weights  device, float [num_tokens, K]
  *   num_tokens    0..max_tokens (0 makes moe_run a no-op)
- *   out           device, BF16 [num_tokens, H]
+ *   out           device, BF16 [num_tokens, H] (FP32 with MOE_OPT_OUT_F32)
  * The binding holds no reference to the plan; destroy it with
  * moe_destroy_binding. */
 MOE_API moe_status moe_bind(moe_plan_t plan, void *scratch, size_t scratch_bytes,

@@ -175,6 +175,19 @@ def test_single_launch_option_follows_the_plan(abi):
     wmx, _ = abi.moe_plan_weights(128, 4096, 1024, "mxfp4", "relu2")
     mx, _, _ = abi.moe_plan(wmx, 4, 64, "mxfp8")
     abi.moe_plan_set_option(mx, abi.MOE_OPT_SINGLE_LAUNCH, 1)
+    # FP32 output (a tensor-parallel rank's partial) excludes the single launch, both ways round
+    with pytest.raises(abi.MoeError) as ei:
+        abi.moe_plan_set_option(mx, abi.MOE_OPT_OUT_F32, 1)
+    assert ei.value.status == abi.MOE_ERR_UNSUPPORTED
+    abi.moe_plan_set_option(mx, abi.MOE_OPT_SINGLE_LAUNCH, 0)
+    abi.moe_plan_set_option(mx, abi.MOE_OPT_OUT_F32, 1)
+    with pytest.raises(abi.MoeError) as ei:
+        abi.moe_plan_set_option(mx, abi.MOE_OPT_SINGLE_LAUNCH, 1)
+    assert ei.value.status == abi.MOE_ERR_UNSUPPORTED
+    with pytest.raises(abi.MoeError) as ei:
+        abi.moe_plan_set_option(mx, abi.MOE_OPT_OUT_F32, 3)
+    assert ei.value.status == abi.MOE_ERR_INVALID_ARG
+    abi.moe_plan_set_option(mx, abi.MOE_OPT_OUT_F32, 0)
     for p in (small, big, mx):
         abi.moe_destroy_plan(p)
     abi.moe_destroy_weight_plan(wp)
