@@ -56,7 +56,7 @@
 
 namespace bqmoe {
 
-constexpr int k2EpiWarps = 4, k2AWarps = 8, k2BWarps = 1;
+constexpr int k2EpiWarps = 8, k2AWarps = 8, k2BWarps = 1;
 constexpr int k2MmaWarp = k2EpiWarps + k2AWarps + k2BWarps;  // warp 13
 constexpr int k2RelayWarp = k2MmaWarp + 1;                     // warp 14
 constexpr int k2LoadWarp = k2RelayWarp + 1;                     // warp 15
@@ -91,13 +91,13 @@ static_assert(k2AWarps * 32 == 256 && 256 % (k2AGroups * 32) == 0, "8 fragment c
 // ------------------------------------------------------------ cluster helpers
 
 
-// Named barrier 1 over the four epilogue warps (threads 0..127).
-__device__ __forceinline__ void epi_bar_sync() { asm volatile("bar.sync 1, 128;" ::: "memory"); }
+// Named barrier 1 over the eight epilogue warps (threads 0..255).
+__device__ __forceinline__ void epi_bar_sync() { asm volatile("bar.sync 1, 256;" ::: "memory"); }
 // The same barrier, returning whether every epilogue thread passed `v`.
 __device__ __forceinline__ bool epi_bar_and(bool v) {
   uint32_t r;
   asm volatile(
-      "{\n\t.reg .pred p, q;\n\tsetp.ne.u32 p, %1, 0;\n\tbar.red.and.pred q, 1, 128, p;\n\tselp.u32 %0, 1, 0, q;\n\t}"
+      "{\n\t.reg .pred p, q;\n\tsetp.ne.u32 p, %1, 0;\n\tbar.red.and.pred q, 1, 256, p;\n\tselp.u32 %0, 1, 0, q;\n\t}"
       : "=r"(r)
       : "r"((uint32_t)v)
       : "memory");
@@ -558,38 +558,28 @@ __global__ void __launch_bounds__(k2Threads, 1) k_grouped_tc2(const GroupedArgs 
     // epilogue) and read back as broadcast vector loads.  The four warps decide
     // together (barrier with an AND vote) whether to go on, so none waits at
     // the barrier for a warp that has stopped.
-    const int m = warp * 32 + lane;  // accumulator row = TMEM lane
+    const int m = (warp & 3) * 32 + lane;    // accumulator row = TMEM lane (quadrant warp % 4)
+    const int cbase = (warp >> 2) * (k2MaxN / 2);  // this warp's half of the tile's columns
+    const int et = threadIdx.x;              // 0..255: the column whose factor this thread fetches
     const uint32_t tempty_leader = mapa(tempty0, 0);
     float *__restrict__ outp = a.out;
-    int pn[2];
-    auto fetch_pairs = [&](const Tc2Item &it) {
-#pragma unroll
-      for (int q = 0; q < 2; ++q) {
-        const int nl = m + 128 * q;
-        pn[q] = nl < it.ntok ? a.sorted_pair[it.s0 + nl] : -1;
-      }
-    };
-    float cn[2], gn = 1.f;
+    int pn;
+    auto fetch_pairs = [&](const Tc2Item &it) { pn = et < it.ntok ? a.sorted_pair[it.s0 + et] : -1; };
+    float cn, gn = 1.f;
     auto fetch_factors = [&](const Tc2Item &it) {
       // the expert's global scale of this thread's rows (gate / up / single
       // matrix), applied in the epilogue; the down projection's goes into the
       // column factor
       gn = a.globals[4 * it.e + ((STAGE == STAGE_GATED && (m & 15) >= 8) ? 1 : 0)];
       const float g2 = STAGE == STAGE_DOWN ? a.globals[4 * it.e + 2] : 1.f;
-#pragma unroll
-      for (int q = 0; q < 2; ++q) {
-        cn[q] = 0.f;
-        if (pn[q] >= 0) {
-          const int sl = it.s0 + m + 128 * q;
-          const float f = a.act_g ? a.act_g[a.act_by_token ? (int64_t)(pn[q] / a.top_k) : (int64_t)sl] : 1.f;
-          cn[q] = STAGE == STAGE_DOWN ? f * (a.topk_weights[pn[q]] * g2) : f;
-        }
+      cn = 0.f;
+      if (pn >= 0) {
+        const int sl = it.s0 + et;
+        const float f = a.act_g ? a.act_g[a.act_by_token ? (int64_t)(pn / a.top_k) : (int64_t)sl] : 1.f;
+        cn = STAGE == STAGE_DOWN ? f * (a.topk_weights[pn] * g2) : f;
       }
     };
-    auto put_factors = [&](int buf) {
-#pragma unroll
-      for (int q = 0; q < 2; ++q) colinfo[buf * k2MaxN + m + 128 * q] = cn[q];
-    };
+    auto put_factors = [&](int buf) { colinfo[buf * k2MaxN + et] = cn; };
     pdl_wait();  // row factors come from the preceding kernels
     Tc2Item it_next{};
     float gsel_next = 1.f;
@@ -621,9 +611,9 @@ __global__ void __launch_bounds__(k2Threads, 1) k_grouped_tc2(const GroupedArgs 
         const int blk = 2 * it.bp + (int)rank;
         const int tile = 8 * blk + (m >> 4), rr = m & 15;
         const float *colc = colinfo + b * k2MaxN;
-        for (int c0 = 0; c0 < it.n; c0 += 32) {
+        for (int c0 = cbase; c0 < min(it.n, cbase + k2MaxN / 2); c0 += 32) {
           uint32_t raw[32];
-          tc_ld32(tmem + ((uint32_t)(warp * 32) << 16) + (uint32_t)(b * k2AccCols + c0), raw);
+          tc_ld32(tmem + ((uint32_t)((warp & 3) * 32) << 16) + (uint32_t)(b * k2AccCols + c0), raw);
           float v[32];
 #pragma unroll
           for (int q = 0; q < 8; ++q) {
