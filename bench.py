@@ -200,10 +200,11 @@ def tensor_peak(cfg, afmt, pairs):
     """Dense tensor peak (TFLOP/s) of the MMA kind the large-batch GEMMs run on.
 
     FP16/BF16 operands (kind::f16: the register-dequant kernel and the W4A16 and
-    MXFP4 tcgen05 kernels) take the measured cuBLAS BF16 figure, sustained since
-    the GEMMs run inside a long step; NVFP4 x NVFP4 batches of 1024+ pairs run on
-    the block-scaled FP4 kind and take that figure x 6 (13.5 / 2.25 PFLOP/s
-    nominal)."""
+    MXFP4 x BF16 tcgen05 kernels) take the measured cuBLAS BF16 figure, sustained
+    since the GEMMs run inside a long step; NVFP4 x NVFP4 batches of 1024+ pairs
+    run on the block-scaled FP4 kind and take that figure x 6 (13.5 / 2.25
+    PFLOP/s nominal), MXFP4 x MXFP8 batches of 1024+ pairs on the block-scaled
+    FP8 kind, x 2 (4.5 / 2.25)."""
     try:
         with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
             bf16, src = float(json.load(f)["bf16_tflops_sustained"]), "measured"
@@ -211,6 +212,8 @@ def tensor_peak(cfg, afmt, pairs):
         bf16, src = 1700.0, "fallback"
     if cfg["wfmt"] == "nvfp4" and afmt == "nvfp4" and pairs >= 1024:
         return bf16 * 13.5 / 2.25, f"{src} bf16 sustained x 13.5/2.25 (fp4)"
+    if cfg["wfmt"] == "mxfp4" and afmt == "mxfp8" and pairs >= 1024:
+        return bf16 * 4.5 / 2.25, f"{src} bf16 sustained x 4.5/2.25 (mx fp8)"
     return bf16, f"{src} bf16 sustained"
 
 

@@ -49,6 +49,10 @@ def test_tensor_peak_follows_the_mma_kind():
     # below 1024 pairs every expert runs on the register-dequant (FP16 MMA) kernel
     small, _ = bench.tensor_peak(w4a4, w4a4["afmt"], 1000)
     assert small == pytest.approx(f16)
+    # MXFP4 weights with MXFP8 activations: the block-scaled FP8 kind, twice the FP16 rate
+    mx = synth.CONFIGS["mxfp4_mxfp8_relu2_e128_h4096_i1024_k4"]
+    fp8, kind = bench.tensor_peak(mx, mx["afmt"], 16384)
+    assert fp8 == pytest.approx(f16 * 2) and "fp8" in kind
 
 
 def test_traffic_is_reported_only_for_the_measured_source(tmp_path, monkeypatch):
