@@ -826,7 +826,17 @@ __global__ void __launch_bounds__(256) k_gather_slot_rows(const uint4 *__restric
     if (p < 0) continue;
     const uint4 *a = src + (int64_t)(p / top_k) * row_chunks;
     uint4 *b = dst + s * row_chunks;
-    for (int c = lane; c < row_chunks; c += 32) b[c] = a[c];
+    // eight 16-byte loads in flight per lane before their stores; the rows are
+    // written once and read back by the tensor copies of the next kernel
+    int c = lane;
+    for (; c + 7 * 32 < row_chunks; c += 8 * 32) {
+      uint4 v[8];
+#pragma unroll
+      for (int i = 0; i < 8; ++i) v[i] = __ldg(a + c + 32 * i);
+#pragma unroll
+      for (int i = 0; i < 8; ++i) __stcs(b + c + 32 * i, v[i]);
+    }
+    for (; c < row_chunks; c += 32) __stcs(b + c, __ldg(a + c));
   }
 }
 
