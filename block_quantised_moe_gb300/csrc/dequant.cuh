@@ -138,6 +138,49 @@ __device__ __forceinline__ void stage_row_slots(const void *act, const uint8_t *
   }
 }
 
+// The CTA-pair kernel's K order: within every 64-element step the 32
+// slot-ordered pairs (32-bit words) are transposed as a 4 x 8 matrix: pair
+// 4 (w & 7) + (w >> 3) of the slot order is pair w of the row.  A warp converts
+// eight steps at a time through shared memory: `sbuf` holds them in the slot
+// order with a row stride of 36 words (so that both the 16-byte writes and the
+// transposing 4-byte reads are free of bank conflicts); each lane then writes one
+// 16-byte chunk of the reordered steps per round, the warp's chunks contiguous.
+constexpr int kPairStride = 36;  // words per staged step in shared memory
+__device__ __forceinline__ void pair_order_flush(const uint32_t *sbuf, uint4 *dst, int nsteps, int lane) {
+  for (int c = lane; c < 8 * nsteps; c += 32) {
+    const int st = c >> 3, i = c & 7;
+    const uint32_t *src = sbuf + st * kPairStride + 16 * (i & 1) + (i >> 1);  // pairs 4t + (i >> 1) (+ 16)
+    dst[c] = make_uint4(src[0], src[4], src[8], src[12]);
+  }
+}
+
+// Row `rid` of a source as 16-bit values times inv in the CTA-pair kernel's K
+// order, written to dst by the 32 lanes of a warp; sbuf: 8 x kPairStride words
+// of shared memory private to the warp.
+template <int SRC, bool BF16OUT = false>
+__device__ __forceinline__ void stage_row_pair_order(const void *act, const uint8_t *act_scales, int64_t rid, int K,
+                                                     float inv, __half *dst, uint32_t *sbuf, int lane) {
+  for (int st0 = 0; st0 < K / 64; st0 += 8) {
+    const int ns = min(8, K / 64 - st0);
+    // slot-order groups of 16 values, one per lane (4 per step)
+    if (lane < 4 * ns) {
+      const int g = 4 * st0 + lane;
+      const int k = slot_group_k(g);
+      float lo[8], hi[8];
+      src_load8<SRC>(act, act_scales, rid, k, K, lo);
+      src_load8<SRC>(act, act_scales, rid, k + 16, K, hi);
+      uint4 o0, o1;
+      to_16bit_slots<BF16OUT>(lo, hi, inv, o0, o1);
+      uint4 *sb = reinterpret_cast<uint4 *>(sbuf + (lane >> 2) * kPairStride + 8 * (lane & 3));
+      sb[0] = o0;
+      sb[1] = o1;
+    }
+    __syncwarp();
+    pair_order_flush(sbuf, reinterpret_cast<uint4 *>(dst + 64 * st0), ns, lane);
+    __syncwarp();
+  }
+}
+
 // The same, two slot groups per lane at a time with both groups' loads issued
 // before either is stored (a store to shared memory may alias the source, so
 // the compiler would otherwise keep each group's loads behind the previous

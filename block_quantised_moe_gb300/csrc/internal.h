@@ -171,10 +171,12 @@ bool mx8_tc_supported(int rows_total, int K);
 cudaError_t launch_grouped_mx8(int stage, const GroupedArgs &a, int rows_total, cudaStream_t s);
 // h (or its re-quantised codes) as 16-bit rows for the tcgen05 GEMM2: FP16 with a
 // per-row factor, or BF16 with factor 1 (out_bf16; also MXFP8 x^ -> BF16 rows).
-// rows_dev (device, nullable) caps the rows actually converted.
+// rows_dev (device, nullable) caps the rows actually converted.  pair_order:
+// the CTA-pair kernel's K order (h rows) instead of the slot order (x rows that
+// the slot-order gather reorders).
 cudaError_t launch_stage_h16(int src, const void *act, const uint8_t *act_scales, const float *act_g, int K,
                              int64_t rows, const int32_t *rows_dev, __half *h16, float *fac, bool out_bf16,
-                             cudaStream_t s);
+                             bool pair_order, cudaStream_t s);
 
 // Single-launch decode forward (unified.cuh): supported formats and sizes,
 // and the launch (args filled by the caller; nst / ngroups set here).

@@ -184,7 +184,8 @@ __device__ __forceinline__ void tc2_commit_both(uint32_t bar) {
 // One fragment chunk of a packed 64-K step (16 code bytes of lane `ln` of
 // 16-row tile `tile`, and the lane group's block scales), dequantised to
 // 16-bit values (NVFP4: E2M1 x E4M3 in FP16, exact; MXFP4: E2M1 x 2^X in BF16,
-// exact) and stored at its slot positions in the 128-byte-swizzled K-major tile.
+// exact) and stored in the pair kernel's K order in the 128-byte-swizzled
+// K-major tile.
 template <int WF>
 __device__ __forceinline__ void dequant_chunk_store(uint8_t *tileA, uint4 cch, uint2 sch, int tile, int ln) {
   const int g = ln >> 2, c4 = ln & 3;
@@ -222,14 +223,17 @@ __device__ __forceinline__ void dequant_chunk_store(uint8_t *tileA, uint4 cch, u
       }
     }
   }
-#pragma unroll
-  for (int j = 0; j < 4; ++j) {
-    const int k = 16 * j + 2 * c4;
-    *reinterpret_cast<uint32_t *>(tileA + sw128_elem(r0, k)) = o[j][0];
-    *reinterpret_cast<uint32_t *>(tileA + sw128_elem(r1, k)) = o[j][1];
-    *reinterpret_cast<uint32_t *>(tileA + sw128_elem(r0, k + 8)) = o[j][2];
-    *reinterpret_cast<uint32_t *>(tileA + sw128_elem(r1, k + 8)) = o[j][3];
-  }
+  // Lane c of a quad holds, of rows r0 and r1, the 16 values of slot positions
+  // 16 j + 8 h + 2 c + e (word j, pair h, element e); the pair kernel's K order
+  // puts them at 16 c + 4 j + 2 h + e, so each row's 16 values are two
+  // contiguous 16-byte chunks (the activation rows are written in that order).
+  auto put = [&](int r, int ch, uint4 v) {
+    *reinterpret_cast<uint4 *>(tileA + (r >> 3) * 1024 + (r & 7) * 128 + (((ch ^ r) & 7) << 4)) = v;
+  };
+  put(r0, 2 * c4, make_uint4(o[0][0], o[0][2], o[1][0], o[1][2]));
+  put(r0, 2 * c4 + 1, make_uint4(o[2][0], o[2][2], o[3][0], o[3][2]));
+  put(r1, 2 * c4, make_uint4(o[0][1], o[0][3], o[1][1], o[1][3]));
+  put(r1, 2 * c4 + 1, make_uint4(o[2][1], o[2][3], o[3][1], o[3][3]));
 }
 
 // ------------------------------------------------------------------ work items
@@ -811,39 +815,51 @@ cudaError_t encode_rows16_sw128(CUtensorMap *map, const void *base, uint64_t row
 // ------------------------------------------- token rows -> expert-sorted slot rows
 //
 // dst[s] = src[sorted_pair[s] / top_k] for every live slot s < offsets[E] (one
-// warp per row, 16-byte copies), so that the pair kernel's activation tiles
-// are contiguous rows; padding slots are left as they are (they feed only
-// discarded MMA columns).
+// warp per row), so that the pair kernel's activation tiles are contiguous
+// rows, in the pair kernel's K order (the source rows are in the slot order;
+// pair_order_flush transposes every 64-element step's 32 pairs as a 4 x 8
+// matrix).  Padding slots are left as they are (they feed only discarded MMA
+// columns).
 __global__ void __launch_bounds__(256) k_gather_slot_rows(const uint4 *__restrict__ src, const int32_t *__restrict__ sorted,
                                                           const int32_t *__restrict__ n_live, int top_k, int row_chunks,
                                                           uint4 *__restrict__ dst) {
+  __shared__ __align__(16) uint32_t sbuf_all[8][8 * kPairStride];
+  uint32_t *sbuf = sbuf_all[threadIdx.x >> 5];
   pdl_trigger();
   pdl_wait();
   const int lane = threadIdx.x & 31;
   const int64_t live = *n_live;
+  const int steps = row_chunks / 8;  // 64-element steps of 8 16-byte chunks
   for (int64_t s = (int64_t)blockIdx.x * 8 + (threadIdx.x >> 5); s < live; s += (int64_t)gridDim.x * 8) {
     const int p = sorted[s];
     if (p < 0) continue;
     const uint4 *a = src + (int64_t)(p / top_k) * row_chunks;
     uint4 *b = dst + s * row_chunks;
-    // eight 16-byte loads in flight per lane before their stores; the rows are
-    // written once and read back by the tensor copies of the next kernel
-    int c = lane;
-    for (; c + 7 * 32 < row_chunks; c += 8 * 32) {
-      uint4 v[8];
+    for (int st0 = 0; st0 < steps; st0 += 8) {
+      const int ns = min(8, steps - st0);
+      // the eight steps' 64 chunks, two per lane, coalesced
+      uint4 v[2];
 #pragma unroll
-      for (int i = 0; i < 8; ++i) v[i] = __ldg(a + c + 32 * i);
+      for (int h = 0; h < 2; ++h) {
+        const int c = lane + 32 * h;
+        if (c < 8 * ns) v[h] = __ldg(a + 8 * st0 + c);
+      }
 #pragma unroll
-      for (int i = 0; i < 8; ++i) __stcs(b + c + 32 * i, v[i]);
+      for (int h = 0; h < 2; ++h) {
+        const int c = lane + 32 * h;
+        if (c < 8 * ns) *reinterpret_cast<uint4 *>(sbuf + (c >> 3) * kPairStride + 4 * (c & 7)) = v[h];
+      }
+      __syncwarp();
+      pair_order_flush(sbuf, b + 8 * st0, ns, lane);
+      __syncwarp();
     }
-    for (; c < row_chunks; c += 32) __stcs(b + c, __ldg(a + c));
   }
 }
 
 cudaError_t launch_gather_slot_rows(const void *src, const int32_t *sorted, const int32_t *n_live, int top_k,
                                     int cols16, int64_t cap_rows, void *dst, cudaStream_t s) {
   if (cap_rows <= 0) return cudaSuccess;
-  if (cols16 % 8) return cudaErrorInvalidValue;
+  if (cols16 % 64) return cudaErrorInvalidValue;
   int dev = 0, sms = 0;
   cudaError_t err;
   if ((err = cudaGetDevice(&dev)) != cudaSuccess) return err;

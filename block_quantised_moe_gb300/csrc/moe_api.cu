@@ -504,7 +504,7 @@ static moe_status run_forward(moe_binding b, cudaStream_t stream, cudaEvent_t *e
   const int stage1 = L.act == MOE_ACT_SILU_GATED ? STAGE_GATED : STAGE_RELU2;
   if (!nv && P.tc2_on) {  // MXFP4 tcgen05 operands: x or x^ as BF16 slot-order rows, factor 1
     err = launch_stage_h16(P.afmt == MOE_A_MXFP8 ? SRC_H_MXFP8 : SRC_X_BF16, x_src, x_src_scales, nullptr, H, T,
-                           nullptr, at<__half>(sc, S.xb16), nullptr, true, stream);
+                           nullptr, at<__half>(sc, S.xb16), nullptr, true, false, stream);
     if (err != cudaSuccess) return MOE_ERR_CUDA;
   }
   if (P.tc2_on) {  // the pair kernel reads GEMM1's activation rows in slot order, one tensor copy per stage
@@ -576,7 +576,7 @@ static moe_status run_forward(moe_binding b, cudaStream_t stream, cudaEvent_t *e
   // GEMM2 * topk_weight -> partials, then the ordered combine
   if (P.tc2_on) {  // 16-bit slot-order rows of h (or of its re-quantised codes) for the CTA-pair GEMM2
     err = launch_stage_h16(src2, a.act, a.act_scales, a.act_g, I, S.cap_sorted, offsets + E, at<__half>(sc, S.h16),
-                           nv ? at<float>(sc, S.h16fac) : nullptr, !nv, stream);
+                           nv ? at<float>(sc, S.h16fac) : nullptr, !nv, true, stream);
     if (err != cudaSuccess) return MOE_ERR_CUDA;
   }
   a.codes = b->packed + L.off_c2;
