@@ -88,9 +88,6 @@ constexpr int k2TmemCols = 2 * k2AccCols;   // double buffered
 constexpr int k2Bars = k2AStages + k2BStages + k2Pairs + k2RStages + 4 + 1 + 2 * k2RawStages;
 static_assert(k2AWarps * 32 == 256 && 256 % (k2AGroups * 32) == 0, "8 fragment chunks per k-block over the A groups");
 
-// ------------------------------------------------------------ cluster helpers
-
-
 // Named barrier 1 over the eight epilogue warps (threads 0..255).
 __device__ __forceinline__ void epi_bar_sync() { asm volatile("bar.sync 1, 256;" ::: "memory"); }
 // The same barrier, returning whether every epilogue thread passed `v`.
@@ -104,50 +101,6 @@ __device__ __forceinline__ bool epi_bar_and(bool v) {
   return r != 0;
 }
 
-__device__ __forceinline__ uint32_t cluster_rank() {
-  uint32_t r;
-  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
-  return r;
-}
-__device__ __forceinline__ uint32_t cluster_id_x() {
-  uint32_t r;
-  asm volatile("mov.u32 %0, %%clusterid.x;" : "=r"(r));
-  return r;
-}
-__device__ __forceinline__ uint32_t cluster_count_x() {
-  uint32_t r;
-  asm volatile("mov.u32 %0, %%nclusterid.x;" : "=r"(r));
-  return r;
-}
-// Shared-memory address of the same variable in CTA `rank` of the cluster.
-__device__ __forceinline__ uint32_t mapa(uint32_t addr, uint32_t rank) {
-  uint32_t r;
-  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(addr), "r"(rank));
-  return r;
-}
-__device__ __forceinline__ void mbar_arrive_remote(uint32_t cluster_addr) {
-  asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr) : "memory");
-}
-__device__ __forceinline__ bool mbar_try_wait_c(uint32_t bar, uint32_t parity) {
-  uint32_t ok;
-  asm volatile(
-      "{\n\t.reg .pred p;\n\tmbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
-      "selp.u32 %0, 1, 0, p;\n\t}"
-      : "=r"(ok)
-      : "r"(bar), "r"(parity)
-      : "memory");
-  return ok != 0;
-}
-// Bounded wait with cluster-scope acquire (arrivals come from the peer CTA
-// and from the pair's tensor-core commits); false on timeout.
-__device__ __forceinline__ bool mbar_wait_c(uint32_t bar, uint32_t parity) {
-  if (mbar_try_wait_c(bar, parity)) return true;
-  const unsigned long long t0 = globaltimer_ns();
-  for (uint32_t it = 1;; ++it) {
-    if (mbar_try_wait_c(bar, parity)) return true;
-    if ((it & 255u) == 0 && globaltimer_ns() - t0 > kWaitNs) return false;
-  }
-}
 // 2-D tiled tensor copy global -> shared with completion (bytes) on `bar`.
 __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap *map, int x, int y, uint32_t bar) {
   asm volatile(
@@ -161,9 +114,6 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap *map
 __device__ __forceinline__ void cp_async_arrive_noinc(uint32_t bar) {
   asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(bar) : "memory");
 }
-__device__ __forceinline__ void cluster_sync_all() {
-  asm volatile("barrier.cluster.arrive.release;\n\tbarrier.cluster.wait.acquire;" ::: "memory");
-}
 
 __device__ __forceinline__ void tc2_mma_f16(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
                                             uint32_t accumulate) {
@@ -171,14 +121,6 @@ __device__ __forceinline__ void tc2_mma_f16(uint32_t d_tmem, uint64_t adesc, uin
       "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
       "tcgen05.mma.cta_group::2.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
       "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate));
-}
-// Arrive (once the pair's earlier MMAs have completed) on the mbarrier at the
-// same offset in both CTAs of the pair.
-__device__ __forceinline__ void tc2_commit_both(uint32_t bar) {
-  asm volatile(
-      "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;" ::"r"(bar),
-      "h"((uint16_t)3)
-      : "memory");
 }
 
 // One fragment chunk of a packed 64-K step (16 code bytes of lane `ln` of
@@ -506,9 +448,7 @@ __global__ void __launch_bounds__(k2Threads, 1) k_grouped_tc2(const GroupedArgs 
           if (rank == 0)
             mbar_arrive(ready0 + 8u * (q % k2RStages));
           else
-            asm volatile("mbarrier.arrive.relaxed.cluster.shared::cluster.b64 _, [%0];" ::"r"(
-                             ready_leader + 8u * (q % k2RStages))
-                         : "memory");
+            mbar_arrive_remote_relaxed(ready_leader + 8u * (q % k2RStages));
         }
       }
     }
@@ -701,7 +641,9 @@ __global__ void __launch_bounds__(k2Threads, 1) k_grouped_tc2(const GroupedArgs 
         }
         tc_fence_before();
         __syncwarp();
-        if (lane == 0) mbar_arrive_remote(tempty_leader + 8u * b);
+        // relaxed: the accumulator has been read (tcgen05.wait::ld), and this
+        // warp's output stores need not complete before the MMA reuses it
+        if (lane == 0) mbar_arrive_remote_relaxed(tempty_leader + 8u * b);
       }
       if (more) {
         put_factors((li + 1) & 1);

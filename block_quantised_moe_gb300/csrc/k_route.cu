@@ -49,6 +49,26 @@ __device__ void stage_x_row(const __nv_bfloat16 *__restrict__ x, int H, __half *
   if (threadIdx.x == 0) xfac[row] = f;
 }
 
+// The same for many rows: warp w of staging CTA c (of n) takes rows
+// 32 c + w, + 32 n, ...; one warp per row (a CTA of 1024 threads per row left
+// the large launches bound by CTA scheduling).
+__device__ void stage_x_rows_by_warp(const RouteStaging &st, int64_t c, int64_t n) {
+  const int lane = threadIdx.x & 31;
+  for (int64_t i = c * kRouteThreads + threadIdx.x; i < st.zero_n; i += n * kRouteThreads) st.zero[i] = 0.f;
+  for (int64_t row = c * kRouteWarps + (threadIdx.x >> 5); row < st.T; row += n * kRouteWarps) {
+    float m = 0.f;
+    for (int k = lane * 8; k < st.H; k += 256) {
+      float v[8];
+      src_load8<SRC_X_BF16>(st.x, nullptr, row, k, st.H, v);
+#pragma unroll
+      for (int i = 0; i < 8; ++i) m = fmaxf(m, fabsf(v[i]));
+    }
+    const float f = stage_factor(warp_max(m));
+    stage_row_slots<SRC_X_BF16>(st.x, nullptr, row, st.H, __frcp_rn(f), st.x16 + row * st.H, lane, 32);
+    if (lane == 0) st.xfac[row] = f;
+  }
+}
+
 // Ranks the pairs [p0, p0 + kRouteThreads) of `ids` (thread i takes p0 + i).
 // warp_hist ([E][kRouteWarps], expert-major so the per-expert scans read
 // consecutive words) must be zero on entry.  On return (after a barrier):
@@ -140,7 +160,7 @@ k_route_one(const int32_t *__restrict__ ids, int P, int E, int pad, int ntok, in
 // P > kRouteThreads, first launch: CTA c < nchunk ranks chunk c, writing
 // chunk_hist[c][0..E-1] = its expert counts, chunk_hist[c][E] = its invalid ids
 // and pair_pos[p] = the pair's rank among the chunk's pairs of its expert (-1
-// for an invalid id); CTAs past nchunk stage x rows.
+// for an invalid id); CTAs past nchunk stage x rows, one warp per row.
 __global__ void __launch_bounds__(kRouteThreads)
 k_route_rank(const int32_t *__restrict__ ids, int P, int E, int nchunk, int32_t *__restrict__ chunk_hist,
              int32_t *__restrict__ pair_pos, RouteStaging st) {
@@ -148,7 +168,7 @@ k_route_rank(const int32_t *__restrict__ ids, int P, int E, int nchunk, int32_t 
   pdl_trigger();
   pdl_wait();
   if ((int)blockIdx.x >= nchunk) {
-    stage_x_row(st.x, st.H, st.x16, st.xfac, st.zero, st.zero_n, blockIdx.x - nchunk, gridDim.x - nchunk);
+    stage_x_rows_by_warp(st, blockIdx.x - nchunk, gridDim.x - nchunk);
     return;
   }
   int32_t *hist = sm;           // [E]
@@ -260,7 +280,8 @@ cudaError_t launch_route(const int32_t *ids, int P, int E, int pad, int ntok, in
   if ((err = cudaFuncSetAttribute(k_route_rank, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem1)) !=
       cudaSuccess)
     return err;
-  if ((err = launch_pdl(k_route_rank, dim3(nchunk + T), dim3(kRouteThreads), smem1, s, ids, P, E, nchunk,
+  const int nstage = (T + kRouteWarps - 1) / kRouteWarps;  // x staging CTAs, a row per warp
+  if ((err = launch_pdl(k_route_rank, dim3(nchunk + nstage), dim3(kRouteThreads), smem1, s, ids, P, E, nchunk,
                         chunk_hist, pair_pos, st)) != cudaSuccess)
     return err;
   const int G = kRouteThreads / (E + 1);
