@@ -21,11 +21,14 @@
 //   alternate k-blocks (one warp's chain of conversions, stores and proxy
 //   fence per k-block is latency bound), dequantised to FP16 (NVFP4: E2M1 x
 //   E4M3 is exact) or BF16 (MXFP4: E2M1 x 2^X is exact) and written in the
-//   UMMA K-major 128-byte-swizzled layout; a 6-stage ring.
+//   UMMA K-major 128-byte-swizzled layout; a 6-stage ring.  The K order of
+//   both operands within a 64-element step is the pair order (below), in
+//   which a producer lane's two rows take four 16-byte stores.
 // * B: the tile's activation rows are consecutive slots of the expert-sorted
 //   list (GEMM1's x rows are gathered into slot order beforehand, GEMM2's h
-//   rows already are), so a CTA's B half of a k-block is one 2-D tensor copy
-//   (TMA, 128 rows x 64 columns, 128-byte swizzle); a 6-stage ring.
+//   rows already are, both written in the pair order), so a CTA's B half of a
+//   k-block is one 2-D tensor copy (TMA, 128 rows x 64 columns, 128-byte
+//   swizzle); a 6-stage ring.
 // * Token tiles: an expert with c pairs is cut into ceil(c / 256) tiles of
 //   equal size (rounded up to 16), so no tile is a nearly empty remainder;
 //   the MMA's N is the tile's size rounded up to 16.
@@ -33,9 +36,11 @@
 //   in shared memory" into one arrival on the leader's ready barrier; the
 //   leader's MMA thread waits on that one barrier, issues 8 MMAs into one of
 //   two TMEM accumulators (2 x 256 columns) and releases both CTAs' two
-//   stages with one multicast tcgen05.commit.  K is a multiple of 128.  Each CTA's four epilogue warps read their
-//   128 rows of the accumulator (SiLU(gate)*up, ReLU^2, or the topk_weight
-//   scaling of the down projection) while the next tile's MMAs run.
+//   stages with one multicast tcgen05.commit.  K is a multiple of 128.
+// * Each CTA's eight epilogue warps (lane quadrant, column half) read its 128
+//   rows of the accumulator (SiLU(gate)*up, ReLU^2, or the topk_weight scaling
+//   of the down projection) while the next tile's MMAs run, and hand the
+//   buffer back with a relaxed arrive.
 // * Work items are (large expert, token tile, pair of 128-row blocks), dealt
 //   round-robin over persistent clusters (one CTA per SM).
 // * Every wait is a bounded mbarrier wait; on a timeout the kernel sets the
@@ -57,9 +62,9 @@
 namespace bqmoe {
 
 constexpr int k2EpiWarps = 8, k2AWarps = 8, k2BWarps = 1;
-constexpr int k2MmaWarp = k2EpiWarps + k2AWarps + k2BWarps;  // warp 13
-constexpr int k2RelayWarp = k2MmaWarp + 1;                     // warp 14
-constexpr int k2LoadWarp = k2RelayWarp + 1;                     // warp 15
+constexpr int k2MmaWarp = k2EpiWarps + k2AWarps + k2BWarps;  // warp 17
+constexpr int k2RelayWarp = k2MmaWarp + 1;                     // warp 18
+constexpr int k2LoadWarp = k2RelayWarp + 1;                     // warp 19
 constexpr int k2Threads = (k2LoadWarp + 1) * 32;
 constexpr int k2MaxN = 256;                 // tokens per pair tile
 constexpr int k2HalfRows = k2MaxN / 2;      // B rows per CTA
@@ -497,9 +502,9 @@ __global__ void __launch_bounds__(k2Threads, 1) k_grouped_tc2(const GroupedArgs 
     // ------------------------------------------------------ epilogue (both CTAs)
     // Each column's factor (activation factor; for the down projection times
     // the topk weight and the expert's global scale) is fetched one item ahead
-    // into shared memory by the 128 epilogue threads (slot -> pair -> factors:
+    // into shared memory by the 256 epilogue threads (slot -> pair -> factors:
     // dependent global loads whose latency then overlaps the previous item's
-    // epilogue) and read back as broadcast vector loads.  The four warps decide
+    // epilogue) and read back as broadcast vector loads.  The eight warps decide
     // together (barrier with an AND vote) whether to go on, so none waits at
     // the barrier for a warp that has stopped.
     const int m = (warp & 3) * 32 + lane;    // accumulator row = TMEM lane (quadrant warp % 4)
