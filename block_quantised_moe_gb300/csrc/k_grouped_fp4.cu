@@ -90,6 +90,12 @@ static_assert(kP4SfCols % 4 == 0 && kP4SfCol0 % 4 == 0, "scale-factor TMEM addre
 // the pair), K = 64.
 constexpr uint32_t kP4Idesc = (1u << 7) | (1u << 10) | ((uint32_t)(kP4N >> 3) << 17) | ((uint32_t)(256 >> 4) << 24);
 
+// Two floats as round-to-nearest BF16 in one word, the first in the low half.
+__device__ __forceinline__ uint32_t bf16x2_bits(float lo, float hi) {
+  const __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);
+  return *reinterpret_cast<const uint32_t *>(&h);
+}
+
 struct F4Item {
   int e, bp, s0, ntok;
 };
@@ -385,60 +391,79 @@ __global__ void __launch_bounds__(kP4Threads, 1) k_grouped_fp4(const GroupedArgs
     // Per column (one per lane and 32-column chunk, broadcast with shuffles):
     // the activation row's FP32 global, times the topk weight and the global
     // scale for the down projection; per row the expert's global scale of the
-    // gate / up / single matrix.  They are fetched one item ahead (slot -> pair
-    // -> factors are dependent loads): the pairs before the wait for the
-    // current accumulator, the factors right after it, so both round trips
-    // overlap the current item's epilogue instead of preceding it.
-    F4Item it_n{};
-    int p_n[kCh];
-    float c_n[kCh], gsel_n = 1.f;
-    auto fetch_pairs = [&](const F4Item &it) {
+    // gate / up / single matrix.  Item record -> the tile's pairs -> their
+    // factors are three dependent global loads; they run as a pipeline over the
+    // items (the record three items ahead, the pairs two, the factors one), so
+    // each load has a whole item's epilogue to return.  (As a chain started one
+    // item ahead they held up every GEMM2 item by about a microsecond.)
+    auto pairs_of = [&](const F4Item &it, int (&p)[kCh]) {
 #pragma unroll
       for (int ch = 0; ch < kCh; ++ch) {
         const int nl = cbase + 32 * ch + lane;
-        p_n[ch] = nl < it.ntok ? a.sorted_pair[it.s0 + nl] : -1;
+        p[ch] = nl < it.ntok ? a.sorted_pair[it.s0 + nl] : -1;
       }
     };
-    auto fetch_factors = [&](const F4Item &it) {
-      gsel_n = a.globals[4 * it.e + ((STAGE == STAGE_GATED && (m & 15) >= 8) ? 1 : 0)];
+    auto factors_of = [&](const F4Item &it, const int (&p)[kCh], float (&c)[kCh], float &gs) {
+      gs = a.globals[4 * it.e + ((STAGE == STAGE_GATED && (m & 15) >= 8) ? 1 : 0)];
       const float g2 = STAGE == STAGE_DOWN ? a.globals[4 * it.e + 2] : 1.f;
 #pragma unroll
       for (int ch = 0; ch < kCh; ++ch) {
         const int nl = cbase + 32 * ch + lane;
-        c_n[ch] = 0.f;
-        if (p_n[ch] >= 0) {
-          const float f = a.act_g[by_token ? (int64_t)(p_n[ch] / a.top_k) : (int64_t)(it.s0 + nl)];
-          c_n[ch] = STAGE == STAGE_DOWN ? f * (a.topk_weights[p_n[ch]] * g2) : f;
+        c[ch] = 0.f;
+        if (p[ch] >= 0) {
+          const float f = a.act_g[by_token ? (int64_t)(p[ch] / a.top_k) : (int64_t)(it.s0 + nl)];
+          c[ch] = STAGE == STAGE_DOWN ? f * (a.topk_weights[p[ch]] * g2) : f;
         }
       }
     };
     pdl_wait();                      // activation globals come from the preceding kernel
-    int4 rec = make_int4(0, 0, 0, 0);  // record of the item after next
+    F4Item it0{}, it1{};             // the current item and the next
+    int p1[kCh];                     // the next item's pairs
+    float c0[kCh], gs0 = 1.f;        // the current item's factors
+    int4 rec2 = make_int4(0, 0, 0, 0);  // record of the item after next
+#pragma unroll
+    for (int ch = 0; ch < kCh; ++ch) {
+      p1[ch] = -1;
+      c0[ch] = 0.f;
+    }
     if (w0 < W) {
-      it_n = fp4_item(rec0, w0, nbp);
-      if (w0 + wstep < W) rec = fp4_record(a, w0 + wstep, nbp);
-      fetch_pairs(it_n);
-      fetch_factors(it_n);
+      it0 = fp4_item(rec0, w0, nbp);
+      int p0[kCh];
+      pairs_of(it0, p0);
+      factors_of(it0, p0, c0, gs0);
+      if (w0 + wstep < W) {
+        it1 = fp4_item(fp4_record(a, w0 + wstep, nbp), w0 + wstep, nbp);
+        pairs_of(it1, p1);
+      }
+      if (w0 + 2 * wstep < W) rec2 = fp4_record(a, w0 + 2 * wstep, nbp);
     }
     int li = 0;
     for (int w = w0; w < W && ok; w += wstep, ++li) {
-      const F4Item it = it_n;
-      const float gsel = gsel_n;
+      const F4Item it = it0;
+      const float gsel = gs0;
       float c_l[kCh];
 #pragma unroll
-      for (int ch = 0; ch < kCh; ++ch) c_l[ch] = c_n[ch];
-      const bool more = w + wstep < W;
-      if (more) {
-        it_n = fp4_item(rec, w + wstep, nbp);
-        if (w + 2 * wstep < W) rec = fp4_record(a, w + 2 * wstep, nbp);
-        fetch_pairs(it_n);
+      for (int ch = 0; ch < kCh; ++ch) c_l[ch] = c0[ch];
+      // the next items' loads, consumed one item later
+      float c1[kCh], gs1 = 1.f;
+      F4Item it2{};
+      int p2[kCh];
+#pragma unroll
+      for (int ch = 0; ch < kCh; ++ch) {
+        c1[ch] = 0.f;
+        p2[ch] = -1;
       }
+      if (w + wstep < W) factors_of(it1, p1, c1, gs1);
+      if (w + 2 * wstep < W) {
+        it2 = fp4_item(rec2, w + 2 * wstep, nbp);
+        pairs_of(it2, p2);
+      }
+      if (w + 3 * wstep < W) rec2 = fp4_record(a, w + 3 * wstep, nbp);
       const int b = li & 1;
       if (!mbar_wait(tfull0 + 8u * b, (li >> 1) & 1)) {
         ok = false;
         break;
       }
-      if (more) fetch_factors(it_n);
       tc_fence_after();
       const int blk = 2 * it.bp + (int)rank;
       const int tile = 8 * blk + (m >> 4), rr = m & 15;
@@ -472,6 +497,38 @@ __global__ void __launch_bounds__(kP4Threads, 1) k_grouped_fp4(const GroupedArgs
             const float r = fmaxf(v[j] * gsel, 0.f);
             if (n < it.ntok) outp[(size_t)(it.s0 + n) * a.n_rows + tile * 16 + rr] = r * r;
           }
+        } else if (a.out_bf16) {
+          // BF16 partials in 16-byte stores: an 8 x 8 transpose within each
+          // group of 8 lanes (three butterfly stages of shuffles) leaves lane
+          // 8g + t with column c0 + 8 jb + t of the group's 8 rows, stored as
+          // one 16-byte run.  (One 2-byte store per lane and column made the
+          // stores most of this epilogue's time, and the epilogue GEMM2's pace.)
+          const int t = lane & 7;
+          __nv_bfloat16 *ob = reinterpret_cast<__nv_bfloat16 *>(a.out) + (size_t)it.s0 * a.n_rows + blk * 128 + (m - t);
+#pragma unroll
+          for (int jb = 0; jb < 4; ++jb) {
+            float *x = v + 8 * jb;
+#pragma unroll
+            for (int sh = 4; sh >= 1; sh >>= 1) {
+              const bool up = (t & sh) != 0;
+#pragma unroll
+              for (int e = 0; e < 8; ++e) {
+                if (e & sh) continue;
+                const float recv = __shfl_xor_sync(0xffffffffu, up ? x[e] : x[e + sh], sh);
+                if (up) x[e] = recv;
+                else x[e + sh] = recv;
+              }
+            }
+            const int n = c0 + 8 * jb + t;
+            if (n < it.ntok) {
+              uint4 pk;
+              pk.x = bf16x2_bits(x[0], x[1]);
+              pk.y = bf16x2_bits(x[2], x[3]);
+              pk.z = bf16x2_bits(x[4], x[5]);
+              pk.w = bf16x2_bits(x[6], x[7]);
+              *reinterpret_cast<uint4 *>(ob + (size_t)n * a.n_rows) = pk;
+            }
+          }
         } else {
 #pragma unroll
           for (int j = 0; j < 32; ++j) {
@@ -485,6 +542,14 @@ __global__ void __launch_bounds__(kP4Threads, 1) k_grouped_fp4(const GroupedArgs
       // relaxed: the accumulator has been read (tcgen05.wait::ld), and this
       // warp's output stores need not complete before the MMA reuses it
       if (lane == 0) mbar_arrive_remote_relaxed(tempty_leader + 8u * b);
+      it0 = it1;
+      gs0 = gs1;
+      it1 = it2;
+#pragma unroll
+      for (int ch = 0; ch < kCh; ++ch) {
+        c0[ch] = c1[ch];
+        p1[ch] = p2[ch];
+      }
     }
   }
 
