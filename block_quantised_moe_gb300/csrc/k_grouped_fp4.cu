@@ -90,12 +90,6 @@ static_assert(kP4SfCols % 4 == 0 && kP4SfCol0 % 4 == 0, "scale-factor TMEM addre
 // the pair), K = 64.
 constexpr uint32_t kP4Idesc = (1u << 7) | (1u << 10) | ((uint32_t)(kP4N >> 3) << 17) | ((uint32_t)(256 >> 4) << 24);
 
-// Two floats as round-to-nearest BF16 in one word, the first in the low half.
-__device__ __forceinline__ uint32_t bf16x2_bits(float lo, float hi) {
-  const __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);
-  return *reinterpret_cast<const uint32_t *>(&h);
-}
-
 struct F4Item {
   int e, bp, s0, ntok;
 };
@@ -394,8 +388,7 @@ __global__ void __launch_bounds__(kP4Threads, 1) k_grouped_fp4(const GroupedArgs
     // gate / up / single matrix.  Item record -> the tile's pairs -> their
     // factors are three dependent global loads; they run as a pipeline over the
     // items (the record three items ahead, the pairs two, the factors one), so
-    // each load has a whole item's epilogue to return.  (As a chain started one
-    // item ahead they held up every GEMM2 item by about a microsecond.)
+    // each load has a whole item's epilogue to return.
     auto pairs_of = [&](const F4Item &it, int (&p)[kCh]) {
 #pragma unroll
       for (int ch = 0; ch < kCh; ++ch) {
@@ -496,38 +489,6 @@ __global__ void __launch_bounds__(kP4Threads, 1) k_grouped_fp4(const GroupedArgs
             const int n = c0 + j;
             const float r = fmaxf(v[j] * gsel, 0.f);
             if (n < it.ntok) outp[(size_t)(it.s0 + n) * a.n_rows + tile * 16 + rr] = r * r;
-          }
-        } else if (a.out_bf16) {
-          // BF16 partials in 16-byte stores: an 8 x 8 transpose within each
-          // group of 8 lanes (three butterfly stages of shuffles) leaves lane
-          // 8g + t with column c0 + 8 jb + t of the group's 8 rows, stored as
-          // one 16-byte run.  (One 2-byte store per lane and column made the
-          // stores most of this epilogue's time, and the epilogue GEMM2's pace.)
-          const int t = lane & 7;
-          __nv_bfloat16 *ob = reinterpret_cast<__nv_bfloat16 *>(a.out) + (size_t)it.s0 * a.n_rows + blk * 128 + (m - t);
-#pragma unroll
-          for (int jb = 0; jb < 4; ++jb) {
-            float *x = v + 8 * jb;
-#pragma unroll
-            for (int sh = 4; sh >= 1; sh >>= 1) {
-              const bool up = (t & sh) != 0;
-#pragma unroll
-              for (int e = 0; e < 8; ++e) {
-                if (e & sh) continue;
-                const float recv = __shfl_xor_sync(0xffffffffu, up ? x[e] : x[e + sh], sh);
-                if (up) x[e] = recv;
-                else x[e + sh] = recv;
-              }
-            }
-            const int n = c0 + 8 * jb + t;
-            if (n < it.ntok) {
-              uint4 pk;
-              pk.x = bf16x2_bits(x[0], x[1]);
-              pk.y = bf16x2_bits(x[2], x[3]);
-              pk.z = bf16x2_bits(x[4], x[5]);
-              pk.w = bf16x2_bits(x[6], x[7]);
-              *reinterpret_cast<uint4 *>(ob + (size_t)n * a.n_rows) = pk;
-            }
           }
         } else {
 #pragma unroll
